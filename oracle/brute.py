@@ -1,0 +1,95 @@
+"""A second, independent statement of the three chains in pure Python.
+
+TEST INFRASTRUCTURE ONLY (pins the C oracle; never used by the product path).
+It shares no code with ``fc_oracle.c``: different language, the library's
+``math.erf`` / ``math.exp`` / ``math.log`` rather than C's, softplus written as
+log(1 + e^z) directly (no max/log1p form), tanh of it via
+(e^{2s} - 1) / (e^{2s} + 1), and sums via ``math.fsum`` (exactly rounded).
+Only for tiny inputs: every loop is explicit.
+"""
+from __future__ import annotations
+
+import math
+
+
+def gelu(v):
+    return 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
+
+
+def _softplus(z):
+    if z > 40.0:               # log(1 + e^z) = z + log(1 + e^-z) = z to double precision
+        return z
+    return math.log(1.0 + math.exp(z)) if z > -30.0 else math.exp(z)
+
+
+def _tanh_pos(s):
+    # s = softplus(z) > 0; tanh(s) = (e^{2s} - 1) / (e^{2s} + 1)
+    if s > 20.0:
+        return 1.0
+    e = math.exp(2.0 * s)
+    return (e - 1.0) / (e + 1.0) if s > 1e-3 else math.tanh(s)
+
+
+def mish(z):
+    return z * _tanh_pos(_softplus(z))
+
+
+ACTS = {"gelu": gelu, "mish": mish, "mish_mish": lambda v: mish(mish(v)), "none": lambda v: v}
+
+
+def conv3x3(x, w, b):
+    """x: nested lists [N][Cin][H][W]; w: [Cout][Cin][3][3]; b: [Cout] -> [N][Cout][H-2][W-2]."""
+    N, Cin, H, W = len(x), len(x[0]), len(x[0][0]), len(x[0][0][0])
+    Cout = len(w)
+    out = []
+    for n in range(N):
+        planes = []
+        for co in range(Cout):
+            rows = []
+            for oh in range(H - 2):
+                row = []
+                for ow in range(W - 2):
+                    terms = [b[co]]
+                    for ci in range(Cin):
+                        for kh in range(3):
+                            for kw in range(3):
+                                terms.append(x[n][ci][oh + kh][ow + kw] * w[co][ci][kh][kw])
+                    row.append(math.fsum(terms))
+                rows.append(row)
+            planes.append(rows)
+        out.append(planes)
+    return out
+
+
+def conv3x3_act(x, w, b, act):
+    f = ACTS[act]
+    return [[[[f(v) for v in row] for row in plane] for plane in img] for img in conv3x3(x, w, b)]
+
+
+def conv3x3_act_pool(x, w, b, act):
+    out = []
+    for img in conv3x3_act(x, w, b, act):
+        out.append([math.fsum(v for row in plane for v in row) / (len(plane) * len(plane[0]))
+                    for plane in img])
+    return out
+
+
+def logsumexp(t):
+    m = max(t)
+    return m + math.log(math.fsum(math.exp(v - m) for v in t))
+
+
+def linear_lse_mish(x, Wt, b, scale, lo, hi):
+    """x: [M][K]; Wt: [Nout][K]; b: [Nout] -> (y[M], lse[M])."""
+    ys, ls = [], []
+    for xr in x:
+        t = []
+        for j, wr in enumerate(Wt):
+            v = math.fsum([b[j]] + [xk * wk for xk, wk in zip(xr, wr)])
+            v = v * scale
+            v = v + v
+            t.append(min(max(v, lo), hi))
+        lse = logsumexp(t)
+        ls.append(lse)
+        ys.append(lse * mish(lse))
+    return ys, ls

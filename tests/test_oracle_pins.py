@@ -1,0 +1,238 @@
+"""Pins of the oracle to facts outside itself (CPU only).
+
+Each test checks the fp64 oracle against something it cannot agree with by
+construction: printed table values, closed forms, invariants of the
+definitions, special cases that reduce to a crop of the input or to a
+constant, and an independent pure-Python brute force on tiny inputs.  The
+cases are chosen so that a plausible slip anywhere in the oracle (a flipped
+kernel, a transposed weight, a scaling applied once, the clamp in the wrong
+place, the wrong pool divisor, the tail missing its factor) fails one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import brute
+import fc_inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _tolist(a):
+    return np.asarray(a, dtype=np.float64).tolist()
+
+
+# ------------------------------------------------------------------ GELU pins
+
+def test_gelu_matches_normal_cdf_table():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "normal_cdf.txt")) if l.strip() and l[0] != "#"]
+    assert len(rows) >= 8
+    for xs, phis in rows:
+        x, phi = float(xs), float(phis)
+        assert oracle.gelu(x) == pytest.approx(x * phi, abs=1e-15, rel=1e-14)
+
+
+def test_gelu_invariants():
+    assert oracle.gelu(0.0) == 0.0
+    for x in np.linspace(-7, 7, 57):
+        # GELU(x) - GELU(-x) = x Phi(x) + x Phi(x) - x = x   (Phi(-x) = 1 - Phi(x))
+        assert oracle.gelu(x) - oracle.gelu(-x) == pytest.approx(x, abs=1e-14)
+    for x in (8.0, 10.0, 30.0):
+        assert abs(oracle.gelu(x) - x) < 1e-14
+        assert abs(oracle.gelu(-x)) < 1e-14
+
+
+# ------------------------------------------------------------------ Mish pins
+
+def _mish_closed_form(z):
+    # tanh(log(1+e^z)) = ((1+e^z)^2 - 1) / ((1+e^z)^2 + 1) = n / (n + 2), n = e^z (e^z + 2)
+    ez = math.exp(z)
+    n = ez * (ez + 2.0)
+    return z * n / (n + 2.0)
+
+
+def test_mish_closed_form_identity():
+    assert oracle.mish(0.0) == 0.0
+    for z in np.linspace(-20, 20, 81):
+        assert oracle.mish(z) == pytest.approx(_mish_closed_form(z), rel=1e-13, abs=1e-300)
+
+
+def test_mish_limits():
+    for z in (25.0, 50.0, 500.0):
+        assert oracle.mish(z) == pytest.approx(z, rel=1e-15)
+    for z in (-30.0, -50.0, -200.0):
+        # mish(z) ~ z e^z as z -> -inf (tanh(s) ~ s ~ e^z)
+        assert oracle.mish(z) == pytest.approx(z * math.exp(z), rel=1e-10)
+    assert oracle.act("mish_mish", 1.0) == pytest.approx(_mish_closed_form(_mish_closed_form(1.0)), rel=1e-13)
+
+
+def test_softplus_stable_form():
+    for z in (-800.0, -40.0, -1.0, 0.0, 1.0, 40.0, 800.0):
+        ref = z + math.log1p(math.exp(-z)) if z > 0 else math.log1p(math.exp(z))
+        assert oracle.softplus(z) == pytest.approx(ref, rel=1e-15, abs=1e-320)
+
+
+# ------------------------------------------------------------------ conv pins
+
+def test_conv_delta_kernel_reproduces_shifted_crop():
+    rng = np.random.default_rng(5)
+    N, Cin, H, W, Cout = 2, 3, 7, 9, 4
+    x = rng.standard_normal((N, Cin, H, W)).astype(np.float32)
+    for (cip, a, c) in [(0, 0, 0), (1, 2, 1), (2, 1, 2), (1, 0, 2)]:
+        w = np.zeros((Cout, Cin, 3, 3), np.float32)
+        w[:, cip, a, c] = 1.0
+        b = np.zeros(Cout, np.float32)
+        pre = oracle.conv3x3_preact(x, w, b)
+        crop = x[:, cip, a:a + H - 2, c:c + W - 2].astype(np.float64)
+        for co in range(Cout):
+            np.testing.assert_array_equal(pre[:, co], crop)
+
+
+def test_conv_linear_in_weights_and_bias_only_when_w_zero():
+    x, w1, _ = (fc_inputs.conv_inputs(2, 3, 8, 7, 5, seeds=(11, 12, 13))[k] for k in ("x", "w", "b"))
+    w2 = fc_inputs.conv_inputs(2, 3, 8, 7, 5, seeds=(11, 14, 15))["w"]
+    zb = np.zeros(5, np.float32)
+    p1 = oracle.conv3x3_preact(x, w1, zb)
+    p2 = oracle.conv3x3_preact(x, w2, zb)
+    p12 = oracle.conv3x3_preact(x, (w1.astype(np.float64) + w2).astype(np.float32), zb)
+    # w1 + w2 is rounded to fp32 once; compare against the exact fp64 sum of the two convs
+    # with a bound of that rounding (|w| < 0.2, 27 taps, |x| < 6 -> 27 * 6 * 2^-24 * 0.4)
+    np.testing.assert_allclose(p12, p1 + p2, atol=1e-5)
+    b = np.linspace(-0.3, 0.3, 5).astype(np.float32)
+    pre0 = oracle.conv3x3_preact(x, np.zeros_like(w1), b)
+    for co in range(5):
+        assert np.all(pre0[:, co] == np.float64(b[co]))
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 5, 5, 3), (2, 3, 7, 6, 4)])
+@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish"])
+def test_conv_act_against_brute_force(shape, act):
+    N, Cin, H, W, Cout = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, seeds=(21, 22, 23))
+    x, w, b = d["x"], d["w"], d["b"]
+    ref = np.array(brute.conv3x3_act(_tolist(x), _tolist(w), _tolist(b), act))
+    got = oracle.conv3x3_act(x, w, b, act)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+    ref_pool = np.array(brute.conv3x3_act_pool(_tolist(x), _tolist(w), _tolist(b), act))
+    got_pool = oracle.conv3x3_act_pool(x, w, b, act)
+    np.testing.assert_allclose(got_pool, ref_pool, rtol=1e-12, atol=1e-14)
+    # sampled entry points agree with the full ones
+    flat = np.arange(got.size)[::3]
+    np.testing.assert_array_equal(oracle.conv3x3_act_at(x, w, b, flat, act), got.reshape(-1)[flat])
+    flat_nc = np.arange(N * Cout)[::2]
+    np.testing.assert_array_equal(oracle.conv3x3_act_pool_at(x, w, b, flat_nc, act), got_pool.reshape(-1)[flat_nc])
+
+
+def test_pool_with_zero_weights_is_act_of_bias():
+    d = fc_inputs.conv_inputs(2, 3, 9, 11, 6, seeds=(31, 32, 33))
+    y = oracle.conv3x3_act_pool(d["x"], np.zeros_like(d["w"]), d["b"], "gelu")
+    for co in range(6):
+        # the mean of OH*OW equal terms is that term, up to the rounding of the fp64 sum
+        np.testing.assert_allclose(y[:, co], oracle.gelu(float(d["b"][co])), rtol=1e-14, atol=0)
+
+
+def test_pool_of_constant_plane_is_act_of_constant_conv():
+    N, Cin, H, W, Cout = 1, 2, 6, 8, 3
+    x = np.full((N, Cin, H, W), 0.75, np.float32)
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, seeds=(41, 42, 43))
+    w, b = d["w"], d["b"]
+    y = oracle.conv3x3_act_pool(x, w, b, "gelu")
+    for co in range(Cout):
+        v = math.fsum([float(b[co])] + [0.75 * float(t) for t in w[co].reshape(-1)])
+        assert y[0, co] == pytest.approx(oracle.gelu(v), rel=1e-13)
+
+
+# ------------------------------------------------------------------- LSE pins
+
+def test_lse_constant_row_and_shift_invariance():
+    for n in (1, 7, 8192):
+        for c in (-3.5, 0.0, 2.25, 10.0):
+            assert oracle.logsumexp(np.full(n, c)) == pytest.approx(c + math.log(n), abs=1e-12)
+    t = np.random.default_rng(1).standard_normal(1000) * 3
+    for a in (-100.0, 0.5, 700.0):
+        assert oracle.logsumexp(t + a) == pytest.approx(oracle.logsumexp(t) + a, rel=1e-13)
+    one_hot = np.full(100, -50.0)
+    one_hot[37] = 60.0
+    # exactly 60 + log(1 + 99 e^-110)
+    assert oracle.logsumexp(one_hot) == pytest.approx(60.0 + math.log1p(99 * math.exp(-110.0)), rel=1e-15)
+
+
+def test_linear_zero_weights_closed_form():
+    M, K, Nout = 3, 16, 8192
+    x = np.random.default_rng(3).standard_normal((M, K)).astype(np.float32)
+    for c, expect_t in [(0.5, 2.0), (3.0, 10.0), (-4.0, -10.0), (-1.25, -5.0)]:
+        b = np.full(Nout, c, np.float32)
+        y, l = oracle.linear_lse_mish(x, np.zeros((Nout, K), np.float32), b, return_lse=True)
+        # t = clamp((c*2) + (c*2)) for every column -> l = clamp(4c) + ln Nout
+        np.testing.assert_allclose(l, expect_t + math.log(Nout), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(y, l * np.array([_mish_closed_form(v) for v in l]), rtol=1e-13)
+
+
+def test_linear_lse_bounds_and_tail():
+    M, K, Nout = 4, 32, 64
+    d = fc_inputs.linear_inputs(M, K, Nout, seeds=(51, 52, 53))
+    x = d["x"] * 40.0           # drive |4t| far past 10 so the clamp is active
+    y, l = oracle.linear_lse_mish(x, d["W"], d["b"], return_lse=True)
+    assert np.all(l >= -10.0 + math.log(Nout) - 1e-12)
+    assert np.all(l <= 10.0 + math.log(Nout) + 1e-12)
+    # the tail is l * mish(l) (~ l^2 for large l), not mish(l)
+    for v in (11.68, 15.0):
+        yv = v * oracle.mish(v)
+        assert yv == pytest.approx(v * v, rel=1e-9)
+    assert 11.68 * oracle.mish(11.68) == pytest.approx(136.4224, abs=1e-3)
+
+
+@pytest.mark.parametrize("scale_x", [1.0, 30.0])
+def test_linear_against_brute_force(scale_x):
+    M, K, Nout = 3, 5, 7
+    d = fc_inputs.linear_inputs(M, K, Nout, seeds=(61, 62, 63))
+    x = (d["x"] * scale_x).astype(np.float32)
+    ys, ls = brute.linear_lse_mish(_tolist(x), _tolist(d["W"]), _tolist(d["b"]), 2.0, -10.0, 10.0)
+    y, l = oracle.linear_lse_mish(x, d["W"], d["b"], return_lse=True)
+    np.testing.assert_allclose(l, ls, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(y, ys, rtol=1e-12, atol=1e-13)
+    # row subsets agree with the full call
+    y2 = oracle.linear_lse_mish(x, d["W"], d["b"], rows=[2, 0])
+    np.testing.assert_array_equal(y2, y[[2, 0]])
+
+
+def test_linear_is_x_times_w_transposed():
+    # a non-square W with one non-zero entry W[j0, k0] selects x[:, k0] into column j0
+    M, K, Nout, j0, k0 = 2, 6, 3, 2, 4
+    x = np.arange(M * K, dtype=np.float32).reshape(M, K) / 10.0
+    Wt = np.zeros((Nout, K), np.float32)
+    Wt[j0, k0] = 1.0
+    b = np.zeros(Nout, np.float32)
+    _, l = oracle.linear_lse_mish(x, Wt, b, return_lse=True)
+    for m in range(M):
+        t = [0.0] * Nout
+        t[j0] = min(max(4.0 * float(x[m, k0]), -10.0), 10.0)
+        assert l[m] == pytest.approx(max(t) + math.log(sum(math.exp(v - max(t)) for v in t)), rel=1e-14)
+
+
+# ---------------------------------------------------------- input generator
+
+def test_bf16_rounding_is_nearest_even():
+    vals = np.array([1.0, 1.0 + 2**-8, 1.0 + 2**-8 + 2**-20, 1.0 + 3 * 2**-8, -2.5, 3.1415927], np.float32)
+    bits = fc_inputs.bf16_bits(vals)
+    back = fc_inputs.bf16_bits_to_f32(bits)
+    assert back[0] == 1.0
+    assert back[1] == 1.0                       # tie -> even
+    assert back[2] == np.float32(1.0 + 2**-7)   # above the tie -> up
+    assert back[3] == np.float32(1.0 + 2**-6)   # tie -> even (up)
+    assert back[4] == -2.5
+    assert abs(back[5] - 3.1415927) <= 2**-7 * 2
+
+
+def test_inputs_are_seeded_and_shaped():
+    a = fc_inputs.conv_inputs(2, 8, 32, 32, 64)
+    b = fc_inputs.conv_inputs(2, 8, 32, 32, 64)
+    assert a["x"].shape == (2, 8, 32, 32) and a["w"].shape == (64, 8, 3, 3)
+    np.testing.assert_array_equal(a["x"], b["x"])
+    bound = 1 / math.sqrt(72)
+    assert np.all(np.abs(a["w"]) <= bound) and np.all(np.abs(a["b"]) <= bound)
+    assert abs(float(a["x"].mean())) < 0.05 and abs(float(a["x"].std()) - 1) < 0.05
