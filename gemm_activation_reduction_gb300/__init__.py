@@ -1,0 +1,220 @@
+"""GB300 (sm_103a) fused contraction + activation + reduction kernels.
+
+Thin ctypes binding over the C ABI in ``include/fc.h``: the functions below
+carry the C names, check that the torch tensors they are given are CUDA,
+contiguous and of the right dtype, allocate the output and the workspace
+with torch (device memory only), and pass raw pointers plus the current
+CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or eager-PyTorch fallback, and calling any op
+without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import _build
+
+__all__ = [
+    "FCError", "load", "build", "library_path",
+    "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish",
+    "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
+    "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
+    "FC_F32", "FC_BF16", "ACTS", "OPS",
+]
+
+FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
+FC_F32, FC_BF16 = 0, 1
+ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2}
+OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
+
+# Every symbol include/fc.h declares.
+EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_workspace_bytes",
+           "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FCError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fc_status_string(status)} (status {status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree for sm_103a; returns its path."""
+    return _build.build(force=force)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the CUDA library (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P, I, F, S, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
+        conv = [P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+        lib.fc_conv3x3_act_pool.argtypes = conv
+        lib.fc_conv3x3_act_pool.restype = I
+        lib.fc_conv3x3_act.argtypes = conv
+        lib.fc_conv3x3_act.restype = I
+        lib.fc_linear_lse_mish.argtypes = [P, P, P, P, I, I, I, F, F, F, I, P, S, P]
+        lib.fc_linear_lse_mish.restype = I
+        lib.fc_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        lib.fc_workspace_bytes.restype = S
+        lib.fc_status_string.argtypes = [I]
+        lib.fc_status_string.restype = ctypes.c_char_p
+        lib.fc_device_status.argtypes = [I]
+        lib.fc_device_status.restype = I
+        lib.fc_selftest_watchdog.argtypes = [Z, P]
+        lib.fc_selftest_watchdog.restype = I
+        lib.fc_version.restype = I
+        _lib = lib
+        return lib
+
+
+def fc_status_string(status: int) -> str:
+    return load().fc_status_string(int(status)).decode()
+
+
+def fc_version() -> int:
+    return load().fc_version()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtypes, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _dtype_code(t):
+    torch = _torch()
+    return FC_F32 if t.dtype == torch.float32 else FC_BF16
+
+
+def _raise(status, where):
+    if status != FC_OK:
+        raise FCError(status, where)
+
+
+def fc_workspace_bytes(op: str, n_or_m: int, cin_or_k: int, h: int, w: int, cout_or_nout: int,
+                       dtype: int = FC_F32) -> int:
+    """Workspace bytes a call needs on the current device (0 when the arguments are invalid)."""
+    return int(load().fc_workspace_bytes(OPS[op], n_or_m, cin_or_k, h, w, cout_or_nout, dtype))
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        # the library itself checks the size (FC_ERR_WORKSPACE)
+        _check(workspace, "workspace", (torch.uint8,), device)
+        return workspace, workspace.numel()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape):
+    torch = _torch()
+    lib = load()
+    dts = (torch.float32, torch.bfloat16)
+    _check(x, "x", dts)
+    _check(w, "w", (x.dtype,), x.device)
+    _check(b, "b", (x.dtype,), x.device)
+    if x.dim() != 4 or w.dim() != 4 or tuple(w.shape[1:]) != (x.shape[1], 3, 3) or b.shape != (w.shape[0],):
+        raise ValueError("expected x [N,Cin,H,W], w [Cout,Cin,3,3], b [Cout]")
+    N, Cin, H, W = (int(s) for s in x.shape)
+    Cout = int(w.shape[0])
+    shape = out_shape(N, Cout, H, W)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    else:
+        _check(out, "out", (torch.float32,), x.device)
+        if tuple(out.shape) != shape:
+            raise ValueError(f"out must have shape {shape}")
+    dt = _dtype_code(x)
+    with torch.cuda.device(x.device):
+        nbytes = int(lib.fc_workspace_bytes(OPS[op], N, Cin, H, W, Cout, dt))
+        ws, wsb = _workspace(nbytes, x.device, workspace)
+        st = getattr(lib, cname)(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W, Cout, dt,
+                                 ACTS[act], None if ws is None else ws.data_ptr(), wsb, _stream_handle(stream))
+    _raise(st, cname)
+    return out
+
+
+def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None):
+    """y[N, Cout] = mean over the (H-2)x(W-2) plane of act(conv3x3(x, w) + b); fp32 output."""
+    return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream,
+                 lambda N, Cout, H, W: (N, Cout))
+
+
+def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None):
+    """y[N, Cout, H-2, W-2] = act(conv3x3(x, w) + b); fp32 output."""
+    return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream,
+                 lambda N, Cout, H, W: (N, Cout, H - 2, W - 2))
+
+
+def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,
+                       out=None, workspace=None, stream=None):
+    """y[M, 1] = l * mish(l), l = logsumexp_j clamp(u + u), u = (x W^T + b) * scale."""
+    torch = _torch()
+    lib = load()
+    _check(x, "x", (torch.float32, torch.bfloat16))
+    _check(W, "W", (x.dtype,), x.device)
+    _check(b, "b", (x.dtype,), x.device)
+    if x.dim() != 2 or W.dim() != 2 or W.shape[1] != x.shape[1] or b.shape != (W.shape[0],):
+        raise ValueError("expected x [M,K], W [Nout,K], b [Nout]")
+    M, K = (int(s) for s in x.shape)
+    Nout = int(W.shape[0])
+    if out is None:
+        out = torch.empty((M, 1), dtype=torch.float32, device=x.device)
+    else:
+        _check(out, "out", (torch.float32,), x.device)
+        if out.numel() != M:
+            raise ValueError(f"out must hold {M} values")
+    dt = _dtype_code(x)
+    with torch.cuda.device(x.device):
+        nbytes = int(lib.fc_workspace_bytes(OPS["linear_lse_mish"], M, K, 1, 1, Nout, dt))
+        ws, wsb = _workspace(nbytes, x.device, workspace)
+        st = lib.fc_linear_lse_mish(x.data_ptr(), W.data_ptr(), b.data_ptr(), out.data_ptr(), M, K, Nout,
+                                    float(scale), float(clamp_lo), float(clamp_hi), dt,
+                                    None if ws is None else ws.data_ptr(), wsb, _stream_handle(stream))
+    _raise(st, "fc_linear_lse_mish")
+    return out
+
+
+def fc_device_status(clear: bool = True) -> int:
+    """Synchronize the current device and return (and by default clear) its watchdog word."""
+    return int(load().fc_device_status(1 if clear else 0))
+
+
+def fc_selftest_watchdog(budget_cycles: int, stream=None) -> None:
+    """Enqueue the watchdog self-test kernel (a wait that must time out)."""
+    _raise(load().fc_selftest_watchdog(int(budget_cycles), _stream_handle(stream)), "fc_selftest_watchdog")

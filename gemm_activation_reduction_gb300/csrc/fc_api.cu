@@ -1,0 +1,192 @@
+// fc_api.cu -- the C ABI: argument validation, workspace sizing, the device
+// status word, and dispatch to the fused kernels.  No entry point allocates
+// memory or falls back to anything but its CUDA kernels.
+#include "../../include/fc.h"
+#include "fc_internal.h"
+#include "fc_ptx.cuh"
+
+#include <cstdint>
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+__device__ int g_fc_status = 0;
+
+struct DeviceState {
+    std::once_flag once;
+    int sm_count = 0;
+    int* status = nullptr;   // device address of g_fc_status on this device
+    cudaError_t err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+// SM count and status-word address of the current device.
+fc_status device_state(DeviceState** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FC_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    std::call_once(d.once, [&d, dev]() {
+        d.err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fc_status);
+    });
+    if (d.err != cudaSuccess) return FC_ERR_CUDA;
+    *out = &d;
+    return FC_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fc_status conv_common(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
+                      fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes, fc_stream_t stream,
+                      int pool)
+{
+    if (!x || !w || !b || !y) return FC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
+    if (N < 1 || Cin < 1 || H < 3 || W < 3 || Cout < 1) return FC_ERR_INVALID_ARG;
+    if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
+    if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH) return FC_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    fc::ConvPlan plan;
+    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, dtype == FC_BF16, pool, d->sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    const size_t need = plan.ws_weights_bytes + plan.ws_pool_bytes;
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return FC_ERR_WORKSPACE;
+    cudaError_t e = fc::conv_launch(plan, x, w, b, y, static_cast<int>(act), workspace,
+                                    reinterpret_cast<cudaStream_t>(stream), d->status, fc::kWaitBudgetCycles);
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
+__global__ void watchdog_kernel(long long budget, int* status)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        fc::mbar_init(&bar, 1);
+        abort_flag = 0;
+        fc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the bounded wait must give up and record the timeout.
+        fc::mbar_wait(&bar, 0, &abort_flag, status, budget);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+namespace fc {
+cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int* status)
+{
+    watchdog_kernel<<<1, 32, 0, stream>>>(budget, status);
+    return cudaGetLastError();
+}
+}  // namespace fc
+
+extern "C" {
+
+fc_status fc_conv3x3_act_pool(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W,
+                              int Cout, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
+                              fc_stream_t stream)
+{
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, dtype, act, workspace, workspace_bytes, stream, 1);
+}
+
+fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
+                         fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes, fc_stream_t stream)
+{
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, dtype, act, workspace, workspace_bytes, stream, 0);
+}
+
+fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y, int M, int K, int Nout,
+                             float scale, float clamp_lo, float clamp_hi, fc_dtype dtype, void* workspace,
+                             size_t workspace_bytes, fc_stream_t stream)
+{
+    if (!x || !W || !b || !y) return FC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || Nout < 1) return FC_ERR_INVALID_ARG;
+    if (!(clamp_lo <= clamp_hi)) return FC_ERR_INVALID_ARG;   // also rejects NaN bounds
+    if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
+    if (dtype != FC_F32) return FC_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    fc::LinearPlan plan;
+    if (fc::linear_plan(&plan, M, K, Nout, d->sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FC_ERR_WORKSPACE;
+    cudaError_t e = fc::linear_launch(plan, static_cast<const float*>(x), static_cast<const float*>(W),
+                                      static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, workspace,
+                                      reinterpret_cast<cudaStream_t>(stream), d->status, fc::kWaitBudgetCycles);
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
+size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int cout_or_nout, fc_dtype dtype)
+{
+    DeviceState* d = nullptr;
+    if (device_state(&d) != FC_OK) return 0;
+    if (dtype != FC_F32 && dtype != FC_BF16) return 0;
+    if (op == FC_OP_CONV3X3_ACT_POOL || op == FC_OP_CONV3X3_ACT) {
+        if (n_or_m < 1 || cin_or_k < 1 || h < 3 || w < 3 || cout_or_nout < 1) return 0;
+        fc::ConvPlan plan;
+        if (fc::conv_plan(&plan, n_or_m, cin_or_k, h, w, cout_or_nout, dtype == FC_BF16,
+                          op == FC_OP_CONV3X3_ACT_POOL, d->sm_count) != 0)
+            return 0;
+        return plan.ws_weights_bytes + plan.ws_pool_bytes;
+    }
+    if (op == FC_OP_LINEAR_LSE_MISH) {
+        if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1) return 0;
+        fc::LinearPlan plan;
+        if (fc::linear_plan(&plan, n_or_m, cin_or_k, cout_or_nout, d->sm_count) != 0) return 0;
+        return plan.ws_bytes;
+    }
+    return 0;
+}
+
+const char* fc_status_string(fc_status s)
+{
+    switch (s) {
+    case FC_OK: return "ok";
+    case FC_ERR_INVALID_ARG: return "invalid argument";
+    case FC_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case FC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FC_ERR_CUDA: return "CUDA error";
+    case FC_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    default: return "unknown status";
+    }
+}
+
+fc_status fc_device_status(int clear)
+{
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FC_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FC_ERR_CUDA;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FC_ERR_CUDA;
+    }
+    return v == 0 ? FC_OK : static_cast<fc_status>(v);
+}
+
+fc_status fc_selftest_watchdog(unsigned long long budget_cycles, fc_stream_t stream)
+{
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    if (budget_cycles > 4000000000ull) return FC_ERR_INVALID_ARG;
+    cudaError_t e = fc::watchdog_selftest_launch(static_cast<long long>(budget_cycles),
+                                                 reinterpret_cast<cudaStream_t>(stream), d->status);
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
+int fc_version(void) { return 100; }
+
+}  // extern "C"

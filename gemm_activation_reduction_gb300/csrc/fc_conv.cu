@@ -1,0 +1,155 @@
+// fc_conv.cu -- host side of the fused conv3x3 operators: the launch plan
+// (tiling, pipeline depth, tensor-memory buffers, workspace layout), the
+// once-per-call weight re-layout kernel, the fixed-order pool combine kernel,
+// and the launch sequence.  The fused kernel itself is in fc_conv_kernel.cuh.
+#include "fc_conv_kernel.cuh"
+
+#include <algorithm>
+
+namespace fc {
+using namespace convk;
+namespace {
+
+// Re-lay w [Cout][Cin][3][3] into [K block][tap][half][co][G] (G = 4 fp32 rounded
+// to TF32, or 8 bf16), zero-padding channels past Cin.
+template <bool BF16>
+__global__ void conv_weight_relayout_kernel(const void* w, void* wr, int Cin, int Cout, int ncb)
+{
+    constexpr int G = BF16 ? 8 : 4;
+    const long long total = static_cast<long long>(ncb) * 9 * 2 * Cout * G;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long f = i;
+        const int e = static_cast<int>(f % G);
+        f /= G;
+        const int co = static_cast<int>(f % Cout);
+        f /= Cout;
+        const int half = static_cast<int>(f % 2);
+        f /= 2;
+        const int tap = static_cast<int>(f % 9);
+        const int cb = static_cast<int>(f / 9);
+        const int ci = cb * 2 * G + half * G + e;
+        const size_t src = (static_cast<size_t>(co) * Cin + ci) * 9 + tap;
+        if constexpr (BF16) {
+            const unsigned short* ws = reinterpret_cast<const unsigned short*>(w);
+            reinterpret_cast<unsigned short*>(wr)[i] = ci < Cin ? ws[src] : static_cast<unsigned short>(0);
+        } else {
+            const float* ws = reinterpret_cast<const float*>(w);
+            reinterpret_cast<float*>(wr)[i] = ci < Cin ? to_tf32(ws[src]) : 0.0f;
+        }
+    }
+}
+
+// y[n, co] = (fixed-order sum of the partials of every CTA that covered image n) / (OH * OW).
+__global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Cout, long long tpi, long long base,
+                                         int rem, int J, double inv_count)
+{
+    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (idx >= static_cast<long long>(N) * Cout) return;
+    const int n = static_cast<int>(idx / Cout);
+    const int co = static_cast<int>(idx - static_cast<long long>(n) * Cout);
+    const long long big = static_cast<long long>(rem) * (base + 1);
+    auto cta_of = [&](long long t) -> long long { return t < big ? t / (base + 1) : rem + (t - big) / base; };
+    auto start_of = [&](long long c) -> long long { return c * base + (c < rem ? c : rem); };
+    const long long t0 = static_cast<long long>(n) * tpi;
+    const long long c0 = cta_of(t0), c1 = cta_of(t0 + tpi - 1);
+    double s = 0.0;
+    for (long long c = c0; c <= c1; ++c) {
+        const long long nf = start_of(c) / tpi;
+        const float* p = ws + ((c * J + (n - nf)) * 4) * static_cast<long long>(Cout) + co;
+        for (int q = 0; q < 4; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
+    }
+    y[idx] = static_cast<float>(s * inv_count);
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count)
+{
+    *p = ConvPlan{};
+    if (Cout < 32 || Cout > 256 || Cout % 32 != 0) return 2;
+    p->N = N; p->Cin = Cin; p->H = H; p->W = W; p->Cout = Cout;
+    p->OH = H - 2; p->OW = W - 2;
+    p->bf16 = bf16; p->pool = pool;
+    p->esize = bf16 ? 2 : 4;
+    p->cb_ch = bf16 ? 16 : 8;
+    p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch;
+    p->RB = (p->OH + kPatchRows - 1) / kPatchRows;
+    p->CS = (p->OW + kPatchCols - 1) / kPatchCols;
+    p->tpi = static_cast<long long>(p->RB) * p->CS;
+    p->num_tiles = static_cast<long long>(N) * p->tpi;
+    p->grid = static_cast<int>(std::min<long long>(p->num_tiles, std::max(sm_count, 1)));
+    p->base = p->num_tiles / p->grid;
+    p->rem = static_cast<int>(p->num_tiles % p->grid);
+    p->J = static_cast<int>((p->base + 1 + p->tpi - 1) / p->tpi) + 1;
+    p->w_block_bytes = 9u * 2u * static_cast<uint32_t>(Cout) * 16u;
+    const unsigned long long wtot = static_cast<unsigned long long>(p->w_block_bytes) * p->ncb;
+    if (wtot > 0xFFFFFFFFull) return 2;
+    p->w_total_bytes = static_cast<uint32_t>(wtot);
+    p->resident = p->w_total_bytes <= kResidentMax;
+    if (p->resident) {
+        p->stages = 4;
+    } else {
+        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + kStripBytes)));
+        if (p->stages < 2) return 2;
+    }
+    p->nacc = std::min(4, 512 / Cout);
+    int cols = 32;
+    while (cols < p->nacc * Cout) cols <<= 1;
+    p->tmem_cols = cols;
+    p->strip_off = 0;
+    p->w_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
+    p->bar_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
+    p->bar_off = (p->bar_off + 127u) & ~127u;
+    // barriers (19 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
+    p->smem_bytes = p->bar_off + 256u + 1024u;
+    p->ws_weights_bytes = align256(p->w_total_bytes);
+    p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
+    return 0;
+}
+
+cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const void* b, float* y, int act,
+                        void* workspace, cudaStream_t stream, int* status, long long budget)
+{
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    void* wr = ws;
+    float* pool_ws = reinterpret_cast<float*>(ws + p.ws_weights_bytes);
+
+    {
+        const long long total = static_cast<long long>(p.ncb) * 9 * 2 * p.Cout * (p.bf16 ? 8 : 4);
+        const int threads = 256;
+        const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, 4096));
+        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, wr, p.Cin, p.Cout, p.ncb);
+        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, wr, p.Cin, p.Cout, p.ncb);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    ConvArgs a{};
+    a.x = x; a.wr = wr; a.bias = b;
+    a.out = p.pool ? pool_ws : y;
+    a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.OH = p.OH; a.OW = p.OW;
+    a.ncb = p.ncb; a.CS = p.CS; a.tpi = p.tpi; a.base = p.base; a.rem = p.rem; a.J = p.J;
+    a.stages = p.stages; a.resident = p.resident; a.nacc = p.nacc; a.tmem_cols = p.tmem_cols;
+    a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes;
+    a.strip_off = p.strip_off; a.w_off = p.w_off; a.bar_off = p.bar_off;
+    a.status = status; a.budget = budget;
+
+    cudaError_t e = p.bf16 ? launch_main_bf16(a, p.pool, act, p.grid, p.smem_bytes, stream)
+                           : launch_main_tf32(a, p.pool, act, p.grid, p.smem_bytes, stream);
+    if (e != cudaSuccess) return e;
+
+    if (p.pool) {
+        const long long outs = static_cast<long long>(p.N) * p.Cout;
+        const int threads = 256;
+        const int blocks = static_cast<int>((outs + threads - 1) / threads);
+        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Cout, p.tpi, p.base, p.rem, p.J,
+                                                                  1.0 / (static_cast<double>(p.OH) * p.OW));
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace fc

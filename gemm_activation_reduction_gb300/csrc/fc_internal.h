@@ -1,0 +1,74 @@
+// fc_internal.h -- declarations shared by the library's translation units
+// (never installed, never part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+// Value a kernel writes into the device status word when a bounded wait runs
+// out; equal to FC_ERR_TIMEOUT of the public header.
+#define FC_DEVICE_TIMEOUT 5
+
+namespace fc {
+
+// Default spin budget of every mbarrier wait, in SM clock cycles (~1 s at 2 GHz).
+constexpr long long kWaitBudgetCycles = 2000000000LL;
+
+// ---------------------------------------------------------------- conv
+
+// Geometry and resources of one fused conv3x3 call; computed on the host by
+// conv_plan() and passed by value to the kernel.
+struct ConvPlan {
+    int N, Cin, H, W, Cout, OH, OW;
+    int bf16, pool;
+    int esize;            // bytes per stored element (4 or 2)
+    int cb_ch;            // input channels per K block (8 fp32, 16 bf16)
+    int ncb;              // K blocks = ceil(Cin / cb_ch)
+    int RB, CS;           // output row blocks (16 rows) and column strips (8 columns) per image
+    long long tpi;        // tiles per image = RB * CS
+    long long num_tiles;  // N * tpi
+    int grid;             // CTAs (persistent)
+    long long base;       // tiles per CTA (the first `rem` CTAs take one more)
+    int rem;
+    int J;                // image slots per CTA in the pool partial buffer
+    int stages;           // shared-memory pipeline depth
+    int resident;         // whole re-laid weight tensor kept in shared memory
+    int nacc;             // tensor-memory accumulator buffers
+    int tmem_cols;        // tensor-memory columns allocated
+    uint32_t w_block_bytes;   // re-laid weights of one K block: 9 taps * 2 halves * Cout * 16 B
+    uint32_t w_total_bytes;   // ncb * w_block_bytes
+    uint32_t strip_off, w_off, bar_off, smem_bytes;
+    size_t ws_weights_bytes;  // re-laid weights in the workspace
+    size_t ws_pool_bytes;     // pool partial sums in the workspace
+};
+
+// Fills `plan`; returns 0 on success, 2 (unsupported) when the shape is outside
+// what the kernels cover.
+int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count);
+
+cudaError_t conv_launch(const ConvPlan& plan, const void* x, const void* w, const void* b, float* y, int act,
+                        void* workspace, cudaStream_t stream, int* status, long long budget);
+
+// ---------------------------------------------------------------- linear
+
+struct LinearPlan {
+    int M, K, Nout;
+    int m_blocks, n_blocks, k_blocks;
+    int num_tiles, grid;
+    uint32_t smem_bytes;
+    size_t ws_bytes;      // (max, sum-exp) partial per row and column tile
+};
+
+int linear_plan(LinearPlan* plan, int M, int K, int Nout, int sm_count);
+
+cudaError_t linear_launch(const LinearPlan& plan, const float* x, const float* W, const float* b, float* y,
+                          float scale, float lo, float hi, void* workspace, cudaStream_t stream, int* status,
+                          long long budget);
+
+// ---------------------------------------------------------------- misc
+
+cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int* status);
+
+}  // namespace fc

@@ -1,0 +1,306 @@
+// fc_linear.cu -- fused Linear + bias -> x*scale -> x+x -> clamp -> row logsumexp
+// -> x*mish(x) (page "Kimi-K2.6 l2_p22": the module's forward; the stable
+// logsumexp and the streaming "running max with rescaled sum" it weighs).
+//
+// Main kernel: persistent TF32 GEMM on tcgen05.  Tile 128 x 256 x 32; both
+// operands are K-major (x [M][K] rows and nn.Linear's W [Nout][K] rows are
+// contiguous in K), loaded by TMA with 128-byte swizzle into a 4-stage
+// shared-memory ring; the accumulator lives in tensor memory, double-buffered
+// (2 x 256 columns) so the epilogue of tile i overlaps the MMAs of tile i+1.
+// The epilogue reads each accumulator row, applies bias, the two scalings and
+// the clamp, and reduces the 256 columns to one (max, sum exp(t - max)) pair
+// with the online rescaling update; the pairs of all column tiles of a row are
+// merged by a second, one-thread-per-row kernel in fixed order, which also
+// applies the x * mish(x) tail.  The (M x Nout) intermediate never exists.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 tensor-memory
+// allocator + MMA issuer, warps 2-5 epilogue (lane quarter = warp % 4).
+#include "fc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+namespace fc {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 32, kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 4;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 4;  // 32 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kBarOff = kStages * (kABytes + kBBytes);
+constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
+
+struct LinArgs {
+    const float* bias;
+    float2* partials;   // [n_blocks][M]
+    int M, N, K;
+    int m_blocks, n_blocks, k_blocks, num_tiles;
+    float scale, lo, hi;
+    int* status;
+    long long budget;
+};
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long budget)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > budget) break;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_lse_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const LinArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint64_t* full = bars;         // [4]
+    uint64_t* empty = bars + 4;    // [4]
+    uint64_t* tfull = bars + 8;    // [2]
+    uint64_t* tempty = bars + 10;  // [2]
+    uint64_t* mdone = bars + 12;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], 128);
+        }
+        mbar_init(mdone, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmx);
+        prefetch_tmap(&tmw);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
+                const int mb = t % a.m_blocks, nb = t / a.m_blocks;
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
+                    mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+                    tma_load_2d(sA + stage * kABytes, &tmx, &full[stage], kb * kBK, mb * kBM);
+                    tma_load_2d(sB + stage * kBBytes, &tmw, &full[stage], kb * kBK, nb * kBN);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // after an abort, wait for the most recent fill of each slot to land
+                const long long first = issued > kStages ? issued - kStages : 0;
+                for (long long i = first; i < issued; ++i)
+                    drain_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.budget);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(kFmtTF32, kBM, kBN);
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+                if (!(ok = mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!(ok = mbar_wait(&full[stage], phase, abort_flag, a.status, a.budget))) break;
+                    tc_fence_after();
+                    const uint32_t as = a0 + stage * kABytes, bs = b0 + stage * kBBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 8; ++k) {
+                        const uint64_t ad = smem_desc(as + k * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = smem_desc(bs + k * 32, 16, 1024, kLayoutSw128);
+                        mma_tf32(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(&tfull[acc]);
+            }
+            mma_commit(mdone);
+            drain_wait(mdone, 0, a.budget);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++it) {
+            const int mb = t % a.m_blocks, nb = t / a.m_blocks;
+            const int acc = it & 1;
+            const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+            const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+            float run_m = -INFINITY, run_s = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                float v[32];
+                tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
+                const int n0 = nb * kBN + c * 32;
+                float cm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = n0 + j;
+                    if (n < a.N) {
+                        float u = (v[j] + __ldg(a.bias + n)) * a.scale;
+                        u = u + u;
+                        v[j] = fminf(fmaxf(u, a.lo), a.hi);
+                    } else {
+                        v[j] = -INFINITY;
+                    }
+                    cm = fmaxf(cm, v[j]);
+                }
+                if (cm > -INFINITY) {
+                    const float nm = fmaxf(run_m, cm);
+                    float s = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s += __expf(v[j] - nm);
+                    run_s = run_s * __expf(run_m - nm) + s;
+                    run_m = nm;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            const int m = mb * kBM + row;
+            if (m < a.M) a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Merge the per-column-tile (max, sum) pairs of each row in fixed order, then
+// lse = M + log S and y = lse * mish(lse), mish(l) = l * tanh(softplus(l)).
+__global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks)
+{
+    const int m = blockIdx.x * blockDim.x + threadIdx.x;
+    if (m >= M) return;
+    float mx = -INFINITY;
+    for (int i = 0; i < n_blocks; ++i) mx = fmaxf(mx, partials[static_cast<size_t>(i) * M + m].x);
+    float s = 0.0f;
+    for (int i = 0; i < n_blocks; ++i) {
+        const float2 p = partials[static_cast<size_t>(i) * M + m];
+        s += p.y * expf(p.x - mx);
+    }
+    const float l = mx + logf(s);
+    const float sp = fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l)));
+    y[m] = l * (l * tanhf(sp));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Row-major [rows][cols] fp32 matrix, box = box_rows x 32 columns (128 B), 128-byte swizzle.
+bool make_kmajor_map(CUtensorMap* map, const float* base, int rows, int cols, int box_rows)
+{
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * sizeof(float)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
+{
+    *p = LinearPlan{};
+    if (K % 4 != 0) return 2;
+    p->M = M; p->K = K; p->Nout = Nout;
+    p->m_blocks = (M + kBM - 1) / kBM;
+    p->n_blocks = (Nout + kBN - 1) / kBN;
+    p->k_blocks = (K + kBK - 1) / kBK;
+    const long long tiles = static_cast<long long>(p->m_blocks) * p->n_blocks;
+    if (tiles > 0x7FFFFFFFLL) return 2;
+    p->num_tiles = static_cast<int>(tiles);
+    p->grid = std::min(p->num_tiles, std::max(sm_count, 1));
+    p->smem_bytes = kSmemBytes;
+    p->ws_bytes = (static_cast<size_t>(p->n_blocks) * M * sizeof(float2) + 255) & ~static_cast<size_t>(255);
+    return 0;
+}
+
+cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, const float* b, float* y, float scale,
+                          float lo, float hi, void* workspace, cudaStream_t stream, int* status, long long budget)
+{
+    CUtensorMap tmx, tmw;
+    if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN))
+        return cudaErrorInvalidValue;
+    LinArgs a{};
+    a.bias = b;
+    a.partials = reinterpret_cast<float2*>(workspace);
+    a.M = p.M; a.N = p.Nout; a.K = p.K;
+    a.m_blocks = p.m_blocks; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
+    a.scale = scale; a.lo = lo; a.hi = hi;
+    a.status = status; a.budget = budget;
+    cudaError_t e = cudaFuncSetAttribute(linear_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(p.smem_bytes));
+    if (e != cudaSuccess) return e;
+    linear_lse_kernel<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace fc

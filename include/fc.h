@@ -1,0 +1,161 @@
+/*
+ * fc.h -- C ABI of the GB300 (sm_103a) fused contraction + activation +
+ * reduction library.
+ *
+ * Three fused operators, each a dense contraction on the 5th-generation
+ * tensor cores (tcgen05, accumulators in tensor memory) with its pointwise
+ * activation and its reduction done in the epilogue, so the contraction's
+ * full-size result never goes to HBM (it is written out only where the
+ * operator's output IS the full result, fc_conv3x3_act).
+ *
+ * The three source pages are reasoning traces, each titled by its problem:
+ *   "Kimi-K2.6 l2_p67": Conv2d(3x3) -> GELU -> adaptive_avg_pool2d(1) -> squeeze
+ *   "Kimi-K2.6 l2_p4" : Conv2d(3x3) -> Mish -> Mish
+ *   "Kimi-K2.6 l2_p22": Linear -> x*scale -> x+x -> clamp -> logsumexp(dim 1) -> x*mish(x)
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is caller-owned DEVICE memory, contiguous, row-major
+ *     (C order), at least 16-byte aligned.  The library allocates nothing and
+ *     keeps no state between calls apart from per-device launch attributes.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream).  A
+ *     FC_OK return means the work was enqueued; the outputs are fully
+ *     overwritten (never accumulated into).
+ *   - Argument errors (null pointer, misalignment, non-positive or too-small
+ *     sizes, clamp_lo > clamp_hi, workspace too small, unknown enum) return an
+ *     error BEFORE anything is enqueued.  Shapes the kernels do not cover
+ *     return FC_ERR_UNSUPPORTED; there is no CPU or library fallback.
+ *   - `workspace` is caller-owned device scratch of at least
+ *     fc_workspace_bytes(...) bytes (256-byte aligned); its contents on entry
+ *     do not matter.  Two calls that share a workspace must not overlap.
+ *   - Floating point: fp32 inputs run on TF32 tensor cores (operands rounded
+ *     to nearest TF32), bf16 inputs on BF16 tensor cores; accumulation,
+ *     activation and reduction are fp32; outputs are fp32.
+ */
+#ifndef FC_H_
+#define FC_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fc_stream_t;
+
+typedef enum {
+    FC_OK = 0,
+    FC_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or enum value */
+    FC_ERR_UNSUPPORTED = 2,   /* valid request outside the shapes the kernels cover */
+    FC_ERR_WORKSPACE = 3,     /* workspace missing or smaller than fc_workspace_bytes() */
+    FC_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
+    FC_ERR_TIMEOUT = 5        /* a kernel's bounded wait ran out (see fc_device_status) */
+} fc_status;
+
+typedef enum { FC_F32 = 0, FC_BF16 = 1 } fc_dtype;
+
+typedef enum {
+    FC_ACT_GELU_ERF = 0,      /* 0.5 v (1 + erf(v / sqrt 2)), torch's exact GELU */
+    FC_ACT_MISH = 1,          /* v tanh(softplus(v)) */
+    FC_ACT_MISH_MISH = 2      /* mish(mish(v)) */
+} fc_act;
+
+typedef enum {
+    FC_OP_CONV3X3_ACT_POOL = 0,
+    FC_OP_CONV3X3_ACT = 1,
+    FC_OP_LINEAR_LSE_MISH = 2
+} fc_op;
+
+/*
+ * y[n, co] = mean_{oh < H-2, ow < W-2} act( b[co] + sum_{ci, kh<3, kw<3}
+ *                                   x[n, ci, oh+kh, ow+kw] * w[co, ci, kh, kw] )
+ *
+ * Page "Kimi-K2.6 l2_p67", problem statement: Conv2d(Cin -> Cout, kernel 3,
+ * stride 1, padding 0, bias) then GELU then adaptive_avg_pool2d(1) then
+ * squeeze, i.e. the mean of the activated conv output over its whole
+ * (H-2) x (W-2) plane; the trace fixes GELU to the exact erf form.
+ *
+ *   x   [N, Cin, H, W]     fp32 or bf16 (dtype), NCHW
+ *   w   [Cout, Cin, 3, 3]  same dtype, OIHW
+ *   b   [Cout]             same dtype
+ *   y   [N, Cout]          fp32 output
+ *   Requires N, Cin >= 1; H, W >= 3; 32 <= Cout <= 256 with Cout % 32 == 0
+ *   (else FC_ERR_UNSUPPORTED).  The mean is a fixed-order two-stage sum:
+ *   results are bit-identical run to run on the same GPU model.
+ */
+fc_status fc_conv3x3_act_pool(const void* x, const void* w, const void* b, float* y,
+                              int N, int Cin, int H, int W, int Cout,
+                              fc_dtype dtype, fc_act act,
+                              void* workspace, size_t workspace_bytes, fc_stream_t stream);
+
+/*
+ * y[n, co, oh, ow] = act( b[co] + sum_{ci, kh, kw} x[n, ci, oh+kh, ow+kw] * w[co, ci, kh, kw] )
+ *
+ * Page "Kimi-K2.6 l2_p4", problem statement: Conv2d(Cin -> Cout, kernel 3,
+ * stride 1, padding 0, bias) then Mish then Mish (act = FC_ACT_MISH_MISH);
+ * the full output is written.
+ *
+ *   x, w, b as for fc_conv3x3_act_pool;  y [N, Cout, H-2, W-2] fp32, NCHW.
+ *   Same shape limits as fc_conv3x3_act_pool.
+ */
+fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y,
+                         int N, int Cin, int H, int W, int Cout,
+                         fc_dtype dtype, fc_act act,
+                         void* workspace, size_t workspace_bytes, fc_stream_t stream);
+
+/*
+ * t[m, j] = clamp( u + u, clamp_lo, clamp_hi ),  u = (b[j] + sum_k x[m, k] W[j, k]) * scale
+ * l[m]    = log sum_j exp(t[m, j])
+ * y[m]    = l[m] * mish(l[m])
+ *
+ * Page "Kimi-K2.6 l2_p22", problem statement (the module's forward):
+ * nn.Linear(K -> Nout) then x * scale_factor then x + x then torch.clamp then
+ * torch.logsumexp(dim=1, keepdim=True) then x * mish(x).  The row logsumexp
+ * is taken as per-tile (max, sum of exp) pairs combined across column tiles.
+ *
+ *   x [M, K] fp32;  W [Nout, K] fp32 (nn.Linear weight layout);  b [Nout] fp32
+ *   y [M] fp32 (the (M, 1) output, contiguous)
+ *   Requires M, Nout >= 1, K >= 4 with K % 4 == 0 (16-byte row pitch),
+ *   clamp_lo <= clamp_hi, dtype == FC_F32 (bf16 returns FC_ERR_UNSUPPORTED).
+ */
+fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y,
+                             int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,
+                             fc_dtype dtype,
+                             void* workspace, size_t workspace_bytes, fc_stream_t stream);
+
+/*
+ * Workspace bytes the given call needs on the CURRENT device (0 is possible).
+ * Argument order follows the call: (N, Cin, H, W, Cout) for the conv ops,
+ * (M, K, -, -, Nout) for the linear op.  Returns 0 for invalid arguments.
+ */
+size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int cout_or_nout,
+                          fc_dtype dtype);
+
+/* Static English text for a status code. */
+const char* fc_status_string(fc_status status);
+
+/*
+ * Watchdog word of the current device.  Every spin-wait in the kernels is
+ * bounded; on expiry a kernel records FC_ERR_TIMEOUT here, stops its loops,
+ * drains its own copies and returns (the context stays usable).  This call
+ * synchronizes the device, returns the recorded status (FC_OK if none) and,
+ * when clear != 0, resets it.
+ */
+fc_status fc_device_status(int clear);
+
+/*
+ * Self-test of the watchdog path: enqueues one tiny kernel that waits on an
+ * mbarrier nothing will ever arrive on, with a budget of `budget_cycles`
+ * SM clock cycles.  The wait must give up, record FC_ERR_TIMEOUT and return.
+ * Read the result with fc_device_status().  Faults and hangs nothing.
+ */
+fc_status fc_selftest_watchdog(unsigned long long budget_cycles, fc_stream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FC_H_ */

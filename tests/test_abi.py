@@ -1,0 +1,82 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the public
+header declares, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_activation_reduction_gb300 as fc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(fc_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_fused_ops():
+    names = declared_functions()
+    for n in ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_workspace_bytes"):
+        assert n in names
+    assert set(names) == set(fc.EXPORTS)
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    lib = fc.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # dynamic symbol table of the shared object, read with nm
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fc.library_path()], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+
+
+def test_status_strings_and_version():
+    assert fc.fc_status_string(fc.FC_OK) == "ok"
+    assert "timed out" in fc.fc_status_string(fc.FC_ERR_TIMEOUT)
+    assert fc.fc_version() >= 100
+
+
+def _call_pool(lib, x=16, w=16, b=16, y=16, N=1, Cin=8, H=8, W=8, Cout=64, dtype=0, act=0, ws=None, wsb=0):
+    return lib.fc_conv3x3_act_pool(x, w, b, y, N, Cin, H, W, Cout, dtype, act, ws, wsb, None)
+
+
+def test_host_validation_rejects_bad_arguments_before_any_launch():
+    lib = fc.load()
+    assert _call_pool(lib, x=None) == fc.FC_ERR_INVALID_ARG
+    assert _call_pool(lib, y=0) == fc.FC_ERR_INVALID_ARG
+    assert _call_pool(lib, x=0x1004) == fc.FC_ERR_INVALID_ARG           # not 16-byte aligned
+    assert _call_pool(lib, H=2) == fc.FC_ERR_INVALID_ARG
+    assert _call_pool(lib, N=0) == fc.FC_ERR_INVALID_ARG
+    assert _call_pool(lib, dtype=7) == fc.FC_ERR_INVALID_ARG
+    assert _call_pool(lib, act=9) == fc.FC_ERR_INVALID_ARG
+    assert lib.fc_conv3x3_act(16, 16, 16, 16, 1, 8, 2, 8, 64, 0, 2, None, 0, None) == fc.FC_ERR_INVALID_ARG
+    lin = lib.fc_linear_lse_mish
+    assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, 1.0, -1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG  # lo > hi
+    assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, float("nan"), 1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG
+    assert lin(16, 16, 16, 16, 0, 8, 8, 2.0, -1.0, 1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG
+    assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, -1.0, 1.0, 1, None, 0, None) == fc.FC_ERR_UNSUPPORTED  # bf16
+
+
+def test_without_a_device_calls_report_cuda_errors_not_crashes():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = fc.load()
+    assert _call_pool(lib) == fc.FC_ERR_CUDA
+    assert lib.fc_workspace_bytes(0, 1, 8, 8, 8, 64, 0) == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 8, 8, 8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fc.fc_conv3x3_act_pool(x, torch.zeros(64, 8, 3, 3), torch.zeros(64))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fc.fc_linear_lse_mish(torch.zeros(4, 8), torch.zeros(8, 8), torch.zeros(8))

@@ -1,0 +1,217 @@
+"""Parity of the CUDA path with the fp64 oracle, element by element, on the
+same seeded inputs (GPU only; every call goes through the C ABI).
+
+Tolerance (the one the fused-op contract states): |gpu - ref| <= tol * (1 + |ref|)
+with tol = 2e-3 for fp32 inputs on TF32 tensor cores and 2e-2 for bf16 inputs.
+Small and ragged shapes are checked in full; the five workloads at full size
+are checked in the launch configuration the benchmark times, on outputs the
+oracle computes one by one (random samples plus every border row/column of
+a few planes).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import fc_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 2e-3, "bf16": 2e-2}
+
+
+def _dev(arr):
+    import torch
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def _check(got, ref, tol, what):
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref) / (1.0 + np.abs(ref))
+    i = int(np.argmax(err))
+    assert err[i] <= tol, f"{what}: scaled error {err[i]:.3e} > {tol} at {i} (gpu {got[i]!r}, ref {ref[i]!r})"
+    return float(err[i])
+
+
+# ------------------------------------------------------------------ conv + pool
+
+POOL_SHAPES = [
+    # (N, Cin, H, W, Cout, dtype, act)
+    (2, 8, 32, 32, 64, "f32", "gelu"),       # the tiny workload, exhaustively
+    (1, 1, 3, 3, 32, "f32", "gelu"),         # degenerate: a 1x1 output plane
+    (3, 3, 19, 13, 32, "f32", "gelu"),       # ragged rows and columns, Cin < one K block
+    (2, 13, 20, 37, 96, "f32", "gelu"),      # Cin not a multiple of 8, Cout = 96
+    (1, 8, 40, 17, 256, "f32", "gelu"),      # Cout = 256, resident weights
+    (1, 64, 21, 18, 128, "f32", "gelu"),     # streamed weights
+    (2, 8, 23, 29, 64, "f32", "mish"),
+    (2, 16, 18, 20, 64, "bf16", "gelu"),
+    (1, 128, 12, 12, 256, "bf16", "gelu"),   # streamed bf16 weights
+    (1, 24, 35, 9, 32, "bf16", "gelu"),      # Cin not a multiple of 16
+]
+
+
+@pytest.mark.parametrize("shape", POOL_SHAPES, ids=lambda s: "x".join(map(str, s[:5])) + f"-{s[5]}-{s[6]}")
+def test_conv_pool_small(cuda_lib, shape):
+    N, Cin, H, W, Cout, dt, act = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, dt)
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act).cpu().numpy()
+    ref = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], act)
+    _check(y, ref, TOL[dt], f"pool {shape}")
+
+
+ACT_SHAPES = [
+    (1, 3, 11, 13, 32, "f32", "mish_mish"),
+    (2, 64, 20, 19, 128, "f32", "mish_mish"),
+    (1, 8, 34, 34, 64, "f32", "mish_mish"),
+    (1, 5, 17, 21, 96, "f32", "gelu"),
+    (1, 32, 14, 12, 64, "bf16", "mish_mish"),
+    (2, 16, 19, 10, 256, "bf16", "mish"),
+]
+
+
+@pytest.mark.parametrize("shape", ACT_SHAPES, ids=lambda s: "x".join(map(str, s[:5])) + f"-{s[5]}-{s[6]}")
+def test_conv_act_small(cuda_lib, shape):
+    N, Cin, H, W, Cout, dt, act = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, dt)
+    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act).cpu().numpy()
+    ref = oracle.conv3x3_act(d["x32"], d["w32"], d["b32"], act)
+    _check(y, ref, TOL[dt], f"act {shape}")
+
+
+# ------------------------------------------------------------------ linear chain
+
+LIN_SHAPES = [
+    # (M, K, Nout, x scale)
+    (1, 4, 1, 1.0),
+    (3, 36, 17, 1.0),
+    (130, 520, 300, 1.0),     # ragged in M, K and Nout
+    (129, 64, 513, 30.0),     # clamp active on most entries
+    (256, 1024, 2048, 1.0),
+]
+
+
+@pytest.mark.parametrize("shape", LIN_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_linear_small(cuda_lib, shape):
+    M, K, Nout, sx = shape
+    d = fc_inputs.linear_inputs(M, K, Nout)
+    x = (d["x"] * np.float32(sx)).astype(np.float32)
+    y = cuda_lib.fc_linear_lse_mish(_dev(x), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
+    ref = oracle.linear_lse_mish(x, d["W"], d["b"])
+    _check(y, ref, TOL["f32"], f"linear {shape}")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def test_workload_B_full_size_sampled(cuda_lib):
+    wl = fc_inputs.WORKLOADS["B"]
+    d = fc_inputs.workload_inputs("B")
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="gelu").cpu().numpy()
+    rng = np.random.default_rng(7)
+    flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 192, replace=False),
+                                     np.arange(wl.Cout), np.arange((wl.N - 1) * wl.Cout, wl.N * wl.Cout)]))
+    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, "gelu")
+    _check(y.reshape(-1)[flat], ref, TOL["f32"], "workload B")
+
+
+def test_workload_C_full_size_sampled(cuda_lib):
+    import torch
+    wl = fc_inputs.WORKLOADS["C"]
+    d = fc_inputs.workload_inputs("C")
+    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="mish_mish")
+    OH, OW = wl.OH, wl.OW
+    rng = np.random.default_rng(8)
+    total = wl.N * wl.Cout * OH * OW
+    samples = [rng.choice(total, 1 << 17, replace=False)]
+    for (n, co) in [(0, 0), (wl.N - 1, wl.Cout - 1), (17, 77)]:
+        base = (n * wl.Cout + co) * OH * OW
+        rows = np.concatenate([np.arange(OW), (OH - 1) * OW + np.arange(OW)])
+        cols = np.concatenate([np.arange(OH) * OW, np.arange(OH) * OW + OW - 1])
+        samples.append(base + np.concatenate([rows, cols]))
+    flat = np.unique(np.concatenate(samples))
+    got = y.view(-1)[torch.from_numpy(flat).cuda()].cpu().numpy()
+    del y
+    ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, "mish_mish")
+    _check(got, ref, TOL["f32"], "workload C")
+
+
+def test_workload_D_full_size_sampled(cuda_lib):
+    wl = fc_inputs.WORKLOADS["D"]
+    d = fc_inputs.workload_inputs("D")
+    y = cuda_lib.fc_linear_lse_mish(_dev(d["x"]), _dev(d["W"]), _dev(d["b"]), wl.scale, wl.clamp_lo,
+                                    wl.clamp_hi).cpu().numpy().reshape(-1)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(wl.M - 8, wl.M),
+                                     np.random.default_rng(9).choice(wl.M, 112, replace=False)]))
+    ref = oracle.linear_lse_mish(d["x"], d["W"], d["b"], wl.scale, wl.clamp_lo, wl.clamp_hi, rows=rows)
+    _check(y[rows], ref, TOL["f32"], "workload D")
+    # clamped logsumexp bound: l in [lo + ln n, hi + ln n] -> y = l mish(l) within the image of that range
+    lo_l, hi_l = wl.clamp_lo + math.log(wl.Nout), wl.clamp_hi + math.log(wl.Nout)
+    f = lambda l: l * oracle.mish(l)
+    assert np.all(y >= min(f(lo_l), 0.0) - 1e-3) and np.all(y <= f(hi_l) + 1e-2)
+
+
+def test_workload_E_full_size_sampled(cuda_lib):
+    wl = fc_inputs.WORKLOADS["E"]
+    d = fc_inputs.workload_inputs("E")
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="gelu").cpu().numpy()
+    rng = np.random.default_rng(10)
+    flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 96, replace=False), np.arange(wl.Cout)]))
+    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, "gelu")
+    _check(y.reshape(-1)[flat], ref, TOL["bf16"], "workload E")
+
+
+# ------------------------------------------------------------------ properties, errors, watchdog
+
+def test_results_are_bit_identical_run_to_run(cuda_lib):
+    d = fc_inputs.conv_inputs(4, 8, 64, 64, 64)
+    x, w, b = _dev(d["x"]), _dev(d["w"]), _dev(d["b"])
+    y1 = cuda_lib.fc_conv3x3_act_pool(x, w, b).cpu().numpy()
+    y2 = cuda_lib.fc_conv3x3_act_pool(x, w, b).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    dl = fc_inputs.linear_inputs(200, 256, 700)
+    xl, Wl, bl = _dev(dl["x"]), _dev(dl["W"]), _dev(dl["b"])
+    z1 = cuda_lib.fc_linear_lse_mish(xl, Wl, bl).cpu().numpy()
+    z2 = cuda_lib.fc_linear_lse_mish(xl, Wl, bl).cpu().numpy()
+    assert np.array_equal(z1.view(np.uint32), z2.view(np.uint32))
+
+
+def test_zero_weights_give_activation_of_bias(cuda_lib):
+    import torch
+    d = fc_inputs.conv_inputs(2, 8, 30, 22, 64)
+    w0 = torch.zeros(64, 8, 3, 3, device="cuda")
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), w0, _dev(d["b"])).cpu().numpy()
+    ref = np.array([oracle.gelu(float(v)) for v in d["b"]])
+    _check(y, np.broadcast_to(ref, y.shape), TOL["f32"], "w = 0")
+
+
+def test_workspace_too_small_is_rejected(cuda_lib):
+    import torch
+    d = fc_inputs.conv_inputs(1, 8, 16, 16, 64)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cuda_lib.FCError) as e:
+        cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), workspace=small)
+    assert e.value.status in (cuda_lib.FC_ERR_WORKSPACE,)
+
+
+def test_unsupported_cout_is_reported(cuda_lib):
+    d = fc_inputs.conv_inputs(1, 8, 16, 16, 48)
+    with pytest.raises(cuda_lib.FCError) as e:
+        cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]))
+    assert e.value.status == cuda_lib.FC_ERR_UNSUPPORTED
+
+
+def test_watchdog_times_out_and_context_stays_usable(cuda_lib):
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+    cuda_lib.fc_selftest_watchdog(2_000_000)   # ~1 ms: nothing ever arrives on the barrier
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_ERR_TIMEOUT
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+    d = fc_inputs.conv_inputs(2, 8, 32, 32, 64)
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"])).cpu().numpy()
+    ref = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu")
+    _check(y, ref, TOL["f32"], "after watchdog")
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
