@@ -1,0 +1,420 @@
+"""Benchmark of the fused contraction + activation + reduction library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload B] [--impl reference]
+
+A "step" is one call of the fused operator on one batch of the workload
+(default: conv3x3 + erf-GELU + global average pool, x (128, 8, 256, 256) fp32,
+Cout 64 -- the Conv2d->GELU->pool page's full problem), inputs resident in
+HBM.  Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own
+shard of images on its own GPU (no collective on the data path); the timed
+region is bracketed by a barrier + synchronize and the max over ranks is used.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import fc_inputs  # noqa: E402
+
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
+METRIC = "fused-op TFLOP/s, ms/call and % of roofline (conv3x3+act(+pool), GEMM+LSE)"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def tensor_peak(wl, pk):
+    bf16 = pk["bf16_tflops"]
+    if getattr(wl, "dtype", "f32") == "bf16":
+        return bf16, f"bf16 burst ({pk['source']})"
+    return bf16 * TF32_OVER_BF16, f"tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ profile summary (ncu traffic)
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_activation_reduction_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_key):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when that summary was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload_key}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_sources_hash():
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _dev(torch, a, device):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def make_call(fc, torch, key, d, device):
+    wl = fc_inputs.WORKLOADS[key]
+    if isinstance(wl, fc_inputs.LinearWorkload):
+        x, W, b = (_dev(torch, d[k], device) for k in ("x", "W", "b"))
+        out = torch.empty((wl.M, 1), dtype=torch.float32, device=device)
+        ws = torch.empty(fc.fc_workspace_bytes("linear_lse_mish", wl.M, wl.K, 1, 1, wl.Nout), dtype=torch.uint8,
+                         device=device)
+
+        def call():
+            fc.fc_linear_lse_mish(x, W, b, wl.scale, wl.clamp_lo, wl.clamp_hi, out=out, workspace=ws)
+        return call, 2, out
+    x, w, b = (_dev(torch, d[k], device) for k in ("x", "w", "b"))
+    dt = fc.FC_BF16 if wl.dtype == "bf16" else fc.FC_F32
+    op = "conv3x3_act_pool" if wl.pool else "conv3x3_act"
+    shape = (wl.N, wl.Cout) if wl.pool else (wl.N, wl.Cout, wl.OH, wl.OW)
+    out = torch.empty(shape, dtype=torch.float32, device=device)
+    ws = torch.empty(max(1, fc.fc_workspace_bytes(op, wl.N, wl.Cin, wl.H, wl.W, wl.Cout, dt)), dtype=torch.uint8,
+                     device=device)
+    f = fc.fc_conv3x3_act_pool if wl.pool else fc.fc_conv3x3_act
+
+    def call():
+        f(x, w, b, act=wl.act, out=out, workspace=ws)
+    return call, (3 if wl.pool else 2), out
+
+
+def time_device(torch, call, steps, warmup, dist=None):
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        call()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    total = evs[0].elapsed_time(evs[-1])
+    if dist is not None:
+        t = torch.tensor([total], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+        dist.barrier()
+    torch.cuda.synchronize()
+    return total, per
+
+
+def time_e2e(fc, torch, key, d, device, steps, warmup):
+    """Same operator through the public API with pinned-host inputs: H2D of the
+    inputs, the call, and D2H of the result inside the timed region."""
+    wl = fc_inputs.WORKLOADS[key]
+    names = ("x", "W", "b") if isinstance(wl, fc_inputs.LinearWorkload) else ("x", "w", "b")
+    host = []
+    for k in names:
+        a = d[k]
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a))
+        host.append(t.pin_memory())
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    bf16 = getattr(wl, "dtype", "f32") == "bf16"
+
+    def step():
+        dev = [t.to(device, non_blocking=True) for t in host]
+        if bf16:
+            dev = [t.view(torch.bfloat16) for t in dev]
+        if isinstance(wl, fc_inputs.LinearWorkload):
+            y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi)
+        elif wl.pool:
+            y = fc.fc_conv3x3_act_pool(*dev, act=wl.act)
+        else:
+            y = fc.fc_conv3x3_act(*dev, act=wl.act)
+        return y.to("cpu", non_blocking=False)
+
+    for _ in range(warmup):
+        y = step()
+    d2h = y.numel() * y.element_size()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) * 1e3 / steps, h2d, d2h
+
+
+def oracle_sample(key, budget_s=12.0):
+    """The oracle on a bounded sample of the workload: returns (flops done, seconds, sample text, threads)."""
+    import oracle
+    wl = fc_inputs.WORKLOADS[key]
+    d = fc_inputs.workload_inputs(key)
+    threads = oracle.threads()
+    if isinstance(wl, fc_inputs.LinearWorkload):
+        unit_flops = 2.0 * wl.K * wl.Nout        # one row
+        run = lambda idx: oracle.linear_lse_mish(d["x"], d["W"], d["b"], wl.scale, wl.clamp_lo, wl.clamp_hi,
+                                                 rows=idx)
+        total_units, what = wl.M, "rows"
+    elif wl.pool:
+        unit_flops = 2.0 * wl.OH * wl.OW * wl.Cin * 9   # one (n, co) pooled output
+        run = lambda idx: oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], idx, wl.act)
+        total_units, what = wl.N * wl.Cout, "(image, channel) pooled outputs"
+    else:
+        unit_flops = 2.0 * wl.Cin * 9                    # one output element
+        run = lambda idx: oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], idx, wl.act)
+        total_units, what = wl.N * wl.Cout * wl.OH * wl.OW, "output elements"
+    n = min(total_units, max(threads, 4))
+    t0 = time.perf_counter()
+    run(np.arange(n))
+    dt = time.perf_counter() - t0
+    n2 = int(min(total_units, max(n, n * budget_s / max(dt, 1e-6))))
+    n2 = max(threads, (n2 // threads) * threads) if n2 >= threads else n2
+    t0 = time.perf_counter()
+    run(np.arange(n2))
+    dt2 = time.perf_counter() - t0
+    return (unit_flops * n2, dt2, f"first {n2} of {total_units} {what} of workload {key}", threads, run, unit_flops,
+            total_units)
+
+
+def reference_arm(args):
+    """--impl reference: the fp64 oracle on the host cores, K timed steps of a bounded sample."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    key = args.workload
+    wl = fc_inputs.WORKLOADS[key]
+    oracle.build()
+    flops_cal, dt_cal, _, threads, run, unit_flops, total_units = oracle_sample(key, budget_s=0.5)
+    per_unit = dt_cal / (flops_cal / unit_flops)
+    # size each step so that warmup + steps fit in about two minutes
+    steps, warmup = args.steps or 5, max(args.warmup, 3)
+    per_step_s = max(0.05, min(10.0, 60.0 / (steps + warmup)))
+    n = min(total_units, max(1, int(per_step_s / max(per_unit, 1e-9))))
+    idx = np.arange(n)
+    for _ in range(warmup):
+        run(idx)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run(idx)
+    sec = (time.perf_counter() - t0) / steps
+    value = unit_flops * n / sec / 1e12
+    sample = f"first {n} units of workload {key} per step ({unit_flops:.3e} flop each)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "sample_per_step": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def gpu_arm(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import gemm_activation_reduction_gb300 as fc
+    fc.load()
+    key = args.workload
+    wl = fc_inputs.WORKLOADS[key]
+    # weak scaling: each rank owns its own shard (batch) of the workload, seeded by rank
+    seeds = (fc_inputs.SEED_X + 1000 * rank, fc_inputs.SEED_W, fc_inputs.SEED_B)
+    if isinstance(wl, fc_inputs.LinearWorkload):
+        d = fc_inputs.linear_inputs(wl.M, wl.K, wl.Nout, seeds=seeds)
+    else:
+        d = fc_inputs.conv_inputs(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.dtype, seeds=seeds)
+    call, launches_per_call, out = make_call(fc, torch, key, d, device)
+
+    warmup = max(3, args.warmup)
+    # auto-size the timed region to ~2 s of device time unless --steps is given
+    if args.steps:
+        steps = args.steps
+    else:
+        _, per = time_device(torch, call, 5, 2)
+        steps = int(min(5000, max(20, 2000.0 / max(statistics.median(per), 1e-3))))
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, per = time_device(torch, call, steps, warmup, dist)
+    clocks = sampler.stop()
+    status = fc.fc_device_status(clear=True)
+    if status != fc.FC_OK:
+        raise RuntimeError(f"device status after the timed region: {fc.fc_status_string(status)}")
+
+    ms = total_ms / steps
+    flops = wl.flops()
+    value = flops * world / (ms * 1e-3) / 1e12
+    pk = peaks()
+    peak, peak_note = tensor_peak(wl, pk)
+    kernel_ms = statistics.mean(per)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = time_e2e(fc, torch, key, d, device, steps=max(3, min(20, steps // 10)), warmup=2)
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return 0
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(key),
+                "peak_source": peak_note,
+                "duration_source": "CUDA events around each call on its stream (relayout + fused kernel"
+                                   + (" + combine" if launches_per_call == 3 else "") + ")"}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            fl, sec, sample, threads, _, _, _ = oracle_sample(key)
+            cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": sample, "seconds": sec}
+        except Exception as e:  # the line still prints; the failure is recorded
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+    cfg = {"workload": wl.name, "l2": "inputs larger than L2" if wl.compulsory_bytes() > 129e6 else
+           "inputs smaller than L2 (timed back to back)",
+           "compulsory_bytes": wl.compulsory_bytes(), "flops_per_step": flops,
+           "roofline_ms": max(flops / (peak * 1e12), wl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3,
+           "parallelism": f"shard-by-batch x{world}" if world > 1 else "single GPU"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if getattr(wl, "dtype", "f32") == "bf16" else "tf32",
+            "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(fan_in)) weights)", "config": cfg,
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": steps * launches_per_call, "clocks": clocks,
+            "pct_of_roofline": 100.0 * cfg["roofline_ms"] / ms}
+    if not args.no_others and world == 1:
+        others = {}
+        for k in args.others.split(","):
+            if not k or k == key:
+                continue
+            owl = fc_inputs.WORKLOADS[k]
+            od = fc_inputs.workload_inputs(k)
+            ocall, _, oout = make_call(fc, torch, k, od, device)
+            ot, oper = time_device(torch, ocall, 20, 3)
+            oms = ot / 20
+            opeak, _ = tensor_peak(owl, pk)
+            rl = max(owl.flops() / (opeak * 1e12), owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3
+            others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
+                         "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+            del od, ocall, oout
+            torch.cuda.empty_cache()
+        line["other_workloads"] = others
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: about 2 s of device time)")
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="B", choices=sorted(fc_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
+    ap.add_argument("--others", default="C,D,E", help="other workloads timed briefly into other_workloads")
+    ap.add_argument("--no-others", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

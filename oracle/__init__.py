@@ -79,6 +79,13 @@ def _p(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _indices(idx, limit, what):
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    if idx.size and (idx.min() < 0 or idx.max() >= limit):
+        raise IndexError(f"{what} index out of range [0, {limit})")
+    return idx
+
+
 def threads() -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
     return _load().oracle_threads()
@@ -128,7 +135,7 @@ def conv3x3_act_at(x, w, b, flat_idx, act="mish_mish"):
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
-    idx = np.ascontiguousarray(flat_idx, dtype=np.int64)
+    idx = _indices(flat_idx, N * Cout * (H - 2) * (W - 2), "output")
     out = np.empty(idx.size, dtype=np.float64)
     _load().oracle_conv3x3_act_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, ACT[act],
                                   _p(idx), idx.size, _p(out))
@@ -149,7 +156,7 @@ def conv3x3_act_pool_at(x, w, b, flat_nc, act="gelu"):
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
-    idx = np.ascontiguousarray(flat_nc, dtype=np.int64)
+    idx = _indices(flat_nc, N * Cout, "pooled output")
     out = np.empty(idx.size, dtype=np.float64)
     _load().oracle_conv3x3_act_pool_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, ACT[act],
                                        _p(idx), idx.size, _p(out))
@@ -165,7 +172,7 @@ def linear_lse_mish(x, Wt, b, scale=2.0, clamp_lo=-10.0, clamp_hi=10.0, rows=Non
     if rows is None:
         r, count = None, M
     else:
-        r = np.ascontiguousarray(rows, dtype=np.int64)
+        r = _indices(rows, M, "row")
         count = r.size
     y = np.empty(count, dtype=np.float64)
     lse = np.empty(count, dtype=np.float64)

@@ -236,3 +236,14 @@ def test_inputs_are_seeded_and_shaped():
     bound = 1 / math.sqrt(72)
     assert np.all(np.abs(a["w"]) <= bound) and np.all(np.abs(a["b"]) <= bound)
     assert abs(float(a["x"].mean())) < 0.05 and abs(float(a["x"].std()) - 1) < 0.05
+
+
+def test_sampled_entry_points_reject_out_of_range_indices():
+    d = fc_inputs.conv_inputs(1, 2, 5, 5, 3)
+    with pytest.raises(IndexError):
+        oracle.conv3x3_act_pool_at(d["x"], d["w"], d["b"], [3], "gelu")
+    with pytest.raises(IndexError):
+        oracle.conv3x3_act_at(d["x"], d["w"], d["b"], [-1], "gelu")
+    dl = fc_inputs.linear_inputs(2, 4, 3)
+    with pytest.raises(IndexError):
+        oracle.linear_lse_mish(dl["x"], dl["W"], dl["b"], rows=[2])
