@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "FCError", "load", "build", "library_path",
-    "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish",
+    "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
     "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
     "FC_F32", "FC_BF16", "ACTS", "OPS",
@@ -29,8 +29,8 @@ ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2}
 OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
 # Every symbol include/fc.h declares.
-EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_workspace_bytes",
-           "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
+EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
+           "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -218,3 +218,34 @@ def fc_device_status(clear: bool = True) -> int:
 def fc_selftest_watchdog(budget_cycles: int, stream=None) -> None:
     """Enqueue the watchdog self-test kernel (a wait that must time out)."""
     _raise(load().fc_selftest_watchdog(int(budget_cycles), _stream_handle(stream)), "fc_selftest_watchdog")
+
+
+def fc_linear_lse_mish_noalloc(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,
+                               out=None, stream=None):
+    """fc_linear_lse_mish for callers that cannot allocate device memory: the
+    library's own static 1 MiB device scratch replaces the workspace.  Only
+    `out` is allocated here when not given; pass `out` to allocate nothing.
+    Calls that overlap on the GPU share that scratch and race."""
+    torch = _torch()
+    lib = load()
+    fn = lib.fc_linear_lse_mish_noalloc
+    fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_float] * 3 + [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    _check(x, "x", (torch.float32,))
+    _check(W, "W", (torch.float32,), x.device)
+    _check(b, "b", (torch.float32,), x.device)
+    if x.dim() != 2 or W.dim() != 2 or W.shape[1] != x.shape[1] or b.shape != (W.shape[0],):
+        raise ValueError("expected x [M,K], W [Nout,K], b [Nout]")
+    M, K = (int(s) for s in x.shape)
+    Nout = int(W.shape[0])
+    if out is None:
+        out = torch.empty((M, 1), dtype=torch.float32, device=x.device)
+    else:
+        _check(out, "out", (torch.float32,), x.device)
+        if out.numel() != M:
+            raise ValueError(f"out must hold {M} values")
+    with torch.cuda.device(x.device):
+        st = fn(x.data_ptr(), W.data_ptr(), b.data_ptr(), out.data_ptr(), M, K, Nout, float(scale),
+                float(clamp_lo), float(clamp_hi), _stream_handle(stream))
+    _raise(st, "fc_linear_lse_mish_noalloc")
+    return out

@@ -86,6 +86,15 @@ cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int*
     watchdog_kernel<<<1, 32, 0, stream>>>(budget, status);
     return cudaGetLastError();
 }
+
+cudaError_t current_device_info(int* sm_count, int** status)
+{
+    DeviceState* d = nullptr;
+    if (device_state(&d) != FC_OK) return cudaErrorInvalidDevice;
+    *sm_count = d->sm_count;
+    *status = d->status;
+    return cudaSuccess;
+}
 }  // namespace fc
 
 extern "C" {

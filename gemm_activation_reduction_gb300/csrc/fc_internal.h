@@ -71,4 +71,7 @@ cudaError_t linear_launch(const LinearPlan& plan, const float* x, const float* W
 
 cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int* status);
 
+// SM count and device address of the watchdog word of the current device.
+cudaError_t current_device_info(int* sm_count, int** status);
+
 }  // namespace fc

@@ -1,0 +1,66 @@
+// fc_noalloc.cu -- fc_linear_lse_mish_noalloc: the Linear + logsumexp + x*mish(x)
+// operator for callers that cannot allocate device memory.
+//
+// fc_linear_lse_mish needs caller-provided scratch for its per-tile
+// (max, sum-exp) pairs.  Some callers have no way to provide it: code whose
+// device memory is owned by somebody else's allocator or a fixed budget,
+// plain C hosts with no allocator of their own, or loops where a cudaMalloc
+// (which can synchronize the whole device) is not acceptable.  This entry
+// point keeps that scratch in a file-scope device array instead, so a call
+// needs only its inputs and outputs and performs no allocation.
+#include "../../include/fc.h"
+#include "fc_internal.h"
+
+#include <mutex>
+
+namespace {
+
+// 1 MiB of scratch, resident on every device that loads the library until the
+// process exits: room for ceil(Nout / 256) * M (max, sum-exp) pairs of 8 bytes,
+// i.e. M * ceil(Nout / 256) <= 131072 (for example M = 1024 with Nout up to 32768).
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+struct ScratchAddress {
+    std::once_flag once;
+    void* ptr = nullptr;      // device address of g_noalloc_scratch on this device
+    cudaError_t err = cudaSuccess;
+};
+ScratchAddress g_scratch[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, const void* b, float* y, int M, int K,
+                                                int Nout, float scale, float clamp_lo, float clamp_hi,
+                                                fc_stream_t stream)
+{
+    if (!x || !W || !b || !y) return FC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || Nout < 1) return FC_ERR_INVALID_ARG;
+    if (!(clamp_lo <= clamp_hi)) return FC_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FC_ERR_CUDA;
+    // Host code cannot use g_noalloc_scratch's name as a device address: look the
+    // address up once per device, with that device current (it is: this call runs
+    // on the caller's current device).
+    ScratchAddress& s = g_scratch[dev];
+    std::call_once(s.once, [&s]() { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
+    if (s.err != cudaSuccess || s.ptr == nullptr) return FC_ERR_CUDA;
+    int sm_count = 0;
+    int* status = nullptr;
+    if (fc::current_device_info(&sm_count, &status) != cudaSuccess) return FC_ERR_CUDA;
+    fc::LinearPlan plan;
+    if (fc::linear_plan(&plan, M, K, Nout, sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    if (plan.ws_bytes > kNoAllocScratchBytes) return FC_ERR_UNSUPPORTED;
+    // Every (max, sum-exp) pair the combine kernel reads is written by the main
+    // kernel of the same call, so the array needs no clearing between calls.
+    cudaError_t e = fc::linear_launch(plan, static_cast<const float*>(x), static_cast<const float*>(W),
+                                      static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, s.ptr,
+                                      reinterpret_cast<cudaStream_t>(stream), status, fc::kWaitBudgetCycles);
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}

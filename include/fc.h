@@ -124,6 +124,28 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
                              void* workspace, size_t workspace_bytes, fc_stream_t stream);
 
 /*
+ * fc_linear_lse_mish without a workspace argument, for callers that cannot
+ * allocate device memory: code whose device memory belongs to another
+ * allocator or a fixed budget, C hosts with no allocator of their own, or
+ * loops where a cudaMalloc (which may synchronize the device) is not
+ * acceptable.  The pages have no counterpart to this entry point; it is an
+ * interface convenience, not part of the method.
+ *
+ * Same operator, arguments, limits and errors as fc_linear_lse_mish (fp32
+ * only).  Its scratch is a 1 MiB array in device memory that the library
+ * holds on every device that loads it, until the process exits; requests
+ * needing more (M * ceil(Nout / 256) > 131072) return FC_ERR_UNSUPPORTED.
+ * The call allocates nothing.  The first call on a device looks up that
+ * array's device address (a one-time set-up); make that first call before
+ * any stream capture.  All calls share the one array: calls that overlap on
+ * the GPU (other streams, or other host threads) race on it and give wrong
+ * results.  Nothing in it needs to start at zero.
+ */
+fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, const void* b, float* y,
+                                     int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,
+                                     fc_stream_t stream);
+
+/*
  * Workspace bytes the given call needs on the CURRENT device (0 is possible).
  * Argument order follows the call: (N, Cin, H, W, Cout) for the conv ops,
  * (M, K, -, -, Nout) for the linear op.  Returns 0 for invalid arguments.

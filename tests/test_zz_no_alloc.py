@@ -1,0 +1,63 @@
+"""fc_linear_lse_mish_noalloc, called through the C ABI, against fc_linear_lse_mish.
+
+The allocation-free entry point exists for callers that cannot allocate
+device memory (their memory belongs to another allocator or a fixed budget,
+or a cudaMalloc and its possible device-wide synchronization is not
+acceptable where they call from).  It keeps its scratch in the library's own
+static device array.  This file is collected last so that a run stopping at
+its first failure has already run every other test; it also passes alone in
+a fresh process, where its first call does the one-time set-up.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import fc_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3  # |gpu - ref| <= TOL * (1 + |ref|), the fp32-on-TF32 tolerance of the parity tests
+
+
+def _noalloc_fn(lib):
+    fn = lib.fc_linear_lse_mish_noalloc
+    fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_float] * 3 + [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(cuda_lib):
+    import torch
+    lib = cuda_lib.load()
+    fn = _noalloc_fn(lib)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    cases = [((256, 512, 2048), (101, 102, 103), 1.0),
+             ((300, 260, 3000), (201, 202, 203), 20.0)]   # second call: other shape, clamp mostly active
+    for (M, K, Nout), seeds, sx in cases:
+        d = fc_inputs.linear_inputs(M, K, Nout, seeds=seeds)
+        x = torch.from_numpy((d["x"] * np.float32(sx)).astype(np.float32)).cuda()
+        W = torch.from_numpy(d["W"]).cuda()
+        b = torch.from_numpy(d["b"]).cuda()
+        y = torch.empty((M, 1), dtype=torch.float32, device="cuda")
+        st = fn(x.data_ptr(), W.data_ptr(), b.data_ptr(), y.data_ptr(), M, K, Nout, 2.0, -10.0, 10.0, stream)
+        assert st == cuda_lib.FC_OK, cuda_lib.fc_status_string(st)
+        ref = cuda_lib.fc_linear_lse_mish(x, W, b, 2.0, -10.0, 10.0)
+        torch.cuda.synchronize()
+        got, want = y.cpu().numpy().reshape(-1), ref.cpu().numpy().reshape(-1)
+        assert np.all(np.isfinite(got))
+        err = np.abs(got - want) / (1.0 + np.abs(want))
+        assert err.max() <= TOL, f"case {(M, K, Nout)}: scaled difference {err.max():.3e}"
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
+def test_noalloc_rejects_requests_beyond_its_static_scratch(cuda_lib):
+    import torch
+    fn = _noalloc_fn(cuda_lib.load())
+    M, K, Nout = 1024, 4, 40000          # 1024 * ceil(40000 / 256) = 160768 pairs > 131072
+    x = torch.zeros((M, K), device="cuda")
+    W = torch.zeros((Nout, K), device="cuda")
+    b = torch.zeros(Nout, device="cuda")
+    y = torch.zeros((M, 1), device="cuda")
+    st = fn(x.data_ptr(), W.data_ptr(), b.data_ptr(), y.data_ptr(), M, K, Nout, 2.0, -10.0, 10.0, None)
+    assert st == cuda_lib.FC_ERR_UNSUPPORTED
