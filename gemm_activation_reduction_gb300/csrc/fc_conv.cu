@@ -11,14 +11,41 @@ using namespace convk;
 namespace {
 
 // Re-lay w [Cout][Cin][3][3] into [K block][tap][half][co][G] (G = 4 fp32 rounded
-// to TF32, or 8 bf16), zero-padding channels past Cin.
+// to TF32, or 8 bf16), zero-padding channels past Cin; then append the B
+// operand of the bias K step, [half][co][G]: half 0 holds, per channel, the
+// bias (fp32: its TF32 high part in k 0 and the TF32 remainder in k 2; bf16:
+// the bias in k 0) and the padding value in k 1; half 1 is zero.
 template <bool BF16>
-__global__ void conv_weight_relayout_kernel(const void* w, void* wr, int Cin, int Cout, int ncb)
+__global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Cout, int ncb)
 {
     constexpr int G = BF16 ? 8 : 4;
-    const long long total = static_cast<long long>(ncb) * 9 * 2 * Cout * G;
+    const long long wtotal = static_cast<long long>(ncb) * 9 * 2 * Cout * G;
+    const long long total = wtotal + 2LL * Cout * G;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        if (i >= wtotal) {
+            const long long f = i - wtotal;
+            const int e = static_cast<int>(f % G);
+            const int co = static_cast<int>((f / G) % Cout);
+            const int half = static_cast<int>(f / (static_cast<long long>(G) * Cout));
+            if constexpr (BF16) {
+                const unsigned short bv = reinterpret_cast<const unsigned short*>(b)[co];
+                const unsigned short pad = static_cast<unsigned short>(__float_as_uint(kPadValue) >> 16);
+                unsigned short v = 0;
+                if (half == 0 && e == 0) v = bv;
+                if (half == 0 && e == 1) v = pad;
+                reinterpret_cast<unsigned short*>(wr)[i] = v;
+            } else {
+                const float bv = reinterpret_cast<const float*>(b)[co];
+                const float hi = to_tf32(bv);
+                float v = 0.0f;
+                if (half == 0 && e == 0) v = hi;
+                if (half == 0 && e == 1) v = kPadValue;
+                if (half == 0 && e == 2) v = to_tf32(bv - hi);
+                reinterpret_cast<float*>(wr)[i] = v;
+            }
+            continue;
+        }
         long long f = i;
         const int e = static_cast<int>(f % G);
         f /= G;
@@ -88,6 +115,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     const unsigned long long wtot = static_cast<unsigned long long>(p->w_block_bytes) * p->ncb;
     if (wtot > 0xFFFFFFFFull) return 2;
     p->w_total_bytes = static_cast<uint32_t>(wtot);
+    p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout) * 16u;
     p->resident = p->w_total_bytes <= kResidentMax;
     if (p->resident) {
         p->stages = 4;
@@ -100,12 +128,14 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;
     p->strip_off = 0;
-    p->w_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
-    p->bar_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
+    p->ind_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
+    p->w_off = p->ind_off + kIndBytes;
+    p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
+    p->bar_off = p->bb_off + p->bias_block_bytes;
     p->bar_off = (p->bar_off + 127u) & ~127u;
     // barriers (19 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
     p->smem_bytes = p->bar_off + 256u + 1024u;
-    p->ws_weights_bytes = align256(p->w_total_bytes);
+    p->ws_weights_bytes = align256(static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes);
     p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
     return 0;
 }
@@ -118,23 +148,23 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     float* pool_ws = reinterpret_cast<float*>(ws + p.ws_weights_bytes);
 
     {
-        const long long total = static_cast<long long>(p.ncb) * 9 * 2 * p.Cout * (p.bf16 ? 8 : 4);
+        const long long total = (static_cast<long long>(p.ncb) * 9 + 1) * 2 * p.Cout * (p.bf16 ? 8 : 4);
         const int threads = 256;
         const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, 4096));
-        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, wr, p.Cin, p.Cout, p.ncb);
-        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, wr, p.Cin, p.Cout, p.ncb);
+        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb);
+        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
 
     ConvArgs a{};
-    a.x = x; a.wr = wr; a.bias = b;
+    a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
     a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.OH = p.OH; a.OW = p.OW;
-    a.ncb = p.ncb; a.CS = p.CS; a.tpi = p.tpi; a.base = p.base; a.rem = p.rem; a.J = p.J;
+    a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.base = p.base; a.rem = p.rem; a.J = p.J;
     a.stages = p.stages; a.resident = p.resident; a.nacc = p.nacc; a.tmem_cols = p.tmem_cols;
-    a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes;
-    a.strip_off = p.strip_off; a.w_off = p.w_off; a.bar_off = p.bar_off;
+    a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
+    a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.bar_off = p.bar_off;
     a.status = status; a.budget = budget;
 
     cudaError_t e = p.bf16 ? launch_main_bf16(a, p.pool, act, p.grid, p.smem_bytes, stream)

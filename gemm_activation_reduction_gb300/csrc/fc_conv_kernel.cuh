@@ -24,10 +24,20 @@
 // async copies (resident in shared memory when they fit, else streamed per K
 // block).
 //
+// Bias and the ragged-edge mask ride on the tensor core too: every tile starts
+// with one extra K step whose A operand is a per-tile "indicator" tile (column
+// 0 and 2: 1 for an output pixel inside the image; column 1: 1 for a pixel of
+// the tile past the image edge) and whose B operand holds, per output channel,
+// the bias split into two TF32 halves (columns 0 and 2) and -1e4 (column 1).
+// The accumulator therefore starts at bias for real pixels and near -1e4 for
+// padding pixels, whose GELU / Mish is exactly -0: the epilogue needs no bias
+// loads and no masking.
+//
 // Warp roles (416 threads, one CTA per SM, persistent over a contiguous tile range):
 //   warps 0-7  epilogue: tcgen05.ld of the accumulator (lane quarter = warp % 4,
-//              column half = warp / 4), bias + activation, then either a
-//              warp-transpose sum over the 32 pixels (pool) or coalesced stores.
+//              column half = warp / 4), activation, then either a running
+//              per-thread sum (pool; reduced across the warp's 32 pixels only
+//              when the image changes) or coalesced stores.
 //   warps 8-11 producers: one shared-memory stage slot each.
 //   warp 12    tensor-memory allocator and single-thread MMA issuer.
 #pragma once
@@ -50,28 +60,69 @@ constexpr int kStripPos = kStripRows * kStripCols;       // 180 staged pixels
 constexpr int kStripIters = (kStripPos + 31) / 32;       // 6 per lane
 constexpr uint32_t kStripPlane = kStripPos * 16;         // one channel group: 2880 B
 constexpr uint32_t kStripBytes = 2 * kStripPlane;        // one K block: 5760 B
+constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
+constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
 constexpr uint32_t kResidentMax = 96 * 1024;
 constexpr uint32_t kSmemBudget = 200 * 1024;
+constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 
 struct ConvArgs {
     const void* x;
-    const void* wr;      // re-laid weights (workspace)
-    const void* bias;
+    const void* wr;      // re-laid weights, then the bias block (workspace)
     float* out;          // full output (store) or pool partials (pool)
     int N, Cin, H, W, Cout, OH, OW;
-    int ncb, CS;
+    int ncb, RB, CS;
     long long tpi, base;
     int rem, J, stages, resident, nacc, tmem_cols;
-    uint32_t w_block_bytes, w_total_bytes, strip_off, w_off, bar_off;
+    uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;
+    uint32_t strip_off, ind_off, w_off, bb_off, bar_off;
     int* status;
     long long budget;
 };
 
-__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-__device__ __forceinline__ float softplus_stable(float z) { return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z))); }
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-__device__ __forceinline__ float mish(float z) { return z * tanhf(softplus_stable(z)); }
+// Exact (erf) GELU, 0.5 z (1 + erf(z / sqrt 2)), with erf from Hastings' rational
+// approximation as printed in Abramowitz & Stegun, Handbook of Mathematical
+// Functions, eq. 7.1.26: for u >= 0, erf(u) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^{-u^2},
+// t = 1 / (1 + p u), |error| <= 1.5e-7.  Here u = |z| / sqrt 2, so p u = (p / sqrt 2) |z|
+// and e^{-u^2} = 2^{-(log2 e / 2) z^2}; erf is odd.  One reciprocal and one
+// exponential (the SFU), eleven FP32 operations.
+__device__ __forceinline__ float gelu_erf(float z)
+{
+    const float a = fabsf(z);
+    const float t = rcp_approx(fmaf(0.3275911f * 0.70710678118654752f, a, 1.0f));
+    float q = fmaf(1.061405429f, t, -1.453152027f);
+    q = fmaf(q, t, 1.421413741f);
+    q = fmaf(q, t, -0.284496736f);
+    q = fmaf(q, t, 0.254829592f);
+    const float e = ex2_approx((a * -0.72134752044448170f) * a);
+    const float erf_abs = fmaf(-(q * t), e, 1.0f);
+    const float h = 0.5f * z;
+    return fmaf(h, copysignf(erf_abs, z), h);
+}
+
+// Mish(z) = z tanh(softplus(z)), with tanh(log(1 + e^z)) = n / (n + 2), n = e^z (e^z + 2).
+// Beyond z = 15 the factor is 1 in fp32 (and n would overflow near z = 44).
+__device__ __forceinline__ float mish(float z)
+{
+    const float e = ex2_approx(z * 1.4426950408889634f);
+    const float n = (e + 2.0f) * e;
+    const float m = z * n * rcp_approx(n + 2.0f);
+    return z > 15.0f ? z : m;
+}
 
 // Activation codes follow fc_act: 0 erf-GELU, 1 Mish, 2 Mish twice.
 template <int ACT>
@@ -80,17 +131,6 @@ __device__ __forceinline__ float apply_act(float z)
     if constexpr (ACT == 0) return gelu_erf(z);
     else if constexpr (ACT == 1) return mish(z);
     else return mish(mish(z));
-}
-
-template <bool BF16>
-__device__ __forceinline__ float load_bias(const void* b, int co)
-{
-    if constexpr (BF16) {
-        const unsigned short u = __ldg(reinterpret_cast<const unsigned short*>(b) + co);
-        return __uint_as_float(static_cast<uint32_t>(u) << 16);
-    } else {
-        return __ldg(reinterpret_cast<const float*>(b) + co);
-    }
 }
 
 // After the call lane L holds sum over the warp's 32 lanes of v[L] (v is clobbered).
@@ -111,7 +151,7 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane)
 
 // Tile t of the flattened (image, row block, column strip) grid.
 struct TileCoord {
-    int n, oh0, ow0;
+    int n, rb, cs;
 };
 
 __device__ __forceinline__ TileCoord tile_coord(long long t, long long tpi, int CS)
@@ -119,9 +159,8 @@ __device__ __forceinline__ TileCoord tile_coord(long long t, long long tpi, int 
     TileCoord c;
     c.n = static_cast<int>(t / tpi);
     const int r = static_cast<int>(t - static_cast<long long>(c.n) * tpi);
-    const int rb = r / CS;
-    c.oh0 = rb * kPatchRows;
-    c.ow0 = (r - rb * CS) * kPatchCols;
+    c.rb = r / CS;
+    c.cs = r - c.rb * CS;
     return c;
 }
 
@@ -196,6 +235,35 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
     }
 }
 
+// Indicator planes for the bias K step: variant v (bit 1: last row block,
+// bit 0: last column strip) marks which of the 128 tile pixels lie inside the
+// output; plane 4 is zero (the second K core matrix).
+template <bool BF16>
+__device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
+                                                       int nthreads)
+{
+    const int rows_last = OH - (RB - 1) * kPatchRows;   // valid rows in the last row block
+    const int cols_last = OW - (CS - 1) * kPatchCols;   // valid columns in the last column strip
+    for (int i = tid; i < 5 * 128; i += nthreads) {
+        const int v = i >> 7, r = i & 127;
+        const int pr = r >> 3, pc = r & 7;
+        const bool in = v < 4 && (!(v & 2) || pr < rows_last) && (!(v & 1) || pc < cols_last);
+        const bool pad = v < 4 && !in;
+        uint32_t w0, w1, w2;
+        if constexpr (BF16) {
+            w0 = (in ? 0x3F80u : 0u) | ((pad ? 0x3F80u : 0u) << 16);   // bf16 1.0 in k 0 / k 1
+            w1 = 0u;
+            w2 = 0u;
+        } else {
+            w0 = in ? 0x3F800000u : 0u;      // k 0: bias high half
+            w1 = pad ? 0x3F800000u : 0u;     // k 1: padding value
+            w2 = in ? 0x3F800000u : 0u;      // k 2: bias low half
+        }
+        st_shared_v4(smem_u32(ind) + static_cast<uint32_t>(v) * kIndPlane + static_cast<uint32_t>(r) * 16u, w0, w1,
+                     w2, 0u);
+    }
+}
+
 template <bool BF16, bool POOL, int ACT>
 __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const ConvArgs a)
 {
@@ -204,7 +272,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
     uint64_t* full = bars;        // [4] strip (+ streamed weights) ready
     uint64_t* empty = bars + 4;   // [4] stage consumed by the MMA
-    uint64_t* wfull = bars + 8;   // resident weights landed
+    uint64_t* wfull = bars + 8;   // bias block (+ resident weights) landed
     uint64_t* tfull = bars + 9;   // [4] accumulator ready for the epilogue
     uint64_t* tempty = bars + 13; // [4] accumulator drained by the epilogue
     uint64_t* mdone = bars + 17;  // every MMA issued by this CTA completed
@@ -228,6 +296,10 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if (warp < kEpiWarps) {
+        build_indicator_planes<BF16>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
+        fence_proxy_async_smem();
+    }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
         tmem_relinquish();
@@ -240,14 +312,17 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kNumProd) {
         // ------------------------------------------------------------ producers
         const int pw = warp - kProdWarp0;
+        if (pw == 0 && lane == 0) {
+            // bias block, plus the whole weight tensor when it stays resident
+            const uint8_t* bias_src = reinterpret_cast<const uint8_t*>(a.wr) + a.w_total_bytes;
+            mbar_arrive_expect_tx(wfull, a.bias_block_bytes + (a.resident ? a.w_total_bytes : 0u));
+            bulk_g2s(smem + a.bb_off, bias_src, a.bias_block_bytes, wfull);
+            if (a.resident) bulk_g2s(smem + a.w_off, a.wr, a.w_total_bytes, wfull);
+        }
         if (pw < a.stages) {
             const uint32_t slot = static_cast<uint32_t>(pw);
             const uint32_t strip = smem_u32(smem + a.strip_off) + slot * kStripBytes;
-            uint8_t* wslot = smem + a.w_off + (a.resident ? 0u : slot * a.w_block_bytes);
-            if (a.resident && pw == 0 && lane == 0) {
-                mbar_arrive_expect_tx(wfull, a.w_total_bytes);
-                bulk_g2s(smem + a.w_off, a.wr, a.w_total_bytes, wfull);
-            }
+            uint8_t* wslot = smem + a.w_off + slot * a.w_block_bytes;
             const long long total = n_tiles * a.ncb;
             uint32_t use = 0;
             for (long long g = pw; g < total; g += a.stages, ++use) {
@@ -266,25 +341,24 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                         mbar_arrive(&full[slot]);
                     }
                 }
-                fill_strip<BF16>(strip, a.x, tc.n, cb, tc.oh0, tc.ow0, a.Cin, a.H, a.W, lane);
+                fill_strip<BF16>(strip, a.x, tc.n, cb, tc.rb * kPatchRows, tc.cs * kPatchCols, a.Cin, a.H, a.W, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(&full[slot]);
             }
-            if (*abort_flag && lane == 0) {
-                if (!a.resident && use > 0) drain_wait(&full[slot], (use - 1u) & 1u, a.budget);
-                if (a.resident && pw == 0) drain_wait(wfull, 0, a.budget);
-            }
+            if (*abort_flag && lane == 0 && !a.resident && use > 0) drain_wait(&full[slot], (use - 1u) & 1u, a.budget);
         }
+        if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, a.budget);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, 128, a.Cout);
             const uint32_t strip0 = smem_u32(smem + a.strip_off);
+            const uint32_t ind0 = smem_u32(smem + a.ind_off);
             const uint32_t w0 = smem_u32(smem + a.w_off);
+            const uint32_t bb = smem_u32(smem + a.bb_off);
             const uint32_t wtap = 2u * static_cast<uint32_t>(a.Cout) * 16u;
             const uint32_t w_lbo = static_cast<uint32_t>(a.Cout) * 16u;
-            bool ok = true;
-            if (a.resident) ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget);
+            bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget);
             long long g = 0;
             for (long long lt = 0; ok && lt < n_tiles; ++lt) {
                 const int acc = static_cast<int>(lt % a.nacc);
@@ -292,6 +366,15 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                 if (!(ok = mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
+                {
+                    // bias + padding K step (overwrites the accumulator)
+                    const TileCoord tc = tile_coord(t_begin + lt, a.tpi, a.CS);
+                    const uint32_t v = (tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u);
+                    const uint64_t ad = smem_desc(ind0 + v * kIndPlane, (4u - v) * kIndPlane, 128u, kLayoutNone);
+                    const uint64_t bd = smem_desc(bb, w_lbo, 128u, kLayoutNone);
+                    if constexpr (BF16) mma_f16(d, ad, bd, idesc, 0u);
+                    else mma_tf32(d, ad, bd, idesc, 0u);
+                }
                 for (int cb = 0; cb < a.ncb; ++cb, ++g) {
                     const uint32_t slot = static_cast<uint32_t>(g % a.stages);
                     const uint32_t use = static_cast<uint32_t>(g / a.stages);
@@ -306,9 +389,8 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                             smem_desc(abase + static_cast<uint32_t>(kh * kStripCols + kw) * 16u, kStripPlane,
                                       kStripCols * 16u, kLayoutNone);
                         const uint64_t bd = smem_desc(bbase + static_cast<uint32_t>(tap) * wtap, w_lbo, 128u, kLayoutNone);
-                        const uint32_t accum = (cb | tap) != 0 ? 1u : 0u;
-                        if constexpr (BF16) mma_f16(d, ad, bd, idesc, accum);
-                        else mma_tf32(d, ad, bd, idesc, accum);
+                        if constexpr (BF16) mma_f16(d, ad, bd, idesc, 1u);
+                        else mma_tf32(d, ad, bd, idesc, 1u);
                     }
                     mma_commit(&empty[slot]);
                 }
@@ -326,7 +408,20 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
         const int r = q * 32 + lane;
         const int pr = r >> 3, pc = r & 7;
         const long long n_first = t_begin / a.tpi;
+        // pool: running per-thread sums over the tiles of one image; with at most
+        // two 32-channel chunks per warp they stay in registers (reg[k][j] for
+        // channel (h + 2k) * 32 + j at this thread's pixel slot) and are reduced
+        // across the warp only when the image changes; otherwise each tile is
+        // reduced at once into psum[k] (lane j holds channel (h + 2k) * 32 + j).
+        const bool in_regs = nchunks <= 4;
+        float reg[2][32];
         float psum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (POOL) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) reg[k][j] = 0.0f;
+        }
         int cur_n = -1;
         bool ok = true;
 
@@ -336,7 +431,14 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = h + 2 * k;
-                if (c < nchunks) dst[c * 32 + lane] = psum[k];
+                if (c < nchunks) {
+                    if (k < 2 && in_regs) {
+                        psum[k] = warp_transpose_sum(reg[k], lane);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) reg[k][j] = 0.0f;
+                    }
+                    dst[c * 32 + lane] = psum[k];
+                }
                 psum[k] = 0.0f;
             }
         };
@@ -357,8 +459,6 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                 break;
             }
             tc_fence_after();
-            const int oh = tc.oh0 + pr, ow = tc.ow0 + pc;
-            const bool valid = oh < a.OH && ow < a.OW;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.Cout);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -367,22 +467,22 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                     float v[32];
                     tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
                     if constexpr (POOL) {
+                        if (k < 2 && in_regs) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float z = v[j] + load_bias<BF16>(a.bias, c * 32 + j);
-                            v[j] = valid ? apply_act<ACT>(z) : 0.0f;
+                            for (int j = 0; j < 32; ++j) reg[k][j] += apply_act<ACT>(v[j]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = apply_act<ACT>(v[j]);
+                            psum[k] += warp_transpose_sum(v, lane);
                         }
-                        psum[k] += warp_transpose_sum(v, lane);
                     } else {
-                        if (valid) {
+                        const int oh = tc.rb * kPatchRows + pr, ow = tc.cs * kPatchCols + pc;
+                        if (oh < a.OH && ow < a.OW) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * 32) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float z = v[j] + load_bias<BF16>(a.bias, c * 32 + j);
-                                o[j * plane] = apply_act<ACT>(z);
-                            }
+                            for (int j = 0; j < 32; ++j) o[j * plane] = apply_act<ACT>(v[j]);
                         }
                     }
                 }

@@ -39,8 +39,9 @@ struct ConvPlan {
     int tmem_cols;        // tensor-memory columns allocated
     uint32_t w_block_bytes;   // re-laid weights of one K block: 9 taps * 2 halves * Cout * 16 B
     uint32_t w_total_bytes;   // ncb * w_block_bytes
-    uint32_t strip_off, w_off, bar_off, smem_bytes;
-    size_t ws_weights_bytes;  // re-laid weights in the workspace
+    uint32_t bias_block_bytes;  // B operand of the bias K step: 2 halves * Cout * 16 B
+    uint32_t strip_off, ind_off, w_off, bb_off, bar_off, smem_bytes;
+    size_t ws_weights_bytes;  // re-laid weights + bias block in the workspace
     size_t ws_pool_bytes;     // pool partial sums in the workspace
 };
 

@@ -215,3 +215,23 @@ def test_watchdog_times_out_and_context_stays_usable(cuda_lib):
     ref = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu")
     _check(y, ref, TOL["f32"], "after watchdog")
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
+@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish"])
+def test_activation_accuracy_through_a_delta_kernel(cuda_lib, act):
+    """A delta 3x3 kernel makes the pre-activation equal to the input (values on a
+    1/64 grid are exact in TF32), so the output is the kernel's activation of
+    known points: checked against the oracle's fp64 activation to fp32-level
+    absolute error over [-12, 12] plus large-magnitude points."""
+    import torch
+    pts = np.concatenate([np.arange(-768, 769) / 64.0, [-80.0, -40.0, -20.0, 20.0, 40.0, 80.0]]).astype(np.float32)
+    W = pts.size + 2
+    x = np.zeros((1, 1, 3, W), np.float32)
+    x[0, 0, 0, :pts.size] = pts
+    w = np.zeros((32, 1, 3, 3), np.float32)
+    w[:, 0, 0, 0] = 1.0
+    b = np.zeros(32, np.float32)
+    y = cuda_lib.fc_conv3x3_act(_dev(x), _dev(w), _dev(b), act=act).cpu().numpy()[0, :, 0, :pts.size]
+    ref = np.array([oracle.act(act, float(v)) for v in pts])
+    err = np.abs(y - ref[None, :]) / np.maximum(1.0, np.abs(ref[None, :]))
+    assert err.max() <= 2e-6, f"{act}: max error {err.max():.3e} at x = {pts[int(np.argmax(err.max(0)))]}"
