@@ -4,7 +4,10 @@
 // and the launch sequence.  The fused kernel itself is in fc_conv_kernel.cuh.
 #include "fc_conv_kernel.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstring>
 
 namespace fc {
 using namespace convk;
@@ -116,11 +119,14 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     if (wtot > 0xFFFFFFFFull) return 2;
     p->w_total_bytes = static_cast<uint32_t>(wtot);
     p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout) * 16u;
+    p->raw_bytes = bf16 ? RawBox<true>::kBytes : RawBox<false>::kBytes;
+    // TMA needs 16-byte multiples for every global stride: the row pitch W * esize decides
+    p->use_tma = (static_cast<long long>(W) * p->esize) % 16 == 0;
     p->resident = p->w_total_bytes <= kResidentMax;
     if (p->resident) {
         p->stages = 4;
     } else {
-        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + kStripBytes)));
+        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + kStripBytes + p->raw_bytes)));
         if (p->stages < 2) return 2;
     }
     p->nacc = std::min(4, 512 / Cout);
@@ -128,12 +134,13 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;
     p->strip_off = 0;
-    p->ind_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
+    p->raw_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
+    p->ind_off = p->raw_off + static_cast<uint32_t>(p->stages) * p->raw_bytes;
     p->w_off = p->ind_off + kIndBytes;
     p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
     p->bar_off = p->bb_off + p->bias_block_bytes;
     p->bar_off = (p->bar_off + 127u) & ~127u;
-    // barriers (19 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
+    // barriers (23 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
     p->smem_bytes = p->bar_off + 256u + 1024u;
     p->ws_weights_bytes = align256(static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes);
     p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
@@ -157,6 +164,27 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         if (e != cudaSuccess) return e;
     }
 
+    // x as a 4-D tensor (W, H, Cin, N); one box = [K-block channels][18 rows][12 or 16 columns]
+    CUtensorMap tmx;
+    std::memset(&tmx, 0, sizeof(tmx));
+    if (p.use_tma) {
+        auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+        if (enc == nullptr) return cudaErrorNotSupported;
+        const cuuint64_t es = static_cast<cuuint64_t>(p.esize);
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.Cin),
+                              static_cast<cuuint64_t>(p.N)};
+        cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
+        cuuint32_t box[4] = {static_cast<cuuint32_t>(p.bf16 ? RawBox<true>::kCols : RawBox<false>::kCols),
+                             static_cast<cuuint32_t>(kStripRows),
+                             static_cast<cuuint32_t>(p.bf16 ? RawBox<true>::kCh : RawBox<false>::kCh), 1u};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = enc(&tmx, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                         const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+
     ConvArgs a{};
     a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
@@ -164,11 +192,12 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.base = p.base; a.rem = p.rem; a.J = p.J;
     a.stages = p.stages; a.resident = p.resident; a.nacc = p.nacc; a.tmem_cols = p.tmem_cols;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
-    a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.bar_off = p.bar_off;
+    a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.raw_off = p.raw_off;
+    a.bar_off = p.bar_off; a.use_tma = p.use_tma;
     a.status = status; a.budget = budget;
 
-    cudaError_t e = p.bf16 ? launch_main_bf16(a, p.pool, act, p.grid, p.smem_bytes, stream)
-                           : launch_main_tf32(a, p.pool, act, p.grid, p.smem_bytes, stream);
+    cudaError_t e = p.bf16 ? launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                           : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
     if (e != cudaSuccess) return e;
 
     if (p.pool) {

@@ -5,15 +5,16 @@
 namespace fc {
 namespace convk {
 
-cudaError_t launch_main_bf16(const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, cudaStream_t stream)
+cudaError_t launch_main_bf16(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes,
+                             cudaStream_t stream)
 {
     switch (pool * 3 + act) {
-    case 0: return launch_variant<true, false, 0>(a, grid, smem_bytes, stream);
-    case 1: return launch_variant<true, false, 1>(a, grid, smem_bytes, stream);
-    case 2: return launch_variant<true, false, 2>(a, grid, smem_bytes, stream);
-    case 3: return launch_variant<true, true, 0>(a, grid, smem_bytes, stream);
-    case 4: return launch_variant<true, true, 1>(a, grid, smem_bytes, stream);
-    case 5: return launch_variant<true, true, 2>(a, grid, smem_bytes, stream);
+    case 0: return launch_variant<true, false, 0>(tmx, a, grid, smem_bytes, stream);
+    case 1: return launch_variant<true, false, 1>(tmx, a, grid, smem_bytes, stream);
+    case 2: return launch_variant<true, false, 2>(tmx, a, grid, smem_bytes, stream);
+    case 3: return launch_variant<true, true, 0>(tmx, a, grid, smem_bytes, stream);
+    case 4: return launch_variant<true, true, 1>(tmx, a, grid, smem_bytes, stream);
+    case 5: return launch_variant<true, true, 2>(tmx, a, grid, smem_bytes, stream);
     default: return cudaErrorInvalidValue;
     }
 }

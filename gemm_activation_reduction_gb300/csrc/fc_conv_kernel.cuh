@@ -38,7 +38,9 @@
 //              column half = warp / 4), activation, then either a running
 //              per-thread sum (pool; reduced across the warp's 32 pixels only
 //              when the image changes) or coalesced stores.
-//   warps 8-11 producers: one shared-memory stage slot each.
+//   warps 8-11 producers: one shared-memory stage slot each; x arrives as a TMA box
+//              (channel-major, zero-filled past the image) that the warp re-lays
+//              into the staged strip while its next box is in flight.
 //   warp 12    tensor-memory allocator and single-thread MMA issuer.
 #pragma once
 
@@ -63,7 +65,7 @@ constexpr uint32_t kStripBytes = 2 * kStripPlane;        // one K block: 5760 B
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
 constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
 constexpr uint32_t kResidentMax = 96 * 1024;
-constexpr uint32_t kSmemBudget = 200 * 1024;
+constexpr uint32_t kSmemBudget = 210 * 1024;
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 
 struct ConvArgs {
@@ -75,7 +77,8 @@ struct ConvArgs {
     long long tpi, base;
     int rem, J, stages, resident, nacc, tmem_cols;
     uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;
-    uint32_t strip_off, ind_off, w_off, bb_off, bar_off;
+    uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
+    int use_tma;         // x staged by TMA boxes + in-warp transpose (else plain loads)
     int* status;
     long long budget;
 };
@@ -162,6 +165,88 @@ __device__ __forceinline__ TileCoord tile_coord(long long t, long long tpi, int 
     c.rb = r / CS;
     c.cs = r - c.rb * CS;
     return c;
+}
+
+// Next tile in (image, row block, column strip) order.
+__device__ __forceinline__ void next_tile(TileCoord& c, int RB, int CS)
+{
+    if (++c.cs == CS) {
+        c.cs = 0;
+        if (++c.rb == RB) {
+            c.rb = 0;
+            ++c.n;
+        }
+    }
+}
+
+// Raw TMA box of one K block: [channel][18 rows][kRawCols columns], channel-major as in x.
+template <bool BF16>
+struct RawBox {
+    static constexpr int kCols = BF16 ? 16 : 12;        // >= 10 staged columns, row = 32 or 48 bytes
+    static constexpr int kCh = BF16 ? 16 : 8;
+    static constexpr uint32_t kBytes = kCh * kStripRows * kCols * (BF16 ? 2 : 4);
+};
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Re-lay a landed raw box into the staged strip [group][180 pixels][16 B].
+template <bool BF16>
+__device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
+{
+    using RB_ = RawBox<BF16>;
+    if constexpr (!BF16) {
+        // item = (group g, staged pixel s): 4 channels of one pixel -> one 16-byte row
+        constexpr uint32_t kPlane = kStripRows * RB_::kCols * 4;   // one channel: 864 B
+#pragma unroll 4
+        for (int i = lane; i < 2 * kStripPos; i += 32) {
+            const int g = i >= kStripPos ? 1 : 0;
+            const int s = i - g * kStripPos;
+            const int row = s / kStripCols, col = s - (s / kStripCols) * kStripCols;
+            const uint32_t src = raw + static_cast<uint32_t>(4 * g) * kPlane + static_cast<uint32_t>(row * RB_::kCols + col) * 4u;
+            const float v0 = __uint_as_float(ld_shared_u32(src));
+            const float v1 = __uint_as_float(ld_shared_u32(src + kPlane));
+            const float v2 = __uint_as_float(ld_shared_u32(src + 2 * kPlane));
+            const float v3 = __uint_as_float(ld_shared_u32(src + 3 * kPlane));
+            st_shared_v4(strip + static_cast<uint32_t>(g) * kStripPlane + static_cast<uint32_t>(s) * 16u,
+                         __float_as_uint(to_tf32(v0)), __float_as_uint(to_tf32(v1)), __float_as_uint(to_tf32(v2)),
+                         __float_as_uint(to_tf32(v3)));
+        }
+    } else {
+        // item = (group g, staged row, column pair): 8 channels x 2 columns -> two 16-byte rows
+        constexpr uint32_t kPlane = kStripRows * RB_::kCols * 2;   // one channel: 576 B
+        constexpr int kPairs = kStripCols / 2;                     // 5
+        constexpr int kItems = 2 * kStripRows * kPairs;            // 180
+#pragma unroll 2
+        for (int i = lane; i < kItems; i += 32) {
+            const int g = i >= kItems / 2 ? 1 : 0;
+            const int r = i - g * (kItems / 2);
+            const int row = r / kPairs, cp = r - (r / kPairs) * kPairs;
+            const uint32_t src = raw + static_cast<uint32_t>(8 * g) * kPlane + static_cast<uint32_t>(row * RB_::kCols + 2 * cp) * 2u;
+            uint32_t w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) w[c] = ld_shared_u32(src + static_cast<uint32_t>(c) * kPlane);
+            const uint32_t dst = strip + static_cast<uint32_t>(g) * kStripPlane +
+                                 static_cast<uint32_t>(row * kStripCols + 2 * cp) * 16u;
+            st_shared_v4(dst, __byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410),
+                         __byte_perm(w[4], w[5], 0x5410), __byte_perm(w[6], w[7], 0x5410));
+            st_shared_v4(dst + 16u, __byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632),
+                         __byte_perm(w[4], w[5], 0x7632), __byte_perm(w[6], w[7], 0x7632));
+        }
+    }
 }
 
 // Stage one K block of the 18 x 10 halo patch as [group][pixel][16 B].
@@ -265,24 +350,26 @@ __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int
 }
 
 template <bool BF16, bool POOL, int ACT>
-__global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const ConvArgs a)
+__global__ void __launch_bounds__(kConvThreads, 1)
+    conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
-    uint64_t* full = bars;        // [4] strip (+ streamed weights) ready
-    uint64_t* empty = bars + 4;   // [4] stage consumed by the MMA
-    uint64_t* wfull = bars + 8;   // bias block (+ resident weights) landed
-    uint64_t* tfull = bars + 9;   // [4] accumulator ready for the epilogue
-    uint64_t* tempty = bars + 13; // [4] accumulator drained by the epilogue
-    uint64_t* mdone = bars + 17;  // every MMA issued by this CTA completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+    uint64_t* full = bars;         // [4] strip (+ streamed weights) ready
+    uint64_t* empty = bars + 4;    // [4] stage consumed by the MMA
+    uint64_t* wfull = bars + 8;    // bias block (+ resident weights) landed
+    uint64_t* tfull = bars + 9;    // [4] accumulator ready for the epilogue
+    uint64_t* tempty = bars + 13;  // [4] accumulator drained by the epilogue
+    uint64_t* mdone = bars + 17;   // every MMA issued by this CTA completed
+    uint64_t* rawfull = bars + 18; // [4] a producer warp's raw x box landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long t_begin = static_cast<long long>(blockIdx.x) * a.base + min(static_cast<int>(blockIdx.x), a.rem);
-    const long long n_tiles = a.base + (static_cast<int>(blockIdx.x) < a.rem ? 1 : 0);
+    const int n_tiles = static_cast<int>(a.base + (static_cast<int>(blockIdx.x) < a.rem ? 1 : 0));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
@@ -290,11 +377,13 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
             mbar_init(&empty[s], 1);
             mbar_init(&tfull[s], 1);
             mbar_init(&tempty[s], kEpiWarps * 32);
+            mbar_init(&rawfull[s], 1);
         }
         mbar_init(wfull, 1);
         mbar_init(mdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        if (a.use_tma) prefetch_tmap(&tmx);
     }
     if (warp < kEpiWarps) {
         build_indicator_planes<BF16>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
@@ -308,6 +397,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const TileCoord first = tile_coord(t_begin, a.tpi, a.CS);
 
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kNumProd) {
         // ------------------------------------------------------------ producers
@@ -320,18 +410,29 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
             if (a.resident) bulk_g2s(smem + a.w_off, a.wr, a.w_total_bytes, wfull);
         }
         if (pw < a.stages) {
+            // this warp owns slot pw and handles stages g = pw, pw + S, pw + 2S, ...
             const uint32_t slot = static_cast<uint32_t>(pw);
             const uint32_t strip = smem_u32(smem + a.strip_off) + slot * kStripBytes;
             uint8_t* wslot = smem + a.w_off + slot * a.w_block_bytes;
-            const long long total = n_tiles * a.ncb;
-            uint32_t use = 0;
-            for (long long g = pw; g < total; g += a.stages, ++use) {
+            uint8_t* raw = smem + a.raw_off + slot * RawBox<BF16>::kBytes;
+            TileCoord tc = first;
+            int lt = 0, cb = pw;
+            while (cb >= a.ncb) {
+                cb -= a.ncb;
+                ++lt;
+                next_tile(tc, a.RB, a.CS);
+            }
+            auto issue_raw = [&](const TileCoord& c, int kb) {
+                mbar_arrive_expect_tx(&rawfull[slot], RawBox<BF16>::kBytes);
+                tma_load_4d(raw, &tmx, &rawfull[slot], c.cs * kPatchCols, c.rb * kPatchRows, kb * RawBox<BF16>::kCh, c.n);
+            };
+            if (a.use_tma && lt < n_tiles && lane == 0) issue_raw(tc, cb);
+            uint32_t use = 0, rph = 0;
+            bool issued_raw = a.use_tma && lt < n_tiles;
+            while (lt < n_tiles) {
                 bool ok = mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.status, a.budget);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 fence_proxy_async_smem();
-                const long long lt = g / a.ncb;
-                const int cb = static_cast<int>(g - lt * a.ncb);
-                const TileCoord tc = tile_coord(t_begin + lt, a.tpi, a.CS);
                 if (lane == 0) {
                     if (!a.resident) {
                         mbar_arrive_expect_tx(&full[slot], a.w_block_bytes);
@@ -341,11 +442,40 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                         mbar_arrive(&full[slot]);
                     }
                 }
-                fill_strip<BF16>(strip, a.x, tc.n, cb, tc.rb * kPatchRows, tc.cs * kPatchCols, a.Cin, a.H, a.W, lane);
-                fence_proxy_async_smem();
+                // the stage after this one for this warp
+                TileCoord ntc = tc;
+                int nlt = lt, ncb = cb + a.stages;
+                while (ncb >= a.ncb) {
+                    ncb -= a.ncb;
+                    ++nlt;
+                    next_tile(ntc, a.RB, a.CS);
+                }
+                if (a.use_tma) {
+                    ok = mbar_wait(&rawfull[slot], rph, abort_flag, a.status, a.budget);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    rph ^= 1u;
+                    issued_raw = false;
+                    transpose_raw<BF16>(smem_u32(raw), strip, lane);
+                    fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
+                    __syncwarp();
+                    if (nlt < n_tiles) {
+                        if (lane == 0) issue_raw(ntc, ncb);
+                        issued_raw = true;
+                    }
+                } else {
+                    fill_strip<BF16>(strip, a.x, tc.n, cb, tc.rb * kPatchRows, tc.cs * kPatchCols, a.Cin, a.H, a.W, lane);
+                    fence_proxy_async_smem();
+                }
                 mbar_arrive(&full[slot]);
+                tc = ntc;
+                lt = nlt;
+                cb = ncb;
+                ++use;
             }
-            if (*abort_flag && lane == 0 && !a.resident && use > 0) drain_wait(&full[slot], (use - 1u) & 1u, a.budget);
+            if (*abort_flag && lane == 0) {
+                if (!a.resident && use > 0) drain_wait(&full[slot], (use - 1u) & 1u, a.budget);
+                if (issued_raw) drain_wait(&rawfull[slot], rph, a.budget);
+            }
         }
         if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, a.budget);
     } else if (warp == kMmaWarp) {
@@ -359,26 +489,23 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
             const uint32_t wtap = 2u * static_cast<uint32_t>(a.Cout) * 16u;
             const uint32_t w_lbo = static_cast<uint32_t>(a.Cout) * 16u;
             bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget);
-            long long g = 0;
-            for (long long lt = 0; ok && lt < n_tiles; ++lt) {
-                const int acc = static_cast<int>(lt % a.nacc);
-                const uint32_t aph = static_cast<uint32_t>((lt / a.nacc) & 1);
+            TileCoord tc = first;
+            int acc = 0;
+            uint32_t aph = 0, slot = 0, sph = 0;
+            for (int lt = 0; ok && lt < n_tiles; ++lt) {
                 if (!(ok = mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 {
                     // bias + padding K step (overwrites the accumulator)
-                    const TileCoord tc = tile_coord(t_begin + lt, a.tpi, a.CS);
                     const uint32_t v = (tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u);
                     const uint64_t ad = smem_desc(ind0 + v * kIndPlane, (4u - v) * kIndPlane, 128u, kLayoutNone);
                     const uint64_t bd = smem_desc(bb, w_lbo, 128u, kLayoutNone);
                     if constexpr (BF16) mma_f16(d, ad, bd, idesc, 0u);
                     else mma_tf32(d, ad, bd, idesc, 0u);
                 }
-                for (int cb = 0; cb < a.ncb; ++cb, ++g) {
-                    const uint32_t slot = static_cast<uint32_t>(g % a.stages);
-                    const uint32_t use = static_cast<uint32_t>(g / a.stages);
-                    if (!(ok = mbar_wait(&full[slot], use & 1u, abort_flag, a.status, a.budget))) break;
+                for (int cb = 0; cb < a.ncb; ++cb) {
+                    if (!(ok = mbar_wait(&full[slot], sph, abort_flag, a.status, a.budget))) break;
                     tc_fence_after();
                     const uint32_t abase = strip0 + slot * kStripBytes;
                     const uint32_t bbase = w0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * a.w_block_bytes;
@@ -393,8 +520,17 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
                         else mma_tf32(d, ad, bd, idesc, 1u);
                     }
                     mma_commit(&empty[slot]);
+                    if (++slot == static_cast<uint32_t>(a.stages)) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
                 }
                 if (ok) mma_commit(&tfull[acc]);
+                if (++acc == a.nacc) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+                next_tile(tc, a.RB, a.CS);
             }
             mma_commit(mdone);
             drain_wait(mdone, 0, a.budget);
@@ -407,7 +543,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
         const int nchunks = a.Cout / 32;
         const int r = q * 32 + lane;
         const int pr = r >> 3, pc = r & 7;
-        const long long n_first = t_begin / a.tpi;
+        const int n_first = first.n;
         // pool: running per-thread sums over the tiles of one image; with at most
         // two 32-channel chunks per warp they stay in registers (reg[k][j] for
         // channel (h + 2k) * 32 + j at this thread's pixel slot) and are reduced
@@ -443,16 +579,16 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
             }
         };
 
-        for (long long lt = 0; lt < n_tiles; ++lt) {
-            const TileCoord tc = tile_coord(t_begin + lt, a.tpi, a.CS);
+        TileCoord tc = first;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int lt = 0; lt < n_tiles; ++lt) {
             if constexpr (POOL) {
                 if (tc.n != cur_n) {
                     if (cur_n >= 0) flush(cur_n);
                     cur_n = tc.n;
                 }
             }
-            const int acc = static_cast<int>(lt % a.nacc);
-            const uint32_t aph = static_cast<uint32_t>((lt / a.nacc) & 1);
             ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status, a.budget);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
@@ -489,6 +625,11 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
+            if (++acc == a.nacc) {
+                acc = 0;
+                aph ^= 1u;
+            }
+            next_tile(tc, a.RB, a.CS);
         }
         if constexpr (POOL) {
             if (ok && cur_n >= 0) flush(cur_n);
@@ -504,19 +645,22 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv3x3_fused_kernel(const Co
 }
 
 template <bool BF16, bool POOL, int ACT>
-cudaError_t launch_variant(const ConvArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream)
+cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
+                           cudaStream_t stream)
 {
     auto kern = conv3x3_fused_kernel<BF16, POOL, ACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kConvThreads, smem_bytes, stream>>>(a);
+    kern<<<grid, kConvThreads, smem_bytes, stream>>>(tmx, a);
     return cudaGetLastError();
 }
 
 // One instantiation per (pool, activation) for the given operand type; defined
 // in fc_conv_tf32.cu and fc_conv_bf16.cu so the variants compile in parallel.
-cudaError_t launch_main_tf32(const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, cudaStream_t stream);
-cudaError_t launch_main_bf16(const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_main_tf32(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes,
+                             cudaStream_t stream);
+cudaError_t launch_main_bf16(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes,
+                             cudaStream_t stream);
 
 }  // namespace convk
 }  // namespace fc

@@ -40,7 +40,9 @@ struct ConvPlan {
     uint32_t w_block_bytes;   // re-laid weights of one K block: 9 taps * 2 halves * Cout * 16 B
     uint32_t w_total_bytes;   // ncb * w_block_bytes
     uint32_t bias_block_bytes;  // B operand of the bias K step: 2 halves * Cout * 16 B
-    uint32_t strip_off, ind_off, w_off, bb_off, bar_off, smem_bytes;
+    uint32_t raw_bytes;       // one TMA box of x per K block (channel-major)
+    int use_tma;              // x rows are 16-byte multiples: stage x with TMA boxes
+    uint32_t strip_off, raw_off, ind_off, w_off, bb_off, bar_off, smem_bytes;
     size_t ws_weights_bytes;  // re-laid weights + bias block in the workspace
     size_t ws_pool_bytes;     // pool partial sums in the workspace
 };
@@ -71,6 +73,9 @@ cudaError_t linear_launch(const LinearPlan& plan, const float* x, const float* W
 // ---------------------------------------------------------------- misc
 
 cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int* status);
+
+// cuTensorMapEncodeTiled from the driver (as a PFN_cuTensorMapEncodeTiled_v12000), or null.
+void* tensor_map_encoder();
 
 // SM count and device address of the watchdog word of the current device.
 cudaError_t current_device_info(int* sm_count, int** status);

@@ -232,24 +232,10 @@ __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int 
     y[m] = l * (l * tanhf(sp));
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // Row-major [rows][cols] fp32 matrix, box = box_rows x 32 columns (128 B), 128-byte swizzle.
 bool make_kmajor_map(CUtensorMap* map, const float* base, int rows, int cols, int box_rows)
 {
-    auto enc = get_encode();
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     if (enc == nullptr) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * sizeof(float)};
@@ -262,6 +248,20 @@ bool make_kmajor_map(CUtensorMap* map, const float* base, int rows, int cols, in
 }
 
 }  // namespace
+
+void* tensor_map_encoder()
+{
+    static void* fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    }
+    return fn;
+}
 
 int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
 {
