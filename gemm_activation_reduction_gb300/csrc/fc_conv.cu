@@ -94,6 +94,25 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Tile geometry of one call: the pooled ops use the 16 x 8 patch, the full-output op the 1 x 128 row.
+struct Geometry {
+    int PR, PC, SR, box_cols, box_ch;
+    uint32_t strip_bytes, raw_bytes;
+};
+
+template <bool BF16, bool WIDE>
+Geometry geometry_of()
+{
+    return Geometry{Shape<WIDE>::PR, Shape<WIDE>::PC, Shape<WIDE>::SR, RawBox<BF16, WIDE>::kCols,
+                    RawBox<BF16, WIDE>::kCh, Shape<WIDE>::STRIP, RawBox<BF16, WIDE>::kBytes};
+}
+
+Geometry geometry(int bf16, int pool)
+{
+    if (bf16) return pool ? geometry_of<true, false>() : geometry_of<true, true>();
+    return pool ? geometry_of<false, false>() : geometry_of<false, true>();
+}
+
 }  // namespace
 
 int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count)
@@ -106,8 +125,9 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->esize = bf16 ? 2 : 4;
     p->cb_ch = bf16 ? 16 : 8;
     p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch;
-    p->RB = (p->OH + kPatchRows - 1) / kPatchRows;
-    p->CS = (p->OW + kPatchCols - 1) / kPatchCols;
+    const Geometry geo = geometry(bf16, pool);
+    p->RB = (p->OH + geo.PR - 1) / geo.PR;
+    p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
     p->num_tiles = static_cast<long long>(N) * p->tpi;
     p->grid = static_cast<int>(std::min<long long>(p->num_tiles, std::max(sm_count, 1)));
@@ -119,14 +139,15 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     if (wtot > 0xFFFFFFFFull) return 2;
     p->w_total_bytes = static_cast<uint32_t>(wtot);
     p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout) * 16u;
-    p->raw_bytes = bf16 ? RawBox<true>::kBytes : RawBox<false>::kBytes;
+    p->raw_bytes = geo.raw_bytes;
+    p->strip_bytes = geo.strip_bytes;
     // TMA needs 16-byte multiples for every global stride: the row pitch W * esize decides
     p->use_tma = (static_cast<long long>(W) * p->esize) % 16 == 0;
     p->resident = p->w_total_bytes <= kResidentMax;
     if (p->resident) {
         p->stages = 4;
     } else {
-        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + kStripBytes + p->raw_bytes)));
+        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + p->strip_bytes + p->raw_bytes)));
         if (p->stages < 2) return 2;
     }
     p->nacc = std::min(4, 512 / Cout);
@@ -134,7 +155,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;
     p->strip_off = 0;
-    p->raw_off = p->strip_off + static_cast<uint32_t>(p->stages) * kStripBytes;
+    p->raw_off = p->strip_off + static_cast<uint32_t>(p->stages) * p->strip_bytes;
     p->ind_off = p->raw_off + static_cast<uint32_t>(p->stages) * p->raw_bytes;
     p->w_off = p->ind_off + kIndBytes;
     p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
@@ -164,7 +185,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         if (e != cudaSuccess) return e;
     }
 
-    // x as a 4-D tensor (W, H, Cin, N); one box = [K-block channels][18 rows][12 or 16 columns]
+    // x as a 4-D tensor (W, H, Cin, N); one box = [K-block channels][staged rows][staged columns]
     CUtensorMap tmx;
     std::memset(&tmx, 0, sizeof(tmx));
     if (p.use_tma) {
@@ -174,9 +195,9 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.Cin),
                               static_cast<cuuint64_t>(p.N)};
         cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
-        cuuint32_t box[4] = {static_cast<cuuint32_t>(p.bf16 ? RawBox<true>::kCols : RawBox<false>::kCols),
-                             static_cast<cuuint32_t>(kStripRows),
-                             static_cast<cuuint32_t>(p.bf16 ? RawBox<true>::kCh : RawBox<false>::kCh), 1u};
+        const Geometry geo = geometry(p.bf16, p.pool);
+        cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_cols), static_cast<cuuint32_t>(geo.SR),
+                             static_cast<cuuint32_t>(geo.box_ch), 1u};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         CUresult r = enc(&tmx, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                          const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -54,19 +54,39 @@ constexpr int kEpiWarps = 8;
 constexpr int kProdWarp0 = 8;
 constexpr int kNumProd = 4;
 constexpr int kMmaWarp = 12;
-constexpr int kPatchRows = 16;
-constexpr int kPatchCols = 8;
-constexpr int kStripCols = kPatchCols + 2;               // 10
-constexpr int kStripRows = kPatchRows + 2;               // 18
-constexpr int kStripPos = kStripRows * kStripCols;       // 180 staged pixels
-constexpr int kStripIters = (kStripPos + 31) / 32;       // 6 per lane
-constexpr uint32_t kStripPlane = kStripPos * 16;         // one channel group: 2880 B
-constexpr uint32_t kStripBytes = 2 * kStripPlane;        // one K block: 5760 B
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
 constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
 constexpr uint32_t kResidentMax = 96 * 1024;
 constexpr uint32_t kSmemBudget = 210 * 1024;
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
+
+// Output pixels of one 128-row MMA tile.  The pooled ops use a 16-row x 8-column
+// patch (least halo: 18 x 10 staged pixels per 128 outputs); the full-output op
+// uses one row of 128 columns so that each warp stores 32 consecutive pixels of
+// a row (128 contiguous bytes) per output channel.  Either way the 8-pixel
+// core-matrix groups of the tile lie at one constant stride in the staged
+// strip (SBO): the next patch row (16 x 8), or the next 8 pixels (1 x 128).
+template <bool WIDE>
+struct Shape {
+    static constexpr int PR = WIDE ? 1 : 16;               // output rows per tile
+    static constexpr int PC = WIDE ? 128 : 8;              // output columns per tile
+    static constexpr int SR = PR + 2;                      // staged rows (halo)
+    static constexpr int SC = PC + 2;                      // staged columns (halo)
+    static constexpr int SPOS = SR * SC;                   // staged pixels
+    static constexpr uint32_t PLANE = SPOS * 16;           // one channel group of the strip
+    static constexpr uint32_t STRIP = (2 * PLANE + 127) / 128 * 128;  // one K block, slot pitch
+    static constexpr uint32_t SBO = WIDE ? 128u : SC * 16u;
+};
+
+// Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
+// order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.
+template <bool BF16, bool WIDE>
+struct RawBox {
+    static constexpr int kCh = BF16 ? 16 : 8;
+    static constexpr int kCols = BF16 ? (Shape<WIDE>::SC + 7) / 8 * 8 : (Shape<WIDE>::SC + 3) / 4 * 4;
+    static constexpr uint32_t kChPlane = Shape<WIDE>::SR * kCols * (BF16 ? 2 : 4);
+    static constexpr uint32_t kBytes = (kCh * kChPlane + 127) / 128 * 128;
+};
 
 struct ConvArgs {
     const void* x;
@@ -180,13 +200,6 @@ __device__ __forceinline__ void next_tile(TileCoord& c, int RB, int CS)
 }
 
 // Raw TMA box of one K block: [channel][18 rows][kRawCols columns], channel-major as in x.
-template <bool BF16>
-struct RawBox {
-    static constexpr int kCols = BF16 ? 16 : 12;        // >= 10 staged columns, row = 32 or 48 bytes
-    static constexpr int kCh = BF16 ? 16 : 8;
-    static constexpr uint32_t kBytes = kCh * kStripRows * kCols * (BF16 ? 2 : 4);
-};
-
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t* bar, int c0, int c1, int c2, int c3)
 {
     asm volatile(
@@ -203,44 +216,45 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
-// Re-lay a landed raw box into the staged strip [group][180 pixels][16 B].
-template <bool BF16>
+// Re-lay a landed raw box into the staged strip [group][SPOS pixels][16 B].
+template <bool BF16, bool WIDE>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
 {
-    using RB_ = RawBox<BF16>;
+    using S = Shape<WIDE>;
+    using RB_ = RawBox<BF16, WIDE>;
     if constexpr (!BF16) {
         // item = (group g, staged pixel s): 4 channels of one pixel -> one 16-byte row
-        constexpr uint32_t kPlane = kStripRows * RB_::kCols * 4;   // one channel: 864 B
 #pragma unroll 4
-        for (int i = lane; i < 2 * kStripPos; i += 32) {
-            const int g = i >= kStripPos ? 1 : 0;
-            const int s = i - g * kStripPos;
-            const int row = s / kStripCols, col = s - (s / kStripCols) * kStripCols;
-            const uint32_t src = raw + static_cast<uint32_t>(4 * g) * kPlane + static_cast<uint32_t>(row * RB_::kCols + col) * 4u;
+        for (int i = lane; i < 2 * S::SPOS; i += 32) {
+            const int g = i >= S::SPOS ? 1 : 0;
+            const int s = i - g * S::SPOS;
+            const int row = s / S::SC, col = s - (s / S::SC) * S::SC;
+            const uint32_t src = raw + static_cast<uint32_t>(4 * g) * RB_::kChPlane +
+                                 static_cast<uint32_t>(row * RB_::kCols + col) * 4u;
             const float v0 = __uint_as_float(ld_shared_u32(src));
-            const float v1 = __uint_as_float(ld_shared_u32(src + kPlane));
-            const float v2 = __uint_as_float(ld_shared_u32(src + 2 * kPlane));
-            const float v3 = __uint_as_float(ld_shared_u32(src + 3 * kPlane));
-            st_shared_v4(strip + static_cast<uint32_t>(g) * kStripPlane + static_cast<uint32_t>(s) * 16u,
+            const float v1 = __uint_as_float(ld_shared_u32(src + RB_::kChPlane));
+            const float v2 = __uint_as_float(ld_shared_u32(src + 2 * RB_::kChPlane));
+            const float v3 = __uint_as_float(ld_shared_u32(src + 3 * RB_::kChPlane));
+            st_shared_v4(strip + static_cast<uint32_t>(g) * S::PLANE + static_cast<uint32_t>(s) * 16u,
                          __float_as_uint(to_tf32(v0)), __float_as_uint(to_tf32(v1)), __float_as_uint(to_tf32(v2)),
                          __float_as_uint(to_tf32(v3)));
         }
     } else {
         // item = (group g, staged row, column pair): 8 channels x 2 columns -> two 16-byte rows
-        constexpr uint32_t kPlane = kStripRows * RB_::kCols * 2;   // one channel: 576 B
-        constexpr int kPairs = kStripCols / 2;                     // 5
-        constexpr int kItems = 2 * kStripRows * kPairs;            // 180
+        constexpr int kPairs = S::SC / 2;
+        constexpr int kHalf = S::SR * kPairs;
 #pragma unroll 2
-        for (int i = lane; i < kItems; i += 32) {
-            const int g = i >= kItems / 2 ? 1 : 0;
-            const int r = i - g * (kItems / 2);
+        for (int i = lane; i < 2 * kHalf; i += 32) {
+            const int g = i >= kHalf ? 1 : 0;
+            const int r = i - g * kHalf;
             const int row = r / kPairs, cp = r - (r / kPairs) * kPairs;
-            const uint32_t src = raw + static_cast<uint32_t>(8 * g) * kPlane + static_cast<uint32_t>(row * RB_::kCols + 2 * cp) * 2u;
+            const uint32_t src = raw + static_cast<uint32_t>(8 * g) * RB_::kChPlane +
+                                 static_cast<uint32_t>(row * RB_::kCols + 2 * cp) * 2u;
             uint32_t w[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) w[c] = ld_shared_u32(src + static_cast<uint32_t>(c) * kPlane);
-            const uint32_t dst = strip + static_cast<uint32_t>(g) * kStripPlane +
-                                 static_cast<uint32_t>(row * kStripCols + 2 * cp) * 16u;
+            for (int c = 0; c < 8; ++c) w[c] = ld_shared_u32(src + static_cast<uint32_t>(c) * RB_::kChPlane);
+            const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
+                                 static_cast<uint32_t>(row * S::SC + 2 * cp) * 16u;
             st_shared_v4(dst, __byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410),
                          __byte_perm(w[4], w[5], 0x5410), __byte_perm(w[6], w[7], 0x5410));
             st_shared_v4(dst + 16u, __byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632),
@@ -249,63 +263,44 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
     }
 }
 
-// Stage one K block of the 18 x 10 halo patch as [group][pixel][16 B].
-template <bool BF16>
+// Fallback staging with plain loads (when x's row pitch is not a 16-byte
+// multiple and TMA cannot address it): one K block of the halo patch as
+// [group][SPOS pixels][16 B], zero past the image and past Cin.
+template <bool BF16, bool WIDE>
 __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
                                            int Cin, int H, int W, int lane)
 {
+    using S = Shape<WIDE>;
     const size_t HW = static_cast<size_t>(H) * W;
-    if constexpr (!BF16) {
-        const float* x = reinterpret_cast<const float*>(xv);
-        const int ci0 = cb * 8;
-        float v[kStripIters][8];
-#pragma unroll
-        for (int i = 0; i < kStripIters; ++i) {
-            const int s = lane + 32 * i;
-            const int rr = s / kStripCols, cc = s - (s / kStripCols) * kStripCols;
-            const int ih = oh0 + rr, iw = ow0 + cc;
-            const bool ok = (s < kStripPos) && ih < H && iw < W;
+    for (int s = lane; s < S::SPOS; s += 32) {
+        const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
+        const int ih = oh0 + rr, iw = ow0 + cc;
+        const bool ok = ih < H && iw < W;
+        const uint32_t a = strip + static_cast<uint32_t>(s) * 16u;
+        if constexpr (!BF16) {
+            const float* x = reinterpret_cast<const float*>(xv);
+            const int ci0 = cb * 8;
             const size_t off = ok ? ((static_cast<size_t>(n) * Cin + ci0) * HW + static_cast<size_t>(ih) * W + iw) : 0;
+            float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[i][e] = (ok && ci0 + e < Cin) ? __ldg(x + off + e * HW) : 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < kStripIters; ++i) {
-            const int s = lane + 32 * i;
-            if (s < kStripPos) {
-                const uint32_t a = strip + static_cast<uint32_t>(s) * 16u;
-                st_shared_v4(a, __float_as_uint(to_tf32(v[i][0])), __float_as_uint(to_tf32(v[i][1])),
-                             __float_as_uint(to_tf32(v[i][2])), __float_as_uint(to_tf32(v[i][3])));
-                st_shared_v4(a + kStripPlane, __float_as_uint(to_tf32(v[i][4])), __float_as_uint(to_tf32(v[i][5])),
-                             __float_as_uint(to_tf32(v[i][6])), __float_as_uint(to_tf32(v[i][7])));
-            }
-        }
-    } else {
-        const unsigned short* x = reinterpret_cast<const unsigned short*>(xv);
-        const int ci0 = cb * 16;
-        uint32_t v[kStripIters][8];
-#pragma unroll
-        for (int i = 0; i < kStripIters; ++i) {
-            const int s = lane + 32 * i;
-            const int rr = s / kStripCols, cc = s - (s / kStripCols) * kStripCols;
-            const int ih = oh0 + rr, iw = ow0 + cc;
-            const bool ok = (s < kStripPos) && ih < H && iw < W;
+            for (int e = 0; e < 8; ++e) v[e] = (ok && ci0 + e < Cin) ? __ldg(x + off + e * HW) : 0.0f;
+            st_shared_v4(a, __float_as_uint(to_tf32(v[0])), __float_as_uint(to_tf32(v[1])),
+                         __float_as_uint(to_tf32(v[2])), __float_as_uint(to_tf32(v[3])));
+            st_shared_v4(a + S::PLANE, __float_as_uint(to_tf32(v[4])), __float_as_uint(to_tf32(v[5])),
+                         __float_as_uint(to_tf32(v[6])), __float_as_uint(to_tf32(v[7])));
+        } else {
+            const unsigned short* x = reinterpret_cast<const unsigned short*>(xv);
+            const int ci0 = cb * 16;
             const size_t off = ok ? ((static_cast<size_t>(n) * Cin + ci0) * HW + static_cast<size_t>(ih) * W + iw) : 0;
+            uint32_t v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t lo = (ok && ci0 + 2 * e < Cin) ? __ldg(x + off + (2 * e) * HW) : 0u;
                 const uint32_t hi = (ok && ci0 + 2 * e + 1 < Cin) ? __ldg(x + off + (2 * e + 1) * HW) : 0u;
-                v[i][e] = lo | (hi << 16);
+                v[e] = lo | (hi << 16);
             }
-        }
-#pragma unroll
-        for (int i = 0; i < kStripIters; ++i) {
-            const int s = lane + 32 * i;
-            if (s < kStripPos) {
-                const uint32_t a = strip + static_cast<uint32_t>(s) * 16u;
-                st_shared_v4(a, v[i][0], v[i][1], v[i][2], v[i][3]);
-                st_shared_v4(a + kStripPlane, v[i][4], v[i][5], v[i][6], v[i][7]);
-            }
+            st_shared_v4(a, v[0], v[1], v[2], v[3]);
+            st_shared_v4(a + S::PLANE, v[4], v[5], v[6], v[7]);
         }
     }
 }
@@ -323,15 +318,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
 // Indicator planes for the bias K step: variant v (bit 1: last row block,
 // bit 0: last column strip) marks which of the 128 tile pixels lie inside the
 // output; plane 4 is zero (the second K core matrix).
-template <bool BF16>
+template <bool BF16, bool WIDE>
 __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
                                                        int nthreads)
 {
-    const int rows_last = OH - (RB - 1) * kPatchRows;   // valid rows in the last row block
-    const int cols_last = OW - (CS - 1) * kPatchCols;   // valid columns in the last column strip
+    using S = Shape<WIDE>;
+    const int rows_last = OH - (RB - 1) * S::PR;   // valid rows in the last row block
+    const int cols_last = OW - (CS - 1) * S::PC;   // valid columns in the last column strip
     for (int i = tid; i < 5 * 128; i += nthreads) {
         const int v = i >> 7, r = i & 127;
-        const int pr = r >> 3, pc = r & 7;
+        const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const bool in = v < 4 && (!(v & 2) || pr < rows_last) && (!(v & 1) || pc < cols_last);
         const bool pad = v < 4 && !in;
         uint32_t w0, w1, w2;
@@ -353,6 +349,9 @@ template <bool BF16, bool POOL, int ACT>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
+    constexpr bool WIDE = !POOL;
+    using S = Shape<WIDE>;
+    using RBox = RawBox<BF16, WIDE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         if (a.use_tma) prefetch_tmap(&tmx);
     }
     if (warp < kEpiWarps) {
-        build_indicator_planes<BF16>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
+        build_indicator_planes<BF16, WIDE>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
@@ -412,9 +411,9 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         if (pw < a.stages) {
             // this warp owns slot pw and handles stages g = pw, pw + S, pw + 2S, ...
             const uint32_t slot = static_cast<uint32_t>(pw);
-            const uint32_t strip = smem_u32(smem + a.strip_off) + slot * kStripBytes;
+            const uint32_t strip = smem_u32(smem + a.strip_off) + slot * S::STRIP;
             uint8_t* wslot = smem + a.w_off + slot * a.w_block_bytes;
-            uint8_t* raw = smem + a.raw_off + slot * RawBox<BF16>::kBytes;
+            uint8_t* raw = smem + a.raw_off + slot * RBox::kBytes;
             TileCoord tc = first;
             int lt = 0, cb = pw;
             while (cb >= a.ncb) {
@@ -423,8 +422,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 next_tile(tc, a.RB, a.CS);
             }
             auto issue_raw = [&](const TileCoord& c, int kb) {
-                mbar_arrive_expect_tx(&rawfull[slot], RawBox<BF16>::kBytes);
-                tma_load_4d(raw, &tmx, &rawfull[slot], c.cs * kPatchCols, c.rb * kPatchRows, kb * RawBox<BF16>::kCh, c.n);
+                mbar_arrive_expect_tx(&rawfull[slot], RBox::kBytes);
+                tma_load_4d(raw, &tmx, &rawfull[slot], c.cs * S::PC, c.rb * S::PR, kb * RBox::kCh, c.n);
             };
             if (a.use_tma && lt < n_tiles && lane == 0) issue_raw(tc, cb);
             uint32_t use = 0, rph = 0;
@@ -455,7 +454,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     if (!__all_sync(0xffffffffu, ok)) break;
                     rph ^= 1u;
                     issued_raw = false;
-                    transpose_raw<BF16>(smem_u32(raw), strip, lane);
+                    transpose_raw<BF16, WIDE>(smem_u32(raw), strip, lane);
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
                     if (nlt < n_tiles) {
@@ -463,7 +462,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         issued_raw = true;
                     }
                 } else {
-                    fill_strip<BF16>(strip, a.x, tc.n, cb, tc.rb * kPatchRows, tc.cs * kPatchCols, a.Cin, a.H, a.W, lane);
+                    fill_strip<BF16, WIDE>(strip, a.x, tc.n, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin, a.H, a.W, lane);
                     fence_proxy_async_smem();
                 }
                 mbar_arrive(&full[slot]);
@@ -507,14 +506,13 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     if (!(ok = mbar_wait(&full[slot], sph, abort_flag, a.status, a.budget))) break;
                     tc_fence_after();
-                    const uint32_t abase = strip0 + slot * kStripBytes;
+                    const uint32_t abase = strip0 + slot * S::STRIP;
                     const uint32_t bbase = w0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * a.w_block_bytes;
 #pragma unroll
                     for (int tap = 0; tap < 9; ++tap) {
                         const int kh = tap / 3, kw = tap - (tap / 3) * 3;
-                        const uint64_t ad =
-                            smem_desc(abase + static_cast<uint32_t>(kh * kStripCols + kw) * 16u, kStripPlane,
-                                      kStripCols * 16u, kLayoutNone);
+                        const uint64_t ad = smem_desc(abase + static_cast<uint32_t>(kh * S::SC + kw) * 16u, S::PLANE,
+                                                      S::SBO, kLayoutNone);
                         const uint64_t bd = smem_desc(bbase + static_cast<uint32_t>(tap) * wtap, w_lbo, 128u, kLayoutNone);
                         if constexpr (BF16) mma_f16(d, ad, bd, idesc, 1u);
                         else mma_tf32(d, ad, bd, idesc, 1u);
@@ -542,7 +540,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         const int h = warp >> 2;
         const int nchunks = a.Cout / 32;
         const int r = q * 32 + lane;
-        const int pr = r >> 3, pc = r & 7;
+        const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const int n_first = first.n;
         // pool: running per-thread sums over the tiles of one image; with at most
         // two 32-channel chunks per warp they stay in registers (reg[k][j] for
@@ -612,13 +610,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                             psum[k] += warp_transpose_sum(v, lane);
                         }
                     } else {
-                        const int oh = tc.rb * kPatchRows + pr, ow = tc.cs * kPatchCols + pc;
+                        const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
                         if (oh < a.OH && ow < a.OW) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * 32) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
+                            // streaming stores: the output is written once and not re-read here
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j * plane] = apply_act<ACT>(v[j]);
+                            for (int j = 0; j < 32; ++j) __stcs(o + j * plane, apply_act<ACT>(v[j]));
                         }
                     }
                 }

@@ -26,7 +26,7 @@ struct ConvPlan {
     int esize;            // bytes per stored element (4 or 2)
     int cb_ch;            // input channels per K block (8 fp32, 16 bf16)
     int ncb;              // K blocks = ceil(Cin / cb_ch)
-    int RB, CS;           // output row blocks (16 rows) and column strips (8 columns) per image
+    int RB, CS;           // output row blocks and column strips per image (tiles of 16 x 8, or 1 x 128)
     long long tpi;        // tiles per image = RB * CS
     long long num_tiles;  // N * tpi
     int grid;             // CTAs (persistent)
@@ -41,6 +41,7 @@ struct ConvPlan {
     uint32_t w_total_bytes;   // ncb * w_block_bytes
     uint32_t bias_block_bytes;  // B operand of the bias K step: 2 halves * Cout * 16 B
     uint32_t raw_bytes;       // one TMA box of x per K block (channel-major)
+    uint32_t strip_bytes;     // one staged K block, channel-blocked
     int use_tma;              // x rows are 16-byte multiples: stage x with TMA boxes
     uint32_t strip_off, raw_off, ind_off, w_off, bb_off, bar_off, smem_bytes;
     size_t ws_weights_bytes;  // re-laid weights + bias block in the workspace
