@@ -372,10 +372,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
-            mbar_init(&full[s], 33);
+            mbar_init(&full[s], 2);            // lane 0: before (with the weight bytes) and after the fill
             mbar_init(&empty[s], 1);
             mbar_init(&tfull[s], 1);
-            mbar_init(&tempty[s], kEpiWarps * 32);
+            mbar_init(&tempty[s], kEpiWarps);  // lane 0 of each epilogue warp
             mbar_init(&rawfull[s], 1);
         }
         mbar_init(wfull, 1);
@@ -464,8 +464,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 } else {
                     fill_strip<BF16, WIDE>(strip, a.x, tc.n, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin, a.H, a.W, lane);
                     fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                mbar_arrive(&full[slot]);
+                // every lane fenced its strip writes and the warp has synchronised
+                if (lane == 0) mbar_arrive(&full[slot]);
                 tc = ntc;
                 lt = nlt;
                 cb = ncb;
@@ -481,12 +483,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, 128, a.Cout);
-            const uint32_t strip0 = smem_u32(smem + a.strip_off);
-            const uint32_t ind0 = smem_u32(smem + a.ind_off);
-            const uint32_t w0 = smem_u32(smem + a.w_off);
-            const uint32_t bb = smem_u32(smem + a.bb_off);
-            const uint32_t wtap = 2u * static_cast<uint32_t>(a.Cout) * 16u;
-            const uint32_t w_lbo = static_cast<uint32_t>(a.Cout) * 16u;
+            // Descriptors are built once; each MMA only moves the start-address field
+            // (bits 0-13, 16-byte units).  Every address stays below 256 KB, so the
+            // field never carries into the LBO bits above it.
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem + a.strip_off), S::PLANE, S::SBO, kLayoutNone);
+            const uint64_t i_desc0 = smem_desc(smem_u32(smem + a.ind_off), 0u, 128u, kLayoutNone);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + a.w_off), static_cast<uint32_t>(a.Cout) * 16u, 128u,
+                                               kLayoutNone);
+            const uint64_t bb_desc = smem_desc(smem_u32(smem + a.bb_off), static_cast<uint32_t>(a.Cout) * 16u, 128u,
+                                               kLayoutNone);
+            const uint32_t wtap16 = 2u * static_cast<uint32_t>(a.Cout);   // one tap of weights, 16-byte units
+            const uint32_t wblk16 = a.w_block_bytes >> 4;
+            constexpr uint32_t kStrip16 = S::STRIP >> 4;
+            constexpr uint32_t kInd16 = kIndPlane >> 4;
             bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget);
             TileCoord tc = first;
             int acc = 0;
@@ -496,26 +505,23 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 {
-                    // bias + padding K step (overwrites the accumulator)
+                    // bias + padding K step (overwrites the accumulator); LBO points at the zero plane
                     const uint32_t v = (tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u);
-                    const uint64_t ad = smem_desc(ind0 + v * kIndPlane, (4u - v) * kIndPlane, 128u, kLayoutNone);
-                    const uint64_t bd = smem_desc(bb, w_lbo, 128u, kLayoutNone);
-                    if constexpr (BF16) mma_f16(d, ad, bd, idesc, 0u);
-                    else mma_tf32(d, ad, bd, idesc, 0u);
+                    const uint64_t ad = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
+                    if constexpr (BF16) mma_f16(d, ad, bb_desc, idesc, 0u);
+                    else mma_tf32(d, ad, bb_desc, idesc, 0u);
                 }
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     if (!(ok = mbar_wait(&full[slot], sph, abort_flag, a.status, a.budget))) break;
                     tc_fence_after();
-                    const uint32_t abase = strip0 + slot * S::STRIP;
-                    const uint32_t bbase = w0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * a.w_block_bytes;
+                    const uint64_t ab = a_desc0 + slot * kStrip16;
+                    const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
 #pragma unroll
                     for (int tap = 0; tap < 9; ++tap) {
-                        const int kh = tap / 3, kw = tap - (tap / 3) * 3;
-                        const uint64_t ad = smem_desc(abase + static_cast<uint32_t>(kh * S::SC + kw) * 16u, S::PLANE,
-                                                      S::SBO, kLayoutNone);
-                        const uint64_t bd = smem_desc(bbase + static_cast<uint32_t>(tap) * wtap, w_lbo, 128u, kLayoutNone);
-                        if constexpr (BF16) mma_f16(d, ad, bd, idesc, 1u);
-                        else mma_tf32(d, ad, bd, idesc, 1u);
+                        constexpr int kSC = S::SC;
+                        const uint32_t aoff = static_cast<uint32_t>((tap / 3) * kSC + (tap % 3));
+                        if constexpr (BF16) mma_f16(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
+                        else mma_tf32(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
                     }
                     mma_commit(&empty[slot]);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
@@ -623,7 +629,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
             if (++acc == a.nacc) {
                 acc = 0;
                 aph ^= 1u;

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&tfull[s], 1);
-            mbar_init(&tempty[s], 128);
+            mbar_init(&tempty[s], 4);   // lane 0 of each epilogue warp
         }
         mbar_init(mdone, 1);
         *abort_flag = 0;
@@ -125,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc(kFmtTF32, kBM, kBN);
-            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            // Descriptors built once; stages and K steps only move the start-address
+            // field (16-byte units; addresses stay below 256 KB, so no carry).
+            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, kLayoutSw128);
+            const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, kLayoutSw128);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -139,13 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait(&full[stage], phase, abort_flag, a.status, a.budget))) break;
                     tc_fence_after();
-                    const uint32_t as = a0 + stage * kABytes, bs = b0 + stage * kBBytes;
+                    const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kABytes >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kBBytes >> 4);
 #pragma unroll
-                    for (int k = 0; k < kBK / 8; ++k) {
-                        const uint64_t ad = smem_desc(as + k * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t bd = smem_desc(bs + k * 32, 16, 1024, kLayoutSw128);
-                        mma_tf32(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kBK / 8; ++k)   // 32-byte K steps inside the 128-byte swizzle row
+                        mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
@@ -200,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
             const int m = mb * kBM + row;
             if (m < a.M) a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
         }
