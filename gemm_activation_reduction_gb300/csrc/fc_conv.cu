@@ -118,7 +118,7 @@ Geometry geometry(int bf16, int pool)
 int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count)
 {
     *p = ConvPlan{};
-    if (Cout < 32 || Cout > 256 || Cout % 32 != 0) return 2;
+    if (Cout < 16 || Cout > 256 || Cout % 16 != 0) return 2;
     p->N = N; p->Cin = Cin; p->H = H; p->W = W; p->Cout = Cout;
     p->OH = H - 2; p->OW = W - 2;
     p->bf16 = bf16; p->pool = pool;

@@ -33,15 +33,15 @@
 // padding pixels, whose GELU / Mish is exactly -0: the epilogue needs no bias
 // loads and no masking.
 //
-// Warp roles (416 threads, one CTA per SM, persistent over a contiguous tile range):
-//   warps 0-7  epilogue: tcgen05.ld of the accumulator (lane quarter = warp % 4,
-//              column half = warp / 4), activation, then either a running
+// Warp roles (672 threads, one CTA per SM, persistent over a contiguous tile range):
+//   warps 0-15 epilogue: tcgen05.ld of the accumulator (lane quarter = warp % 4,
+//              16-column slices h, h+4, ... with h = warp / 4), activation, then either a running
 //              per-thread sum (pool; reduced across the warp's 32 pixels only
 //              when the image changes) or coalesced stores.
-//   warps 8-11 producers: one shared-memory stage slot each; x arrives as a TMA box
+//   warps 16-19 producers: one shared-memory stage slot each; x arrives as a TMA box
 //              (channel-major, zero-filled past the image) that the warp re-lays
 //              into the staged strip while its next box is in flight.
-//   warp 12    tensor-memory allocator and single-thread MMA issuer.
+//   warp 20    tensor-memory allocator and single-thread MMA issuer.
 #pragma once
 
 #include "fc_ptx.cuh"
@@ -49,11 +49,12 @@
 namespace fc {
 namespace convk {
 
-constexpr int kConvThreads = 13 * 32;
-constexpr int kEpiWarps = 8;
-constexpr int kProdWarp0 = 8;
+constexpr int kEpiWarps = 16;                 // 4 per TMEM lane quarter
+constexpr int kEpiCols = 16;                  // accumulator columns per TMEM load
+constexpr int kProdWarp0 = kEpiWarps;
 constexpr int kNumProd = 4;
-constexpr int kMmaWarp = 12;
+constexpr int kMmaWarp = kProdWarp0 + kNumProd;
+constexpr int kConvThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
 constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
 constexpr uint32_t kResidentMax = 96 * 1024;
@@ -170,6 +171,41 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane)
         }
     }
     return v[0];
+}
+
+// 16 values per lane: after the call lane L holds sum over the warp's 32 lanes of
+// v[L % 16] (v is clobbered).
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 16);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = upper ? v[i] : v[i + w];
+            const float keep = upper ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
+// 16 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Tile t of the flattened (image, row block, column strip) grid.
@@ -512,8 +548,9 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     else mma_tf32(d, ad, bb_desc, idesc, 0u);
                 }
                 for (int cb = 0; cb < a.ncb; ++cb) {
+                    // Operand readiness needs no tcgen05 fence: the stage barrier (after the
+                    // producers' async-proxy fence, or the bulk copy's complete_tx) orders it.
                     if (!(ok = mbar_wait(&full[slot], sph, abort_flag, a.status, a.budget))) break;
-                    tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16;
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
 #pragma unroll
@@ -542,25 +579,27 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         __syncwarp();
     } else if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
+        // warp = (lane quarter q, column group h): this warp owns TMEM lanes 32q..32q+31
+        // (tile pixels) and the 16-column accumulator slices c = h, h + 4, h + 8, h + 12.
         const int q = warp & 3;
         const int h = warp >> 2;
-        const int nchunks = a.Cout / 32;
+        const int nsub = a.Cout / kEpiCols;
         const int r = q * 32 + lane;
         const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const int n_first = first.n;
-        // pool: running per-thread sums over the tiles of one image; with at most
-        // two 32-channel chunks per warp they stay in registers (reg[k][j] for
-        // channel (h + 2k) * 32 + j at this thread's pixel slot) and are reduced
-        // across the warp only when the image changes; otherwise each tile is
-        // reduced at once into psum[k] (lane j holds channel (h + 2k) * 32 + j).
-        const bool in_regs = nchunks <= 4;
-        float reg[2][32];
+        // pool: running per-thread sums over the tiles of one image; with at most two
+        // slices per warp they stay in registers (reg[k][j] for channel
+        // (h + 4k) * 16 + j at this thread's pixel slot) and are reduced across the
+        // warp only when the image changes; otherwise each tile is reduced at once
+        // into psum[k] (lane j < 16 holds channel (h + 4k) * 16 + j).
+        const bool in_regs = nsub <= 2 * (kEpiWarps / 4);
+        float reg[2][kEpiCols];
         float psum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if constexpr (POOL) {
 #pragma unroll
             for (int k = 0; k < 2; ++k)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) reg[k][j] = 0.0f;
+                for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
         }
         int cur_n = -1;
         bool ok = true;
@@ -570,14 +609,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                                      static_cast<size_t>(a.Cout);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = h + 2 * k;
-                if (c < nchunks) {
+                const int c = h + 4 * k;
+                if (c < nsub) {
                     if (k < 2 && in_regs) {
-                        psum[k] = warp_transpose_sum(reg[k], lane);
+                        psum[k] = warp_transpose_sum16(reg[k], lane);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) reg[k][j] = 0.0f;
+                        for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
                     }
-                    dst[c * 32 + lane] = psum[k];
+                    if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k];
                 }
                 psum[k] = 0.0f;
             }
@@ -602,28 +641,28 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.Cout);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = h + 2 * k;
-                if (c < nchunks) {
-                    float v[32];
-                    tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
+                const int c = h + 4 * k;
+                if (c < nsub) {
+                    float v[kEpiCols];
+                    tmem_ld16(tbase + static_cast<uint32_t>(c * kEpiCols), v);
                     if constexpr (POOL) {
                         if (k < 2 && in_regs) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) reg[k][j] += apply_act<ACT>(v[j]);
+                            for (int j = 0; j < kEpiCols; ++j) reg[k][j] += apply_act<ACT>(v[j]);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = apply_act<ACT>(v[j]);
-                            psum[k] += warp_transpose_sum(v, lane);
+                            for (int j = 0; j < kEpiCols; ++j) v[j] = apply_act<ACT>(v[j]);
+                            psum[k] += warp_transpose_sum16(v, lane);
                         }
                     } else {
                         const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
                         if (oh < a.OH && ow < a.OW) {
-                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * 32) * a.OH + oh) *
+                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
                             // streaming stores: the output is written once and not re-read here
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) __stcs(o + j * plane, apply_act<ACT>(v[j]));
+                            for (int j = 0; j < kEpiCols; ++j) __stcs(o + j * plane, apply_act<ACT>(v[j]));
                         }
                     }
                 }

@@ -141,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait(&full[stage], phase, abort_flag, a.status, a.budget))) break;
-                    tc_fence_after();
                     const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kABytes >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kBBytes >> 4);
 #pragma unroll

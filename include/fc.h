@@ -79,7 +79,7 @@ typedef enum {
  *   w   [Cout, Cin, 3, 3]  same dtype, OIHW
  *   b   [Cout]             same dtype
  *   y   [N, Cout]          fp32 output
- *   Requires N, Cin >= 1; H, W >= 3; 32 <= Cout <= 256 with Cout % 32 == 0
+ *   Requires N, Cin >= 1; H, W >= 3; 16 <= Cout <= 256 with Cout % 16 == 0
  *   (else FC_ERR_UNSUPPORTED).  The mean is a fixed-order two-stage sum:
  *   results are bit-identical run to run on the same GPU model.
  */

@@ -53,6 +53,8 @@ POOL_SHAPES = [
     (2, 16, 18, 20, 64, "bf16", "gelu"),
     (1, 128, 12, 12, 256, "bf16", "gelu"),   # streamed bf16 weights
     (1, 24, 35, 9, 32, "bf16", "gelu"),      # Cin not a multiple of 16
+    (2, 5, 21, 26, 48, "f32", "gelu"),       # Cout = 48 (a multiple of 16, not of 32)
+    (1, 16, 19, 30, 16, "bf16", "gelu"),     # the smallest Cout, 16
 ]
 
 
@@ -72,6 +74,7 @@ ACT_SHAPES = [
     (1, 5, 17, 21, 96, "f32", "gelu"),
     (1, 32, 14, 12, 64, "bf16", "mish_mish"),
     (2, 16, 19, 10, 256, "bf16", "mish"),
+    (1, 7, 9, 140, 80, "f32", "mish_mish"),  # Cout = 80; rows wider than one 128-pixel tile
 ]
 
 
@@ -199,7 +202,7 @@ def test_workspace_too_small_is_rejected(cuda_lib):
 
 
 def test_unsupported_cout_is_reported(cuda_lib):
-    d = fc_inputs.conv_inputs(1, 8, 16, 16, 48)
+    d = fc_inputs.conv_inputs(1, 8, 16, 16, 40)   # not a multiple of 16
     with pytest.raises(cuda_lib.FCError) as e:
         cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]))
     assert e.value.status == cuda_lib.FC_ERR_UNSUPPORTED
