@@ -61,6 +61,8 @@ struct LinearPlan {
     int M, K, Nout;
     int m_blocks, n_blocks, k_blocks;
     int num_tiles, grid;
+    int use_pair;         // CTA pairs with M = 256 MMAs (tcgen05 cta_group::2)
+    int m_pairs;          // 256-row blocks in pair mode
     uint32_t smem_bytes;
     size_t ws_bytes;      // (max, sum-exp) partial per row and column tile
 };

@@ -215,6 +215,206 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ---------------------------------------------------------------- CTA-pair variant
+//
+// Two CTAs of a cluster compute one 256 x 256 tile with M = 256 MMAs
+// (tcgen05 cta_group::2): CTA r holds rows 128r..128r+127 of the x tile and rows
+// 128r..128r+127 of the W tile (half of N), so per SM the operand fetch per MMA
+// halves for W while the MMA's work per SM is unchanged.  Both CTAs' TMA loads
+// signal the leader's (rank 0) stage barrier; the leader issues the MMAs and
+// multicasts its commits to both CTAs' barriers; each CTA's epilogue reads its
+// own 128 accumulator rows and tells the leader through a remote arrive.
+constexpr int kPBM = 128;                                  // rows per CTA (256 per pair)
+constexpr int kPBN = 256;                                  // columns per pair tile
+constexpr int kPStages = 6;
+constexpr uint32_t kPABytes = kPBM * kBK * 4;              // 16 KB
+constexpr uint32_t kPBBytes = (kPBN / 2) * kBK * 4;        // 16 KB (this CTA's half of W)
+constexpr uint32_t kPBarOff = kPStages * (kPABytes + kPBBytes);
+constexpr uint32_t kPSmemBytes = kPBarOff + 256 + 1024;
+
+struct LinPairArgs {
+    const float* bias;
+    float2* partials;   // [n_blocks][M]
+    int M, N, K;
+    int m_pairs, n_blocks, k_blocks, num_tiles;
+    float scale, lo, hi;
+    int* status;
+    long long budget;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_lse_pair_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                           const LinPairArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kPStages * kPABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPBarOff);
+    uint64_t* full = bars;            // [6] leader: both CTAs' stage bytes landed
+    uint64_t* empty = bars + 6;       // [6] both: stage consumed (multicast commit)
+    uint64_t* tfull = bars + 12;      // [2] both: accumulator ready (multicast commit)
+    uint64_t* tempty = bars + 14;     // [2] leader: both CTAs' epilogues drained it
+    uint64_t* mdone = bars + 16;      // leader: every MMA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], 8);   // lane 0 of the 4 epilogue warps of each CTA
+        }
+        mbar_init(mdone, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmx);
+        prefetch_tmap(&tmw);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised before any remote arrive or copy
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < a.num_tiles; t += nclusters) {
+                const int mp = t % a.m_pairs, nb = t / a.m_pairs;
+                const int m0 = mp * 2 * kPBM + static_cast<int>(rank) * kPBM;
+                const int n0 = nb * kPBN + static_cast<int>(rank) * (kPBN / 2);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
+                    const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPABytes + kPBBytes));
+                    tma_load_2d_pair(sA + stage * kPABytes, &tmx, fbar, kb * kBK, m0);
+                    tma_load_2d_pair(sB + stage * kPBBytes, &tmw, fbar, kb * kBK, n0);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // after an abort, give copies already issued time to land before the CTA exits
+                const long long t0 = clock64();
+                while (clock64() - t0 < a.budget / 8) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            const uint32_t idesc = make_idesc(kFmtTF32, 2 * kPBM, kPBN);
+            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, kLayoutSw128);
+            const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, kLayoutSw128);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = cluster; ok && t < a.num_tiles; t += nclusters, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+                if (!(ok = mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kPBN);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!(ok = mbar_wait_cluster(&full[stage], phase, abort_flag, a.status, a.budget))) break;
+                    const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kPABytes >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kPBBytes >> 4);
+#pragma unroll
+                    for (int k = 0; k < kBK / 8; ++k)
+                        mma_tf32_pair(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) mma_commit_pair_multicast(&tfull[acc], 0x3);
+            }
+            mma_commit_pair_multicast(mdone, 0x1);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(mdone, 0) && clock64() - t0 < a.budget) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int t = cluster; t < a.num_tiles; t += nclusters, ++it) {
+            const int mp = t % a.m_pairs, nb = t / a.m_pairs;
+            const int acc = it & 1;
+            const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
+            const bool ok = mbar_wait_cluster(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPBN);
+            float run_m = -INFINITY, run_s = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < kPBN / 32; ++c) {
+                float v[32];
+                tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
+                const int n0 = nb * kPBN + c * 32;
+                float cm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = n0 + j;
+                    if (n < a.N) {
+                        float u = (v[j] + __ldg(a.bias + n)) * a.scale;
+                        u = u + u;
+                        v[j] = fminf(fmaxf(u, a.lo), a.hi);
+                    } else {
+                        v[j] = -INFINITY;
+                    }
+                    cm = fmaxf(cm, v[j]);
+                }
+                if (cm > -INFINITY) {
+                    const float nm = fmaxf(run_m, cm);
+                    float s = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s += __expf(v[j] - nm);
+                    run_s = run_s * __expf(run_m - nm) + s;
+                    run_m = nm;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+            const int m = mp * 2 * kPBM + static_cast<int>(rank) * kPBM + row;
+            if (m < a.M) a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();   // the leader's MMAs into both CTAs' tensor memory are complete
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
 // Merge the per-column-tile (max, sum) pairs of each row in fixed order, then
 // lse = M + log S and y = lse * mish(lse), mish(l) = l * tanh(softplus(l)).
 __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks)
@@ -277,6 +477,14 @@ int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
     p->num_tiles = static_cast<int>(tiles);
     p->grid = std::min(p->num_tiles, std::max(sm_count, 1));
     p->smem_bytes = kSmemBytes;
+    // CTA pairs (M = 256 MMAs) once there is more than one 128-row block
+    p->use_pair = M > kBM && sm_count >= 2;
+    if (p->use_pair) {
+        p->m_pairs = (M + 2 * kPBM - 1) / (2 * kPBM);
+        p->num_tiles = p->m_pairs * p->n_blocks;
+        p->grid = 2 * std::min(p->num_tiles, std::max(sm_count / 2, 1));
+        p->smem_bytes = kPSmemBytes;
+    }
     p->ws_bytes = (static_cast<size_t>(p->n_blocks) * M * sizeof(float2) + 255) & ~static_cast<size_t>(255);
     return 0;
 }
@@ -285,6 +493,36 @@ cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, c
                           float lo, float hi, void* workspace, cudaStream_t stream, int* status, long long budget)
 {
     CUtensorMap tmx, tmw;
+    if (p.use_pair) {
+        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kPBN / 2))
+            return cudaErrorInvalidValue;
+        LinPairArgs a{};
+        a.bias = b;
+        a.partials = reinterpret_cast<float2*>(workspace);
+        a.M = p.M; a.N = p.Nout; a.K = p.K;
+        a.m_pairs = p.m_pairs; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
+        a.scale = scale; a.lo = lo; a.hi = hi;
+        a.status = status; a.budget = budget;
+        cudaError_t e = cudaFuncSetAttribute(linear_lse_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(p.smem_bytes));
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = p.smem_bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, linear_lse_pair_kernel, tmx, tmw, a);
+        if (e != cudaSuccess) return e;
+        lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);
+        return cudaGetLastError();
+    }
     if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN))
         return cudaErrorInvalidValue;
     LinArgs a{};
