@@ -13,24 +13,34 @@ namespace fc {
 using namespace convk;
 namespace {
 
-// Re-lay w [Cout][Cin][3][3] into [K block][tap][half][co][G] (G = 4 fp32 rounded
-// to TF32, or 8 bf16), zero-padding channels past Cin; then append the B
-// operand of the bias K step, [half][co][G]: half 0 holds, per channel, the
-// bias (fp32: its TF32 high part in k 0 and the TF32 remainder in k 2; bf16:
-// the bias in k 0) and the padding value in k 1; half 1 is zero.
+// Re-lay w [Cout][Cin][3][3] for `halves` CTAs of a group (2 for a CTA pair, else 1):
+// CTA r holds output channels [r hc, (r+1) hc), hc = Cout / halves.  Layout
+// [r][K block][tap][half][co'][G]
+// (G = 4 fp32 rounded to TF32, or 8 bf16; co' the channel within the half),
+// zero-padding channels past Cin; then the B operands of the bias K step,
+// [r][half][co'][G]: half 0 holds the bias (fp32: its TF32 high part in k 0 and
+// the TF32 remainder in k 2; bf16: the bias in k 0) and the padding value in k 1;
+// half 1 is zero.
 template <bool BF16>
-__global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Cout, int ncb)
+__global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Cout, int ncb,
+                                            int halves)
 {
     constexpr int G = BF16 ? 8 : 4;
-    const long long wtotal = static_cast<long long>(ncb) * 9 * 2 * Cout * G;
-    const long long total = wtotal + 2LL * Cout * G;
+    const int hc = Cout / halves;
+    const long long per_rank = static_cast<long long>(ncb) * 9 * 2 * hc * G;
+    const long long wtotal = halves * per_rank;
+    const long long total = wtotal + static_cast<long long>(halves) * 2 * hc * G;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (i >= wtotal) {
-            const long long f = i - wtotal;
+            long long f = i - wtotal;
             const int e = static_cast<int>(f % G);
-            const int co = static_cast<int>((f / G) % Cout);
-            const int half = static_cast<int>(f / (static_cast<long long>(G) * Cout));
+            f /= G;
+            const int col = static_cast<int>(f % hc);
+            f /= hc;
+            const int half = static_cast<int>(f % 2);
+            const int rank = static_cast<int>(f / 2);
+            const int co = rank * hc + col;
             if constexpr (BF16) {
                 const unsigned short bv = reinterpret_cast<const unsigned short*>(b)[co];
                 const unsigned short pad = static_cast<unsigned short>(__float_as_uint(kPadValue) >> 16);
@@ -52,12 +62,15 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
         long long f = i;
         const int e = static_cast<int>(f % G);
         f /= G;
-        const int co = static_cast<int>(f % Cout);
-        f /= Cout;
+        const int col = static_cast<int>(f % hc);
+        f /= hc;
         const int half = static_cast<int>(f % 2);
         f /= 2;
         const int tap = static_cast<int>(f % 9);
-        const int cb = static_cast<int>(f / 9);
+        f /= 9;
+        const int cb = static_cast<int>(f % ncb);
+        const int rank = static_cast<int>(f / ncb);
+        const int co = rank * hc + col;
         const int ci = cb * 2 * G + half * G + e;
         const size_t src = (static_cast<size_t>(co) * Cin + ci) * 9 + tap;
         if constexpr (BF16) {
@@ -70,24 +83,32 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
     }
 }
 
-// y[n, co] = (fixed-order sum of the partials of every CTA that covered image n) / (OH * OW).
-__global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Cout, long long tpi, long long base,
-                                         int rem, int J, double inv_count)
+// y[n, co] = (fixed-order sum of every image-n record of the CTAs whose tiles can
+// touch image n) / (OH * OW).  Cluster c handles tile groups [P(c), P(c+1)) of
+// `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles step * g + r.
+// Records a CTA never reached hold zeros.
+__global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Cout, long long tpi, long long pbase,
+                                         int prem, int J, int step, double inv_count)
 {
     const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (idx >= static_cast<long long>(N) * Cout) return;
     const int n = static_cast<int>(idx / Cout);
     const int co = static_cast<int>(idx - static_cast<long long>(n) * Cout);
-    const long long big = static_cast<long long>(rem) * (base + 1);
-    auto cta_of = [&](long long t) -> long long { return t < big ? t / (base + 1) : rem + (t - big) / base; };
-    auto start_of = [&](long long c) -> long long { return c * base + (c < rem ? c : rem); };
+    const long long big = static_cast<long long>(prem) * (pbase + 1);
+    auto cluster_of = [&](long long p) -> long long { return p < big ? p / (pbase + 1) : prem + (p - big) / pbase; };
+    auto start_of = [&](long long c) -> long long { return c * pbase + (c < prem ? c : prem); };
     const long long t0 = static_cast<long long>(n) * tpi;
-    const long long c0 = cta_of(t0), c1 = cta_of(t0 + tpi - 1);
+    const long long c0 = cluster_of(t0 / step), c1 = cluster_of((t0 + tpi - 1) / step);
     double s = 0.0;
     for (long long c = c0; c <= c1; ++c) {
-        const long long nf = start_of(c) / tpi;
-        const float* p = ws + ((c * J + (n - nf)) * 4) * static_cast<long long>(Cout) + co;
-        for (int q = 0; q < 4; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
+        for (int r = 0; r < step; ++r) {
+            const long long cta = step * c + r;
+            const long long nf = (step * start_of(c) + r) / tpi;
+            const long long slot = n - nf;
+            if (slot < 0 || slot >= J) continue;
+            const float* p = ws + ((cta * J + slot) * 4) * static_cast<long long>(Cout) + co;
+            for (int q = 0; q < 4; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
+        }
     }
     y[idx] = static_cast<float>(s * inv_count);
 }
@@ -130,15 +151,24 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
     p->num_tiles = static_cast<long long>(N) * p->tpi;
-    p->grid = static_cast<int>(std::min<long long>(p->num_tiles, std::max(sm_count, 1)));
-    p->base = p->num_tiles / p->grid;
-    p->rem = static_cast<int>(p->num_tiles % p->grid);
-    p->J = static_cast<int>((p->base + 1 + p->tpi - 1) / p->tpi) + 1;
-    p->w_block_bytes = 9u * 2u * static_cast<uint32_t>(Cout) * 16u;
+    // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) when the weight
+    // operand dominates the per-MMA fetch, i.e. Cout > 128; single CTAs otherwise.
+    p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
+    const int step = p->pair ? 2 : 1;
+    // cluster c (a CTA pair, or one CTA) takes a contiguous range of tile groups
+    const long long groups = (p->num_tiles + step - 1) / step;
+    const int clusters = static_cast<int>(std::min<long long>(groups, std::max(sm_count / step, 1)));
+    p->grid = step * clusters;
+    p->pbase = groups / clusters;
+    p->prem = static_cast<int>(groups % clusters);
+    // a CTA's tiles span at most step * (pbase + 1) - 1 consecutive tiles
+    p->J = static_cast<int>((step * (p->pbase + 1) + p->tpi - 1) / p->tpi) + 1;
+    // per CTA of a group: Cout / step output channels
+    p->w_block_bytes = 9u * 2u * static_cast<uint32_t>(Cout / step) * 16u;
     const unsigned long long wtot = static_cast<unsigned long long>(p->w_block_bytes) * p->ncb;
     if (wtot > 0xFFFFFFFFull) return 2;
     p->w_total_bytes = static_cast<uint32_t>(wtot);
-    p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout) * 16u;
+    p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout / step) * 16u;
     p->raw_bytes = geo.raw_bytes;
     p->strip_bytes = geo.strip_bytes;
     // TMA needs 16-byte multiples for every global stride: the row pitch W * esize decides
@@ -163,7 +193,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->bar_off = (p->bar_off + 127u) & ~127u;
     // barriers (23 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
     p->smem_bytes = p->bar_off + 256u + 1024u;
-    p->ws_weights_bytes = align256(static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes);
+    p->ws_weights_bytes = align256(step * (static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes));
     p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
     return 0;
 }
@@ -179,8 +209,9 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         const long long total = (static_cast<long long>(p.ncb) * 9 + 1) * 2 * p.Cout * (p.bf16 ? 8 : 4);
         const int threads = 256;
         const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, 4096));
-        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb);
-        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb);
+        const int halves = p.pair ? 2 : 1;
+        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb, halves);
+        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb, halves);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -210,22 +241,29 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
     a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.OH = p.OH; a.OW = p.OW;
-    a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.base = p.base; a.rem = p.rem; a.J = p.J;
+    a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
+    a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.resident = p.resident; a.nacc = p.nacc; a.tmem_cols = p.tmem_cols;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
     a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.raw_off = p.raw_off;
     a.bar_off = p.bar_off; a.use_tma = p.use_tma;
     a.status = status; a.budget = budget;
 
-    cudaError_t e = p.bf16 ? launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
-                           : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+    cudaError_t e;
+    if (p.bf16)
+        e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+    else
+        e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
     if (e != cudaSuccess) return e;
 
     if (p.pool) {
         const long long outs = static_cast<long long>(p.N) * p.Cout;
         const int threads = 256;
         const int blocks = static_cast<int>((outs + threads - 1) / threads);
-        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Cout, p.tpi, p.base, p.rem, p.J,
+        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Cout, p.tpi, p.pbase, p.prem, p.J,
+                                                                  p.pair ? 2 : 1,
                                                                   1.0 / (static_cast<double>(p.OH) * p.OW));
         e = cudaGetLastError();
     }

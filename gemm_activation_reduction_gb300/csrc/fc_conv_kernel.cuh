@@ -57,9 +57,9 @@ constexpr int kMmaWarp = kProdWarp0 + kNumProd;
 constexpr int kConvThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
 constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
+constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 constexpr uint32_t kResidentMax = 96 * 1024;
 constexpr uint32_t kSmemBudget = 210 * 1024;
-constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 
 // Output pixels of one 128-row MMA tile.  The pooled ops use a 16-row x 8-column
 // patch (least halo: 18 x 10 staged pixels per 128 outputs); the full-output op
@@ -95,9 +95,12 @@ struct ConvArgs {
     float* out;          // full output (store) or pool partials (pool)
     int N, Cin, H, W, Cout, OH, OW;
     int ncb, RB, CS;
-    long long tpi, base;
-    int rem, J, stages, resident, nacc, tmem_cols;
-    uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;
+    long long tpi;
+    long long num_tiles;  // tiles of the whole call
+    long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
+    int prem, J, stages, resident, nacc, tmem_cols;
+    int pair;             // 1: CTA pairs with M = 256 MMAs (group = 2 tiles); 0: single CTAs
+    uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;   // per CTA of the pair (its half of Cout)
     uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
     int use_tma;         // x staged by TMA boxes + in-warp transpose (else plain loads)
     int* status;
@@ -351,9 +354,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
     }
 }
 
-// Indicator planes for the bias K step: variant v (bit 1: last row block,
-// bit 0: last column strip) marks which of the 128 tile pixels lie inside the
-// output; plane 4 is zero (the second K core matrix).
+// A operand of the bias K step, one 128-row plane per edge variant v (bit 1: the
+// tile is in the last row block, bit 0: in the last column strip) plus a zero
+// plane (the second K core matrix).  A pixel inside the output gets a 1 in the
+// bias columns (fp32: k 0 and k 2 for the two TF32 halves; bf16: k 0); a padding
+// pixel past the image gets a 1 in k 1, whose B entry is the padding value, so
+// its accumulator starts near -1e4 and activates to exactly -0.  CTA pairs share
+// one descriptor for two tiles, so they use plane 0 (all inside) and mask in the
+// epilogue instead.
 template <bool BF16, bool WIDE>
 __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
                                                        int nthreads)
@@ -381,7 +389,35 @@ __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int
     }
 }
 
-template <bool BF16, bool POOL, int ACT>
+// One MMA of the tile group: M = 256 over the CTA pair, or M = 128 in this CTA.
+// (A kernel may use only one of the two tcgen05 CTA-group forms.)
+template <bool BF16, bool PAIR>
+__device__ __forceinline__ void issue_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    if constexpr (BF16 && PAIR) mma_f16_pair(d, ad, bd, idesc, acc);
+    else if constexpr (BF16) mma_f16(d, ad, bd, idesc, acc);
+    else if constexpr (PAIR) mma_tf32_pair(d, ad, bd, idesc, acc);
+    else mma_tf32(d, ad, bd, idesc, acc);
+}
+
+// Bounded wait; barriers that the peer CTA signals need cluster-scope acquire.
+template <bool PAIR>
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                         long long budget)
+{
+    if constexpr (PAIR) return mbar_wait_cluster(bar, parity, abort_flag, status, budget);
+    else return mbar_wait(bar, parity, abort_flag, status, budget);
+}
+
+// Commit this thread's MMAs to `bar` in the CTAs of `mask` (pair) or in this CTA.
+template <bool PAIR>
+__device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
+{
+    if constexpr (PAIR) mma_commit_pair_multicast(bar, mask);
+    else mma_commit(bar);
+}
+
+template <bool BF16, bool POOL, int ACT, bool PAIR>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -391,30 +427,39 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
-    uint64_t* full = bars;         // [4] strip (+ streamed weights) ready
-    uint64_t* empty = bars + 4;    // [4] stage consumed by the MMA
-    uint64_t* wfull = bars + 8;    // bias block (+ resident weights) landed
-    uint64_t* tfull = bars + 9;    // [4] accumulator ready for the epilogue
-    uint64_t* tempty = bars + 13;  // [4] accumulator drained by the epilogue
-    uint64_t* mdone = bars + 17;   // every MMA issued by this CTA completed
+    uint64_t* full = bars;         // [4] leader: both CTAs' stage ready; peer: its own stage ready
+    uint64_t* empty = bars + 4;    // [4] both: stage consumed (multicast commit)
+    uint64_t* wfull = bars + 8;    // both: own bias block (+ resident weights) landed
+    uint64_t* tfull = bars + 9;    // [4] both: accumulator ready (multicast commit)
+    uint64_t* tempty = bars + 13;  // [4] leader: both CTAs' epilogues drained the accumulator
+    uint64_t* mdone = bars + 17;   // leader: every MMA completed
     uint64_t* rawfull = bars + 18; // [4] a producer warp's raw x box landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+    uint64_t* wpeer = bars + 22;   // leader: the peer's bias block (+ resident weights) landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long t_begin = static_cast<long long>(blockIdx.x) * a.base + min(static_cast<int>(blockIdx.x), a.rem);
-    const int n_tiles = static_cast<int>(a.base + (static_cast<int>(blockIdx.x) < a.rem ? 1 : 0));
+    constexpr bool pair = PAIR;
+    const uint32_t rank = pair ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int step = pair ? 2 : 1;                      // tiles per group
+    const int cluster = static_cast<int>(blockIdx.x) / step;
+    const long long p_begin = static_cast<long long>(cluster) * a.pbase + min(cluster, a.prem);
+    const int n_pairs = static_cast<int>(a.pbase + (cluster < a.prem ? 1 : 0));   // groups of this CTA
+    const long long t_first = step * p_begin + rank;   // this CTA's tiles: t_first, t_first + step, ...
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s) {
-            mbar_init(&full[s], 2);            // lane 0: before (with the weight bytes) and after the fill
+            // leader: lane 0 before (weight bytes) and after its fill, plus the peer's forward
+            mbar_init(&full[s], (pair && leader) ? 3 : 2);
             mbar_init(&empty[s], 1);
             mbar_init(&tfull[s], 1);
-            mbar_init(&tempty[s], kEpiWarps);  // lane 0 of each epilogue warp
+            mbar_init(&tempty[s], step * kEpiWarps);   // lane 0 of every epilogue warp of the group
             mbar_init(&rawfull[s], 1);
         }
         mbar_init(wfull, 1);
+        mbar_init(wpeer, 1);
         mbar_init(mdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -425,65 +470,79 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any remote arrive
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const TileCoord first = tile_coord(t_begin, a.tpi, a.CS);
+    const TileCoord first = tile_coord(t_first, a.tpi, a.CS);
 
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kNumProd) {
-        // ------------------------------------------------------------ producers
+        // ------------------------------------------------------------ producers (both CTAs)
         const int pw = warp - kProdWarp0;
+        const uint8_t* wmine = reinterpret_cast<const uint8_t*>(a.wr) + static_cast<size_t>(rank) * a.w_total_bytes;
         if (pw == 0 && lane == 0) {
-            // bias block, plus the whole weight tensor when it stays resident
-            const uint8_t* bias_src = reinterpret_cast<const uint8_t*>(a.wr) + a.w_total_bytes;
+            // own bias block, plus the own half of the weights when they stay resident
+            // workspace: [weights of CTA 0 .. step-1][bias blocks of CTA 0 .. step-1]
+            const uint8_t* bias_src = reinterpret_cast<const uint8_t*>(a.wr) +
+                                      static_cast<size_t>(step) * a.w_total_bytes +
+                                      static_cast<size_t>(rank) * a.bias_block_bytes;
             mbar_arrive_expect_tx(wfull, a.bias_block_bytes + (a.resident ? a.w_total_bytes : 0u));
             bulk_g2s(smem + a.bb_off, bias_src, a.bias_block_bytes, wfull);
-            if (a.resident) bulk_g2s(smem + a.w_off, a.wr, a.w_total_bytes, wfull);
+            if (a.resident) bulk_g2s(smem + a.w_off, wmine, a.w_total_bytes, wfull);
+            if (pair && !leader && mbar_wait(wfull, 0, abort_flag, a.status, a.budget))
+                mbar_arrive_remote(mapa_shared(smem_u32(wpeer), 0));
         }
         if (pw < a.stages) {
-            // this warp owns slot pw and handles stages g = pw, pw + S, pw + 2S, ...
+            // this warp owns slot pw and handles stages g = pw, pw + S, ... of the pair sequence
             const uint32_t slot = static_cast<uint32_t>(pw);
             const uint32_t strip = smem_u32(smem + a.strip_off) + slot * S::STRIP;
             uint8_t* wslot = smem + a.w_off + slot * a.w_block_bytes;
             uint8_t* raw = smem + a.raw_off + slot * RBox::kBytes;
+            const uint32_t full_leader = pair ? mapa_shared(smem_u32(&full[slot]), 0) : 0u;
             TileCoord tc = first;
             int lt = 0, cb = pw;
             while (cb >= a.ncb) {
                 cb -= a.ncb;
                 ++lt;
                 next_tile(tc, a.RB, a.CS);
+                if (pair) next_tile(tc, a.RB, a.CS);
             }
             auto issue_raw = [&](const TileCoord& c, int kb) {
                 mbar_arrive_expect_tx(&rawfull[slot], RBox::kBytes);
                 tma_load_4d(raw, &tmx, &rawfull[slot], c.cs * S::PC, c.rb * S::PR, kb * RBox::kCh, c.n);
             };
-            if (a.use_tma && lt < n_tiles && lane == 0) issue_raw(tc, cb);
+            // a tile past the end (the peer's half of a last, odd pair) is staged as zeros by TMA
+            if (a.use_tma && lt < n_pairs && lane == 0) issue_raw(tc, cb);
             uint32_t use = 0, rph = 0;
-            bool issued_raw = a.use_tma && lt < n_tiles;
-            while (lt < n_tiles) {
-                bool ok = mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.status, a.budget);
+            bool issued_raw = a.use_tma && lt < n_pairs;
+            while (lt < n_pairs) {
+                bool ok = wait_bar<PAIR>(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.status, a.budget);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 fence_proxy_async_smem();
                 if (lane == 0) {
                     if (!a.resident) {
                         mbar_arrive_expect_tx(&full[slot], a.w_block_bytes);
-                        bulk_g2s(wslot, reinterpret_cast<const uint8_t*>(a.wr) + static_cast<size_t>(cb) * a.w_block_bytes,
-                                 a.w_block_bytes, &full[slot]);
+                        bulk_g2s(wslot, wmine + static_cast<size_t>(cb) * a.w_block_bytes, a.w_block_bytes, &full[slot]);
                     } else {
                         mbar_arrive(&full[slot]);
                     }
                 }
-                // the stage after this one for this warp
                 TileCoord ntc = tc;
                 int nlt = lt, ncb = cb + a.stages;
                 while (ncb >= a.ncb) {
                     ncb -= a.ncb;
                     ++nlt;
                     next_tile(ntc, a.RB, a.CS);
+                    if (pair) next_tile(ntc, a.RB, a.CS);
                 }
                 if (a.use_tma) {
                     ok = mbar_wait(&rawfull[slot], rph, abort_flag, a.status, a.budget);
@@ -493,17 +552,25 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     transpose_raw<BF16, WIDE>(smem_u32(raw), strip, lane);
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
-                    if (nlt < n_tiles) {
+                    if (nlt < n_pairs) {
                         if (lane == 0) issue_raw(ntc, ncb);
                         issued_raw = true;
                     }
                 } else {
-                    fill_strip<BF16, WIDE>(strip, a.x, tc.n, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin, a.H, a.W, lane);
+                    fill_strip<BF16, WIDE>(strip, a.x, tc.n < a.N ? tc.n : 0, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin,
+                                           tc.n < a.N ? a.H : 0, a.W, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 // every lane fenced its strip writes and the warp has synchronised
-                if (lane == 0) mbar_arrive(&full[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&full[slot]);
+                    if (pair && !leader) {
+                        // forward "my half of this stage is complete" to the leader
+                        if (!mbar_wait(&full[slot], use & 1u, abort_flag, a.status, a.budget)) break;
+                        mbar_arrive_remote(full_leader);
+                    }
+                }
                 tc = ntc;
                 lt = nlt;
                 cb = ncb;
@@ -516,69 +583,65 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         }
         if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, a.budget);
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, 128, a.Cout);
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (leader && lane == 0) {
+            const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, pair ? 256 : 128, a.Cout);
             // Descriptors are built once; each MMA only moves the start-address field
             // (bits 0-13, 16-byte units).  Every address stays below 256 KB, so the
-            // field never carries into the LBO bits above it.
+            // field never carries into the LBO bits above it.  B holds Cout / 2 rows
+            // in each CTA of a pair (all Cout rows for a single CTA).
+            const uint32_t half_co = static_cast<uint32_t>(a.Cout / step);
             const uint64_t a_desc0 = smem_desc(smem_u32(smem + a.strip_off), S::PLANE, S::SBO, kLayoutNone);
             const uint64_t i_desc0 = smem_desc(smem_u32(smem + a.ind_off), 0u, 128u, kLayoutNone);
-            const uint64_t b_desc0 = smem_desc(smem_u32(smem + a.w_off), static_cast<uint32_t>(a.Cout) * 16u, 128u,
-                                               kLayoutNone);
-            const uint64_t bb_desc = smem_desc(smem_u32(smem + a.bb_off), static_cast<uint32_t>(a.Cout) * 16u, 128u,
-                                               kLayoutNone);
-            const uint32_t wtap16 = 2u * static_cast<uint32_t>(a.Cout);   // one tap of weights, 16-byte units
+            constexpr uint32_t kInd16 = kIndPlane >> 4;
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem + a.w_off), half_co * 16u, 128u, kLayoutNone);
+            const uint64_t bb_desc = smem_desc(smem_u32(smem + a.bb_off), half_co * 16u, 128u, kLayoutNone);
+            const uint32_t wtap16 = 2u * half_co;   // one tap of this CTA's weights, 16-byte units
             const uint32_t wblk16 = a.w_block_bytes >> 4;
             constexpr uint32_t kStrip16 = S::STRIP >> 4;
-            constexpr uint32_t kInd16 = kIndPlane >> 4;
-            bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget);
-            TileCoord tc = first;
+            bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget) &&
+                      (!pair || mbar_wait_cluster(wpeer, 0, abort_flag, a.status, a.budget));
             int acc = 0;
             uint32_t aph = 0, slot = 0, sph = 0;
-            for (int lt = 0; ok && lt < n_tiles; ++lt) {
-                if (!(ok = mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
+            TileCoord tc = first;
+            for (int lt = 0; ok && lt < n_pairs; ++lt) {
+                if (!(ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
-                {
-                    // bias + padding K step (overwrites the accumulator); LBO points at the zero plane
-                    const uint32_t v = (tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u);
-                    const uint64_t ad = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
-                    if constexpr (BF16) mma_f16(d, ad, bb_desc, idesc, 0u);
-                    else mma_tf32(d, ad, bb_desc, idesc, 0u);
-                }
+                // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
+                const uint32_t v = PAIR ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
+                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
+                issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
-                    // Operand readiness needs no tcgen05 fence: the stage barrier (after the
-                    // producers' async-proxy fence, or the bulk copy's complete_tx) orders it.
-                    if (!(ok = mbar_wait(&full[slot], sph, abort_flag, a.status, a.budget))) break;
+                    if (!(ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget))) break;
                     const uint64_t ab = a_desc0 + slot * kStrip16;
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
 #pragma unroll
                     for (int tap = 0; tap < 9; ++tap) {
                         constexpr int kSC = S::SC;
                         const uint32_t aoff = static_cast<uint32_t>((tap / 3) * kSC + (tap % 3));
-                        if constexpr (BF16) mma_f16(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
-                        else mma_tf32(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
+                        issue_mma<BF16, PAIR>(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
                     }
-                    mma_commit(&empty[slot]);
+                    commit_to<PAIR>(&empty[slot], 0x3);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
                         slot = 0;
                         sph ^= 1u;
                     }
                 }
-                if (ok) mma_commit(&tfull[acc]);
+                if (ok) commit_to<PAIR>(&tfull[acc], 0x3);
                 if (++acc == a.nacc) {
                     acc = 0;
                     aph ^= 1u;
                 }
                 next_tile(tc, a.RB, a.CS);
+                if constexpr (PAIR) next_tile(tc, a.RB, a.CS);
             }
-            mma_commit(mdone);
+            commit_to<PAIR>(mdone, 0x1);
             drain_wait(mdone, 0, a.budget);
         }
         __syncwarp();
     } else if (warp < kEpiWarps) {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ epilogue (both CTAs)
         // warp = (lane quarter q, column group h): this warp owns TMEM lanes 32q..32q+31
         // (tile pixels) and the 16-column accumulator slices c = h, h + 4, h + 8, h + 12.
         const int q = warp & 3;
@@ -602,11 +665,25 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
         }
         int cur_n = -1;
+        int slots_written = 0;
         bool ok = true;
 
+        auto record = [&](int slot_index) {
+            return a.out + ((static_cast<size_t>(blockIdx.x) * a.J + static_cast<size_t>(slot_index)) * 4 + q) *
+                               static_cast<size_t>(a.Cout);
+        };
+        auto zero_slot = [&](int sl) {
+            float* dst = record(sl);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = h + 4 * k;
+                if (c < nsub && lane < kEpiCols) dst[c * kEpiCols + lane] = 0.0f;
+            }
+        };
         auto flush = [&](int n_img) {
-            float* dst = a.out + ((static_cast<size_t>(blockIdx.x) * a.J + static_cast<size_t>(n_img - n_first)) * 4 + q) *
-                                     static_cast<size_t>(a.Cout);
+            // images this CTA's every-other-tile sequence stepped over get zero records
+            for (int sl = slots_written; sl < n_img - n_first; ++sl) zero_slot(sl);
+            float* dst = record(n_img - n_first);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = h + 4 * k;
@@ -620,25 +697,31 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 }
                 psum[k] = 0.0f;
             }
+            slots_written = n_img - n_first + 1;
         };
 
         TileCoord tc = first;
         int acc = 0;
         uint32_t aph = 0;
-        for (int lt = 0; lt < n_tiles; ++lt) {
+        for (int lt = 0; lt < n_pairs; ++lt) {
+            const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
             if constexpr (POOL) {
-                if (tc.n != cur_n) {
+                if (real && tc.n != cur_n) {
                     if (cur_n >= 0) flush(cur_n);
                     cur_n = tc.n;
                 }
             }
-            ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.Cout);
+            const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
+            const bool valid = real && oh < a.OH && ow < a.OW;
+            // padding pixels of a single CTA's tile already activate to -0 (padding K column)
+            const bool edge = PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = h + 4 * k;
@@ -647,16 +730,20 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     tmem_ld16(tbase + static_cast<uint32_t>(c * kEpiCols), v);
                     if constexpr (POOL) {
                         if (k < 2 && in_regs) {
+                            if (!edge) {
 #pragma unroll
-                            for (int j = 0; j < kEpiCols; ++j) reg[k][j] += apply_act<ACT>(v[j]);
+                                for (int j = 0; j < kEpiCols; ++j) reg[k][j] += apply_act<ACT>(v[j]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < kEpiCols; ++j) reg[k][j] += valid ? apply_act<ACT>(v[j]) : 0.0f;
+                            }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < kEpiCols; ++j) v[j] = apply_act<ACT>(v[j]);
+                            for (int j = 0; j < kEpiCols; ++j) v[j] = valid ? apply_act<ACT>(v[j]) : 0.0f;
                             psum[k] += warp_transpose_sum16(v, lane);
                         }
                     } else {
-                        const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
-                        if (oh < a.OH && ow < a.OW) {
+                        if (valid) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
@@ -669,43 +756,68 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (lane == 0) {
+                if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+                else mbar_arrive(&tempty[acc]);
+            }
             if (++acc == a.nacc) {
                 acc = 0;
                 aph ^= 1u;
             }
             next_tile(tc, a.RB, a.CS);
+            if (pair) next_tile(tc, a.RB, a.CS);
         }
         if constexpr (POOL) {
-            if (ok && cur_n >= 0) flush(cur_n);
+            if (ok) {
+                if (cur_n >= 0) flush(cur_n);
+                // records of image slots this CTA never reached are zero, so the
+                // combine may add every slot a CTA could have written
+                for (int sl = slots_written; sl < a.J; ++sl) zero_slot(sl);
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the leader's MMAs into both CTAs' tensor memory have completed
+    else __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, static_cast<uint32_t>(a.tmem_cols));
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, static_cast<uint32_t>(a.tmem_cols));
+        else tmem_dealloc(tmem, static_cast<uint32_t>(a.tmem_cols));
     }
 }
 
-template <bool BF16, bool POOL, int ACT>
+template <bool BF16, bool POOL, int ACT, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kConvThreads, smem_bytes, stream>>>(tmx, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kConvThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tmx, a);
 }
 
-// One instantiation per (pool, activation) for the given operand type; defined
-// in fc_conv_tf32.cu and fc_conv_bf16.cu so the variants compile in parallel.
-cudaError_t launch_main_tf32(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes,
-                             cudaStream_t stream);
-cudaError_t launch_main_bf16(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes,
-                             cudaStream_t stream);
+// One instantiation per (pool, activation) for each operand type and CTA grouping;
+// defined in fc_conv_{tf32,bf16}{,_pair}.cu so the variants compile in parallel.
+#define FC_CONV_LAUNCH_DECL(name)                                                                                  \
+    cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, \
+                     cudaStream_t stream)
+FC_CONV_LAUNCH_DECL(launch_main_tf32);
+FC_CONV_LAUNCH_DECL(launch_main_tf32_pair);
+FC_CONV_LAUNCH_DECL(launch_main_bf16);
+FC_CONV_LAUNCH_DECL(launch_main_bf16_pair);
 
 }  // namespace convk
 }  // namespace fc

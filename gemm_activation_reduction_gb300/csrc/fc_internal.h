@@ -30,16 +30,17 @@ struct ConvPlan {
     long long tpi;        // tiles per image = RB * CS
     long long num_tiles;  // N * tpi
     int grid;             // CTAs (persistent)
-    long long base;       // tiles per CTA (the first `rem` CTAs take one more)
-    int rem;
+    int pair;             // CTA pairs (clusters of 2, M = 256 MMAs) instead of single CTAs
+    long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
+    int prem;
     int J;                // image slots per CTA in the pool partial buffer
     int stages;           // shared-memory pipeline depth
     int resident;         // whole re-laid weight tensor kept in shared memory
     int nacc;             // tensor-memory accumulator buffers
     int tmem_cols;        // tensor-memory columns allocated
-    uint32_t w_block_bytes;   // re-laid weights of one K block: 9 taps * 2 halves * Cout * 16 B
-    uint32_t w_total_bytes;   // ncb * w_block_bytes
-    uint32_t bias_block_bytes;  // B operand of the bias K step: 2 halves * Cout * 16 B
+    uint32_t w_block_bytes;   // one CTA's re-laid weights of one K block: 9 taps * 2 halves * (Cout/2) * 16 B
+    uint32_t w_total_bytes;   // ncb * w_block_bytes (one CTA of the pair)
+    uint32_t bias_block_bytes;  // one CTA's B operand of the bias K step: 2 halves * (Cout/2) * 16 B
     uint32_t raw_bytes;       // one TMA box of x per K block (channel-major)
     uint32_t strip_bytes;     // one staged K block, channel-blocked
     int use_tma;              // x rows are 16-byte multiples: stage x with TMA boxes
