@@ -180,7 +180,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
         p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + p->strip_bytes + p->raw_bytes)));
         if (p->stages < 2) return 2;
     }
-    p->nacc = std::min(4, 512 / Cout);
+    p->nacc = std::min(kMaxAcc, 512 / Cout);
     int cols = 32;
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;
@@ -191,8 +191,8 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
     p->bar_off = p->bb_off + p->bias_block_bytes;
     p->bar_off = (p->bar_off + 127u) & ~127u;
-    // barriers (23 x 8 B) + tmem slot + abort flag, plus 1 KB for aligning the base
-    p->smem_bytes = p->bar_off + 256u + 1024u;
+    // barriers + tmem slot + abort flag, plus 1 KB for aligning the base
+    p->smem_bytes = p->bar_off + kBarBytes + 1024u;
     p->ws_weights_bytes = align256(step * (static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes));
     p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
     return 0;

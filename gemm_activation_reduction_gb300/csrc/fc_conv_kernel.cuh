@@ -59,6 +59,8 @@ constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane:
 constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 constexpr uint32_t kResidentMax = 96 * 1024;
+constexpr int kMaxAcc = 8;                               // tensor-memory accumulator ring depth
+constexpr uint32_t kBarBytes = 512;                      // barrier block: 9 + 2 kMaxAcc + 6 barriers, slot, flag
 constexpr uint32_t kSmemBudget = 210 * 1024;
 
 // Output pixels of one 128-row MMA tile.  The pooled ops use a 16-row x 8-column
@@ -430,12 +432,12 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     uint64_t* full = bars;         // [4] leader: both CTAs' stage ready; peer: its own stage ready
     uint64_t* empty = bars + 4;    // [4] both: stage consumed (multicast commit)
     uint64_t* wfull = bars + 8;    // both: own bias block (+ resident weights) landed
-    uint64_t* tfull = bars + 9;    // [4] both: accumulator ready (multicast commit)
-    uint64_t* tempty = bars + 13;  // [4] leader: both CTAs' epilogues drained the accumulator
-    uint64_t* mdone = bars + 17;   // leader: every MMA completed
-    uint64_t* rawfull = bars + 18; // [4] a producer warp's raw x box landed
-    uint64_t* wpeer = bars + 22;   // leader: the peer's bias block (+ resident weights) landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
+    uint64_t* tfull = bars + 9;    // [kMaxAcc] both: accumulator ready (multicast commit)
+    uint64_t* tempty = bars + 9 + kMaxAcc;      // [kMaxAcc] leader: both CTAs' epilogues drained it
+    uint64_t* mdone = bars + 9 + 2 * kMaxAcc;   // leader: every MMA completed
+    uint64_t* rawfull = mdone + 1;              // [4] a producer warp's raw x box landed
+    uint64_t* wpeer = rawfull + 4;              // leader: the peer's bias block (+ resident weights) landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wpeer + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -454,9 +456,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             // leader: lane 0 before (weight bytes) and after its fill, plus the peer's forward
             mbar_init(&full[s], (pair && leader) ? 3 : 2);
             mbar_init(&empty[s], 1);
+            mbar_init(&rawfull[s], 1);
+        }
+        for (int s = 0; s < kMaxAcc; ++s) {
             mbar_init(&tfull[s], 1);
             mbar_init(&tempty[s], step * kEpiWarps);   // lane 0 of every epilogue warp of the group
-            mbar_init(&rawfull[s], 1);
         }
         mbar_init(wfull, 1);
         mbar_init(wpeer, 1);
