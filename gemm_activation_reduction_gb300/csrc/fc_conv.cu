@@ -88,7 +88,7 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
 // `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles step * g + r.
 // Records a CTA never reached hold zeros.
 __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Cout, long long tpi, long long pbase,
-                                         int prem, int J, int step, double inv_count)
+                                         int prem, int J, int step, int recs, double inv_count)
 {
     const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (idx >= static_cast<long long>(N) * Cout) return;
@@ -106,8 +106,8 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
             const long long nf = (step * start_of(c) + r) / tpi;
             const long long slot = n - nf;
             if (slot < 0 || slot >= J) continue;
-            const float* p = ws + ((cta * J + slot) * 4) * static_cast<long long>(Cout) + co;
-            for (int q = 0; q < 4; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
+            const float* p = ws + ((cta * J + slot) * recs) * static_cast<long long>(Cout) + co;
+            for (int q = 0; q < recs; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
         }
     }
     y[idx] = static_cast<float>(s * inv_count);
@@ -151,8 +151,9 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
     p->num_tiles = static_cast<long long>(N) * p->tpi;
-    // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) when the weight
-    // operand dominates the per-MMA fetch, i.e. Cout > 128; single CTAs otherwise.
+    // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) for Cout > 128, where
+    // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
+    // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
     p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
     const int step = p->pair ? 2 : 1;
     // cluster c (a CTA pair, or one CTA) takes a contiguous range of tile groups
@@ -174,19 +175,39 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     // TMA needs 16-byte multiples for every global stride: the row pitch W * esize decides
     p->use_tma = (static_cast<long long>(W) * p->esize) % 16 == 0;
     p->resident = p->w_total_bytes <= kResidentMax;
-    if (p->resident) {
-        p->stages = 4;
-    } else {
-        p->stages = static_cast<int>(std::min<uint32_t>(4u, kSmemBudget / (p->w_block_bytes + p->strip_bytes + p->raw_bytes)));
-        if (p->stages < 2) return 2;
-    }
+    // Shared memory: strips and (streamed) weight blocks per stage, kNumProd x raw_depth
+    // TMA boxes, the indicator planes, the (resident) weights and the bias block.
+    const uint32_t fixed = kIndBytes + p->bias_block_bytes + 128u + (p->resident ? p->w_total_bytes : 0u);
+    const uint32_t per_stage = p->strip_bytes + (p->resident ? 0u : p->w_block_bytes);
+    const uint32_t per_depth = static_cast<uint32_t>(kNumProd) * p->raw_bytes;
+    const uint32_t boxes_min = p->use_tma ? per_depth : 0u;
+    if (fixed + 2u * per_stage + boxes_min > kSmemBudget) return 2;
+    p->stages = static_cast<int>(std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed - boxes_min) / per_stage));
+    // the shared memory left buys TMA look-ahead
+    p->raw_depth = 1;
+    if (p->use_tma)
+        p->raw_depth = static_cast<int>(std::min<uint32_t>(
+            kMaxRawDepth, (kSmemBudget - fixed - static_cast<uint32_t>(p->stages) * per_stage) / per_depth));
+    // pooled sums stay in registers while a warp holds at most two 16-column slices
+    p->inregs = pool && Cout <= 128;
     p->nacc = std::min(kMaxAcc, 512 / Cout);
+    // Epilogue tile groups: as many as keep each warp's slices within what it holds in
+    // registers (two running pool sums, or four slices for the full output) and within
+    // the accumulator ring.
+    const int nsub = Cout / 16;
+    const int max_slices = pool ? 2 : 4;
+    p->egroups = 1;
+    for (int g : {4, 2})
+        if ((nsub + 4 / g - 1) / (4 / g) <= max_slices && g <= p->nacc) {
+            p->egroups = g;
+            break;
+        }
     int cols = 32;
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;
     p->strip_off = 0;
     p->raw_off = p->strip_off + static_cast<uint32_t>(p->stages) * p->strip_bytes;
-    p->ind_off = p->raw_off + static_cast<uint32_t>(p->stages) * p->raw_bytes;
+    p->ind_off = p->raw_off + (p->use_tma ? static_cast<uint32_t>(kNumProd * p->raw_depth) * p->raw_bytes : 0u);
     p->w_off = p->ind_off + kIndBytes;
     p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
     p->bar_off = p->bb_off + p->bias_block_bytes;
@@ -194,7 +215,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     // barriers + tmem slot + abort flag, plus 1 KB for aligning the base
     p->smem_bytes = p->bar_off + kBarBytes + 1024u;
     p->ws_weights_bytes = align256(step * (static_cast<size_t>(p->w_total_bytes) + p->bias_block_bytes));
-    p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * 4 * Cout * sizeof(float)) : 0;
+    p->ws_pool_bytes = pool ? align256(static_cast<size_t>(p->grid) * p->J * p->egroups * 4 * Cout * sizeof(float)) : 0;
     return 0;
 }
 
@@ -243,7 +264,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.OH = p.OH; a.OW = p.OW;
     a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
-    a.stages = p.stages; a.resident = p.resident; a.nacc = p.nacc; a.tmem_cols = p.tmem_cols;
+    a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
     a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.raw_off = p.raw_off;
     a.bar_off = p.bar_off; a.use_tma = p.use_tma;
@@ -251,11 +272,11 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
 
     cudaError_t e;
     if (p.bf16)
-        e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
-                   : launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+        e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_bf16(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream);
     else
-        e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
-                   : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+        e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_tf32(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream);
     if (e != cudaSuccess) return e;
 
     if (p.pool) {
@@ -263,7 +284,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         const int threads = 256;
         const int blocks = static_cast<int>((outs + threads - 1) / threads);
         conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Cout, p.tpi, p.pbase, p.prem, p.J,
-                                                                  p.pair ? 2 : 1,
+                                                                  p.pair ? 2 : 1, 4 * p.egroups,
                                                                   1.0 / (static_cast<double>(p.OH) * p.OW));
         e = cudaGetLastError();
     }

@@ -1,5 +1,6 @@
 // fc_conv_bf16.cu -- the fused conv3x3 kernel instantiated for bf16 inputs on BF16 tensor cores
-// in single CTAs (M = 128 MMAs), one variant per (pool or full output) x (erf-GELU, Mish, Mish twice).
+// in single CTAs (M = 128 MMAs), one variant per (pool with sums in registers, pool with per-tile sums, full output)
+// x (erf-GELU, Mish, Mish twice).
 #include "fc_conv_kernel.cuh"
 
 namespace fc {
@@ -7,15 +8,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_bf16)
 {
-    switch (pool * 3 + act) {
-    case 0: return launch_variant<true, false, 0, false>(tmx, a, grid, smem_bytes, stream);
-    case 1: return launch_variant<true, false, 1, false>(tmx, a, grid, smem_bytes, stream);
-    case 2: return launch_variant<true, false, 2, false>(tmx, a, grid, smem_bytes, stream);
-    case 3: return launch_variant<true, true, 0, false>(tmx, a, grid, smem_bytes, stream);
-    case 4: return launch_variant<true, true, 1, false>(tmx, a, grid, smem_bytes, stream);
-    case 5: return launch_variant<true, true, 2, false>(tmx, a, grid, smem_bytes, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    FC_CONV_LAUNCH_BODY(true, false)
 }
 
 }  // namespace convk

@@ -33,15 +33,17 @@
 // padding pixels, whose GELU / Mish is exactly -0: the epilogue needs no bias
 // loads and no masking.
 //
-// Warp roles (672 threads, one CTA per SM, persistent over a contiguous tile range):
-//   warps 0-15 epilogue: tcgen05.ld of the accumulator (lane quarter = warp % 4,
-//              16-column slices h, h+4, ... with h = warp / 4), activation, then either a running
-//              per-thread sum (pool; reduced across the warp's 32 pixels only
-//              when the image changes) or coalesced stores.
-//   warps 16-19 producers: one shared-memory stage slot each; x arrives as a TMA box
-//              (channel-major, zero-filled past the image) that the warp re-lays
-//              into the staged strip while its next box is in flight.
-//   warp 20    tensor-memory allocator and single-thread MMA issuer.
+// Warp roles (640 threads, one CTA per SM, persistent over a contiguous tile range;
+// 20 warps leave 96 registers per thread):
+//   warps 0-15 epilogue: tcgen05.ld of the accumulator (lane quarter = warp % 4; the
+//              column groups h = warp / 4 form 1, 2 or 4 tile groups that take
+//              alternate tiles), activation, then either a running per-thread sum
+//              (pool; reduced across the warp's 32 pixels only when the image
+//              changes) or coalesced stores.
+//   warps 16-18 producers: stage g goes to warp g % 3 and strip slot g % S; x arrives
+//              as TMA boxes (channel-major, zero-filled past the image), several in
+//              flight per warp, that the warp re-lays into the staged strip.
+//   warp 19    tensor-memory allocator and single-thread MMA issuer.
 #pragma once
 
 #include "fc_ptx.cuh"
@@ -52,7 +54,7 @@ namespace convk {
 constexpr int kEpiWarps = 16;                 // 4 per TMEM lane quarter
 constexpr int kEpiCols = 16;                  // accumulator columns per TMEM load
 constexpr int kProdWarp0 = kEpiWarps;
-constexpr int kNumProd = 4;
+constexpr int kNumProd = 3;
 constexpr int kMmaWarp = kProdWarp0 + kNumProd;
 constexpr int kConvThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
@@ -60,7 +62,11 @@ constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a 
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 constexpr uint32_t kResidentMax = 96 * 1024;
 constexpr int kMaxAcc = 8;                               // tensor-memory accumulator ring depth
-constexpr uint32_t kBarBytes = 512;                      // barrier block: 9 + 2 kMaxAcc + 6 barriers, slot, flag
+constexpr int kMaxRawDepth = 4;                          // raw x boxes per producer warp
+constexpr int kMaxStages = 6;                            // staged strip slots
+// barrier block: 2 kMaxStages + 2 kMaxAcc + kNumProd kMaxRawDepth + 3 barriers, slot, flag
+constexpr uint32_t kBarBytes = 512;
+static_assert((2 * kMaxStages + 2 * kMaxAcc + kNumProd * kMaxRawDepth + 3) * 8 + 8 <= kBarBytes, "barrier block");
 constexpr uint32_t kSmemBudget = 210 * 1024;
 
 // Output pixels of one 128-row MMA tile.  The pooled ops use a 16-row x 8-column
@@ -100,7 +106,8 @@ struct ConvArgs {
     long long tpi;
     long long num_tiles;  // tiles of the whole call
     long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
-    int prem, J, stages, resident, nacc, tmem_cols;
+    int prem, J, stages, raw_depth, resident, nacc, tmem_cols;
+    int egroups;          // epilogue tile groups G (1, 2, 4): group g takes every G-th tile
     int pair;             // 1: CTA pairs with M = 256 MMAs (group = 2 tiles); 0: single CTAs
     uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;   // per CTA of the pair (its half of Cout)
     uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
@@ -123,44 +130,62 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// Exact (erf) GELU, 0.5 z (1 + erf(z / sqrt 2)), with erf from Hastings' rational
-// approximation as printed in Abramowitz & Stegun, Handbook of Mathematical
-// Functions, eq. 7.1.26: for u >= 0, erf(u) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^{-u^2},
-// t = 1 / (1 + p u), |error| <= 1.5e-7.  Here u = |z| / sqrt 2, so p u = (p / sqrt 2) |z|
-// and e^{-u^2} = 2^{-(log2 e / 2) z^2}; erf is odd.  One reciprocal and one
-// exponential (the SFU), eleven FP32 operations.
-__device__ __forceinline__ float gelu_erf(float z)
+// ---------------------------------------------------------------- packed activations
+// The epilogue evaluates two accumulator columns per instruction with Blackwell's paired
+// FP32 arithmetic (fma/mul/add.rn.f32x2: two results per issued instruction, same
+// rounding as the scalar forms); only the SFU steps (reciprocal, exponential) and the
+// absolute value / clamp stay per lane.  The epilogue is issue-bound, so this cuts its
+// instruction count by about 40 %.
+__device__ __forceinline__ float2 splat2(float c) { return make_float2(c, c); }
+
+// 2 GELU(z) for two lanes, GELU the exact (erf) form 0.5 z (1 + erf(z / sqrt 2)).
+// erf is Hastings' rational approximation as printed in Abramowitz & Stegun, Handbook of
+// Mathematical Functions, eq. 7.1.26: for u >= 0, erfc(u) = t q(t) e^{-u^2} with
+// q(t) = a1 + t (a2 + t (a3 + t (a4 + t a5))), t = 1 / (1 + p u), |error| <= 1.5e-7.
+// With a = |z|, u = a / sqrt 2: p u = (p / sqrt 2) a and e^{-u^2} = 2^{-(log2 e / 2) z^2}.
+// erf is odd, so z erf(z / sqrt 2) = a erf(u) and 2 GELU(z) = (z + a) - a erfc(u): no
+// 1 - erf cancellation for negative z (there z + a is exactly 0).  The factor 1/2 is
+// applied by the caller (once per pooled sum, or per stored value), and q is evaluated
+// with negated coefficients so that the last step is one fused multiply-add.
+__device__ __forceinline__ float2 gelu2_doubled(float2 z)
 {
-    const float a = fabsf(z);
-    const float t = rcp_approx(fmaf(0.3275911f * 0.70710678118654752f, a, 1.0f));
-    float q = fmaf(1.061405429f, t, -1.453152027f);
-    q = fmaf(q, t, 1.421413741f);
-    q = fmaf(q, t, -0.284496736f);
-    q = fmaf(q, t, 0.254829592f);
-    const float e = ex2_approx((a * -0.72134752044448170f) * a);
-    const float erf_abs = fmaf(-(q * t), e, 1.0f);
-    const float h = 0.5f * z;
-    return fmaf(h, copysignf(erf_abs, z), h);
+    const float2 a = make_float2(fabsf(z.x), fabsf(z.y));
+    const float2 d = __ffma2_rn(a, splat2(0.3275911f * 0.70710678118654752f), splat2(1.0f));
+    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 q = __ffma2_rn(splat2(-1.061405429f), t, splat2(1.453152027f));
+    q = __ffma2_rn(q, t, splat2(-1.421413741f));
+    q = __ffma2_rn(q, t, splat2(0.284496736f));
+    q = __ffma2_rn(q, t, splat2(-0.254829592f));
+    const float2 w = __fmul2_rn(__fmul2_rn(a, splat2(-0.72134752044448170f)), a);   // -(log2 e / 2) z^2
+    const float2 e = make_float2(ex2_approx(w.x), ex2_approx(w.y));
+    const float2 r = __fmul2_rn(__fmul2_rn(q, t), e);                                // -erfc(a / sqrt 2)
+    return __ffma2_rn(a, r, __fadd2_rn(z, a));
 }
 
-// Mish(z) = z tanh(softplus(z)), with tanh(log(1 + e^z)) = n / (n + 2), n = e^z (e^z + 2).
-// Beyond z = 15 the factor is 1 in fp32 (and n would overflow near z = 44).
-__device__ __forceinline__ float mish(float z)
+// Mish(z) = z tanh(softplus(z)) for two lanes, with tanh(log(1 + e^z)) = n / (n + 2),
+// n = e^z (e^z + 2).  The exponent is clamped at 15, where n / (n + 2) is already 1 in
+// fp32, so that n cannot overflow (it would near z = 44) and no select is needed.
+__device__ __forceinline__ float2 mish2(float2 z)
 {
-    const float e = ex2_approx(z * 1.4426950408889634f);
-    const float n = (e + 2.0f) * e;
-    const float m = z * n * rcp_approx(n + 2.0f);
-    return z > 15.0f ? z : m;
+    const float2 s = __fmul2_rn(make_float2(fminf(z.x, 15.0f), fminf(z.y, 15.0f)), splat2(1.4426950408889634f));
+    const float2 e = make_float2(ex2_approx(s.x), ex2_approx(s.y));
+    const float2 n = __fmul2_rn(__fadd2_rn(e, splat2(2.0f)), e);
+    const float2 d = __fadd2_rn(n, splat2(2.0f));
+    const float2 r = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    return __fmul2_rn(__fmul2_rn(z, n), r);
 }
 
-// Activation codes follow fc_act: 0 erf-GELU, 1 Mish, 2 Mish twice.
+// Activation codes follow fc_act: 0 erf-GELU, 1 Mish, 2 Mish twice.  act2 returns
+// kActScale<ACT>^-1 times the activation: the caller multiplies by kActScale.
 template <int ACT>
-__device__ __forceinline__ float apply_act(float z)
+__device__ __forceinline__ float2 act2(float2 z)
 {
-    if constexpr (ACT == 0) return gelu_erf(z);
-    else if constexpr (ACT == 1) return mish(z);
-    else return mish(mish(z));
+    if constexpr (ACT == 0) return gelu2_doubled(z);
+    else if constexpr (ACT == 1) return mish2(z);
+    else return mish2(mish2(z));
 }
+template <int ACT>
+constexpr float kActScale = ACT == 0 ? 0.5f : 1.0f;
 
 // After the call lane L holds sum over the warp's 32 lanes of v[L] (v is clobbered).
 __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane)
@@ -197,20 +222,42 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane)
     return v[0];
 }
 
-// 16 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// Start loading 16 accumulator columns of this warp's 32 TMEM lanes into r; the
+// registers are valid only after tmem_ld16_wait(r).
+__device__ __forceinline__ void tmem_ld16_start(uint32_t taddr, uint32_t (&r)[16])
 {
-    uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n"
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Wait for this thread's TMEM loads into two 16-register sets (see tmem_ld16_wait).
+__device__ __forceinline__ void tmem_ld16x2_wait(uint32_t (&r)[16], uint32_t (&u)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]), "+r"(u[6]),
+                   "+r"(u[7]), "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]), "+r"(u[12]), "+r"(u[13]),
+                   "+r"(u[14]), "+r"(u[15])
+                 :
+                 : "memory");
+}
+
+// Wait for this thread's TMEM loads.  The registers are read-write operands here, so
+// that the compiler cannot read them between the load and this wait.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // Tile t of the flattened (image, row block, column strip) grid.
@@ -257,6 +304,13 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float2 ld_shared_f2(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
 // Re-lay a landed raw box into the staged strip [group][SPOS pixels][16 B].
 template <bool BF16, bool WIDE>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
@@ -264,21 +318,26 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
     using S = Shape<WIDE>;
     using RB_ = RawBox<BF16, WIDE>;
     if constexpr (!BF16) {
-        // item = (group g, staged pixel s): 4 channels of one pixel -> one 16-byte row
-#pragma unroll 4
-        for (int i = lane; i < 2 * S::SPOS; i += 32) {
-            const int g = i >= S::SPOS ? 1 : 0;
-            const int s = i - g * S::SPOS;
-            const int row = s / S::SC, col = s - (s / S::SC) * S::SC;
+        // item = (group g, staged row, column pair): 4 channels x 2 pixels -> two 16-byte rows
+        static_assert(S::SC % 2 == 0 && RB_::kCols % 2 == 0 && RB_::kChPlane % 8 == 0, "8-byte raw reads");
+        constexpr int kPairs = S::SC / 2;
+        constexpr int kHalf = S::SR * kPairs;
+#pragma unroll 2
+        for (int i = lane; i < 2 * kHalf; i += 32) {
+            const int g = i >= kHalf ? 1 : 0;
+            const int r = i - g * kHalf;
+            const int row = r / kPairs, cp = r - (r / kPairs) * kPairs;
             const uint32_t src = raw + static_cast<uint32_t>(4 * g) * RB_::kChPlane +
-                                 static_cast<uint32_t>(row * RB_::kCols + col) * 4u;
-            const float v0 = __uint_as_float(ld_shared_u32(src));
-            const float v1 = __uint_as_float(ld_shared_u32(src + RB_::kChPlane));
-            const float v2 = __uint_as_float(ld_shared_u32(src + 2 * RB_::kChPlane));
-            const float v3 = __uint_as_float(ld_shared_u32(src + 3 * RB_::kChPlane));
-            st_shared_v4(strip + static_cast<uint32_t>(g) * S::PLANE + static_cast<uint32_t>(s) * 16u,
-                         __float_as_uint(to_tf32(v0)), __float_as_uint(to_tf32(v1)), __float_as_uint(to_tf32(v2)),
-                         __float_as_uint(to_tf32(v3)));
+                                 static_cast<uint32_t>(row * RB_::kCols + 2 * cp) * 4u;
+            float2 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = ld_shared_f2(src + static_cast<uint32_t>(c) * RB_::kChPlane);
+            const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
+                                 static_cast<uint32_t>(row * S::SC + 2 * cp) * 16u;
+            st_shared_v4(dst, __float_as_uint(to_tf32(v[0].x)), __float_as_uint(to_tf32(v[1].x)),
+                         __float_as_uint(to_tf32(v[2].x)), __float_as_uint(to_tf32(v[3].x)));
+            st_shared_v4(dst + 16u, __float_as_uint(to_tf32(v[0].y)), __float_as_uint(to_tf32(v[1].y)),
+                         __float_as_uint(to_tf32(v[2].y)), __float_as_uint(to_tf32(v[3].y)));
         }
     } else {
         // item = (group g, staged row, column pair): 8 channels x 2 columns -> two 16-byte rows
@@ -396,10 +455,21 @@ __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int
 template <bool BF16, bool PAIR>
 __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
 {
-    if constexpr (BF16 && PAIR) mma_f16_pair(d, ad, bd, idesc, acc);
-    else if constexpr (BF16) mma_f16(d, ad, bd, idesc, acc);
-    else if constexpr (PAIR) mma_tf32_pair(d, ad, bd, idesc, acc);
-    else mma_tf32(d, ad, bd, idesc, acc);
+    // Executed by the whole MMA warp: one elected lane issues, and the operands stay
+    // warp-uniform, which keeps the issue loop short when other warps compete for
+    // this sub-partition's issue slots.
+#define FC_MMA_ELECT(GROUP, KIND)                                                                  \
+    asm volatile("{\n\t.reg .pred e, p;\n\t"                                                  \
+                 "elect.sync _|e, 0xffffffff;\n\t"                                              \
+                 "setp.ne.b32 p, %4, 0;\n\t"                                                     \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, p;\n\t}\n" \
+                 ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(acc)                                  \
+                 : "memory")
+    if constexpr (BF16 && PAIR) FC_MMA_ELECT("2", "f16");
+    else if constexpr (BF16) FC_MMA_ELECT("1", "f16");
+    else if constexpr (PAIR) FC_MMA_ELECT("2", "tf32");
+    else FC_MMA_ELECT("1", "tf32");
+#undef FC_MMA_ELECT
 }
 
 // Bounded wait; barriers that the peer CTA signals need cluster-scope acquire.
@@ -415,11 +485,21 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 template <bool PAIR>
 __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
 {
-    if constexpr (PAIR) mma_commit_pair_multicast(bar, mask);
-    else mma_commit(bar);
+    // whole MMA warp; one elected lane commits (its MMAs are the warp's MMAs)
+    if constexpr (PAIR) {
+        asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                     "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}\n"
+                     ::"r"(smem_u32(bar)), "h"(mask)
+                     : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n"
+                     ::"r"(smem_u32(bar))
+                     : "memory");
+    }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool INREGS>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -429,14 +509,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
-    uint64_t* full = bars;         // [4] leader: both CTAs' stage ready; peer: its own stage ready
-    uint64_t* empty = bars + 4;    // [4] both: stage consumed (multicast commit)
-    uint64_t* wfull = bars + 8;    // both: own bias block (+ resident weights) landed
-    uint64_t* tfull = bars + 9;    // [kMaxAcc] both: accumulator ready (multicast commit)
-    uint64_t* tempty = bars + 9 + kMaxAcc;      // [kMaxAcc] leader: both CTAs' epilogues drained it
-    uint64_t* mdone = bars + 9 + 2 * kMaxAcc;   // leader: every MMA completed
-    uint64_t* rawfull = mdone + 1;              // [4] a producer warp's raw x box landed
-    uint64_t* wpeer = rawfull + 4;              // leader: the peer's bias block (+ resident weights) landed
+    uint64_t* full = bars;                  // [kMaxStages] leader: both CTAs' stage ready; peer: its own
+    uint64_t* empty = bars + kMaxStages;    // [kMaxStages] both: stage consumed (multicast commit)
+    uint64_t* wfull = bars + 2 * kMaxStages;   // both: own bias block (+ resident weights) landed
+    uint64_t* tfull = wfull + 1;               // [kMaxAcc] both: accumulator ready (multicast commit)
+    uint64_t* tempty = tfull + kMaxAcc;        // [kMaxAcc] leader: both CTAs' epilogues drained it
+    uint64_t* mdone = tempty + kMaxAcc;        // leader: every MMA completed
+    uint64_t* rawfull = mdone + 1;                      // [kNumProd kMaxRawDepth] a raw x box landed (warp-major)
+    uint64_t* wpeer = rawfull + kNumProd * kMaxRawDepth;   // leader: the peer's bias block (+ resident weights) landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wpeer + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -452,15 +532,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     const long long t_first = step * p_begin + rank;   // this CTA's tiles: t_first, t_first + step, ...
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 4; ++s) {
+        for (int s = 0; s < kMaxStages; ++s) {
             // leader: lane 0 before (weight bytes) and after its fill, plus the peer's forward
             mbar_init(&full[s], (pair && leader) ? 3 : 2);
             mbar_init(&empty[s], 1);
-            mbar_init(&rawfull[s], 1);
         }
+        for (int s = 0; s < kNumProd * kMaxRawDepth; ++s) mbar_init(&rawfull[s], 1);
         for (int s = 0; s < kMaxAcc; ++s) {
             mbar_init(&tfull[s], 1);
-            mbar_init(&tempty[s], step * kEpiWarps);   // lane 0 of every epilogue warp of the group
+            mbar_init(&tempty[s], step * kEpiWarps / a.egroups);   // lane 0 of every epilogue warp of the tile group
         }
         mbar_init(wfull, 1);
         mbar_init(wpeer, 1);
@@ -505,61 +585,73 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             if (pair && !leader && mbar_wait(wfull, 0, abort_flag, a.status, a.budget))
                 mbar_arrive_remote(mapa_shared(smem_u32(wpeer), 0));
         }
-        if (pw < a.stages) {
-            // this warp owns slot pw and handles stages g = pw, pw + S, ... of the pair sequence
-            const uint32_t slot = static_cast<uint32_t>(pw);
-            const uint32_t strip = smem_u32(smem + a.strip_off) + slot * S::STRIP;
-            uint8_t* wslot = smem + a.w_off + slot * a.w_block_bytes;
-            uint8_t* raw = smem + a.raw_off + slot * RBox::kBytes;
-            const uint32_t full_leader = pair ? mapa_shared(smem_u32(&full[slot]), 0) : 0u;
-            TileCoord tc = first;
-            int lt = 0, cb = pw;
-            while (cb >= a.ncb) {
-                cb -= a.ncb;
-                ++lt;
-                next_tile(tc, a.RB, a.CS);
-                if (pair) next_tile(tc, a.RB, a.CS);
-            }
-            auto issue_raw = [&](const TileCoord& c, int kb) {
-                mbar_arrive_expect_tx(&rawfull[slot], RBox::kBytes);
-                tma_load_4d(raw, &tmx, &rawfull[slot], c.cs * S::PC, c.rb * S::PR, kb * RBox::kCh, c.n);
+        {
+            // This warp handles stages g = pw, pw + P, ... of the (tile group, K block)
+            // sequence (P producer warps); stage g fills strip slot g % S.  Its x boxes
+            // rotate through a.raw_depth raw buffers of its own, so that many TMA loads
+            // are in flight ahead of the re-layout.
+            const uint32_t S_ = static_cast<uint32_t>(a.stages);
+            const uint32_t strip0 = smem_u32(smem + a.strip_off);
+            const int rd = a.raw_depth;
+            auto advance = [&](TileCoord& c, int& l, int& kb, int k) {
+                kb += k;
+                while (kb >= a.ncb) {
+                    kb -= a.ncb;
+                    ++l;
+                    next_tile(c, a.RB, a.CS);
+                    if (pair) next_tile(c, a.RB, a.CS);
+                }
             };
+            // raw buffer (and its rawfull barrier) of this warp's i-th stage
+            auto raw_buf = [&](uint32_t i) { return static_cast<uint32_t>(pw * rd) + i % static_cast<uint32_t>(rd); };
+            TileCoord tc = first;
+            int lt = 0, cb = 0;
+            advance(tc, lt, cb, pw);
+            // the issue-ahead position: the next of this warp's stages whose box is not yet requested
+            TileCoord atc = tc;
+            int alt = lt, acb = cb;
+            uint32_t issued = 0;
             // a tile past the end (the peer's half of a last, odd pair) is staged as zeros by TMA
-            if (a.use_tma && lt < n_pairs && lane == 0) issue_raw(tc, cb);
-            uint32_t use = 0, rph = 0;
-            bool issued_raw = a.use_tma && lt < n_pairs;
+            auto issue_next = [&]() {
+                const uint32_t r = raw_buf(issued);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&rawfull[r], RBox::kBytes);
+                    tma_load_4d(smem + a.raw_off + r * RBox::kBytes, &tmx, &rawfull[r], atc.cs * S::PC,
+                                atc.rb * S::PR, acb * RBox::kCh, atc.n);
+                }
+                ++issued;
+                advance(atc, alt, acb, kNumProd);
+            };
+            if (a.use_tma)
+                while (static_cast<int>(issued) < rd && alt < n_pairs) issue_next();
+            uint32_t use = 0;                         // this warp's stages whose box was waited for
+            uint32_t g = static_cast<uint32_t>(pw);   // global stage index
+            long long last_w = -1;                    // stage of this warp's last weight copy
             while (lt < n_pairs) {
-                bool ok = wait_bar<PAIR>(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.status, a.budget);
+                const uint32_t slot = g % S_;
+                const uint32_t par = (g / S_) & 1u;
+                bool ok = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 fence_proxy_async_smem();
                 if (lane == 0) {
                     if (!a.resident) {
+                        last_w = g;
                         mbar_arrive_expect_tx(&full[slot], a.w_block_bytes);
-                        bulk_g2s(wslot, wmine + static_cast<size_t>(cb) * a.w_block_bytes, a.w_block_bytes, &full[slot]);
+                        bulk_g2s(smem + a.w_off + slot * a.w_block_bytes, wmine + static_cast<size_t>(cb) * a.w_block_bytes,
+                                 a.w_block_bytes, &full[slot]);
                     } else {
                         mbar_arrive(&full[slot]);
                     }
                 }
-                TileCoord ntc = tc;
-                int nlt = lt, ncb = cb + a.stages;
-                while (ncb >= a.ncb) {
-                    ncb -= a.ncb;
-                    ++nlt;
-                    next_tile(ntc, a.RB, a.CS);
-                    if (pair) next_tile(ntc, a.RB, a.CS);
-                }
+                const uint32_t strip = strip0 + slot * S::STRIP;
                 if (a.use_tma) {
-                    ok = mbar_wait(&rawfull[slot], rph, abort_flag, a.status, a.budget);
+                    const uint32_t r = raw_buf(use);
+                    ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
-                    rph ^= 1u;
-                    issued_raw = false;
-                    transpose_raw<BF16, WIDE>(smem_u32(raw), strip, lane);
+                    transpose_raw<BF16, WIDE>(smem_u32(smem + a.raw_off + r * RBox::kBytes), strip, lane);
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
-                    if (nlt < n_pairs) {
-                        if (lane == 0) issue_raw(ntc, ncb);
-                        issued_raw = true;
-                    }
+                    if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
                     fill_strip<BF16, WIDE>(strip, a.x, tc.n < a.N ? tc.n : 0, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin,
                                            tc.n < a.N ? a.H : 0, a.W, lane);
@@ -571,24 +663,29 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     mbar_arrive(&full[slot]);
                     if (pair && !leader) {
                         // forward "my half of this stage is complete" to the leader
-                        if (!mbar_wait(&full[slot], use & 1u, abort_flag, a.status, a.budget)) break;
-                        mbar_arrive_remote(full_leader);
+                        if (!mbar_wait(&full[slot], par, abort_flag, a.status, a.budget)) break;
+                        mbar_arrive_remote(mapa_shared(smem_u32(&full[slot]), 0));
                     }
                 }
-                tc = ntc;
-                lt = nlt;
-                cb = ncb;
+                advance(tc, lt, cb, kNumProd);
                 ++use;
+                g += kNumProd;
             }
             if (*abort_flag && lane == 0) {
-                if (!a.resident && use > 0) drain_wait(&full[slot], (use - 1u) & 1u, a.budget);
-                if (issued_raw) drain_wait(&rawfull[slot], rph, a.budget);
+                if (last_w >= 0) {
+                    // the weight copy of this warp's last stage
+                    const uint32_t gl = static_cast<uint32_t>(last_w);
+                    drain_wait(&full[gl % S_], (gl / S_) & 1u, a.budget);
+                }
+                // boxes requested but not yet waited for
+                for (uint32_t i = use; i < issued; ++i)
+                    drain_wait(&rawfull[raw_buf(i)], (i / static_cast<uint32_t>(rd)) & 1u, a.budget);
             }
         }
         if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, a.budget);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (leader)
-        if (leader && lane == 0) {
+        if (leader) {
             const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, pair ? 256 : 128, a.Cout);
             // Descriptors are built once; each MMA only moves the start-address field
             // (bits 0-13, 16-byte units).  Every address stays below 256 KB, so the
@@ -605,11 +702,13 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             constexpr uint32_t kStrip16 = S::STRIP >> 4;
             bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget) &&
                       (!pair || mbar_wait_cluster(wpeer, 0, abort_flag, a.status, a.budget));
+            ok = __all_sync(0xffffffffu, ok);
             int acc = 0;
             uint32_t aph = 0, slot = 0, sph = 0;
             TileCoord tc = first;
             for (int lt = 0; ok && lt < n_pairs; ++lt) {
-                if (!(ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
+                ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
@@ -617,7 +716,9 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
                 issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
-                    if (!(ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget))) break;
+                    ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16;
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
 #pragma unroll
@@ -650,16 +751,26 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         // (tile pixels) and the 16-column accumulator slices c = h, h + 4, h + 8, h + 12.
         const int q = warp & 3;
         const int h = warp >> 2;
+        // The four column groups h split into G tile groups: group gi = h / hw takes the
+        // tiles lt = gi, gi + G, ... of this CTA's sequence (G = 1, 2 or 4; hw = 4 / G),
+        // and within a tile this warp owns the slices c = hh + hw k.  More columns per
+        // warp and tile amortise the per-tile hand-offs; groups on different tiles keep
+        // the pipes busy while others wait.
+        const int G = a.egroups;
+        const int hw = 4 / G;
+        const int gi = h / hw;
+        const int hh = h - gi * hw;
         const int nsub = a.Cout / kEpiCols;
+        const int ms = nsub > hh ? min(4, (nsub - hh + hw - 1) / hw) : 0;   // slices of this warp
         const int r = q * 32 + lane;
         const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const int n_first = first.n;
-        // pool: running per-thread sums over the tiles of one image; with at most two
-        // slices per warp they stay in registers (reg[k][j] for channel
-        // (h + 4k) * 16 + j at this thread's pixel slot) and are reduced across the
-        // warp only when the image changes; otherwise each tile is reduced at once
-        // into psum[k] (lane j < 16 holds channel (h + 4k) * 16 + j).
-        const bool in_regs = nsub <= 2 * (kEpiWarps / 4);
+        // pool: running per-thread sums over the tiles of one image.  With at most two
+        // slices per warp (INREGS: Cout <= 128) they stay in registers (reg[k][j] for
+        // channel (hh + hw k) * 16 + j at this thread's pixel slot) and are reduced
+        // across the warp only when the image changes; otherwise each tile is reduced
+        // at once into psum[k] (lane j < 16 holds channel (hh + hw k) * 16 + j).
+        constexpr bool in_regs = INREGS;
         float reg[2][kEpiCols];
         float psum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if constexpr (POOL) {
@@ -672,42 +783,119 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         int slots_written = 0;
         bool ok = true;
 
+        // pool records: [CTA][image slot][tile group][lane quarter][Cout]
         auto record = [&](int slot_index) {
-            return a.out + ((static_cast<size_t>(blockIdx.x) * a.J + static_cast<size_t>(slot_index)) * 4 + q) *
-                               static_cast<size_t>(a.Cout);
+            return a.out +
+                   (((static_cast<size_t>(blockIdx.x) * a.J + static_cast<size_t>(slot_index)) * G + gi) * 4 + q) *
+                       static_cast<size_t>(a.Cout);
         };
         auto zero_slot = [&](int sl) {
             float* dst = record(sl);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = h + 4 * k;
-                if (c < nsub && lane < kEpiCols) dst[c * kEpiCols + lane] = 0.0f;
+                const int c = hh + hw * k;
+                if (k < ms && lane < kEpiCols) dst[c * kEpiCols + lane] = 0.0f;
             }
         };
         auto flush = [&](int n_img) {
-            // images this CTA's every-other-tile sequence stepped over get zero records
+            // images this warp's every-G-th-tile sequence stepped over get zero records
             for (int sl = slots_written; sl < n_img - n_first; ++sl) zero_slot(sl);
             float* dst = record(n_img - n_first);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = h + 4 * k;
-                if (c < nsub) {
+                const int c = hh + hw * k;
+                if (k < ms) {
                     if (k < 2 && in_regs) {
                         psum[k] = warp_transpose_sum16(reg[k], lane);
 #pragma unroll
                         for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
                     }
-                    if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k];
+                    if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k] * kActScale<ACT>;
                 }
                 psum[k] = 0.0f;
             }
             slots_written = n_img - n_first + 1;
         };
 
+        const int tstep = G * step;   // CTA tiles from one of this warp's tiles to the next
         TileCoord tc = first;
-        int acc = 0;
-        uint32_t aph = 0;
-        for (int lt = 0; lt < n_pairs; ++lt) {
+        for (int i = 0; i < gi * step; ++i) next_tile(tc, a.RB, a.CS);
+        int lt = gi;
+        int acc = gi % a.nacc;
+        uint32_t aph = static_cast<uint32_t>(gi / a.nacc) & 1u;
+        auto taddr = [&](int acc_i, int k) {
+            return tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                   static_cast<uint32_t>(acc_i * a.Cout + (hh + hw * k) * kEpiCols);
+        };
+        // The TMEM load of the next slice is in flight while the current one is
+        // computed; a tile's accumulator is released as soon as its last slice is in
+        // registers.
+        if constexpr (POOL && INREGS) {
+            // Pooled sums in registers (at most two slices per warp): per tile, load both
+            // slices, release the accumulator as soon as they are in registers, then run
+            // all activations as one block -- one load latency and one hand-off per tile,
+            // covered by the other tile groups' math.
+            while (lt < n_pairs) {
+                const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
+                if (real && tc.n != cur_n) {
+                    if (cur_n >= 0) flush(cur_n);
+                    cur_n = tc.n;
+                }
+                const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
+                // padding pixels of a single CTA's tile already activate to -0 (padding K column)
+                const bool add = !(PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1)) ||
+                                 (real && oh < a.OH && ow < a.OW);
+                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                tc_fence_after();
+                uint32_t r0[kEpiCols], r1[kEpiCols];
+                if (ms > 0) tmem_ld16_start(taddr(acc, 0), r0);
+                if (ms > 1) tmem_ld16_start(taddr(acc, 1), r1);
+                tmem_ld16x2_wait(r0, r1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    else mbar_arrive(&tempty[acc]);
+                }
+                if (add && ms == 2) {
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; j += 2) {
+                        const float2 g0 = act2<ACT>(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])));
+                        const float2 g1 = act2<ACT>(make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
+                        const float2 s0 = __fadd2_rn(make_float2(reg[0][j], reg[0][j + 1]), g0);
+                        const float2 s1 = __fadd2_rn(make_float2(reg[1][j], reg[1][j + 1]), g1);
+                        reg[0][j] = s0.x;
+                        reg[0][j + 1] = s0.y;
+                        reg[1][j] = s1.x;
+                        reg[1][j + 1] = s1.y;
+                    }
+                } else if (add && ms == 1) {
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; j += 2) {
+                        const float2 g0 = act2<ACT>(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])));
+                        const float2 s0 = __fadd2_rn(make_float2(reg[0][j], reg[0][j + 1]), g0);
+                        reg[0][j] = s0.x;
+                        reg[0][j + 1] = s0.y;
+                    }
+                }
+                acc += G;
+                while (acc >= a.nacc) {
+                    acc -= a.nacc;
+                    aph ^= 1u;
+                }
+                lt += G;
+                for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
+            }
+        }
+        uint32_t rnext[kEpiCols];
+        if (!(POOL && INREGS) && lt < n_pairs) {
+            ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            if (ok && ms > 0) tmem_ld16_start(taddr(acc, 0), rnext);
+        }
+        while (!(POOL && INREGS) && ok && lt < n_pairs) {
             const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
             if constexpr (POOL) {
                 if (real && tc.n != cur_n) {
@@ -715,35 +903,61 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     cur_n = tc.n;
                 }
             }
-            ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.Cout);
             const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
             // padding pixels of a single CTA's tile already activate to -0 (padding K column)
             const bool edge = PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1);
+            const int nlt = lt + G;
+            int nacc_i = acc + G;
+            uint32_t naph = aph;
+            while (nacc_i >= a.nacc) {
+                nacc_i -= a.nacc;
+                naph ^= 1u;
+            }
+            auto release_and_next = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    else mbar_arrive(&tempty[acc]);
+                }
+                if (nlt < n_pairs) {
+                    ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                    if (ok && ms > 0) tmem_ld16_start(taddr(nacc_i, 0), rnext);
+                }
+            };
+            if (ms == 0) release_and_next();   // no columns here, but the group's phases are kept
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int c = h + 4 * k;
-                if (c < nsub) {
+                if (k < ms) {
+                    const int c = hh + hw * k;
+                    tmem_ld16_wait(rnext);
                     float v[kEpiCols];
-                    tmem_ld16(tbase + static_cast<uint32_t>(c * kEpiCols), v);
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rnext[j]);
+                    if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
+                    else release_and_next();
                     if constexpr (POOL) {
                         if (k < 2 && in_regs) {
-                            if (!edge) {
+                            // padding pixels of pair-mode edge tiles add nothing
+                            if (!edge || valid) {
 #pragma unroll
-                                for (int j = 0; j < kEpiCols; ++j) reg[k][j] += apply_act<ACT>(v[j]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < kEpiCols; ++j) reg[k][j] += valid ? apply_act<ACT>(v[j]) : 0.0f;
+                                for (int j = 0; j < kEpiCols; j += 2) {
+                                    const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
+                                    const float2 acc2 = __fadd2_rn(make_float2(reg[k][j], reg[k][j + 1]), g);
+                                    reg[k][j] = acc2.x;
+                                    reg[k][j + 1] = acc2.y;
+                                }
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < kEpiCols; ++j) v[j] = valid ? apply_act<ACT>(v[j]) : 0.0f;
+                            for (int j = 0; j < kEpiCols; j += 2) {
+                                const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
+                                v[j] = valid ? g.x : 0.0f;
+                                v[j + 1] = valid ? g.y : 0.0f;
+                            }
                             psum[k] += warp_transpose_sum16(v, lane);
                         }
                     } else {
@@ -753,28 +967,25 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
                             // streaming stores: the output is written once and not re-read here
 #pragma unroll
-                            for (int j = 0; j < kEpiCols; ++j) __stcs(o + j * plane, apply_act<ACT>(v[j]));
+                            for (int j = 0; j < kEpiCols; j += 2) {
+                                float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
+                                if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
+                                __stcs(o + j * plane, g.x);
+                                __stcs(o + (j + 1) * plane, g.y);
+                            }
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
-                else mbar_arrive(&tempty[acc]);
-            }
-            if (++acc == a.nacc) {
-                acc = 0;
-                aph ^= 1u;
-            }
-            next_tile(tc, a.RB, a.CS);
-            if (pair) next_tile(tc, a.RB, a.CS);
+            acc = nacc_i;
+            aph = naph;
+            lt = nlt;
+            for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
         }
         if constexpr (POOL) {
             if (ok) {
                 if (cur_n >= 0) flush(cur_n);
-                // records of image slots this CTA never reached are zero, so the
+                // records of image slots this warp never reached are zero, so the
                 // combine may add every slot a CTA could have written
                 for (int sl = slots_written; sl < a.J; ++sl) zero_slot(sl);
             }
@@ -791,11 +1002,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool INREGS>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, INREGS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -813,11 +1024,27 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
     return cudaLaunchKernelEx(&cfg, kern, tmx, a);
 }
 
-// One instantiation per (pool, activation) for each operand type and CTA grouping;
-// defined in fc_conv_{tf32,bf16}{,_pair}.cu so the variants compile in parallel.
-#define FC_CONV_LAUNCH_DECL(name)                                                                                  \
-    cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, \
-                     cudaStream_t stream)
+// One instantiation per (pool with sums in registers or per tile, full output) x activation
+// for each operand type and CTA grouping; defined in fc_conv_{tf32,bf16}{,_pair}.cu so the
+// variants compile in parallel.
+#define FC_CONV_LAUNCH_DECL(name)                                                                       \
+    cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int inregs, int act, int grid, \
+                     uint32_t smem_bytes, cudaStream_t stream)
+
+// The variant switch shared by the four translation units.
+#define FC_CONV_LAUNCH_BODY(BF16, PAIR)                                                                   \
+    switch ((pool ? (inregs ? 0 : 1) : 2) * 3 + act) {                                                   \
+    case 0: return launch_variant<BF16, true, 0, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
+    case 1: return launch_variant<BF16, true, 1, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
+    case 2: return launch_variant<BF16, true, 2, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
+    case 3: return launch_variant<BF16, true, 0, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
+    case 4: return launch_variant<BF16, true, 1, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
+    case 5: return launch_variant<BF16, true, 2, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
+    case 6: return launch_variant<BF16, false, 0, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
+    case 7: return launch_variant<BF16, false, 1, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
+    case 8: return launch_variant<BF16, false, 2, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
+    default: return cudaErrorInvalidValue;                                                              \
+    }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair);
 FC_CONV_LAUNCH_DECL(launch_main_bf16);

@@ -34,9 +34,12 @@ struct ConvPlan {
     long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
     int prem;
     int J;                // image slots per CTA in the pool partial buffer
-    int stages;           // shared-memory pipeline depth
+    int stages;           // shared-memory pipeline depth (staged strips, one producer warp each)
+    int raw_depth;        // TMA boxes of x in flight per producer warp (1 .. 4)
     int resident;         // whole re-laid weight tensor kept in shared memory
     int nacc;             // tensor-memory accumulator buffers
+    int egroups;          // epilogue tile groups (1, 2, 4): each takes every egroups-th tile
+    int inregs;           // pool: per-thread running sums in registers (Cout <= 128)
     int tmem_cols;        // tensor-memory columns allocated
     uint32_t w_block_bytes;   // one CTA's re-laid weights of one K block: 9 taps * 2 halves * (Cout/2) * 16 B
     uint32_t w_total_bytes;   // ncb * w_block_bytes (one CTA of the pair)
