@@ -140,26 +140,26 @@ __device__ __forceinline__ float2 splat2(float c) { return make_float2(c, c); }
 
 // 2 GELU(z) for two lanes, GELU the exact (erf) form 0.5 z (1 + erf(z / sqrt 2)).
 // erf is Hastings' rational approximation as printed in Abramowitz & Stegun, Handbook of
-// Mathematical Functions, eq. 7.1.26: for u >= 0, erfc(u) = t q(t) e^{-u^2} with
+// Mathematical Functions, eq. 7.1.26: for u >= 0, erf(u) = 1 - t q(t) e^{-u^2} with
 // q(t) = a1 + t (a2 + t (a3 + t (a4 + t a5))), t = 1 / (1 + p u), |error| <= 1.5e-7.
-// With a = |z|, u = a / sqrt 2: p u = (p / sqrt 2) a and e^{-u^2} = 2^{-(log2 e / 2) z^2}.
-// erf is odd, so z erf(z / sqrt 2) = a erf(u) and 2 GELU(z) = (z + a) - a erfc(u): no
-// 1 - erf cancellation for negative z (there z + a is exactly 0).  The factor 1/2 is
-// applied by the caller (once per pooled sum, or per stored value), and q is evaluated
-// with negated coefficients so that the last step is one fused multiply-add.
-__device__ __forceinline__ float2 gelu2_doubled(float2 z)
+// With u = |z| / sqrt 2: p u = (p / sqrt 2) |z| and e^{-u^2} = 2^{-(log2 e / 2) z^2}.
+// erf is odd, so z erf(z / sqrt 2) = |z| erf(u) and 2 GELU(z) = z + |z| erf(u): one
+// fused multiply-add after erf.  The factor 1/2 is applied by the caller (once per
+// pooled sum, or per stored value).
+__device__ __forceinline__ float2 gelu2(float2 z)
 {
     const float2 a = make_float2(fabsf(z.x), fabsf(z.y));
     const float2 d = __ffma2_rn(a, splat2(0.3275911f * 0.70710678118654752f), splat2(1.0f));
     const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    float2 q = __ffma2_rn(splat2(-1.061405429f), t, splat2(1.453152027f));
-    q = __ffma2_rn(q, t, splat2(-1.421413741f));
-    q = __ffma2_rn(q, t, splat2(0.284496736f));
-    q = __ffma2_rn(q, t, splat2(-0.254829592f));
-    const float2 w = __fmul2_rn(__fmul2_rn(a, splat2(-0.72134752044448170f)), a);   // -(log2 e / 2) z^2
-    const float2 e = make_float2(ex2_approx(w.x), ex2_approx(w.y));
-    const float2 r = __fmul2_rn(__fmul2_rn(q, t), e);                                // -erfc(a / sqrt 2)
-    return __ffma2_rn(a, r, __fadd2_rn(z, a));
+    float2 q = __ffma2_rn(splat2(1.061405429f), t, splat2(-1.453152027f));
+    q = __ffma2_rn(q, t, splat2(1.421413741f));
+    q = __ffma2_rn(q, t, splat2(-0.284496736f));
+    q = __ffma2_rn(q, t, splat2(0.254829592f));
+    const float2 w = __fmul2_rn(__fmul2_rn(z, z), splat2(0.72134752044448170f));   // (log2 e / 2) z^2
+    const float2 e = make_float2(ex2_approx(-w.x), ex2_approx(-w.y));
+    const float2 tq = __fmul2_rn(q, t);
+    const float2 erfv = __ffma2_rn(make_float2(-tq.x, -tq.y), e, splat2(1.0f));   // erf(|z| / sqrt 2)
+    return __ffma2_rn(a, erfv, z);
 }
 
 // Mish(z) = z tanh(softplus(z)) for two lanes, with tanh(log(1 + e^z)) = n / (n + 2),
@@ -180,7 +180,7 @@ __device__ __forceinline__ float2 mish2(float2 z)
 template <int ACT>
 __device__ __forceinline__ float2 act2(float2 z)
 {
-    if constexpr (ACT == 0) return gelu2_doubled(z);
+    if constexpr (ACT == 0) return gelu2(z);
     else if constexpr (ACT == 1) return mish2(z);
     else return mish2(mish2(z));
 }
