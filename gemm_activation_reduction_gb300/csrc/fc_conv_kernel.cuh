@@ -472,6 +472,42 @@ __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t ad, uint64_t bd, 
 #undef FC_MMA_ELECT
 }
 
+// The nine accumulating MMAs of one K block (the 3 x 3 taps) from one asm block, by one
+// elected lane of the MMA warp: tap (kh, kw) reads A (the staged strip) at start
+// a + (kh * SC + kw) * 16 B and B (this tap's weights) at b + tap * bstep * 16 B.  Issuing
+// them back to back, with all descriptor arithmetic done first, keeps the MMA issue rate
+// close to the tensor rate while the epilogue warps compete for this sub-partition.
+template <bool BF16, bool PAIR, int SC>
+__device__ __forceinline__ void issue_mma9(uint32_t d, uint64_t a, uint64_t b, uint64_t bstep, uint32_t idesc)
+{
+#define FC_MMA9(GROUP, KIND)                                                                              \
+    asm volatile("{\n\t.reg .pred e, p;\n\t"                                                              \
+                 ".reg .b64 a1, a2, a3, a4, a5, a6, a7, a8, b1, b2, b3, b4, b5, b6, b7, b8;\n\t"           \
+                 "setp.ne.b32 p, 1, 0;\n\t"                                                               \
+                 "add.s64 a1, %1, 1;\n\tadd.s64 a2, %1, 2;\n\tadd.s64 a3, %1, %5;\n\tadd.s64 a4, %1, %6;\n\t" \
+                 "add.s64 a5, %1, %7;\n\tadd.s64 a6, %1, %8;\n\tadd.s64 a7, %1, %9;\n\tadd.s64 a8, %1, %10;\n\t" \
+                 "add.s64 b1, %2, %4;\n\tadd.s64 b2, b1, %4;\n\tadd.s64 b3, b2, %4;\n\tadd.s64 b4, b3, %4;\n\t"  \
+                 "add.s64 b5, b4, %4;\n\tadd.s64 b6, b5, %4;\n\tadd.s64 b7, b6, %4;\n\tadd.s64 b8, b7, %4;\n\t"  \
+                 "elect.sync _|e, 0xffffffff;\n\t"                                                        \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a1, b1, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a2, b2, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a3, b3, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a4, b4, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a5, b5, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a6, b6, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a7, b7, %3, p;\n\t"            \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], a8, b8, %3, p;\n\t}\n"         \
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "l"(bstep), "n"(SC), "n"(SC + 1), "n"(SC + 2),       \
+                 "n"(2 * SC), "n"(2 * SC + 1), "n"(2 * SC + 2)                                              \
+                 : "memory")
+    if constexpr (BF16 && PAIR) FC_MMA9("2", "f16");
+    else if constexpr (BF16) FC_MMA9("1", "f16");
+    else if constexpr (PAIR) FC_MMA9("2", "tf32");
+    else FC_MMA9("1", "tf32");
+#undef FC_MMA9
+}
+
 // Bounded wait; barriers that the peer CTA signals need cluster-scope acquire.
 template <bool PAIR>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
@@ -721,12 +757,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16;
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
-#pragma unroll
-                    for (int tap = 0; tap < 9; ++tap) {
-                        constexpr int kSC = S::SC;
-                        const uint32_t aoff = static_cast<uint32_t>((tap / 3) * kSC + (tap % 3));
-                        issue_mma<BF16, PAIR>(d, ab + aoff, bbase + static_cast<uint32_t>(tap) * wtap16, idesc, 1u);
-                    }
+                    issue_mma9<BF16, PAIR, S::SC>(d, ab, bbase, wtap16, idesc);
                     commit_to<PAIR>(&empty[slot], 0x3);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
                         slot = 0;
