@@ -191,11 +191,11 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     // pooled sums stay in registers while a warp holds at most two 16-column slices
     p->inregs = pool && Cout <= 128;
     p->nacc = std::min(kMaxAcc, 512 / Cout);
-    // Epilogue tile groups: as many as keep each warp's slices within what it holds in
-    // registers (two running pool sums, or four slices for the full output) and within
-    // the accumulator ring.
+    // Epilogue tile groups: as many as keep each warp at most four 16-column slices per tile
+    // (the registers its running pool sums or its pipelined loads take) and fit the
+    // accumulator ring.
     const int nsub = Cout / 16;
-    const int max_slices = pool ? 2 : 4;
+    const int max_slices = 4;
     p->egroups = 1;
     for (int g : {4, 2})
         if ((nsub + 4 / g - 1) / (4 / g) <= max_slices && g <= p->nacc) {

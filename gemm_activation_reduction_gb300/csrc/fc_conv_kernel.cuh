@@ -235,6 +235,24 @@ __device__ __forceinline__ void tmem_ld16_start(uint32_t taddr, uint32_t (&r)[16
         : "memory");
 }
 
+// One 16-column accumulator slice of this warp's 32 TMEM lanes in the 16x256b fragment
+// shape: two loads (lane bases +0 and +16) of 16 lanes x 16 columns.  Thread t receives, for
+// lane base L in {0, 16}, r[8L/16 + k]: k = 0, 1 lane L + t/4, columns 2(t%4) + {0, 1};
+// k = 2, 3 lane L + t/4 + 8, the same columns; k = 4..7 the same with columns + 8.  So a
+// thread holds 4 pixels x 4 channels, and can pre-sum its pixels per channel.
+__device__ __forceinline__ void tmem_ld_slice16x256_start(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+                 : "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr + (16u << 16))
+                 : "memory");
+}
+
 // Wait for this thread's TMEM loads into two 16-register sets (see tmem_ld16_wait).
 __device__ __forceinline__ void tmem_ld16x2_wait(uint32_t (&r)[16], uint32_t (&u)[16])
 {
@@ -796,20 +814,17 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         const int r = q * 32 + lane;
         const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const int n_first = first.n;
-        // pool: running per-thread sums over the tiles of one image.  With at most two
-        // slices per warp (INREGS: Cout <= 128) they stay in registers (reg[k][j] for
-        // channel (hh + hw k) * 16 + j at this thread's pixel slot) and are reduced
-        // across the warp only when the image changes; otherwise each tile is reduced
-        // at once into psum[k] (lane j < 16 holds channel (hh + hw k) * 16 + j).
+        // pool: running per-thread sums over the tiles of one image.  INREGS (Cout <= 128):
+        // the 16x256b load shape gives each thread 4 pixels x 4 channels of a slice, so it
+        // keeps 4 sums per slice -- sums[k][0] for channels 2(lane%4) + {0, 1} and sums[k][1]
+        // for 8 + 2(lane%4) + {0, 1} of slice c = hh + hw k -- reduced across the 8 lanes that
+        // share lane%4 only when the image changes.  Otherwise each tile is reduced at once into
+        // psum[k] (lane j < 16 holds channel (hh + hw k) * 16 + j).
         constexpr bool in_regs = INREGS;
-        float reg[2][kEpiCols];
+        float2 sums[4][2];
         float psum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if constexpr (POOL) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
-        }
+        for (int k = 0; k < 4; ++k) sums[k][0] = sums[k][1] = make_float2(0.0f, 0.0f);
         int cur_n = -1;
         int slots_written = 0;
         bool ok = true;
@@ -836,12 +851,25 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             for (int k = 0; k < 4; ++k) {
                 const int c = hh + hw * k;
                 if (k < ms) {
-                    if (k < 2 && in_regs) {
-                        psum[k] = warp_transpose_sum16(reg[k], lane);
+                    if constexpr (in_regs) {
+                        float v4[4] = {sums[k][0].x, sums[k][0].y, sums[k][1].x, sums[k][1].y};
 #pragma unroll
-                        for (int j = 0; j < kEpiCols; ++j) reg[k][j] = 0.0f;
+                        for (int e = 0; e < 4; ++e) {
+                            v4[e] += __shfl_xor_sync(0xffffffffu, v4[e], 4);
+                            v4[e] += __shfl_xor_sync(0xffffffffu, v4[e], 8);
+                            v4[e] += __shfl_xor_sync(0xffffffffu, v4[e], 16);
+                        }
+                        if (lane < 4) {
+                            float* o = dst + c * kEpiCols + 2 * lane;
+                            o[0] = v4[0] * kActScale<ACT>;
+                            o[1] = v4[1] * kActScale<ACT>;
+                            o[8] = v4[2] * kActScale<ACT>;
+                            o[9] = v4[3] * kActScale<ACT>;
+                        }
+                        sums[k][0] = sums[k][1] = make_float2(0.0f, 0.0f);
+                    } else {
+                        if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k] * kActScale<ACT>;
                     }
-                    if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k] * kActScale<ACT>;
                 }
                 psum[k] = 0.0f;
             }
@@ -862,60 +890,87 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         // computed; a tile's accumulator is released as soon as its last slice is in
         // registers.
         if constexpr (POOL && INREGS) {
-            // Pooled sums in registers (at most two slices per warp): per tile, load both
-            // slices, release the accumulator as soon as they are in registers, then run
-            // all activations as one block -- one load latency and one hand-off per tile,
-            // covered by the other tile groups' math.
-            while (lt < n_pairs) {
+            // Pooled sums in registers: the slices of this warp's tiles stream through one
+            // pipeline -- the load of the next slice (of this tile, or slice 0 of the next
+            // tile once this one's accumulator is released) is in flight while the current
+            // slice is evaluated.  One barrier hand-off per tile of up to four slices.
+            auto slice_addr = [&](int acc_i, int k) {
+                return tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                       static_cast<uint32_t>(acc_i * a.Cout + (hh + hw * k) * kEpiCols);
+            };
+            // pixels of this thread in the tile: rows (lane / 4) + {0, 8, 16, 24} of the warp's quarter
+            auto pixel_valid = [&](const TileCoord& c, int j) {
+                const int rr = q * 32 + (lane >> 2) + 8 * j;
+                const int pr_ = rr / S::PC, pc_ = rr - (rr / S::PC) * S::PC;
+                return c.rb * S::PR + pr_ < a.OH && c.cs * S::PC + pc_ < a.OW;
+            };
+            uint32_t cur[kEpiCols], nxt[kEpiCols];
+            if (lt < n_pairs) {
+                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), nxt);
+            }
+            while (ok && lt < n_pairs) {
                 const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
                 if (real && tc.n != cur_n) {
                     if (cur_n >= 0) flush(cur_n);
                     cur_n = tc.n;
                 }
-                const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
-                // padding pixels of a single CTA's tile already activate to -0 (padding K column)
-                const bool add = !(PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1)) ||
-                                 (real && oh < a.OH && ow < a.OW);
-                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
-                if (!(ok = __all_sync(0xffffffffu, ok))) break;
-                tc_fence_after();
-                uint32_t r0[kEpiCols], r1[kEpiCols];
-                if (ms > 0) tmem_ld16_start(taddr(acc, 0), r0);
-                if (ms > 1) tmem_ld16_start(taddr(acc, 1), r1);
-                tmem_ld16x2_wait(r0, r1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
-                    else mbar_arrive(&tempty[acc]);
-                }
-                if (add && ms == 2) {
+                // padding pixels of a single CTA's tile already activate to -0 (padding K column);
+                // CTA pairs mask the edge tiles here
+                float m4[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                if (PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1)) {
 #pragma unroll
-                    for (int j = 0; j < kEpiCols; j += 2) {
-                        const float2 g0 = act2<ACT>(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])));
-                        const float2 g1 = act2<ACT>(make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
-                        const float2 s0 = __fadd2_rn(make_float2(reg[0][j], reg[0][j + 1]), g0);
-                        const float2 s1 = __fadd2_rn(make_float2(reg[1][j], reg[1][j + 1]), g1);
-                        reg[0][j] = s0.x;
-                        reg[0][j + 1] = s0.y;
-                        reg[1][j] = s1.x;
-                        reg[1][j + 1] = s1.y;
+                    for (int j = 0; j < 4; ++j) m4[j] = (real && pixel_valid(tc, j)) ? 1.0f : 0.0f;
+                }
+                const int nlt = lt + G;
+                int nacc_i = acc + G;
+                uint32_t naph = aph;
+                while (nacc_i >= a.nacc) {
+                    nacc_i -= a.nacc;
+                    naph ^= 1u;
+                }
+                auto release_and_next = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+                        else mbar_arrive(&tempty[acc]);
                     }
-                } else if (add && ms == 1) {
+                    if (nlt < n_pairs) {
+                        ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                        ok = __all_sync(0xffffffffu, ok);
+                        tc_fence_after();
+                        if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), nxt);
+                    }
+                };
+                if (ms == 0) release_and_next();   // no columns here, but the group's phases are kept
 #pragma unroll
-                    for (int j = 0; j < kEpiCols; j += 2) {
-                        const float2 g0 = act2<ACT>(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])));
-                        const float2 s0 = __fadd2_rn(make_float2(reg[0][j], reg[0][j + 1]), g0);
-                        reg[0][j] = s0.x;
-                        reg[0][j + 1] = s0.y;
+                for (int k = 0; k < 4; ++k) {
+                    if (k < ms) {
+                        tmem_ld16_wait(nxt);
+#pragma unroll
+                        for (int j = 0; j < kEpiCols; ++j) cur[j] = nxt[j];
+                        if (k + 1 < ms) tmem_ld_slice16x256_start(slice_addr(acc, k + 1), nxt);
+                        else release_and_next();
+                        // cur[8h + 4u + 2p + e]: lane base 16h, pixel (lane / 4) + 16h + 8p, channel
+                        // 8u + 2(lane % 4) + e
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+                            for (int hp = 0; hp < 4; ++hp) {
+                                const int base = 8 * (hp >> 1) + 4 * u + 2 * (hp & 1);
+                                float2 g = act2<ACT>(make_float2(__uint_as_float(cur[base]), __uint_as_float(cur[base + 1])));
+                                if constexpr (PAIR) g = __fmul2_rn(g, splat2(m4[hp]));
+                                sums[k][u] = __fadd2_rn(sums[k][u], g);
+                            }
+                        }
                     }
                 }
-                acc += G;
-                while (acc >= a.nacc) {
-                    acc -= a.nacc;
-                    aph ^= 1u;
-                }
-                lt += G;
+                acc = nacc_i;
+                aph = naph;
+                lt = nlt;
                 for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
             }
         }
@@ -936,8 +991,6 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             }
             const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
-            // padding pixels of a single CTA's tile already activate to -0 (padding K column)
-            const bool edge = PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1);
             const int nlt = lt + G;
             int nacc_i = acc + G;
             uint32_t naph = aph;
@@ -971,26 +1024,13 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
                     else release_and_next();
                     if constexpr (POOL) {
-                        if (k < 2 && in_regs) {
-                            // padding pixels of pair-mode edge tiles add nothing
-                            if (!edge || valid) {
 #pragma unroll
-                                for (int j = 0; j < kEpiCols; j += 2) {
-                                    const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
-                                    const float2 acc2 = __fadd2_rn(make_float2(reg[k][j], reg[k][j + 1]), g);
-                                    reg[k][j] = acc2.x;
-                                    reg[k][j + 1] = acc2.y;
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < kEpiCols; j += 2) {
-                                const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
-                                v[j] = valid ? g.x : 0.0f;
-                                v[j + 1] = valid ? g.y : 0.0f;
-                            }
-                            psum[k] += warp_transpose_sum16(v, lane);
+                        for (int j = 0; j < kEpiCols; j += 2) {
+                            const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
+                            v[j] = valid ? g.x : 0.0f;
+                            v[j + 1] = valid ? g.y : 0.0f;
                         }
+                        psum[k] += warp_transpose_sum16(v, lane);
                     } else {
                         if (valid) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * kEpiCols) * a.OH + oh) *
