@@ -904,12 +904,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const int pr_ = rr / S::PC, pc_ = rr - (rr / S::PC) * S::PC;
                 return c.rb * S::PR + pr_ < a.OH && c.cs * S::PC + pc_ < a.OW;
             };
-            uint32_t cur[kEpiCols], nxt[kEpiCols];
+            // two load buffers, used alternately (slice k of a tile in buf[k & 1]); a tile with an
+            // odd number of slices leaves the next tile's slice 0 in buf[1], moved after its wait
+            uint32_t buf[2][kEpiCols];
             if (lt < n_pairs) {
                 ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), nxt);
+                if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), buf[0]);
             }
             while (ok && lt < n_pairs) {
                 const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
@@ -942,17 +944,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                         ok = __all_sync(0xffffffffu, ok);
                         tc_fence_after();
-                        if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), nxt);
+                        if (ok && ms > 0) {
+                            if (ms & 1) tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), buf[1]);
+                            else tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), buf[0]);
+                        }
                     }
                 };
                 if (ms == 0) release_and_next();   // no columns here, but the group's phases are kept
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     if (k < ms) {
-                        tmem_ld16_wait(nxt);
-#pragma unroll
-                        for (int j = 0; j < kEpiCols; ++j) cur[j] = nxt[j];
-                        if (k + 1 < ms) tmem_ld_slice16x256_start(slice_addr(acc, k + 1), nxt);
+                        uint32_t(&cur)[kEpiCols] = buf[k & 1];
+                        tmem_ld16_wait(cur);
+                        if (k + 1 < ms) tmem_ld_slice16x256_start(slice_addr(acc, k + 1), buf[(k + 1) & 1]);
                         else release_and_next();
                         // cur[8h + 4u + 2p + e]: lane base 16h, pixel (lane / 4) + 16h + 8p, channel
                         // 8u + 2(lane % 4) + e
@@ -967,6 +971,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                             }
                         }
                     }
+                }
+                if ((ms & 1) && ok && nlt < n_pairs) {
+                    tmem_ld16_wait(buf[1]);
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; ++j) buf[0][j] = buf[1][j];
                 }
                 acc = nacc_i;
                 aph = naph;
