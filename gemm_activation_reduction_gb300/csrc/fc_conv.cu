@@ -188,8 +188,6 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     if (p->use_tma)
         p->raw_depth = static_cast<int>(std::min<uint32_t>(
             kMaxRawDepth, (kSmemBudget - fixed - static_cast<uint32_t>(p->stages) * per_stage) / per_depth));
-    // pooled sums stay in registers while a warp holds at most two 16-column slices
-    p->inregs = pool && Cout <= 128;
     p->nacc = std::min(kMaxAcc, 512 / Cout);
     // Epilogue tile groups: as many as keep each warp at most four 16-column slices per tile
     // (the registers its running pool sums or its pipelined loads take) and fit the
@@ -272,11 +270,11 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
 
     cudaError_t e;
     if (p.bf16)
-        e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream)
-                   : launch_main_bf16(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream);
+        e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
     else
-        e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream)
-                   : launch_main_tf32(tmx, a, p.pool, p.inregs, act, p.grid, p.smem_bytes, stream);
+        e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                   : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
     if (e != cudaSuccess) return e;
 
     if (p.pool) {

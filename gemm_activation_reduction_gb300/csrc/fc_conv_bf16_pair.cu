@@ -1,6 +1,5 @@
 // fc_conv_bf16_pair.cu -- the fused conv3x3 kernel instantiated for bf16 inputs on BF16 tensor cores
-// in CTA pairs (M = 256 MMAs), one variant per (pool with sums in registers, pool with per-tile sums, full output)
-// x (erf-GELU, Mish, Mish twice).
+// in CTA pairs (M = 256 MMAs), one variant per (pool or full output) x (erf-GELU, Mish, Mish twice).
 #include "fc_conv_kernel.cuh"
 
 namespace fc {

@@ -187,41 +187,6 @@ __device__ __forceinline__ float2 act2(float2 z)
 template <int ACT>
 constexpr float kActScale = ACT == 0 ? 0.5f : 1.0f;
 
-// After the call lane L holds sum over the warp's 32 lanes of v[L] (v is clobbered).
-__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane)
-{
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool upper = (lane & w) != 0;
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-            const float send = upper ? v[i] : v[i + w];
-            const float keep = upper ? v[i + w] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-    }
-    return v[0];
-}
-
-// 16 values per lane: after the call lane L holds sum over the warp's 32 lanes of
-// v[L % 16] (v is clobbered).
-__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane)
-{
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 16);
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
-        const bool upper = (lane & w) != 0;
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-            const float send = upper ? v[i] : v[i + w];
-            const float keep = upper ? v[i + w] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-    }
-    return v[0];
-}
-
 // Start loading 16 accumulator columns of this warp's 32 TMEM lanes into r; the
 // registers are valid only after tmem_ld16_wait(r).
 __device__ __forceinline__ void tmem_ld16_start(uint32_t taddr, uint32_t (&r)[16])
@@ -553,7 +518,7 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool INREGS>
+template <bool BF16, bool POOL, int ACT, bool PAIR>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -814,15 +779,12 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         const int r = q * 32 + lane;
         const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
         const int n_first = first.n;
-        // pool: running per-thread sums over the tiles of one image.  INREGS (Cout <= 128):
-        // the 16x256b load shape gives each thread 4 pixels x 4 channels of a slice, so it
-        // keeps 4 sums per slice -- sums[k][0] for channels 2(lane%4) + {0, 1} and sums[k][1]
-        // for 8 + 2(lane%4) + {0, 1} of slice c = hh + hw k -- reduced across the 8 lanes that
-        // share lane%4 only when the image changes.  Otherwise each tile is reduced at once into
-        // psum[k] (lane j < 16 holds channel (hh + hw k) * 16 + j).
-        constexpr bool in_regs = INREGS;
+        // pool: running per-thread sums over the tiles of one image.  The 16x256b load shape
+        // gives each thread 4 pixels x 4 channels of a slice, so it keeps 4 sums per slice --
+        // sums[k][0] for channels 2(lane%4) + {0, 1} and sums[k][1] for 8 + 2(lane%4) + {0, 1}
+        // of slice c = hh + hw k -- reduced across the 8 lanes that share lane%4 only when the
+        // image changes.
         float2 sums[4][2];
-        float psum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int k = 0; k < 4; ++k) sums[k][0] = sums[k][1] = make_float2(0.0f, 0.0f);
         int cur_n = -1;
@@ -851,7 +813,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             for (int k = 0; k < 4; ++k) {
                 const int c = hh + hw * k;
                 if (k < ms) {
-                    if constexpr (in_regs) {
+                    {
                         float v4[4] = {sums[k][0].x, sums[k][0].y, sums[k][1].x, sums[k][1].y};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -867,11 +829,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                             o[9] = v4[3] * kActScale<ACT>;
                         }
                         sums[k][0] = sums[k][1] = make_float2(0.0f, 0.0f);
-                    } else {
-                        if (lane < kEpiCols) dst[c * kEpiCols + lane] = psum[k] * kActScale<ACT>;
                     }
                 }
-                psum[k] = 0.0f;
             }
             slots_written = n_img - n_first + 1;
         };
@@ -886,10 +845,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             return tmem + (static_cast<uint32_t>(q * 32) << 16) +
                    static_cast<uint32_t>(acc_i * a.Cout + (hh + hw * k) * kEpiCols);
         };
-        // The TMEM load of the next slice is in flight while the current one is
-        // computed; a tile's accumulator is released as soon as its last slice is in
-        // registers.
-        if constexpr (POOL && INREGS) {
+        if constexpr (POOL) {
             // Pooled sums in registers: the slices of this warp's tiles stream through one
             // pipeline -- the load of the next slice (of this tile, or slice 0 of the next
             // tile once this one's accumulator is released) is in flight while the current
@@ -983,21 +939,18 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
             }
         }
+        // Full output: the next slice's TMEM load is in flight while the current one is
+        // activated and stored; a tile's accumulator is released as soon as its last slice
+        // is in registers.
         uint32_t rnext[kEpiCols];
-        if (!(POOL && INREGS) && lt < n_pairs) {
+        if (!POOL && lt < n_pairs) {
             ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (ok && ms > 0) tmem_ld16_start(taddr(acc, 0), rnext);
         }
-        while (!(POOL && INREGS) && ok && lt < n_pairs) {
+        while (!POOL && ok && lt < n_pairs) {
             const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
-            if constexpr (POOL) {
-                if (real && tc.n != cur_n) {
-                    if (cur_n >= 0) flush(cur_n);
-                    cur_n = tc.n;
-                }
-            }
             const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
             const int nlt = lt + G;
@@ -1032,15 +985,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rnext[j]);
                     if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
                     else release_and_next();
-                    if constexpr (POOL) {
-#pragma unroll
-                        for (int j = 0; j < kEpiCols; j += 2) {
-                            const float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
-                            v[j] = valid ? g.x : 0.0f;
-                            v[j + 1] = valid ? g.y : 0.0f;
-                        }
-                        psum[k] += warp_transpose_sum16(v, lane);
-                    } else {
+                    if constexpr (!POOL) {
                         if (valid) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
@@ -1082,11 +1027,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool INREGS>
+template <bool BF16, bool POOL, int ACT, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, INREGS>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1104,26 +1049,22 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
     return cudaLaunchKernelEx(&cfg, kern, tmx, a);
 }
 
-// One instantiation per (pool with sums in registers or per tile, full output) x activation
-// for each operand type and CTA grouping; defined in fc_conv_{tf32,bf16}{,_pair}.cu so the
-// variants compile in parallel.
-#define FC_CONV_LAUNCH_DECL(name)                                                                       \
-    cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int inregs, int act, int grid, \
-                     uint32_t smem_bytes, cudaStream_t stream)
+// One instantiation per (pool or full output) x activation for each operand type and CTA
+// grouping; defined in fc_conv_{tf32,bf16}{,_pair}.cu so the variants compile in parallel.
+#define FC_CONV_LAUNCH_DECL(name)                                                                                  \
+    cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, \
+                     cudaStream_t stream)
 
 // The variant switch shared by the four translation units.
-#define FC_CONV_LAUNCH_BODY(BF16, PAIR)                                                                   \
-    switch ((pool ? (inregs ? 0 : 1) : 2) * 3 + act) {                                                   \
-    case 0: return launch_variant<BF16, true, 0, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
-    case 1: return launch_variant<BF16, true, 1, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
-    case 2: return launch_variant<BF16, true, 2, PAIR, true>(tmx, a, grid, smem_bytes, stream);           \
-    case 3: return launch_variant<BF16, true, 0, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
-    case 4: return launch_variant<BF16, true, 1, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
-    case 5: return launch_variant<BF16, true, 2, PAIR, false>(tmx, a, grid, smem_bytes, stream);          \
-    case 6: return launch_variant<BF16, false, 0, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
-    case 7: return launch_variant<BF16, false, 1, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
-    case 8: return launch_variant<BF16, false, 2, PAIR, false>(tmx, a, grid, smem_bytes, stream);         \
-    default: return cudaErrorInvalidValue;                                                              \
+#define FC_CONV_LAUNCH_BODY(BF16, PAIR)                                                            \
+    switch ((pool ? 0 : 1) * 3 + act) {                                                           \
+    case 0: return launch_variant<BF16, true, 0, PAIR>(tmx, a, grid, smem_bytes, stream);          \
+    case 1: return launch_variant<BF16, true, 1, PAIR>(tmx, a, grid, smem_bytes, stream);          \
+    case 2: return launch_variant<BF16, true, 2, PAIR>(tmx, a, grid, smem_bytes, stream);          \
+    case 3: return launch_variant<BF16, false, 0, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 4: return launch_variant<BF16, false, 1, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 5: return launch_variant<BF16, false, 2, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    default: return cudaErrorInvalidValue;                                                       \
     }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair);

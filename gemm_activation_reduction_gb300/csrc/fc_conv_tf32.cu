@@ -1,6 +1,5 @@
 // fc_conv_tf32.cu -- the fused conv3x3 kernel instantiated for fp32 inputs on TF32 tensor cores
-// in single CTAs (M = 128 MMAs), one variant per (pool with sums in registers, pool with per-tile sums, full output)
-// x (erf-GELU, Mish, Mish twice).
+// in single CTAs (M = 128 MMAs), one variant per (pool or full output) x (erf-GELU, Mish, Mish twice).
 #include "fc_conv_kernel.cuh"
 
 namespace fc {

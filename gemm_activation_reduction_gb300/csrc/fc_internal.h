@@ -39,7 +39,6 @@ struct ConvPlan {
     int resident;         // whole re-laid weight tensor kept in shared memory
     int nacc;             // tensor-memory accumulator buffers
     int egroups;          // epilogue tile groups (1, 2, 4): each takes every egroups-th tile
-    int inregs;           // pool: per-thread running sums in registers (Cout <= 128)
     int tmem_cols;        // tensor-memory columns allocated
     uint32_t w_block_bytes;   // one CTA's re-laid weights of one K block: 9 taps * 2 halves * (Cout/2) * 16 B
     uint32_t w_total_bytes;   // ncb * w_block_bytes (one CTA of the pair)
