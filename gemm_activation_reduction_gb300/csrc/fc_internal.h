@@ -66,6 +66,7 @@ struct LinearPlan {
     int num_tiles, grid;
     int use_pair;         // CTA pairs with M = 256 MMAs (tcgen05 cta_group::2)
     int m_pairs;          // 256-row blocks in pair mode
+    int bn;               // pair mode: columns per tile (a multiple of 32, <= 256)
     uint32_t smem_bytes;
     size_t ws_bytes;      // (max, sum-exp) partial per row and column tile
 };

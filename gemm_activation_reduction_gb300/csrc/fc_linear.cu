@@ -226,10 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // multicasts its commits to both CTAs' barriers; each CTA's epilogue reads its
 // own 128 accumulator rows and tells the leader through a remote arrive.
 constexpr int kPBM = 128;                                  // rows per CTA (256 per pair)
-constexpr int kPBN = 256;                                  // columns per pair tile
+constexpr int kPBN = 256;                                  // most columns per pair tile
 constexpr int kPStages = 6;
 constexpr uint32_t kPABytes = kPBM * kBK * 4;              // 16 KB
-constexpr uint32_t kPBBytes = (kPBN / 2) * kBK * 4;        // 16 KB (this CTA's half of W)
+constexpr uint32_t kPBBytes = (kPBN / 2) * kBK * 4;        // 16 KB: stage slot for this CTA's half of W
 constexpr uint32_t kPBarOff = kPStages * (kPABytes + kPBBytes);
 constexpr uint32_t kPSmemBytes = kPBarOff + 256 + 1024;
 
@@ -238,6 +238,7 @@ struct LinPairArgs {
     float2* partials;   // [n_blocks][M]
     int M, N, K;
     int m_pairs, n_blocks, k_blocks, num_tiles;
+    int bn;             // columns per pair tile: a multiple of 32, <= kPBN
     float scale, lo, hi;
     int* status;
     long long budget;
@@ -300,11 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = cluster; ok && t < a.num_tiles; t += nclusters) {
                 const int mp = t % a.m_pairs, nb = t / a.m_pairs;
                 const int m0 = mp * 2 * kPBM + static_cast<int>(rank) * kPBM;
-                const int n0 = nb * kPBN + static_cast<int>(rank) * (kPBN / 2);
+                const int n0 = nb * a.bn + static_cast<int>(rank) * (a.bn / 2);
+                const uint32_t b_bytes = static_cast<uint32_t>(a.bn / 2) * kBK * 4u;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPABytes + kPBBytes));
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPABytes + b_bytes));
                     tma_load_2d_pair(sA + stage * kPABytes, &tmx, fbar, kb * kBK, m0);
                     tma_load_2d_pair(sB + stage * kPBBytes, &tmw, fbar, kb * kBK, n0);
                     if (++stage == kPStages) {
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
-            const uint32_t idesc = make_idesc(kFmtTF32, 2 * kPBM, kPBN);
+            const uint32_t idesc = make_idesc(kFmtTF32, 2 * kPBM, a.bn);
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, kLayoutSw128);
             const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, kLayoutSw128);
             int stage = 0;
@@ -373,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPBN);
             float run_m = -INFINITY, run_s = 0.0f;
 #pragma unroll 1
-            for (int c = 0; c < kPBN / 32; ++c) {
+            for (int c = 0; c < a.bn / 32; ++c) {
                 float v[32];
                 tmem_ld32(tbase + static_cast<uint32_t>(c * 32), v);
-                const int n0 = nb * kPBN + c * 32;
+                const int n0 = nb * a.bn + c * 32;
                 float cm = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -480,9 +482,24 @@ int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
     // CTA pairs (M = 256 MMAs) once there is more than one 128-row block
     p->use_pair = M > kBM && sm_count >= 2;
     if (p->use_pair) {
+        // Tile width: the multiple of 32 in [128, 256] that minimises waves x width (ties go to
+        // the wider tile), so that the last wave of pair tiles leaves few clusters idle.
         p->m_pairs = (M + 2 * kPBM - 1) / (2 * kPBM);
-        p->num_tiles = p->m_pairs * p->n_blocks;
-        p->grid = 2 * std::min(p->num_tiles, std::max(sm_count / 2, 1));
+        const long long clusters = std::max(sm_count / 2, 1);
+        long long best = -1;
+        for (int bn = kPBN; bn >= 128; bn -= 32) {
+            const long long tiles = static_cast<long long>(p->m_pairs) * ((Nout + bn - 1) / bn);
+            const long long cost = (tiles + clusters - 1) / clusters * bn;
+            if (best < 0 || cost < best) {
+                best = cost;
+                p->bn = bn;
+            }
+        }
+        p->n_blocks = (Nout + p->bn - 1) / p->bn;
+        const long long ptiles = static_cast<long long>(p->m_pairs) * p->n_blocks;
+        if (ptiles > 0x7FFFFFFFLL) return 2;
+        p->num_tiles = static_cast<int>(ptiles);
+        p->grid = 2 * static_cast<int>(std::min<long long>(p->num_tiles, clusters));
         p->smem_bytes = kPSmemBytes;
     }
     p->ws_bytes = (static_cast<size_t>(p->n_blocks) * M * sizeof(float2) + 255) & ~static_cast<size_t>(255);
@@ -494,13 +511,14 @@ cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, c
 {
     CUtensorMap tmx, tmw;
     if (p.use_pair) {
-        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kPBN / 2))
+        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2))
             return cudaErrorInvalidValue;
         LinPairArgs a{};
         a.bias = b;
         a.partials = reinterpret_cast<float2*>(workspace);
         a.M = p.M; a.N = p.Nout; a.K = p.K;
         a.m_pairs = p.m_pairs; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
+        a.bn = p.bn;
         a.scale = scale; a.lo = lo; a.hi = hi;
         a.status = status; a.budget = budget;
         cudaError_t e = cudaFuncSetAttribute(linear_lse_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -16,8 +16,9 @@
 namespace {
 
 // 1 MiB of scratch, resident on every device that loads the library until the
-// process exits: room for ceil(Nout / 256) * M (max, sum-exp) pairs of 8 bytes,
-// i.e. M * ceil(Nout / 256) <= 131072 (for example M = 1024 with Nout up to 32768).
+// process exits: room for 131072 (max, sum-exp) pairs of 8 bytes, one per row and
+// column tile, i.e. M * ceil(Nout / bn) <= 131072 with bn the planned tile width
+// (128 to 256 columns; M = 1024 with Nout = 8192 needs 37 tiles of 224).
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

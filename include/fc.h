@@ -134,7 +134,8 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
  * Same operator, arguments, limits and errors as fc_linear_lse_mish (fp32
  * only).  Its scratch is a 1 MiB array in device memory that the library
  * holds on every device that loads it, until the process exits; requests
- * needing more (M * ceil(Nout / 256) > 131072) return FC_ERR_UNSUPPORTED.
+ * whose scratch (8 bytes per row and column tile: what fc_workspace_bytes
+ * reports for the same shape) exceeds 1 MiB return FC_ERR_UNSUPPORTED.
  * The call allocates nothing.  The first call on a device looks up that
  * array's device address (a one-time set-up); make that first call before
  * any stream capture.  All calls share the one array: calls that overlap on

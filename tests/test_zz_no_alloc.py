@@ -54,7 +54,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row(cuda_lib):
 def test_noalloc_rejects_requests_beyond_its_static_scratch(cuda_lib):
     import torch
     fn = _noalloc_fn(cuda_lib.load())
-    M, K, Nout = 1024, 4, 40000          # 1024 * ceil(40000 / 256) = 160768 pairs > 131072
+    M, K, Nout = 1024, 4, 40000          # >= 1024 * ceil(40000 / 256) = 160768 pairs of 8 B > 1 MiB
     x = torch.zeros((M, K), device="cuda")
     W = torch.zeros((Nout, K), device="cuda")
     b = torch.zeros(Nout, device="cuda")
