@@ -287,6 +287,14 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float2 ld_shared_f2(uint32_t addr)
 {
     float2 v;
@@ -301,26 +309,34 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
     using S = Shape<WIDE>;
     using RB_ = RawBox<BF16, WIDE>;
     if constexpr (!BF16) {
-        // item = (group g, staged row, column pair): 4 channels x 2 pixels -> two 16-byte rows
-        static_assert(S::SC % 2 == 0 && RB_::kCols % 2 == 0 && RB_::kChPlane % 8 == 0, "8-byte raw reads");
-        constexpr int kPairs = S::SC / 2;
-        constexpr int kHalf = S::SR * kPairs;
+        // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
+        // (the last quad of a row holds SC % 4 staged pixels; the raw box is wider)
+        static_assert(RB_::kCols % 4 == 0 && RB_::kChPlane % 16 == 0, "16-byte raw reads");
+        static_assert(S::SC % 4 == 0 || S::SC % 4 == 2, "a row's last quad holds 4 or 2 staged pixels");
+        constexpr int kQuads = (S::SC + 3) / 4;
+        constexpr int kHalf = S::SR * kQuads;
 #pragma unroll 2
         for (int i = lane; i < 2 * kHalf; i += 32) {
             const int g = i >= kHalf ? 1 : 0;
             const int r = i - g * kHalf;
-            const int row = r / kPairs, cp = r - (r / kPairs) * kPairs;
+            const int row = r / kQuads, cq = r - (r / kQuads) * kQuads;
             const uint32_t src = raw + static_cast<uint32_t>(4 * g) * RB_::kChPlane +
-                                 static_cast<uint32_t>(row * RB_::kCols + 2 * cp) * 4u;
-            float2 v[4];
+                                 static_cast<uint32_t>(row * RB_::kCols + 4 * cq) * 4u;
+            float4 v[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = ld_shared_f2(src + static_cast<uint32_t>(c) * RB_::kChPlane);
+            for (int c = 0; c < 4; ++c) v[c] = ld_shared_f4(src + static_cast<uint32_t>(c) * RB_::kChPlane);
             const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
-                                 static_cast<uint32_t>(row * S::SC + 2 * cp) * 16u;
+                                 static_cast<uint32_t>(row * S::SC + 4 * cq) * 16u;
             st_shared_v4(dst, __float_as_uint(to_tf32(v[0].x)), __float_as_uint(to_tf32(v[1].x)),
                          __float_as_uint(to_tf32(v[2].x)), __float_as_uint(to_tf32(v[3].x)));
             st_shared_v4(dst + 16u, __float_as_uint(to_tf32(v[0].y)), __float_as_uint(to_tf32(v[1].y)),
                          __float_as_uint(to_tf32(v[2].y)), __float_as_uint(to_tf32(v[3].y)));
+            if (4 * cq + 2 < S::SC) {
+                st_shared_v4(dst + 32u, __float_as_uint(to_tf32(v[0].z)), __float_as_uint(to_tf32(v[1].z)),
+                             __float_as_uint(to_tf32(v[2].z)), __float_as_uint(to_tf32(v[3].z)));
+                st_shared_v4(dst + 48u, __float_as_uint(to_tf32(v[0].w)), __float_as_uint(to_tf32(v[1].w)),
+                             __float_as_uint(to_tf32(v[2].w)), __float_as_uint(to_tf32(v[3].w)));
+            }
         }
     } else {
         // item = (group g, staged row, column pair): 8 channels x 2 columns -> two 16-byte rows
