@@ -407,7 +407,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="B", choices=sorted(fc_inputs.WORKLOADS))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E", help="other workloads timed briefly into other_workloads")
+    ap.add_argument("--others", default="C,D,E,Bt", help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -51,7 +51,7 @@ class ConvWorkload:
     W: int
     Cout: int
     dtype: str          # "f32" or "bf16"
-    act: str            # "gelu" | "mish" | "mish_mish"
+    act: str            # "gelu" | "mish" | "mish_mish" | "gelu_tanh"
     pool: bool          # True: global mean to (N, Cout); False: full output
 
     @property
@@ -103,6 +103,10 @@ WORKLOADS = {
     "D": LinearWorkload("linear_lse_mish_f32_1024x8192x8192", 1024, 8192, 8192),
     # bf16 variant of the conv->GELU->pool chain at a tensor-core-bound size.
     "E": ConvWorkload("conv3x3_gelu_avgpool_bf16_32x128x128x128_c256", 32, 128, 128, 128, 256, "bf16", "gelu", True),
+    # The conv->GELU->pool page's tanh-approximate GELU (the variant its trace weighs against
+    # the exact form), at the full problem size.
+    "Bt": ConvWorkload("conv3x3_gelu_tanh_avgpool_f32_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu_tanh",
+                       True),
 }
 
 

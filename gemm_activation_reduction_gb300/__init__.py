@@ -25,7 +25,7 @@ __all__ = [
 
 FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
 FC_F32, FC_BF16 = 0, 1
-ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2}
+ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}
 OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
 # Every symbol include/fc.h declares.

@@ -47,7 +47,8 @@ fc_status conv_common(const void* x, const void* w, const void* b, float* y, int
     if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
     if (N < 1 || Cin < 1 || H < 3 || W < 3 || Cout < 1) return FC_ERR_INVALID_ARG;
     if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
-    if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH) return FC_ERR_INVALID_ARG;
+    if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH && act != FC_ACT_GELU_TANH)
+        return FC_ERR_INVALID_ARG;
     DeviceState* d = nullptr;
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;

@@ -175,14 +175,28 @@ __device__ __forceinline__ float2 mish2(float2 z)
     return __fmul2_rn(__fmul2_rn(z, n), r);
 }
 
-// Activation codes follow fc_act: 0 erf-GELU, 1 Mish, 2 Mish twice.  act2 returns
-// kActScale<ACT>^-1 times the activation: the caller multiplies by kActScale.
+// tanh-approximate GELU for two lanes: 0.5 z (1 + tanh(u)) = z sigma(2u) = z / (1 + e^{-2u}),
+// u = sqrt(2/pi) (z + 0.044715 z^3), with 2u log2 e = z (k + k 0.044715 z^2), k = 2 sqrt(2/pi) log2 e.
+// Far below zero e^{-2u} overflows to inf and the result is -0; far above it is z.
+__device__ __forceinline__ float2 gelu_tanh2(float2 z)
+{
+    constexpr float kK = 2.302208198144325f;
+    constexpr float kK3 = 0.1029432395800235f;   // k * 0.044715
+    const float2 w = __fmul2_rn(__ffma2_rn(__fmul2_rn(z, z), splat2(kK3), splat2(kK)), z);   // 2u log2 e
+    const float2 e = make_float2(ex2_approx(-w.x), ex2_approx(-w.y));
+    const float2 d = __fadd2_rn(e, splat2(1.0f));
+    return __fmul2_rn(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// Activation codes follow fc_act: 0 erf-GELU, 1 Mish, 2 Mish twice, 3 tanh-GELU.  act2
+// returns kActScale<ACT>^-1 times the activation: the caller multiplies by kActScale.
 template <int ACT>
 __device__ __forceinline__ float2 act2(float2 z)
 {
     if constexpr (ACT == 0) return gelu2(z);
     else if constexpr (ACT == 1) return mish2(z);
-    else return mish2(mish2(z));
+    else if constexpr (ACT == 2) return mish2(mish2(z));
+    else return gelu_tanh2(z);
 }
 template <int ACT>
 constexpr float kActScale = ACT == 0 ? 0.5f : 1.0f;
@@ -1073,13 +1087,15 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
 
 // The variant switch shared by the four translation units.
 #define FC_CONV_LAUNCH_BODY(BF16, PAIR)                                                            \
-    switch ((pool ? 0 : 1) * 3 + act) {                                                           \
+    switch ((pool ? 0 : 1) * 4 + act) {                                                           \
     case 0: return launch_variant<BF16, true, 0, PAIR>(tmx, a, grid, smem_bytes, stream);          \
     case 1: return launch_variant<BF16, true, 1, PAIR>(tmx, a, grid, smem_bytes, stream);          \
     case 2: return launch_variant<BF16, true, 2, PAIR>(tmx, a, grid, smem_bytes, stream);          \
-    case 3: return launch_variant<BF16, false, 0, PAIR>(tmx, a, grid, smem_bytes, stream);         \
-    case 4: return launch_variant<BF16, false, 1, PAIR>(tmx, a, grid, smem_bytes, stream);         \
-    case 5: return launch_variant<BF16, false, 2, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 3: return launch_variant<BF16, true, 3, PAIR>(tmx, a, grid, smem_bytes, stream);          \
+    case 4: return launch_variant<BF16, false, 0, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 5: return launch_variant<BF16, false, 1, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 6: return launch_variant<BF16, false, 2, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 7: return launch_variant<BF16, false, 3, PAIR>(tmx, a, grid, smem_bytes, stream);         \
     default: return cudaErrorInvalidValue;                                                       \
     }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);

@@ -57,7 +57,10 @@ typedef enum { FC_F32 = 0, FC_BF16 = 1 } fc_dtype;
 typedef enum {
     FC_ACT_GELU_ERF = 0,      /* 0.5 v (1 + erf(v / sqrt 2)), torch's exact GELU */
     FC_ACT_MISH = 1,          /* v tanh(softplus(v)) */
-    FC_ACT_MISH_MISH = 2      /* mish(mish(v)) */
+    FC_ACT_MISH_MISH = 2,     /* mish(mish(v)) */
+    FC_ACT_GELU_TANH = 3      /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))), torch's
+                                 approximate='tanh' GELU, the variant the Conv->GELU->pool
+                                 page weighs against the exact form */
 } fc_act;
 
 typedef enum {

@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-ACT = {"none": -1, "gelu": 0, "mish": 1, "mish_mish": 2}
+ACT = {"none": -1, "gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}
 
 
 def build(force: bool = False) -> str:

@@ -34,7 +34,16 @@ def mish(z):
     return z * _tanh_pos(_softplus(z))
 
 
-ACTS = {"gelu": gelu, "mish": mish, "mish_mish": lambda v: mish(mish(v)), "none": lambda v: v}
+def gelu_tanh(v):
+    # 0.5 v (1 + tanh(u)) written as the logistic v / (1 + e^{-2u}), u = sqrt(2/pi) (v + 0.044715 v^3)
+    u = math.sqrt(2.0 / math.pi) * (v + 0.044715 * v ** 3)
+    if -2.0 * u > 700.0:
+        return 0.0 * v
+    return v / (1.0 + math.exp(-2.0 * u))
+
+
+ACTS = {"gelu": gelu, "mish": mish, "mish_mish": lambda v: mish(mish(v)), "gelu_tanh": gelu_tanh,
+        "none": lambda v: v}
 
 
 def conv3x3(x, w, b):

@@ -31,7 +31,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_ACT_NONE = -1, ORACLE_ACT_GELU = 0, ORACLE_ACT_MISH = 1, ORACLE_ACT_MISH_MISH = 2 };
+enum { ORACLE_ACT_NONE = -1, ORACLE_ACT_GELU = 0, ORACLE_ACT_MISH = 1, ORACLE_ACT_MISH_MISH = 2, ORACLE_ACT_GELU_TANH = 3 };
 
 /* ---------------------------------------------------------------- pointwise */
 
@@ -39,6 +39,14 @@ enum { ORACLE_ACT_NONE = -1, ORACLE_ACT_GELU = 0, ORACLE_ACT_MISH = 1, ORACLE_AC
  * Conv->GELU->pool page: the trace settles on the erf form after rejecting
  * the tanh approximation as a mismatch. */
 double oracle_gelu(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+
+/* tanh-approximate GELU, torch's approximate='tanh':
+ * 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) -- the variant the Conv->GELU->pool
+ * page's trace weighs (and rejects for that module) against the exact form. */
+double oracle_gelu_tanh(double v)
+{
+    return 0.5 * v * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (v + 0.044715 * v * v * v)));
+}
 
 /* softplus(z) = log(1 + e^z), in the overflow-safe form the Mish page uses:
  * max(z, 0) + log1p(exp(-|z|)). */
@@ -53,6 +61,7 @@ double oracle_act(int act, double v)
     case ORACLE_ACT_GELU: return oracle_gelu(v);
     case ORACLE_ACT_MISH: return oracle_mish(v);
     case ORACLE_ACT_MISH_MISH: return oracle_mish(oracle_mish(v));
+    case ORACLE_ACT_GELU_TANH: return oracle_gelu_tanh(v);
     default: return v;
     }
 }

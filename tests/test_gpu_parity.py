@@ -55,6 +55,8 @@ POOL_SHAPES = [
     (1, 24, 35, 9, 32, "bf16", "gelu"),      # Cin not a multiple of 16
     (2, 5, 21, 26, 48, "f32", "gelu"),       # Cout = 48 (a multiple of 16, not of 32)
     (1, 16, 19, 30, 16, "bf16", "gelu"),     # the smallest Cout, 16
+    (2, 8, 33, 30, 64, "f32", "gelu_tanh"),  # tanh-approximate GELU
+    (1, 40, 17, 19, 256, "bf16", "gelu_tanh"),
 ]
 
 
@@ -75,6 +77,7 @@ ACT_SHAPES = [
     (1, 32, 14, 12, 64, "bf16", "mish_mish"),
     (2, 16, 19, 10, 256, "bf16", "mish"),
     (1, 7, 9, 140, 80, "f32", "mish_mish"),  # Cout = 80; rows wider than one 128-pixel tile
+    (1, 9, 13, 150, 64, "f32", "gelu_tanh"),
 ]
 
 
@@ -111,15 +114,16 @@ def test_linear_small(cuda_lib, shape):
 
 # ------------------------------------------------------------------ full-size workloads
 
-def test_workload_B_full_size_sampled(cuda_lib):
-    wl = fc_inputs.WORKLOADS["B"]
-    d = fc_inputs.workload_inputs("B")
-    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="gelu").cpu().numpy()
+@pytest.mark.parametrize("key", ["B", "Bt"])
+def test_workload_B_full_size_sampled(cuda_lib, key):
+    wl = fc_inputs.WORKLOADS[key]
+    d = fc_inputs.workload_inputs(key)
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act).cpu().numpy()
     rng = np.random.default_rng(7)
     flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 192, replace=False),
                                      np.arange(wl.Cout), np.arange((wl.N - 1) * wl.Cout, wl.N * wl.Cout)]))
-    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, "gelu")
-    _check(y.reshape(-1)[flat], ref, TOL["f32"], "workload B")
+    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
+    _check(y.reshape(-1)[flat], ref, TOL["f32"], f"workload {key}")
 
 
 def test_workload_C_full_size_sampled(cuda_lib):
@@ -220,7 +224,7 @@ def test_watchdog_times_out_and_context_stays_usable(cuda_lib):
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
 
 
-@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish"])
+@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish", "gelu_tanh"])
 def test_activation_accuracy_through_a_delta_kernel(cuda_lib, act):
     """A delta 3x3 kernel makes the pre-activation equal to the input (values on a
     1/64 grid are exact in TF32), so the output is the kernel's activation of

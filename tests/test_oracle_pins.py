@@ -46,6 +46,24 @@ def test_gelu_invariants():
         assert abs(oracle.gelu(-x)) < 1e-14
 
 
+def test_gelu_tanh_pins():
+    """The tanh-approximate GELU: odd part exactly x, limits, slope 1/2 at 0, the independent
+    logistic-form statement in oracle/brute.py, and within 5e-4 of the exact GELU everywhere
+    (the approximation's known accuracy) but not equal to it."""
+    g = lambda v: oracle.act("gelu_tanh", v)
+    assert g(0.0) == 0.0
+    for x in np.linspace(-7, 7, 57):
+        # 0.5 x (1 + tanh u(x)) + 0.5 x (1 + tanh u(-x)) ... u is odd, so g(x) - g(-x) = x
+        assert g(x) - g(-x) == pytest.approx(x, abs=1e-14)
+        assert g(x) == pytest.approx(brute.gelu_tanh(float(x)), rel=1e-13, abs=1e-15)
+    for x in (8.0, 10.0, 30.0):
+        assert abs(g(x) - x) < 1e-12 and abs(g(-x)) < 1e-12
+    h = 1e-6
+    assert (g(h) - g(-h)) / (2 * h) == pytest.approx(0.5, abs=1e-9)
+    dev = max(abs(g(x) - oracle.gelu(x)) for x in np.linspace(-8, 8, 4001))
+    assert 1e-4 < dev < 5e-4
+
+
 # ------------------------------------------------------------------ Mish pins
 
 def _mish_closed_form(z):
@@ -109,7 +127,7 @@ def test_conv_linear_in_weights_and_bias_only_when_w_zero():
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 5, 5, 3), (2, 3, 7, 6, 4)])
-@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish"])
+@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish", "gelu_tanh"])
 def test_conv_act_against_brute_force(shape, act):
     N, Cin, H, W, Cout = shape
     d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, seeds=(21, 22, 23))
