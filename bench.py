@@ -145,6 +145,24 @@ def _dev(torch, a, device):
 
 def make_call(fc, torch, key, d, device):
     wl = fc_inputs.WORKLOADS[key]
+    if isinstance(wl, fc_inputs.EpilogueWorkload):
+        v = _dev(torch, d["v"], device)
+        if wl.kind == "act_map":
+            out = torch.empty(wl.shape, dtype=torch.float32, device=device)
+
+            def call():
+                fc.fc_act_map(v, act=wl.act, out=out)
+        elif wl.kind == "act_mean":
+            out = torch.empty(wl.shape[:-2], dtype=torch.float32, device=device)
+
+            def call():
+                fc.fc_act_mean(v, act=wl.act, out=out)
+        else:
+            out = torch.empty((wl.shape[0], 1), dtype=torch.float32, device=device)
+
+            def call():
+                fc.fc_scale_clamp_lse_mish(v, 2.0, -10.0, 10.0, out=out)
+        return call, 1, out
     if isinstance(wl, fc_inputs.LinearWorkload):
         x, W, b = (_dev(torch, d[k], device) for k in ("x", "W", "b"))
         out = torch.empty((wl.M, 1), dtype=torch.float32, device=device)
@@ -166,6 +184,30 @@ def make_call(fc, torch, key, d, device):
     def call():
         f(x, w, b, act=wl.act, out=out, workspace=ws)
     return call, (3 if wl.pool else 2), out
+
+
+def time_graph(torch, call, reps, replays=5):
+    """ms per call: `reps` calls captured once in a CUDA graph, the graph replayed `replays`
+    times between CUDA events on the current stream; the median replay / reps."""
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / reps)
+    return statistics.median(times)
 
 
 def time_device(torch, call, steps, warmup, dist=None):
@@ -385,12 +427,24 @@ def gpu_arm(args):
             owl = fc_inputs.WORKLOADS[k]
             od = fc_inputs.workload_inputs(k)
             ocall, _, oout = make_call(fc, torch, k, od, device)
-            ot, oper = time_device(torch, ocall, 20, 3)
-            oms = ot / 20
-            opeak, _ = tensor_peak(owl, pk)
-            rl = max(owl.flops() / (opeak * 1e12), owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3
-            others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
-                         "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+            if isinstance(owl, fc_inputs.EpilogueWorkload):
+                # short kernels: 20 calls captured in a CUDA graph and replayed, so that host-side
+                # enqueue time (Python, ctypes) stays out of the device time
+                oms = time_graph(torch, ocall, 20)
+            else:
+                ot, oper = time_device(torch, ocall, 20, 3)
+                oms = ot / 20
+            if isinstance(owl, fc_inputs.EpilogueWorkload):
+                # HBM-bound: the roofline is one pass over the compulsory bytes
+                rl = owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9) * 1e3
+                others[k] = {"workload": owl.name, "ms_per_call": oms,
+                             "gbs": owl.compulsory_bytes() / (oms * 1e-3) / 1e9, "bound": "hbm",
+                             "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+            else:
+                opeak, _ = tensor_peak(owl, pk)
+                rl = max(owl.flops() / (opeak * 1e12), owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3
+                others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
+                             "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
             del od, ocall, oout
             torch.cuda.empty_cache()
         line["other_workloads"] = others
@@ -405,9 +459,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0, help="timed steps (default: about 2 s of device time)")
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="B", choices=sorted(fc_inputs.WORKLOADS))
+    ap.add_argument("--workload", default="B",
+                    choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
+                                   if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt", help="other workloads timed briefly into other_workloads")
+    ap.add_argument("--others", default="C,D,E,Bt,K1e,K2e,K3e",
+                    help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

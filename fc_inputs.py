@@ -90,6 +90,32 @@ class LinearWorkload:
         return (self.M * self.K + self.Nout * self.K + self.Nout) * 4 + self.M * 4
 
 
+@dataclasses.dataclass(frozen=True)
+class EpilogueWorkload:
+    """A standalone epilogue over a computed contraction output (the pages' own kernels):
+    kind "act_mean" (act, then the mean of each trailing (H, W) plane), "act_map" (act
+    elementwise) or "lse_row" (scale, x + x, clamp, row logsumexp, l * mish(l))."""
+    name: str
+    kind: str
+    shape: tuple
+    act: str = "gelu"
+    dtype: str = "f32"
+
+    def flops(self) -> float:
+        return 0.0   # no contraction: these are HBM-bound
+
+    def elements(self) -> int:
+        return int(np.prod(self.shape))
+
+    def compulsory_bytes(self) -> int:
+        es = 4 if self.dtype == "f32" else 2
+        if self.kind == "act_map":
+            return self.elements() * (es + 4)
+        if self.kind == "act_mean":
+            return self.elements() * es + int(np.prod(self.shape[:-2])) * 4
+        return self.elements() * 4 + self.shape[0] * 4
+
+
 # The five workloads of the pages, with the shapes each page states.
 WORKLOADS = {
     # Conv2d->GELU->global-average-pool page (Kimi-K2.6 l2_p67), problem statement,
@@ -107,7 +133,21 @@ WORKLOADS = {
     # the exact form), at the full problem size.
     "Bt": ConvWorkload("conv3x3_gelu_tanh_avgpool_f32_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu_tanh",
                        True),
+    # The pages' epilogue-only kernels at their sizes: over the conv output of the GELU->pool page,
+    # the conv output of the Mish->Mish page, and the Linear output of the Linear page.
+    "K1e": EpilogueWorkload("gelu_avgpool_epilogue_f32_128x64x254x254", "act_mean", (128, 64, 254, 254), "gelu"),
+    "K2e": EpilogueWorkload("mish_mish_epilogue_f32_64x128x254x254", "act_map", (64, 128, 254, 254), "mish_mish"),
+    "K3e": EpilogueWorkload("scale_clamp_lse_mish_rows_f32_1024x8192", "lse_row", (1024, 8192)),
 }
+
+
+def epilogue_inputs(shape, seed=SEED_X, dtype="f32", scale=1.0):
+    """A computed contraction output for the standalone epilogues: N(0, scale^2) fp32 (or its
+    bf16 bits), seeded.  The conv outputs of the workloads are close to N(0, 1/3) before the
+    bias (unit-variance inputs, U(+-1/sqrt(fan_in)) weights), the Linear output likewise."""
+    rng = np.random.default_rng(seed)
+    v = (rng.standard_normal(size=shape, dtype=np.float32) * np.float32(scale)).astype(np.float32)
+    return bf16_bits(v) if dtype == "bf16" else v
 
 
 def conv_inputs(N, Cin, H, W, Cout, dtype="f32", seeds=(SEED_X, SEED_W, SEED_B)):
@@ -141,6 +181,9 @@ def linear_inputs(M, K, Nout, seeds=(SEED_X, SEED_W, SEED_B)):
 
 def workload_inputs(key: str):
     wl = WORKLOADS[key]
+    if isinstance(wl, EpilogueWorkload):
+        # conv / Linear outputs of the workloads have a standard deviation near 0.58
+        return {"v": epilogue_inputs(wl.shape, seed=SEED_X, dtype=wl.dtype, scale=0.58)}
     if isinstance(wl, ConvWorkload):
         return conv_inputs(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.dtype)
     return linear_inputs(wl.M, wl.K, wl.Nout)

@@ -18,7 +18,7 @@ from . import _build
 __all__ = [
     "FCError", "load", "build", "library_path",
     "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
-    "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
+    "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
     "FC_F32", "FC_BF16", "ACTS", "OPS",
 ]
@@ -30,7 +30,7 @@ OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
 # Every symbol include/fc.h declares.
 EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
-           "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
+           "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,13 @@ def load():
         lib.fc_conv3x3_act.restype = I
         lib.fc_linear_lse_mish.argtypes = [P, P, P, P, I, I, I, F, F, F, I, P, S, P]
         lib.fc_linear_lse_mish.restype = I
+        L = ctypes.c_longlong
+        lib.fc_act_map.argtypes = [P, P, L, I, I, P]
+        lib.fc_act_map.restype = I
+        lib.fc_act_mean.argtypes = [P, P, L, L, I, I, P]
+        lib.fc_act_mean.restype = I
+        lib.fc_scale_clamp_lse_mish.argtypes = [P, P, I, I, F, F, F, P]
+        lib.fc_scale_clamp_lse_mish.restype = I
         lib.fc_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.fc_workspace_bytes.restype = S
         lib.fc_status_string.argtypes = [I]
@@ -248,4 +255,69 @@ def fc_linear_lse_mish_noalloc(x, W, b, scale: float = 2.0, clamp_lo: float = -1
         st = fn(x.data_ptr(), W.data_ptr(), b.data_ptr(), out.data_ptr(), M, K, Nout, float(scale),
                 float(clamp_lo), float(clamp_hi), _stream_handle(stream))
     _raise(st, "fc_linear_lse_mish_noalloc")
+    return out
+
+
+def fc_act_map(v, act: str = "mish_mish", out=None, stream=None):
+    """out = act(v) elementwise, fp32 (the elementwise epilogue over a computed conv output)."""
+    torch = _torch()
+    lib = load()
+    _check(v, "v", (torch.float32, torch.bfloat16))
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    else:
+        _check(out, "out", (torch.float32,), v.device)
+        if out.numel() != v.numel():
+            raise ValueError(f"out must hold {v.numel()} values")
+    with torch.cuda.device(v.device):
+        st = lib.fc_act_map(v.data_ptr(), out.data_ptr(), v.numel(), _dtype_code(v), ACTS[act],
+                            _stream_handle(stream))
+    _raise(st, "fc_act_map")
+    return out
+
+
+def fc_act_mean(v, act: str = "gelu", out=None, stream=None):
+    """y[..] = mean over the last two dims of act(v): v (N, C, H, W) -> (N, C) fp32."""
+    torch = _torch()
+    lib = load()
+    _check(v, "v", (torch.float32, torch.bfloat16))
+    if v.dim() < 2:
+        raise ValueError("expected at least two dims (the plane is the last two)")
+    lead = tuple(int(s) for s in v.shape[:-2])
+    planes = 1
+    for s in lead:
+        planes *= s
+    plane = int(v.shape[-2]) * int(v.shape[-1])
+    if out is None:
+        out = torch.empty(lead, dtype=torch.float32, device=v.device)
+    else:
+        _check(out, "out", (torch.float32,), v.device)
+        if out.numel() != planes:
+            raise ValueError(f"out must hold {planes} values")
+    with torch.cuda.device(v.device):
+        st = lib.fc_act_mean(v.data_ptr(), out.data_ptr(), planes, plane, _dtype_code(v), ACTS[act],
+                             _stream_handle(stream))
+    _raise(st, "fc_act_mean")
+    return out
+
+
+def fc_scale_clamp_lse_mish(t, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0, out=None,
+                            stream=None):
+    """y[M, 1] = l * mish(l), l = logsumexp_j clamp(t * scale + t * scale) for a computed t [M, N] fp32."""
+    torch = _torch()
+    lib = load()
+    _check(t, "t", (torch.float32,))
+    if t.dim() != 2:
+        raise ValueError("expected t [M, N]")
+    M, N = (int(s) for s in t.shape)
+    if out is None:
+        out = torch.empty((M, 1), dtype=torch.float32, device=t.device)
+    else:
+        _check(out, "out", (torch.float32,), t.device)
+        if out.numel() != M:
+            raise ValueError(f"out must hold {M} values")
+    with torch.cuda.device(t.device):
+        st = lib.fc_scale_clamp_lse_mish(t.data_ptr(), out.data_ptr(), M, N, float(scale), float(clamp_lo),
+                                         float(clamp_hi), _stream_handle(stream))
+    _raise(st, "fc_scale_clamp_lse_mish")
     return out

@@ -136,6 +136,51 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
+namespace {
+bool valid_act(fc_act act)
+{
+    return act == FC_ACT_GELU_ERF || act == FC_ACT_MISH || act == FC_ACT_MISH_MISH || act == FC_ACT_GELU_TANH;
+}
+}  // namespace
+
+fc_status fc_act_map(const void* v, float* out, long long n, fc_dtype dtype, fc_act act, fc_stream_t stream)
+{
+    if (!v || !out || !aligned16(v) || !aligned16(out)) return FC_ERR_INVALID_ARG;
+    if (n < 0 || (dtype != FC_F32 && dtype != FC_BF16) || !valid_act(act)) return FC_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    cudaError_t e = fc::act_map_launch(v, out, n, dtype == FC_BF16, static_cast<int>(act), d->sm_count,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
+fc_status fc_act_mean(const void* v, float* y, long long planes, long long plane_size, fc_dtype dtype, fc_act act,
+                      fc_stream_t stream)
+{
+    if (!v || !y || !aligned16(v) || !aligned16(y)) return FC_ERR_INVALID_ARG;
+    if (planes < 1 || planes > 0x7FFFFFFFLL || plane_size < 1) return FC_ERR_INVALID_ARG;
+    if ((dtype != FC_F32 && dtype != FC_BF16) || !valid_act(act)) return FC_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    cudaError_t e = fc::act_mean_launch(v, y, planes, plane_size, dtype == FC_BF16, static_cast<int>(act),
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
+fc_status fc_scale_clamp_lse_mish(const float* t, float* y, int M, int N, float scale, float clamp_lo,
+                                  float clamp_hi, fc_stream_t stream)
+{
+    if (!t || !y || !aligned16(t) || !aligned16(y)) return FC_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || !(clamp_lo <= clamp_hi)) return FC_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    cudaError_t e = fc::lse_row_launch(t, y, M, N, scale, clamp_lo, clamp_hi, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
+}
+
 size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int cout_or_nout, fc_dtype dtype)
 {
     DeviceState* d = nullptr;

@@ -71,6 +71,12 @@ struct LinearPlan {
     size_t ws_bytes;      // (max, sum-exp) partial per row and column tile
 };
 
+// Standalone epilogues over a computed contraction output (fc_epilogue.cu).
+cudaError_t act_map_launch(const void* v, float* out, long long n, int bf16, int act, int sm_count, cudaStream_t st);
+cudaError_t act_mean_launch(const void* v, float* y, long long planes, long long plane, int bf16, int act,
+                            cudaStream_t st);
+cudaError_t lse_row_launch(const float* t, float* out, int M, int N, float scale, float lo, float hi, cudaStream_t st);
+
 int linear_plan(LinearPlan* plan, int M, int K, int Nout, int sm_count);
 
 cudaError_t linear_launch(const LinearPlan& plan, const float* x, const float* W, const float* b, float* y,

@@ -127,6 +127,32 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
                              void* workspace, size_t workspace_bytes, fc_stream_t stream);
 
 /*
+ * The pages' epilogue-only kernels, for a contraction computed elsewhere (each
+ * page's own deliverable is such a kernel run after cuDNN / cuBLAS).  Inputs are
+ * the contraction's output with the bias already added; fp32 or bf16 input (for
+ * fc_scale_clamp_lse_mish fp32), fp32 output; all pointers device memory, 16-byte
+ * aligned, caller-owned; asynchronous on `stream`; no workspace.
+ *
+ * fc_act_map: out[i] = act(v[i]) for i < n (Conv->Mish->Mish page, its
+ *   elementwise Mish-twice kernel; any fc_act).  n == 0 does nothing.
+ * fc_act_mean: y[p] = mean over i < plane_size of act(v[p * plane_size + i]) for
+ *   p < planes: the (H, W) plane mean of an NCHW tensor with planes = N * C
+ *   (Conv->GELU->pool page, its fused GELU + global-average-pool kernel).
+ *   Requires 1 <= planes <= 2^31 - 1, plane_size >= 1.
+ * fc_scale_clamp_lse_mish: for each row m < M of t (M x N, row-major),
+ *   u = clamp(t * scale + t * scale, clamp_lo, clamp_hi), l = logsumexp_j u_j,
+ *   y[m] = l * mish(l) (Linear page, its row kernel).  Requires 1 <= M <= 2^31 - 1,
+ *   N >= 1, clamp_lo <= clamp_hi.
+ * Errors: FC_ERR_INVALID_ARG for null or misaligned pointers, bad sizes or
+ * enums; FC_ERR_CUDA if a launch fails.
+ */
+fc_status fc_act_map(const void* v, float* out, long long n, fc_dtype dtype, fc_act act, fc_stream_t stream);
+fc_status fc_act_mean(const void* v, float* y, long long planes, long long plane_size, fc_dtype dtype, fc_act act,
+                      fc_stream_t stream);
+fc_status fc_scale_clamp_lse_mish(const float* t, float* y, int M, int N, float scale, float clamp_lo,
+                                  float clamp_hi, fc_stream_t stream);
+
+/*
  * fc_linear_lse_mish without a workspace argument, for callers that cannot
  * allocate device memory: code whose device memory belongs to another
  * allocator or a fixed budget, C hosts with no allocator of their own, or

@@ -55,6 +55,12 @@ def _load():
             getattr(lib, name).restype = D
         lib.oracle_act.argtypes = [I, D]
         lib.oracle_act.restype = D
+        lib.oracle_act_map.argtypes = [P, P, L, I]
+        lib.oracle_act_map.restype = None
+        lib.oracle_act_mean.argtypes = [P, P, L, L, I]
+        lib.oracle_act_mean.restype = None
+        lib.oracle_scale_clamp_lse_mish_rows.argtypes = [P, I, I, D, D, D, P]
+        lib.oracle_scale_clamp_lse_mish_rows.restype = I
         lib.oracle_conv3x3_point.argtypes = [P, P, P, I, I, I, I, I, I, I]
         lib.oracle_conv3x3_point.restype = D
         lib.oracle_conv3x3_preact.argtypes = [P, P, P, P, I, I, I, I, I]
@@ -105,6 +111,36 @@ def mish(v: float) -> float:
 
 def act(name: str, v: float) -> float:
     return _load().oracle_act(ACT[name], float(v))
+
+
+def act_map(v, act: str) -> np.ndarray:
+    """act applied elementwise (the Conv->Mish->Mish page's elementwise epilogue), fp64."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.float64)
+    _load().oracle_act_map(_p(v), _p(out), v.size, ACT[act])
+    return out
+
+
+def act_mean(v, act: str) -> np.ndarray:
+    """Mean of act over each trailing (H, W) plane of v (N, C, H, W) -> (N, C), fp64 (the
+    Conv->GELU->pool page's fused GELU + global-average-pool epilogue)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    planes = int(np.prod(v.shape[:-2]))
+    plane = int(v.shape[-2] * v.shape[-1])
+    out = np.empty(v.shape[:-2], np.float64)
+    _load().oracle_act_mean(_p(v), _p(out), planes, plane, ACT[act])
+    return out
+
+
+def scale_clamp_lse_mish(y, scale=2.0, lo=-10.0, hi=10.0) -> np.ndarray:
+    """The Linear page's row kernel on a computed (M, N) output: t = clamp(2 scale y, lo, hi),
+    l = logsumexp_row(t), out (M, 1) = l * mish(l), fp64."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    M, N = y.shape
+    out = np.empty((M, 1), np.float64)
+    if _load().oracle_scale_clamp_lse_mish_rows(_p(y), M, N, float(scale), float(lo), float(hi), _p(out)) != 0:
+        raise MemoryError("oracle scratch")
+    return out
 
 
 def logsumexp(t) -> float:

@@ -232,6 +232,60 @@ int oracle_linear_lse_mish_rows(const float* x, const float* Wt, const float* b,
     return failed ? -1 : 0;
 }
 
+/* ------------------------------------------------ standalone epilogues
+ * The pages' own deliverables are epilogue kernels over an already computed
+ * contraction output: GELU + global mean over each (n, c) plane (Conv->GELU->pool
+ * page, its fused epilogue kernel), Mish twice elementwise (Conv->Mish->Mish page,
+ * its elementwise kernel), and the scale / clamp / logsumexp / x*mish(x) row kernel
+ * (Linear page, its row kernel).  Plain definitions over fp32 inputs, fp64 math. */
+
+/* out[i] = act(v[i]). */
+void oracle_act_map(const float* v, double* out, int64_t n, int act)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_act(act, (double)v[i]);
+}
+
+/* out[p] = (sum_{i < plane} act(v[p * plane + i])) / plane for each of `planes` planes. */
+void oracle_act_mean(const float* v, double* out, int64_t planes, int64_t plane, int act)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = 0; p < planes; ++p) {
+        const float* q = v + p * plane;
+        double s = 0.0;
+        for (int64_t i = 0; i < plane; ++i) s += oracle_act(act, (double)q[i]);
+        out[p] = s / (double)plane;
+    }
+}
+
+/* The Linear chain's tail on an already computed row y (bias included):
+ * t = y * scale; t = t + t; t = clamp(t, lo, hi); l = logsumexp(t); out = l * mish(l). */
+int oracle_scale_clamp_lse_mish_rows(const float* y, int M, int N, double scale, double lo, double hi, double* out)
+{
+    int failed = 0;
+#pragma omp parallel reduction(| : failed)
+    {
+        double* t = (double*)malloc(sizeof(double) * (size_t)N);
+        if (t == NULL) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int m = 0; m < M; ++m) {
+                const float* r = y + (int64_t)m * N;
+                for (int j = 0; j < N; ++j) {
+                    double u = (double)r[j] * scale;
+                    u = u + u;
+                    t[j] = fmin(fmax(u, lo), hi);
+                }
+                const double l = oracle_logsumexp(t, N);
+                out[m] = l * oracle_mish(l);
+            }
+            free(t);
+        }
+    }
+    return failed ? -1 : 0;
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

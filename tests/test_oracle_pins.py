@@ -265,3 +265,53 @@ def test_sampled_entry_points_reject_out_of_range_indices():
     dl = fc_inputs.linear_inputs(2, 4, 3)
     with pytest.raises(IndexError):
         oracle.linear_lse_mish(dl["x"], dl["W"], dl["b"], rows=[2])
+
+
+# ------------------------------------------------------------ standalone epilogues
+
+@pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish", "gelu_tanh"])
+def test_act_map_matches_independent_statement(act):
+    v = fc_inputs.epilogue_inputs((3, 5, 7), seed=31) * np.float32(3.0)
+    got = oracle.act_map(v, act)
+    ref = np.array([brute.ACTS[act](float(z)) for z in v.reshape(-1)]).reshape(v.shape)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_act_mean_pins():
+    # constant planes: the mean is act(c); against math.fsum of the independent statement;
+    # and the pooled conv is the plane mean of its pre-activation
+    for c in (-3.0, 0.0, 0.7, 9.0):
+        v = np.full((2, 3, 4, 5), c, np.float32)
+        np.testing.assert_allclose(oracle.act_mean(v, "gelu"), oracle.gelu(float(np.float32(c))), rtol=1e-14,
+                                   atol=1e-16)
+    v = fc_inputs.epilogue_inputs((2, 3, 6, 7), seed=32)
+    ref = np.array([[math.fsum(brute.gelu(float(z)) for z in v[n, c].reshape(-1)) / 42.0 for c in range(3)]
+                    for n in range(2)])
+    np.testing.assert_allclose(oracle.act_mean(v, "gelu"), ref, rtol=1e-12, atol=1e-15)
+    d = fc_inputs.conv_inputs(2, 3, 9, 8, 4, seeds=(41, 42, 43))
+    pre = oracle.conv3x3_preact(d["x"], d["w"], d["b"]).astype(np.float32)
+    np.testing.assert_allclose(oracle.act_mean(pre, "mish"), oracle.conv3x3_act_pool(d["x"], d["w"], d["b"], "mish"),
+                               rtol=1e-6, atol=1e-7)
+
+
+def test_scale_clamp_lse_mish_pins():
+    N = 1000
+    # a constant row c: l = clamp(4c) + ln N, y = l * mish(l)
+    for c in (-5.0, -0.3, 0.0, 1.1, 4.0):
+        y = oracle.scale_clamp_lse_mish(np.full((1, N), c, np.float32), 2.0, -10.0, 10.0)[0, 0]
+        l = min(max(4 * float(np.float32(c)), -10.0), 10.0) + math.log(N)
+        assert y == pytest.approx(l * oracle.mish(l), rel=1e-12)
+    # against an independent per-row statement (math.fsum logsumexp, the brute mish)
+    t = fc_inputs.epilogue_inputs((4, 257), seed=33) * np.float32(2.5)
+    got = oracle.scale_clamp_lse_mish(t, 2.0, -10.0, 10.0)[:, 0]
+    for m in range(4):
+        u = [min(max(2.0 * float(z) + 2.0 * float(z), -10.0), 10.0) for z in t[m]]
+        mx = max(u)
+        l = mx + math.log(math.fsum(math.exp(q - mx) for q in u))
+        assert got[m] == pytest.approx(l * brute.mish(l), rel=1e-12)
+    # the Linear chain's tail: rows of x W^T + b through this function give the chain's output
+    d = fc_inputs.linear_inputs(3, 16, 40, seeds=(51, 52, 53))
+    t = (d["x"].astype(np.float64) @ d["W"].astype(np.float64).T + d["b"].astype(np.float64)).astype(np.float32)
+    np.testing.assert_allclose(oracle.scale_clamp_lse_mish(t)[:, 0],
+                               oracle.linear_lse_mish(d["x"], d["W"], d["b"], 2.0, -10.0, 10.0).reshape(-1),
+                               rtol=1e-6)
