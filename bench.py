@@ -166,7 +166,8 @@ def make_call(fc, torch, key, d, device):
     if isinstance(wl, fc_inputs.LinearWorkload):
         x, W, b = (_dev(torch, d[k], device) for k in ("x", "W", "b"))
         out = torch.empty((wl.M, 1), dtype=torch.float32, device=device)
-        ws = torch.empty(fc.fc_workspace_bytes("linear_lse_mish", wl.M, wl.K, 1, 1, wl.Nout), dtype=torch.uint8,
+        ldt = fc.FC_BF16 if wl.dtype == "bf16" else fc.FC_F32
+        ws = torch.empty(fc.fc_workspace_bytes("linear_lse_mish", wl.M, wl.K, 1, 1, wl.Nout, ldt), dtype=torch.uint8,
                          device=device)
 
         def call():
@@ -358,7 +359,7 @@ def gpu_arm(args):
     # weak scaling: each rank owns its own shard (batch) of the workload, seeded by rank
     seeds = (fc_inputs.SEED_X + 1000 * rank, fc_inputs.SEED_W, fc_inputs.SEED_B)
     if isinstance(wl, fc_inputs.LinearWorkload):
-        d = fc_inputs.linear_inputs(wl.M, wl.K, wl.Nout, seeds=seeds)
+        d = fc_inputs.linear_inputs(wl.M, wl.K, wl.Nout, seeds=seeds, dtype=wl.dtype)
     else:
         d = fc_inputs.conv_inputs(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.dtype, seeds=seeds)
     call, launches_per_call, out = make_call(fc, torch, key, d, device)
@@ -463,7 +464,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

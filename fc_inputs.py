@@ -87,7 +87,8 @@ class LinearWorkload:
         return 2.0 * self.M * self.K * self.Nout
 
     def compulsory_bytes(self) -> int:
-        return (self.M * self.K + self.Nout * self.K + self.Nout) * 4 + self.M * 4
+        es = 4 if self.dtype == "f32" else 2
+        return (self.M * self.K + self.Nout * self.K + self.Nout) * es + self.M * 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -127,6 +128,9 @@ WORKLOADS = {
     "C": ConvWorkload("conv3x3_mish_mish_f32_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish", False),
     # Linear->x2->x+x->clamp->logsumexp->x*mish(x) page (Kimi-K2.6 l2_p22), problem statement.
     "D": LinearWorkload("linear_lse_mish_f32_1024x8192x8192", 1024, 8192, 8192),
+    # bf16 variants of the Linear and Mish->Mish chains at the same sizes (precision variants)
+    "Db": LinearWorkload("linear_lse_mish_bf16_1024x8192x8192", 1024, 8192, 8192, dtype="bf16"),
+    "Cb": ConvWorkload("conv3x3_mish_mish_bf16_64x64x256x256_c128", 64, 64, 256, 256, 128, "bf16", "mish_mish", False),
     # bf16 variant of the conv->GELU->pool chain at a tensor-core-bound size.
     "E": ConvWorkload("conv3x3_gelu_avgpool_bf16_32x128x128x128_c256", 32, 128, 128, 128, 256, "bf16", "gelu", True),
     # The conv->GELU->pool page's tanh-approximate GELU (the variant its trace weighs against
@@ -170,13 +174,18 @@ def conv_inputs(N, Cin, H, W, Cout, dtype="f32", seeds=(SEED_X, SEED_W, SEED_B))
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
-def linear_inputs(M, K, Nout, seeds=(SEED_X, SEED_W, SEED_B)):
-    """x (M,K) ~ N(0,1); W (Nout,K), b (Nout) ~ U(+-1/sqrt(K))."""
+def linear_inputs(M, K, Nout, seeds=(SEED_X, SEED_W, SEED_B), dtype="f32"):
+    """x (M,K) ~ N(0,1); W (Nout,K), b (Nout) ~ U(+-1/sqrt(K)).  For dtype "bf16" the arrays are
+    uint16 bf16 bit patterns (round to nearest even of the fp32 draws) and x32 / W32 / b32 hold
+    their exact fp32 values for the oracle."""
     bound = 1.0 / math.sqrt(K)
     x = _normal((M, K), seeds[0])
     Wt = _uniform((Nout, K), bound, seeds[1])
     b = _uniform((Nout,), bound, seeds[2])
-    return dict(x=x, W=Wt, b=b)
+    if dtype == "bf16":
+        xb, wb, bb = bf16_bits(x), bf16_bits(Wt), bf16_bits(b)
+        return dict(x=xb, W=wb, b=bb, x32=bf16_bits_to_f32(xb), W32=bf16_bits_to_f32(wb), b32=bf16_bits_to_f32(bb))
+    return dict(x=x, W=Wt, b=b, x32=x, W32=Wt, b32=b)
 
 
 def workload_inputs(key: str):
@@ -186,4 +195,4 @@ def workload_inputs(key: str):
         return {"v": epilogue_inputs(wl.shape, seed=SEED_X, dtype=wl.dtype, scale=0.58)}
     if isinstance(wl, ConvWorkload):
         return conv_inputs(wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.dtype)
-    return linear_inputs(wl.M, wl.K, wl.Nout)
+    return linear_inputs(wl.M, wl.K, wl.Nout, dtype=wl.dtype)

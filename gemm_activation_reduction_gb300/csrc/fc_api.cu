@@ -122,16 +122,15 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
     if (M < 1 || K < 1 || Nout < 1) return FC_ERR_INVALID_ARG;
     if (!(clamp_lo <= clamp_hi)) return FC_ERR_INVALID_ARG;   // also rejects NaN bounds
     if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
-    if (dtype != FC_F32) return FC_ERR_UNSUPPORTED;
+    if (K % (dtype == FC_BF16 ? 8 : 4) != 0) return FC_ERR_UNSUPPORTED;   // 16-byte row pitch for TMA
     DeviceState* d = nullptr;
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;
     fc::LinearPlan plan;
-    if (fc::linear_plan(&plan, M, K, Nout, d->sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    if (fc::linear_plan(&plan, M, K, Nout, dtype == FC_BF16, d->sm_count) != 0) return FC_ERR_UNSUPPORTED;
     if (workspace == nullptr || workspace_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FC_ERR_WORKSPACE;
-    cudaError_t e = fc::linear_launch(plan, static_cast<const float*>(x), static_cast<const float*>(W),
-                                      static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, workspace,
+    cudaError_t e = fc::linear_launch(plan, x, W, b, y, scale, clamp_lo, clamp_hi, workspace,
                                       reinterpret_cast<cudaStream_t>(stream), d->status, fc::kWaitBudgetCycles);
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
@@ -197,7 +196,7 @@ size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int 
     if (op == FC_OP_LINEAR_LSE_MISH) {
         if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1) return 0;
         fc::LinearPlan plan;
-        if (fc::linear_plan(&plan, n_or_m, cin_or_k, cout_or_nout, d->sm_count) != 0) return 0;
+        if (fc::linear_plan(&plan, n_or_m, cin_or_k, cout_or_nout, dtype == FC_BF16, d->sm_count) != 0) return 0;
         return plan.ws_bytes;
     }
     return 0;

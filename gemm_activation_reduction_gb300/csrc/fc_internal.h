@@ -64,6 +64,7 @@ struct LinearPlan {
     int M, K, Nout;
     int m_blocks, n_blocks, k_blocks;
     int num_tiles, grid;
+    int bf16;             // operands bf16 (kind::f16 MMAs) instead of fp32 (kind::tf32)
     int use_pair;         // CTA pairs with M = 256 MMAs (tcgen05 cta_group::2)
     int m_pairs;          // 256-row blocks in pair mode
     int bn;               // pair mode: columns per tile (a multiple of 32, <= 256)
@@ -77,9 +78,9 @@ cudaError_t act_mean_launch(const void* v, float* y, long long planes, long long
                             cudaStream_t st);
 cudaError_t lse_row_launch(const float* t, float* out, int M, int N, float scale, float lo, float hi, cudaStream_t st);
 
-int linear_plan(LinearPlan* plan, int M, int K, int Nout, int sm_count);
+int linear_plan(LinearPlan* plan, int M, int K, int Nout, int bf16, int sm_count);
 
-cudaError_t linear_launch(const LinearPlan& plan, const float* x, const float* W, const float* b, float* y,
+cudaError_t linear_launch(const LinearPlan& plan, const void* x, const void* W, const void* b, float* y,
                           float scale, float lo, float hi, void* workspace, cudaStream_t stream, int* status,
                           long long budget);
 

@@ -2,8 +2,8 @@
 // -> x*mish(x) (page "Kimi-K2.6 l2_p22": the module's forward; the stable
 // logsumexp and the streaming "running max with rescaled sum" it weighs).
 //
-// Main kernel: persistent TF32 GEMM on tcgen05.  Tile 128 x 256 x 32; both
-// operands are K-major (x [M][K] rows and nn.Linear's W [Nout][K] rows are
+// Main kernel: persistent TF32 (fp32 inputs) or BF16 GEMM on tcgen05.  Tile
+// 128 x 256 x (one 128-byte row of K: 32 fp32 or 64 bf16); both operands are K-major (x [M][K] rows and nn.Linear's W [Nout][K] rows are
 // contiguous in K), loaded by TMA with 128-byte swizzle into a 4-stage
 // shared-memory ring; the accumulator lives in tensor memory, double-buffered
 // (2 x 256 columns) so the epilogue of tile i overlaps the MMAs of tile i+1.
@@ -24,15 +24,19 @@
 namespace fc {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 32, kStages = 4;
-constexpr uint32_t kABytes = kBM * kBK * 4;  // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 4;  // 32 KB
+constexpr int kBM = 128, kBN = 256, kStages = 4;
+constexpr int kKRowBytes = 128;                       // K per stage: one 128-byte swizzle row
+constexpr int kBK = kKRowBytes / 4;                   // fp32 elements of it (bf16: twice as many)
+template <bool BF16>
+constexpr int kKElems = BF16 ? kKRowBytes / 2 : kKRowBytes / 4;
+constexpr uint32_t kABytes = kBM * kKRowBytes;        // 16 KB
+constexpr uint32_t kBBytes = kBN * kKRowBytes;        // 32 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kBarOff = kStages * (kABytes + kBBytes);
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
 
 struct LinArgs {
-    const float* bias;
+    const void* bias;   // fp32 or bf16, as x and W
     float2* partials;   // [n_blocks][M]
     int M, N, K;
     int m_blocks, n_blocks, k_blocks, num_tiles;
@@ -40,6 +44,27 @@ struct LinArgs {
     int* status;
     long long budget;
 };
+
+template <bool BF16>
+__device__ __forceinline__ float bias_at(const void* b, int n)
+{
+    if constexpr (BF16) {
+        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(b) + n);
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    } else {
+        return __ldg(reinterpret_cast<const float*>(b) + n);
+    }
+}
+
+// The four 32-byte K steps of one stage: kind::tf32 (K = 8) or kind::f16 with bf16 (K = 16).
+template <bool BF16, bool PAIR>
+__device__ __forceinline__ void mma_kstep(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    if constexpr (BF16 && PAIR) mma_f16_pair(d, ad, bd, idesc, acc);
+    else if constexpr (BF16) mma_f16(d, ad, bd, idesc, acc);
+    else if constexpr (PAIR) mma_tf32_pair(d, ad, bd, idesc, acc);
+    else mma_tf32(d, ad, bd, idesc, acc);
+}
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long budget)
 {
@@ -49,6 +74,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
     }
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_lse_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const LinArgs a)
 {
@@ -104,8 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-                    tma_load_2d(sA + stage * kABytes, &tmx, &full[stage], kb * kBK, mb * kBM);
-                    tma_load_2d(sB + stage * kBBytes, &tmw, &full[stage], kb * kBK, nb * kBN);
+                    tma_load_2d(sA + stage * kABytes, &tmx, &full[stage], kb * kKElems<BF16>, mb * kBM);
+                    tma_load_2d(sB + stage * kBBytes, &tmw, &full[stage], kb * kKElems<BF16>, nb * kBN);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -124,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = make_idesc(kFmtTF32, kBM, kBN);
+            const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, kBM, kBN);
             // Descriptors built once; stages and K steps only move the start-address
             // field (16-byte units; addresses stay below 256 KB, so no carry).
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, kLayoutSw128);
@@ -144,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kABytes >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kBBytes >> 4);
 #pragma unroll
-                    for (int k = 0; k < kBK / 8; ++k)   // 32-byte K steps inside the 128-byte swizzle row
-                        mma_tf32(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kKRowBytes / 32; ++k)   // 32-byte K steps inside the 128-byte swizzle row
+                        mma_kstep<BF16, false>(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
@@ -182,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j) {
                     const int n = n0 + j;
                     if (n < a.N) {
-                        float u = (v[j] + __ldg(a.bias + n)) * a.scale;
+                        float u = (v[j] + bias_at<BF16>(a.bias, n)) * a.scale;
                         u = u + u;
                         v[j] = fminf(fmaxf(u, a.lo), a.hi);
                     } else {
@@ -228,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kPBM = 128;                                  // rows per CTA (256 per pair)
 constexpr int kPBN = 256;                                  // most columns per pair tile
 constexpr int kPStages = 6;
-constexpr uint32_t kPABytes = kPBM * kBK * 4;              // 16 KB
-constexpr uint32_t kPBBytes = (kPBN / 2) * kBK * 4;        // 16 KB: stage slot for this CTA's half of W
+constexpr uint32_t kPABytes = kPBM * kKRowBytes;           // 16 KB
+constexpr uint32_t kPBBytes = (kPBN / 2) * kKRowBytes;     // 16 KB: stage slot for this CTA's half of W
 constexpr uint32_t kPBarOff = kPStages * (kPABytes + kPBBytes);
 constexpr uint32_t kPSmemBytes = kPBarOff + 256 + 1024;
 
 struct LinPairArgs {
-    const float* bias;
+    const void* bias;   // fp32 or bf16, as x and W
     float2* partials;   // [n_blocks][M]
     int M, N, K;
     int m_pairs, n_blocks, k_blocks, num_tiles;
@@ -244,6 +270,7 @@ struct LinPairArgs {
     long long budget;
 };
 
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_lse_pair_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                            const LinPairArgs a)
@@ -302,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int mp = t % a.m_pairs, nb = t / a.m_pairs;
                 const int m0 = mp * 2 * kPBM + static_cast<int>(rank) * kPBM;
                 const int n0 = nb * a.bn + static_cast<int>(rank) * (a.bn / 2);
-                const uint32_t b_bytes = static_cast<uint32_t>(a.bn / 2) * kBK * 4u;
+                const uint32_t b_bytes = static_cast<uint32_t>(a.bn / 2) * kKRowBytes;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPABytes + b_bytes));
-                    tma_load_2d_pair(sA + stage * kPABytes, &tmx, fbar, kb * kBK, m0);
-                    tma_load_2d_pair(sB + stage * kPBBytes, &tmw, fbar, kb * kBK, n0);
+                    tma_load_2d_pair(sA + stage * kPABytes, &tmx, fbar, kb * kKElems<BF16>, m0);
+                    tma_load_2d_pair(sB + stage * kPBBytes, &tmw, fbar, kb * kKElems<BF16>, n0);
                     if (++stage == kPStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -326,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
-            const uint32_t idesc = make_idesc(kFmtTF32, 2 * kPBM, a.bn);
+            const uint32_t idesc = make_idesc(BF16 ? kFmtBF16 : kFmtTF32, 2 * kPBM, a.bn);
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024, kLayoutSw128);
             const uint64_t b_desc0 = smem_desc(smem_u32(sB), 16, 1024, kLayoutSw128);
             int stage = 0;
@@ -344,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kPABytes >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kPBBytes >> 4);
 #pragma unroll
-                    for (int k = 0; k < kBK / 8; ++k)
-                        mma_tf32_pair(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kKRowBytes / 32; ++k)
+                        mma_kstep<BF16, true>(d, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair_multicast(&empty[stage], 0x3);
                     if (++stage == kPStages) {
                         stage = 0;
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j) {
                     const int n = n0 + j;
                     if (n < a.N) {
-                        float u = (v[j] + __ldg(a.bias + n)) * a.scale;
+                        float u = (v[j] + bias_at<BF16>(a.bias, n)) * a.scale;
                         u = u + u;
                         v[j] = fminf(fmaxf(u, a.lo), a.hi);
                     } else {
@@ -435,16 +462,18 @@ __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int 
     y[m] = l * (l * tanhf(sp));
 }
 
-// Row-major [rows][cols] fp32 matrix, box = box_rows x 32 columns (128 B), 128-byte swizzle.
-bool make_kmajor_map(CUtensorMap* map, const float* base, int rows, int cols, int box_rows)
+// Row-major [rows][cols] fp32 or bf16 matrix, box = box_rows x one 128-byte row of K, 128-byte swizzle.
+bool make_kmajor_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, bool bf16)
 {
     auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     if (enc == nullptr) return false;
+    const cuuint64_t es = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * sizeof(float)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kKRowBytes / es), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                     const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -466,14 +495,16 @@ void* tensor_map_encoder()
     return fn;
 }
 
-int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
+int linear_plan(LinearPlan* p, int M, int K, int Nout, int bf16, int sm_count)
 {
     *p = LinearPlan{};
-    if (K % 4 != 0) return 2;
-    p->M = M; p->K = K; p->Nout = Nout;
+    // TMA needs a 16-byte row pitch: K a multiple of 4 fp32 or 8 bf16
+    if (K % (bf16 ? 8 : 4) != 0) return 2;
+    p->M = M; p->K = K; p->Nout = Nout; p->bf16 = bf16;
     p->m_blocks = (M + kBM - 1) / kBM;
     p->n_blocks = (Nout + kBN - 1) / kBN;
-    p->k_blocks = (K + kBK - 1) / kBK;
+    const int kelems = bf16 ? kKElems<true> : kKElems<false>;
+    p->k_blocks = (K + kelems - 1) / kelems;
     const long long tiles = static_cast<long long>(p->m_blocks) * p->n_blocks;
     if (tiles > 0x7FFFFFFFLL) return 2;
     p->num_tiles = static_cast<int>(tiles);
@@ -506,12 +537,13 @@ int linear_plan(LinearPlan* p, int M, int K, int Nout, int sm_count)
     return 0;
 }
 
-cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, const float* b, float* y, float scale,
+cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, const void* b, float* y, float scale,
                           float lo, float hi, void* workspace, cudaStream_t stream, int* status, long long budget)
 {
     CUtensorMap tmx, tmw;
+    const bool bf16 = p.bf16 != 0;
     if (p.use_pair) {
-        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2))
+        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2, bf16))
             return cudaErrorInvalidValue;
         LinPairArgs a{};
         a.bias = b;
@@ -521,7 +553,8 @@ cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, c
         a.bn = p.bn;
         a.scale = scale; a.lo = lo; a.hi = hi;
         a.status = status; a.budget = budget;
-        cudaError_t e = cudaFuncSetAttribute(linear_lse_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto kern = bf16 ? linear_lse_pair_kernel<true> : linear_lse_pair_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(p.smem_bytes));
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg{};
@@ -536,12 +569,12 @@ cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, c
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, linear_lse_pair_kernel, tmx, tmw, a);
+        e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, a);
         if (e != cudaSuccess) return e;
         lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);
         return cudaGetLastError();
     }
-    if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN))
+    if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN, bf16))
         return cudaErrorInvalidValue;
     LinArgs a{};
     a.bias = b;
@@ -550,10 +583,11 @@ cudaError_t linear_launch(const LinearPlan& p, const float* x, const float* W, c
     a.m_blocks = p.m_blocks; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
     a.scale = scale; a.lo = lo; a.hi = hi;
     a.status = status; a.budget = budget;
-    cudaError_t e = cudaFuncSetAttribute(linear_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = bf16 ? linear_lse_kernel<true> : linear_lse_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(p.smem_bytes));
     if (e != cudaSuccess) return e;
-    linear_lse_kernel<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, a);
+    kern<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);

@@ -56,7 +56,7 @@ extern "C" fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, co
     int* status = nullptr;
     if (fc::current_device_info(&sm_count, &status) != cudaSuccess) return FC_ERR_CUDA;
     fc::LinearPlan plan;
-    if (fc::linear_plan(&plan, M, K, Nout, sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    if (fc::linear_plan(&plan, M, K, Nout, 0, sm_count) != 0) return FC_ERR_UNSUPPORTED;
     if (plan.ws_bytes > kNoAllocScratchBytes) return FC_ERR_UNSUPPORTED;
     // Every (max, sum-exp) pair the combine kernel reads is written by the main
     // kernel of the same call, so the array needs no clearing between calls.

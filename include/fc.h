@@ -116,10 +116,11 @@ fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y,
  * torch.logsumexp(dim=1, keepdim=True) then x * mish(x).  The row logsumexp
  * is taken as per-tile (max, sum of exp) pairs combined across column tiles.
  *
- *   x [M, K] fp32;  W [Nout, K] fp32 (nn.Linear weight layout);  b [Nout] fp32
- *   y [M] fp32 (the (M, 1) output, contiguous)
- *   Requires M, Nout >= 1, K >= 4 with K % 4 == 0 (16-byte row pitch),
- *   clamp_lo <= clamp_hi, dtype == FC_F32 (bf16 returns FC_ERR_UNSUPPORTED).
+ *   x [M, K], W [Nout, K] (nn.Linear weight layout), b [Nout]: all fp32 (TF32
+ *   tensor-core products) or all bf16 (dtype FC_BF16); y [M] fp32 (the (M, 1)
+ *   output, contiguous); fp32 accumulation and epilogue either way.
+ *   Requires M, Nout >= 1, a 16-byte row pitch (K % 4 == 0 for fp32, K % 8 == 0
+ *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.
  */
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y,
                              int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,

@@ -61,7 +61,8 @@ def test_host_validation_rejects_bad_arguments_before_any_launch():
     assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, 1.0, -1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG  # lo > hi
     assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, float("nan"), 1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG
     assert lin(16, 16, 16, 16, 0, 8, 8, 2.0, -1.0, 1.0, 0, None, 0, None) == fc.FC_ERR_INVALID_ARG
-    assert lin(16, 16, 16, 16, 4, 8, 8, 2.0, -1.0, 1.0, 1, None, 0, None) == fc.FC_ERR_UNSUPPORTED  # bf16
+    assert lin(16, 16, 16, 16, 4, 6, 8, 2.0, -1.0, 1.0, 0, None, 0, None) == fc.FC_ERR_UNSUPPORTED  # K % 4
+    assert lin(16, 16, 16, 16, 4, 4, 8, 2.0, -1.0, 1.0, 1, None, 0, None) == fc.FC_ERR_UNSUPPORTED  # bf16, K % 8
 
 
 def test_without_a_device_calls_report_cuda_errors_not_crashes():

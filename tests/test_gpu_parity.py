@@ -112,6 +112,25 @@ def test_linear_small(cuda_lib, shape):
     _check(y, ref, TOL["f32"], f"linear {shape}")
 
 
+LIN_SHAPES_BF16 = [
+    # (M, K, Nout, x scale): single CTAs (M <= 128) and CTA pairs, ragged sizes, clamp active
+    (3, 40, 17, 1.0),
+    (100, 264, 300, 1.0),
+    (129, 64, 513, 30.0),
+    (300, 1032, 1000, 1.0),
+]
+
+
+@pytest.mark.parametrize("shape", LIN_SHAPES_BF16, ids=lambda s: "x".join(map(str, s)))
+def test_linear_small_bf16(cuda_lib, shape):
+    M, K, Nout, sx = shape
+    d = fc_inputs.linear_inputs(M, K, Nout, dtype="bf16")
+    xs = fc_inputs.bf16_bits(d["x32"] * np.float32(sx))
+    y = cuda_lib.fc_linear_lse_mish(_dev(xs), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
+    ref = oracle.linear_lse_mish(fc_inputs.bf16_bits_to_f32(xs), d["W32"], d["b32"])
+    _check(y, ref, TOL["bf16"], f"linear bf16 {shape}")
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("key", ["B", "Bt"])
@@ -126,11 +145,12 @@ def test_workload_B_full_size_sampled(cuda_lib, key):
     _check(y.reshape(-1)[flat], ref, TOL["f32"], f"workload {key}")
 
 
-def test_workload_C_full_size_sampled(cuda_lib):
+@pytest.mark.parametrize("key", ["C", "Cb"])
+def test_workload_C_full_size_sampled(cuda_lib, key):
     import torch
-    wl = fc_inputs.WORKLOADS["C"]
-    d = fc_inputs.workload_inputs("C")
-    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="mish_mish")
+    wl = fc_inputs.WORKLOADS[key]
+    d = fc_inputs.workload_inputs(key)
+    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act)
     OH, OW = wl.OH, wl.OW
     rng = np.random.default_rng(8)
     total = wl.N * wl.Cout * OH * OW
@@ -143,19 +163,20 @@ def test_workload_C_full_size_sampled(cuda_lib):
     flat = np.unique(np.concatenate(samples))
     got = y.view(-1)[torch.from_numpy(flat).cuda()].cpu().numpy()
     del y
-    ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, "mish_mish")
-    _check(got, ref, TOL["f32"], "workload C")
+    ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
+    _check(got, ref, TOL[wl.dtype], f"workload {key}")
 
 
-def test_workload_D_full_size_sampled(cuda_lib):
-    wl = fc_inputs.WORKLOADS["D"]
-    d = fc_inputs.workload_inputs("D")
+@pytest.mark.parametrize("key", ["D", "Db"])
+def test_workload_D_full_size_sampled(cuda_lib, key):
+    wl = fc_inputs.WORKLOADS[key]
+    d = fc_inputs.workload_inputs(key)
     y = cuda_lib.fc_linear_lse_mish(_dev(d["x"]), _dev(d["W"]), _dev(d["b"]), wl.scale, wl.clamp_lo,
                                     wl.clamp_hi).cpu().numpy().reshape(-1)
     rows = np.unique(np.concatenate([np.arange(8), np.arange(wl.M - 8, wl.M),
                                      np.random.default_rng(9).choice(wl.M, 112, replace=False)]))
-    ref = oracle.linear_lse_mish(d["x"], d["W"], d["b"], wl.scale, wl.clamp_lo, wl.clamp_hi, rows=rows)
-    _check(y[rows], ref, TOL["f32"], "workload D")
+    ref = oracle.linear_lse_mish(d["x32"], d["W32"], d["b32"], wl.scale, wl.clamp_lo, wl.clamp_hi, rows=rows)
+    _check(y[rows], ref, TOL[wl.dtype], f"workload {key}")
     # clamped logsumexp bound: l in [lo + ln n, hi + ln n] -> y = l mish(l) within the image of that range
     lo_l, hi_l = wl.clamp_lo + math.log(wl.Nout), wl.clamp_hi + math.log(wl.Nout)
     f = lambda l: l * oracle.mish(l)
