@@ -13,7 +13,8 @@ namespace fc {
 using namespace convk;
 namespace {
 
-// Re-lay w [Cout][Cin][3][3] for `halves` CTAs of a group (2 for a CTA pair, else 1):
+// Re-lay w [Co][Cin][3][3] for `halves` CTAs of a group (2 for a CTA pair, else 1) as
+// Cout >= Co channels (Cout a multiple of 16; channels past Co get zero weights and bias):
 // CTA r holds output channels [r hc, (r+1) hc), hc = Cout / halves.  Layout
 // [r][K block][tap][half][co'][G]
 // (G = 4 fp32 rounded to TF32, or 8 bf16; co' the channel within the half),
@@ -22,8 +23,8 @@ namespace {
 // the TF32 remainder in k 2; bf16: the bias in k 0) and the padding value in k 1;
 // half 1 is zero.
 template <bool BF16>
-__global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Cout, int ncb,
-                                            int halves)
+__global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Co, int Cout,
+                                            int ncb, int halves)
 {
     constexpr int G = BF16 ? 8 : 4;
     const int hc = Cout / halves;
@@ -42,14 +43,14 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
             const int rank = static_cast<int>(f / 2);
             const int co = rank * hc + col;
             if constexpr (BF16) {
-                const unsigned short bv = reinterpret_cast<const unsigned short*>(b)[co];
+                const unsigned short bv = co < Co ? reinterpret_cast<const unsigned short*>(b)[co] : 0;
                 const unsigned short pad = static_cast<unsigned short>(__float_as_uint(kPadValue) >> 16);
                 unsigned short v = 0;
                 if (half == 0 && e == 0) v = bv;
                 if (half == 0 && e == 1) v = pad;
                 reinterpret_cast<unsigned short*>(wr)[i] = v;
             } else {
-                const float bv = reinterpret_cast<const float*>(b)[co];
+                const float bv = co < Co ? reinterpret_cast<const float*>(b)[co] : 0.0f;
                 const float hi = to_tf32(bv);
                 float v = 0.0f;
                 if (half == 0 && e == 0) v = hi;
@@ -73,27 +74,28 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
         const int co = rank * hc + col;
         const int ci = cb * 2 * G + half * G + e;
         const size_t src = (static_cast<size_t>(co) * Cin + ci) * 9 + tap;
+        const bool real = ci < Cin && co < Co;
         if constexpr (BF16) {
             const unsigned short* ws = reinterpret_cast<const unsigned short*>(w);
-            reinterpret_cast<unsigned short*>(wr)[i] = ci < Cin ? ws[src] : static_cast<unsigned short>(0);
+            reinterpret_cast<unsigned short*>(wr)[i] = real ? ws[src] : static_cast<unsigned short>(0);
         } else {
             const float* ws = reinterpret_cast<const float*>(w);
-            reinterpret_cast<float*>(wr)[i] = ci < Cin ? to_tf32(ws[src]) : 0.0f;
+            reinterpret_cast<float*>(wr)[i] = real ? to_tf32(ws[src]) : 0.0f;
         }
     }
 }
 
 // y[n, co] = (fixed-order sum of every image-n record of the CTAs whose tiles can
-// touch image n) / (OH * OW).  Cluster c handles tile groups [P(c), P(c+1)) of
+// touch image n) / (OH * OW), for co < Co; records hold Cout >= Co channels.  Cluster c handles tile groups [P(c), P(c+1)) of
 // `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles step * g + r.
 // Records a CTA never reached hold zeros.
-__global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Cout, long long tpi, long long pbase,
-                                         int prem, int J, int step, int recs, double inv_count)
+__global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Co, int Cout, long long tpi,
+                                         long long pbase, int prem, int J, int step, int recs, double inv_count)
 {
     const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    if (idx >= static_cast<long long>(N) * Cout) return;
-    const int n = static_cast<int>(idx / Cout);
-    const int co = static_cast<int>(idx - static_cast<long long>(n) * Cout);
+    if (idx >= static_cast<long long>(N) * Co) return;
+    const int n = static_cast<int>(idx / Co);
+    const int co = static_cast<int>(idx - static_cast<long long>(n) * Co);
     const long long big = static_cast<long long>(prem) * (pbase + 1);
     auto cluster_of = [&](long long p) -> long long { return p < big ? p / (pbase + 1) : prem + (p - big) / pbase; };
     auto start_of = [&](long long c) -> long long { return c * pbase + (c < prem ? c : prem); };
@@ -139,8 +141,11 @@ Geometry geometry(int bf16, int pool)
 int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count)
 {
     *p = ConvPlan{};
-    if (Cout < 16 || Cout > 256 || Cout % 16 != 0) return 2;
-    p->N = N; p->Cin = Cin; p->H = H; p->W = W; p->Cout = Cout;
+    if (Cout < 1 || Cout > 256) return 2;
+    p->N = N; p->Cin = Cin; p->H = H; p->W = W; p->Co = Cout;
+    // the MMA's N: whole 16-column slices; the padded channels are computed and dropped
+    Cout = (Cout + 15) / 16 * 16;
+    p->Cout = Cout;
     p->OH = H - 2; p->OW = W - 2;
     p->bf16 = bf16; p->pool = pool;
     p->esize = bf16 ? 2 : 4;
@@ -229,8 +234,12 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         const int threads = 256;
         const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, 4096));
         const int halves = p.pair ? 2 : 1;
-        if (p.bf16) conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb, halves);
-        else conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Cout, p.ncb, halves);
+        if (p.bf16)
+            conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Co, p.Cout, p.ncb,
+                                                                               halves);
+        else
+            conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Co, p.Cout, p.ncb,
+                                                                                halves);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -259,7 +268,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     ConvArgs a{};
     a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
-    a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.OH = p.OH; a.OW = p.OW;
+    a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.Co = p.Co; a.OH = p.OH; a.OW = p.OW;
     a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
@@ -278,10 +287,10 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     if (e != cudaSuccess) return e;
 
     if (p.pool) {
-        const long long outs = static_cast<long long>(p.N) * p.Cout;
+        const long long outs = static_cast<long long>(p.N) * p.Co;
         const int threads = 256;
         const int blocks = static_cast<int>((outs + threads - 1) / threads);
-        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Cout, p.tpi, p.pbase, p.prem, p.J,
+        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Co, p.Cout, p.tpi, p.pbase, p.prem, p.J,
                                                                   p.pair ? 2 : 1, 4 * p.egroups,
                                                                   1.0 / (static_cast<double>(p.OH) * p.OW));
         e = cudaGetLastError();

@@ -102,7 +102,9 @@ struct ConvArgs {
     const void* x;
     const void* wr;      // re-laid weights, then the bias block (workspace)
     float* out;          // full output (store) or pool partials (pool)
-    int N, Cin, H, W, Cout, OH, OW;
+    int N, Cin, H, W, OH, OW;
+    int Cout;            // tile width: output channels rounded up to 16
+    int Co;              // output channels stored (<= Cout)
     int ncb, RB, CS;
     long long tpi;
     long long num_tiles;  // tiles of the whole call
@@ -933,16 +935,17 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     else release_and_next();
                     if constexpr (!POOL) {
                         if (valid) {
-                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.Cout + c * kEpiCols) * a.OH + oh) *
+                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.Co + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;
+                            const int jmax = a.Co - c * kEpiCols;   // < 16 only in a padded last slice
                             // streaming stores: the output is written once and not re-read here
 #pragma unroll
                             for (int j = 0; j < kEpiCols; j += 2) {
                                 float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
                                 if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
-                                __stcs(o + j * plane, g.x);
-                                __stcs(o + (j + 1) * plane, g.y);
+                                if (j < jmax) __stcs(o + j * plane, g.x);
+                                if (j + 1 < jmax) __stcs(o + (j + 1) * plane, g.y);
                             }
                         }
                     }

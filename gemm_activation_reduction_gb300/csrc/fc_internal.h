@@ -21,7 +21,10 @@ constexpr long long kWaitBudgetCycles = 2000000000LL;
 // Geometry and resources of one fused conv3x3 call; computed on the host by
 // conv_plan() and passed by value to the kernel.
 struct ConvPlan {
-    int N, Cin, H, W, Cout, OH, OW;
+    int N, Cin, H, W, OH, OW;
+    int Co;               // output channels of the call (any count in 1 .. 256)
+    int Cout;             // Co rounded up to 16: the MMA tile width; channels >= Co carry zero
+                          // weights and bias and are never stored
     int bf16, pool;
     int esize;            // bytes per stored element (4 or 2)
     int cb_ch;            // input channels per K block (8 fp32, 16 bf16)

@@ -82,8 +82,9 @@ typedef enum {
  *   w   [Cout, Cin, 3, 3]  same dtype, OIHW
  *   b   [Cout]             same dtype
  *   y   [N, Cout]          fp32 output
- *   Requires N, Cin >= 1; H, W >= 3; 16 <= Cout <= 256 with Cout % 16 == 0
- *   (else FC_ERR_UNSUPPORTED).  The mean is a fixed-order two-stage sum:
+ *   Requires N, Cin >= 1; H, W >= 3; 1 <= Cout <= 256 (else FC_ERR_UNSUPPORTED).
+ *   A Cout that is not a multiple of 16 runs as the next multiple with the
+ *   extra channels zero and unstored.  The mean is a fixed-order two-stage sum:
  *   results are bit-identical run to run on the same GPU model.
  */
 fc_status fc_conv3x3_act_pool(const void* x, const void* w, const void* b, float* y,

@@ -57,6 +57,12 @@ POOL_SHAPES = [
     (1, 16, 19, 30, 16, "bf16", "gelu"),     # the smallest Cout, 16
     (2, 8, 33, 30, 64, "f32", "gelu_tanh"),  # tanh-approximate GELU
     (1, 40, 17, 19, 256, "bf16", "gelu_tanh"),
+    # output channel counts that are not multiples of 16 (run padded to the next one)
+    (2, 8, 21, 19, 40, "f32", "gelu"),
+    (3, 5, 13, 17, 3, "f32", "gelu"),
+    (1, 3, 10, 9, 1, "bf16", "mish"),
+    (2, 12, 18, 22, 200, "f32", "gelu"),     # CTA pairs, 104 channels each
+    (1, 24, 15, 16, 145, "bf16", "gelu_tanh"),
 ]
 
 
@@ -78,6 +84,9 @@ ACT_SHAPES = [
     (2, 16, 19, 10, 256, "bf16", "mish"),
     (1, 7, 9, 140, 80, "f32", "mish_mish"),  # Cout = 80; rows wider than one 128-pixel tile
     (1, 9, 13, 150, 64, "f32", "gelu_tanh"),
+    (2, 8, 12, 140, 40, "f32", "mish_mish"),   # Cout not a multiple of 16
+    (1, 6, 11, 21, 7, "bf16", "gelu"),
+    (1, 16, 9, 133, 250, "f32", "mish"),       # CTA pairs, padded to 256
 ]
 
 
@@ -227,7 +236,7 @@ def test_workspace_too_small_is_rejected(cuda_lib):
 
 
 def test_unsupported_cout_is_reported(cuda_lib):
-    d = fc_inputs.conv_inputs(1, 8, 16, 16, 40)   # not a multiple of 16
+    d = fc_inputs.conv_inputs(1, 8, 16, 16, 272)   # more than 256 output channels
     with pytest.raises(cuda_lib.FCError) as e:
         cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]))
     assert e.value.status == cuda_lib.FC_ERR_UNSUPPORTED
