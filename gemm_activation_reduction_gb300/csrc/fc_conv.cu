@@ -123,17 +123,21 @@ struct Geometry {
     uint32_t strip_bytes, raw_bytes;
 };
 
-template <bool BF16, bool WIDE>
+template <bool BF16, bool WIDE, int ROWS>
 Geometry geometry_of()
 {
-    return Geometry{Shape<WIDE>::PR, Shape<WIDE>::PC, Shape<WIDE>::SR, RawBox<BF16, WIDE>::kCols,
-                    RawBox<BF16, WIDE>::kCh, Shape<WIDE>::STRIP, RawBox<BF16, WIDE>::kBytes};
+    using S = Shape<WIDE, ROWS>;
+    using R = RawBox<BF16, WIDE, ROWS>;
+    return Geometry{S::PR, S::PC, S::SR, R::kCols, R::kCh, S::STRIP, R::kBytes};
 }
 
-Geometry geometry(int bf16, int pool)
+// The kernel's tile shape: 16 x 8 patches (pool), two rows of 128 (full output, single
+// CTAs) or one row of 128 (full output, CTA pairs).
+Geometry geometry(int bf16, int pool, int pair)
 {
-    if (bf16) return pool ? geometry_of<true, false>() : geometry_of<true, true>();
-    return pool ? geometry_of<false, false>() : geometry_of<false, true>();
+    if (pool) return bf16 ? geometry_of<true, false, 1>() : geometry_of<false, false, 1>();
+    if (pair) return bf16 ? geometry_of<true, true, 1>() : geometry_of<false, true, 1>();
+    return bf16 ? geometry_of<true, true, 2>() : geometry_of<false, true, 2>();
 }
 
 }  // namespace
@@ -151,15 +155,15 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->esize = bf16 ? 2 : 4;
     p->cb_ch = bf16 ? 16 : 8;
     p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch;
-    const Geometry geo = geometry(bf16, pool);
-    p->RB = (p->OH + geo.PR - 1) / geo.PR;
-    p->CS = (p->OW + geo.PC - 1) / geo.PC;
-    p->tpi = static_cast<long long>(p->RB) * p->CS;
-    p->num_tiles = static_cast<long long>(N) * p->tpi;
     // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) for Cout > 128, where
     // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
     // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
     p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
+    const Geometry geo = geometry(bf16, pool, p->pair);
+    p->RB = (p->OH + geo.PR - 1) / geo.PR;
+    p->CS = (p->OW + geo.PC - 1) / geo.PC;
+    p->tpi = static_cast<long long>(p->RB) * p->CS;
+    p->num_tiles = static_cast<long long>(N) * p->tpi;
     const int step = p->pair ? 2 : 1;
     // cluster c (a CTA pair, or one CTA) takes a contiguous range of tile groups
     const long long groups = (p->num_tiles + step - 1) / step;
@@ -254,7 +258,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.Cin),
                               static_cast<cuuint64_t>(p.N)};
         cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
-        const Geometry geo = geometry(p.bf16, p.pool);
+        const Geometry geo = geometry(p.bf16, p.pool, p.pair);
         cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_cols), static_cast<cuuint32_t>(geo.SR),
                              static_cast<cuuint32_t>(geo.box_ch), 1u};
         cuuint32_t estr[4] = {1, 1, 1, 1};

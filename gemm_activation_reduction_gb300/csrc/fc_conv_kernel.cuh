@@ -68,17 +68,24 @@ constexpr int kMaxStages = 6;                            // staged strip slots
 // barrier block: 2 kMaxStages + 2 kMaxAcc + kNumProd kMaxRawDepth + 3 barriers, slot, flag
 constexpr uint32_t kBarBytes = 512;
 static_assert((2 * kMaxStages + 2 * kMaxAcc + kNumProd * kMaxRawDepth + 3) * 8 + 8 <= kBarBytes, "barrier block");
-constexpr uint32_t kSmemBudget = 210 * 1024;
+// everything the plan places, below the 227 KB per-CTA opt-in limit less the barrier
+// block and the 1 KB base alignment
+constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 
-// Output pixels of one 128-row MMA tile.  The pooled ops use a 16-row x 8-column
-// patch (least halo: 18 x 10 staged pixels per 128 outputs); the full-output op
-// uses one row of 128 columns so that each warp stores 32 consecutive pixels of
-// a row (128 contiguous bytes) per output channel.  Either way the 8-pixel
-// core-matrix groups of the tile lie at one constant stride in the staged
-// strip (SBO): the next patch row (16 x 8), or the next 8 pixels (1 x 128).
-template <bool WIDE>
+// Output pixels of one staged tile.  The pooled ops use a 16-row x 8-column
+// patch, one 128-row MMA tile (least halo: 18 x 10 staged pixels per 128
+// outputs); the full-output op uses ROWS rows of 128 columns so that each warp
+// stores 32 consecutive pixels of a row (128 contiguous bytes) per output
+// channel.  Each row of a wide tile is one M = 128 MMA "unit" with its own
+// accumulator; the rows share the staged strip (row u starts u * SC pixels
+// further) and every streamed weight block, so two rows halve the weight
+// traffic per output and stage 4 input rows per 2 output rows instead of 3 per 1.
+// Either way the 8-pixel core-matrix groups of a unit lie at one constant stride
+// in the staged strip (SBO): the next patch row (16 x 8), or the next 8 pixels (1 x 128).
+template <bool WIDE, int ROWS = 1>
 struct Shape {
-    static constexpr int PR = WIDE ? 1 : 16;               // output rows per tile
+    static constexpr int UNITS = WIDE ? ROWS : 1;          // M = 128 MMA units per tile
+    static constexpr int PR = WIDE ? ROWS : 16;            // output rows per tile
     static constexpr int PC = WIDE ? 128 : 8;              // output columns per tile
     static constexpr int SR = PR + 2;                      // staged rows (halo)
     static constexpr int SC = PC + 2;                      // staged columns (halo)
@@ -90,11 +97,12 @@ struct Shape {
 
 // Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
 // order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.
-template <bool BF16, bool WIDE>
+template <bool BF16, bool WIDE, int ROWS = 1>
 struct RawBox {
+    using S = Shape<WIDE, ROWS>;
     static constexpr int kCh = BF16 ? 16 : 8;
-    static constexpr int kCols = BF16 ? (Shape<WIDE>::SC + 7) / 8 * 8 : (Shape<WIDE>::SC + 3) / 4 * 4;
-    static constexpr uint32_t kChPlane = Shape<WIDE>::SR * kCols * (BF16 ? 2 : 4);
+    static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8 : (S::SC + 3) / 4 * 4;
+    static constexpr uint32_t kChPlane = S::SR * kCols * (BF16 ? 2 : 4);
     static constexpr uint32_t kBytes = (kCh * kChPlane + 127) / 128 * 128;
 };
 
@@ -235,11 +243,11 @@ __device__ __forceinline__ float2 ld_shared_f2(uint32_t addr)
 }
 
 // Re-lay a landed raw box into the staged strip [group][SPOS pixels][16 B].
-template <bool BF16, bool WIDE>
+template <bool BF16, bool WIDE, int ROWS>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
 {
-    using S = Shape<WIDE>;
-    using RB_ = RawBox<BF16, WIDE>;
+    using S = Shape<WIDE, ROWS>;
+    using RB_ = RawBox<BF16, WIDE, ROWS>;
     if constexpr (!BF16) {
         // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
         // (the last quad of a row holds SC % 4 staged pixels; the raw box is wider)
@@ -297,11 +305,11 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
 // Fallback staging with plain loads (when x's row pitch is not a 16-byte
 // multiple and TMA cannot address it): one K block of the halo patch as
 // [group][SPOS pixels][16 B], zero past the image and past Cin.
-template <bool BF16, bool WIDE>
+template <bool BF16, bool WIDE, int ROWS>
 __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
                                            int Cin, int H, int W, int lane)
 {
-    using S = Shape<WIDE>;
+    using S = Shape<WIDE, ROWS>;
     const size_t HW = static_cast<size_t>(H) * W;
     for (int s = lane; s < S::SPOS; s += 32) {
         const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
@@ -354,11 +362,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
 // its accumulator starts near -1e4 and activates to exactly -0.  CTA pairs share
 // one descriptor for two tiles, so they use plane 0 (all inside) and mask in the
 // epilogue instead.
-template <bool BF16, bool WIDE>
+template <bool BF16, bool WIDE, int ROWS>
 __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
                                                        int nthreads)
 {
-    using S = Shape<WIDE>;
+    using S = Shape<WIDE, ROWS>;
     const int rows_last = OH - (RB - 1) * S::PR;   // valid rows in the last row block
     const int cols_last = OW - (CS - 1) * S::PC;   // valid columns in the last column strip
     for (int i = tid; i < 5 * 128; i += nthreads) {
@@ -471,8 +479,12 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
     constexpr bool WIDE = !POOL;
-    using S = Shape<WIDE>;
-    using RBox = RawBox<BF16, WIDE>;
+    // full output on single CTAs: two-row tiles (two MMA units sharing each staged strip
+    // and weight block); CTA pairs keep one row per CTA
+    constexpr int ROWS = (WIDE && !PAIR) ? 2 : 1;
+    using S = Shape<WIDE, ROWS>;
+    using RBox = RawBox<BF16, WIDE, ROWS>;
+    constexpr int UPT = S::UNITS;   // accumulator units per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.bar_off);
@@ -517,7 +529,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         if (a.use_tma) prefetch_tmap(&tmx);
     }
     if (warp < kEpiWarps) {
-        build_indicator_planes<BF16, WIDE>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
+        build_indicator_planes<BF16, WIDE, ROWS>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
@@ -615,12 +627,12 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t r = raw_buf(use);
                     ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
-                    transpose_raw<BF16, WIDE>(smem_u32(smem + a.raw_off + r * RBox::kBytes), strip, lane);
+                    transpose_raw<BF16, WIDE, ROWS>(smem_u32(smem + a.raw_off + r * RBox::kBytes), strip, lane);
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
                     if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
-                    fill_strip<BF16, WIDE>(strip, a.x, tc.n < a.N ? tc.n : 0, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin,
+                    fill_strip<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin,
                                            tc.n < a.N ? a.H : 0, a.W, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -670,35 +682,49 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget) &&
                       (!pair || mbar_wait_cluster(wpeer, 0, abort_flag, a.status, a.budget));
             ok = __all_sync(0xffffffffu, ok);
-            int acc = 0;
+            int acc = 0;   // accumulator ring position of the next unit
             uint32_t aph = 0, slot = 0, sph = 0;
             TileCoord tc = first;
             for (int lt = 0; ok && lt < n_pairs; ++lt) {
-                ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                // the tile's UPT units take the next UPT accumulators of the ring
+                uint32_t d[UPT];
+                int accu[UPT];
+#pragma unroll
+                for (int u = 0; u < UPT; ++u) {
+                    accu[u] = acc;
+                    d[u] = tmem + static_cast<uint32_t>(acc * a.Cout);
+                    ok = ok && wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                    if (++acc == a.nacc) {
+                        acc = 0;
+                        aph ^= 1u;
+                    }
+                }
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
                 const uint32_t v = PAIR ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
                 const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
-                issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
+#pragma unroll
+                for (int u = 0; u < UPT; ++u) issue_mma<BF16, PAIR>(d[u], i_desc, bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16;
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
-                    issue_mma9<BF16, PAIR, S::SC>(d, ab, bbase, wtap16, idesc);
+                    // unit u reads the strip from staged row u on (u * SC pixels, 16 B each)
+#pragma unroll
+                    for (int u = 0; u < UPT; ++u)
+                        issue_mma9<BF16, PAIR, S::SC>(d[u], ab + static_cast<uint64_t>(u * S::SC), bbase, wtap16, idesc);
                     commit_to<PAIR>(&empty[slot], 0x3);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
                         slot = 0;
                         sph ^= 1u;
                     }
                 }
-                if (ok) commit_to<PAIR>(&tfull[acc], 0x3);
-                if (++acc == a.nacc) {
-                    acc = 0;
-                    aph ^= 1u;
+                if (ok) {
+#pragma unroll
+                    for (int u = 0; u < UPT; ++u) commit_to<PAIR>(&tfull[accu[u]], 0x3);
                 }
                 next_tile(tc, a.RB, a.CS);
                 if constexpr (PAIR) next_tile(tc, a.RB, a.CS);
@@ -783,9 +809,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             slots_written = n_img - n_first + 1;
         };
 
-        const int tstep = G * step;   // CTA tiles from one of this warp's tiles to the next
+        // Units: the UPT accumulators of every tile of this CTA, in order (unit lt is row
+        // us = lt % UPT of tile lt / UPT); group gi takes units gi, gi + G, ...
+        const int n_units = n_pairs * UPT;
         TileCoord tc = first;
-        for (int i = 0; i < gi * step; ++i) next_tile(tc, a.RB, a.CS);
+        int us = 0;
+        auto advance_units = [&](int k) {
+            us += k;
+            while (us >= UPT) {
+                us -= UPT;
+                for (int i = 0; i < step; ++i) next_tile(tc, a.RB, a.CS);
+            }
+        };
+        advance_units(gi);
         int lt = gi;
         int acc = gi % a.nacc;
         uint32_t aph = static_cast<uint32_t>(gi / a.nacc) & 1u;
@@ -811,14 +847,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             // two load buffers, used alternately (slice k of a tile in buf[k & 1]); a tile with an
             // odd number of slices leaves the next tile's slice 0 in buf[1], moved after its wait
             uint32_t buf[2][kEpiCols];
-            if (lt < n_pairs) {
+            if (lt < n_units) {
                 ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
                 if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), buf[0]);
             }
-            while (ok && lt < n_pairs) {
-                const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
+            while (ok && lt < n_units) {
+                const bool real = t_first + static_cast<long long>(step) * (lt / UPT) < a.num_tiles;   // the peer's half of a last, odd pair is not
                 if (real && tc.n != cur_n) {
                     if (cur_n >= 0) flush(cur_n);
                     cur_n = tc.n;
@@ -844,7 +880,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
                         else mbar_arrive(&tempty[acc]);
                     }
-                    if (nlt < n_pairs) {
+                    if (nlt < n_units) {
                         ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                         ok = __all_sync(0xffffffffu, ok);
                         tc_fence_after();
@@ -876,7 +912,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         }
                     }
                 }
-                if ((ms & 1) && ok && nlt < n_pairs) {
+                if ((ms & 1) && ok && nlt < n_units) {
                     tmem_ld16_wait(buf[1]);
 #pragma unroll
                     for (int j = 0; j < kEpiCols; ++j) buf[0][j] = buf[1][j];
@@ -884,22 +920,22 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 acc = nacc_i;
                 aph = naph;
                 lt = nlt;
-                for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
+                advance_units(G);
             }
         }
         // Full output: the next slice's TMEM load is in flight while the current one is
         // activated and stored; a tile's accumulator is released as soon as its last slice
         // is in registers.
         uint32_t rnext[kEpiCols];
-        if (!POOL && lt < n_pairs) {
+        if (!POOL && lt < n_units) {
             ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (ok && ms > 0) tmem_ld16_start(taddr(acc, 0), rnext);
         }
-        while (!POOL && ok && lt < n_pairs) {
-            const bool real = t_first + static_cast<long long>(step) * lt < a.num_tiles;   // the peer's half of a last, odd pair is not
-            const int oh = tc.rb * S::PR + pr, ow = tc.cs * S::PC + pc;
+        while (!POOL && ok && lt < n_units) {
+            const bool real = t_first + static_cast<long long>(step) * (lt / UPT) < a.num_tiles;   // the peer's half of a last, odd pair is not
+            const int oh = tc.rb * S::PR + us + pr, ow = tc.cs * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
             const int nlt = lt + G;
             int nacc_i = acc + G;
@@ -915,7 +951,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
                     else mbar_arrive(&tempty[acc]);
                 }
-                if (nlt < n_pairs) {
+                if (nlt < n_units) {
                     ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                     ok = __all_sync(0xffffffffu, ok);
                     tc_fence_after();
@@ -954,7 +990,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             acc = nacc_i;
             aph = naph;
             lt = nlt;
-            for (int i = 0; i < tstep; ++i) next_tile(tc, a.RB, a.CS);
+            advance_units(G);
         }
         if constexpr (POOL) {
             if (ok) {
