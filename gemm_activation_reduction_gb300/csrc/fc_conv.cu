@@ -190,8 +190,13 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     const uint32_t per_stage = p->strip_bytes + (p->resident ? 0u : p->w_block_bytes);
     const uint32_t per_depth = static_cast<uint32_t>(kNumProd) * p->raw_bytes;
     const uint32_t boxes_min = p->use_tma ? per_depth : 0u;
-    if (fixed + 2u * per_stage + boxes_min > kSmemBudget) return 2;
+    // At least one strip slot per producer warp: producer w fills stages w, w + P, ... and
+    // waits on empty[slot] by phase parity, which is only unambiguous while the slot's
+    // previous user (stage g - stages) is at most one phase ahead of that producer's own
+    // previous stage (g - P), i.e. stages >= P.
+    if (fixed + static_cast<uint32_t>(kNumProd) * per_stage + boxes_min > kSmemBudget) return 2;
     p->stages = static_cast<int>(std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed - boxes_min) / per_stage));
+    if (p->stages < kNumProd) return 2;
     // the shared memory left buys TMA look-ahead
     p->raw_depth = 1;
     if (p->use_tma)

@@ -68,6 +68,7 @@ constexpr int kMaxStages = 6;                            // staged strip slots
 // barrier block: 2 kMaxStages + 2 kMaxAcc + kNumProd kMaxRawDepth + 3 barriers, slot, flag
 constexpr uint32_t kBarBytes = 512;
 static_assert((2 * kMaxStages + 2 * kMaxAcc + kNumProd * kMaxRawDepth + 3) * 8 + 8 <= kBarBytes, "barrier block");
+static_assert(kMaxStages >= kNumProd, "one strip slot per producer warp at least (parity waits on empty[])");
 // everything the plan places, below the 227 KB per-CTA opt-in limit less the barrier
 // block and the 1 KB base alignment
 constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
