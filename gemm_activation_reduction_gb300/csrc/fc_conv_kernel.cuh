@@ -686,7 +686,38 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             int acc = 0;   // accumulator ring position of the next unit
             uint32_t aph = 0, slot = 0, sph = 0;
             TileCoord tc = first;
-            for (int lt = 0; ok && lt < n_pairs; ++lt) {
+            for (int lt = 0; ok && lt < n_pairs && UPT == 1; ++lt) {
+                // one accumulator per tile (pooled tiles, CTA pairs)
+                ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
+                // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
+                const uint32_t v = PAIR ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
+                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
+                issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
+                for (int cb = 0; cb < a.ncb; ++cb) {
+                    ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    tc_fence_after();
+                    const uint64_t ab = a_desc0 + slot * kStrip16;
+                    const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
+                    issue_mma9<BF16, PAIR, S::SC>(d, ab, bbase, wtap16, idesc);
+                    commit_to<PAIR>(&empty[slot], 0x3);
+                    if (++slot == static_cast<uint32_t>(a.stages)) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
+                }
+                if (ok) commit_to<PAIR>(&tfull[acc], 0x3);
+                if (++acc == a.nacc) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+                next_tile(tc, a.RB, a.CS);
+                if constexpr (PAIR) next_tile(tc, a.RB, a.CS);
+            }
+            for (int lt = 0; ok && lt < n_pairs && UPT > 1; ++lt) {
                 // the tile's UPT units take the next UPT accumulators of the ring
                 uint32_t d[UPT];
                 int accu[UPT];
@@ -816,10 +847,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         TileCoord tc = first;
         int us = 0;
         auto advance_units = [&](int k) {
-            us += k;
-            while (us >= UPT) {
-                us -= UPT;
-                for (int i = 0; i < step; ++i) next_tile(tc, a.RB, a.CS);
+            if constexpr (UPT == 1) {
+                for (int i = 0; i < k * step; ++i) next_tile(tc, a.RB, a.CS);
+            } else {
+                us += k;
+                while (us >= UPT) {
+                    us -= UPT;
+                    for (int i = 0; i < step; ++i) next_tile(tc, a.RB, a.CS);
+                }
             }
         };
         advance_units(gi);
