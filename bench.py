@@ -52,6 +52,9 @@ def tensor_peak(wl, pk):
     bf16 = pk["bf16_tflops"]
     if getattr(wl, "dtype", "f32") == "bf16":
         return bf16, f"bf16 burst ({pk['source']})"
+    if getattr(wl, "precision", "tf32") == "3xtf32":
+        # three TF32 products per term: the contraction's flops take three times the TF32 tensor time
+        return bf16 * TF32_OVER_BF16 / 3.0, f"3xtf32 = tf32 / 3, tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25"
     return bf16 * TF32_OVER_BF16, f"tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25"
 
 
@@ -174,7 +177,8 @@ def make_call(fc, torch, key, d, device):
             fc.fc_linear_lse_mish(x, W, b, wl.scale, wl.clamp_lo, wl.clamp_hi, out=out, workspace=ws)
         return call, 2, out
     x, w, b = (_dev(torch, d[k], device) for k in ("x", "w", "b"))
-    dt = fc.FC_BF16 if wl.dtype == "bf16" else fc.FC_F32
+    dt = fc.FC_BF16 if wl.dtype == "bf16" else (fc.FC_F32_3XTF32 if wl.precision == "3xtf32" else fc.FC_F32)
+    prec = None if wl.dtype == "bf16" else wl.precision
     op = "conv3x3_act_pool" if wl.pool else "conv3x3_act"
     shape = (wl.N, wl.Cout) if wl.pool else (wl.N, wl.Cout, wl.OH, wl.OW)
     out = torch.empty(shape, dtype=torch.float32, device=device)
@@ -183,7 +187,7 @@ def make_call(fc, torch, key, d, device):
     f = fc.fc_conv3x3_act_pool if wl.pool else fc.fc_conv3x3_act
 
     def call():
-        f(x, w, b, act=wl.act, out=out, workspace=ws)
+        f(x, w, b, act=wl.act, out=out, workspace=ws, precision=prec)
     return call, (3 if wl.pool else 2), out
 
 
@@ -256,9 +260,9 @@ def time_e2e(fc, torch, key, d, device, steps, warmup):
         if isinstance(wl, fc_inputs.LinearWorkload):
             y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi)
         elif wl.pool:
-            y = fc.fc_conv3x3_act_pool(*dev, act=wl.act)
+            y = fc.fc_conv3x3_act_pool(*dev, act=wl.act, precision=None if bf16 else wl.precision)
         else:
-            y = fc.fc_conv3x3_act(*dev, act=wl.act)
+            y = fc.fc_conv3x3_act(*dev, act=wl.act, precision=None if bf16 else wl.precision)
         return y.to("cpu", non_blocking=False)
 
     for _ in range(warmup):
@@ -464,7 +468,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -53,6 +53,7 @@ class ConvWorkload:
     dtype: str          # "f32" or "bf16"
     act: str            # "gelu" | "mish" | "mish_mish" | "gelu_tanh"
     pool: bool          # True: global mean to (N, Cout); False: full output
+    precision: str = "tf32"   # fp32 storage: "tf32" or "3xtf32" (split-TF32 products); bf16: "bf16"
 
     @property
     def OH(self):
@@ -137,6 +138,11 @@ WORKLOADS = {
     # the exact form), at the full problem size.
     "Bt": ConvWorkload("conv3x3_gelu_tanh_avgpool_f32_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu_tanh",
                        True),
+    # Split-TF32 (3 products per term, fp32-level contraction error) at the fp32 conv pages' sizes.
+    "B3": ConvWorkload("conv3x3_gelu_avgpool_f32x3_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu", True,
+                       "3xtf32"),
+    "C3": ConvWorkload("conv3x3_mish_mish_f32x3_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish",
+                       False, "3xtf32"),
     # The pages' epilogue-only kernels at their sizes: over the conv output of the GELU->pool page,
     # the conv output of the Mish->Mish page, and the Linear output of the Linear page.
     "K1e": EpilogueWorkload("gelu_avgpool_epilogue_f32_128x64x254x254", "act_mean", (128, 64, 254, 254), "gelu"),

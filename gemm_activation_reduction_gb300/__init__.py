@@ -24,7 +24,7 @@ __all__ = [
 ]
 
 FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
-FC_F32, FC_BF16 = 0, 1
+FC_F32, FC_BF16, FC_F32_3XTF32 = 0, 1, 2
 ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}
 OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
@@ -121,9 +121,19 @@ def _check(t, name, dtypes, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def _dtype_code(t):
+def _dtype_code(t, precision=None):
+    """The fc_dtype of a call: the storage dtype, and for fp32 the tensor-core precision
+    ("tf32", the default, or "3xtf32" for split-TF32 products)."""
     torch = _torch()
-    return FC_F32 if t.dtype == torch.float32 else FC_BF16
+    if t.dtype == torch.bfloat16:
+        if precision not in (None, "bf16"):
+            raise ValueError(f"precision {precision!r} needs fp32 inputs")
+        return FC_BF16
+    if precision in (None, "tf32"):
+        return FC_F32
+    if precision == "3xtf32":
+        return FC_F32_3XTF32
+    raise ValueError(f"unknown precision {precision!r} (expected 'tf32' or '3xtf32')")
 
 
 def _raise(status, where):
@@ -148,7 +158,7 @@ def _workspace(nbytes, device, workspace):
     return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
 
 
-def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape):
+def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape, precision=None):
     torch = _torch()
     lib = load()
     dts = (torch.float32, torch.bfloat16)
@@ -166,7 +176,7 @@ def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape):
         _check(out, "out", (torch.float32,), x.device)
         if tuple(out.shape) != shape:
             raise ValueError(f"out must have shape {shape}")
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, precision)
     with torch.cuda.device(x.device):
         nbytes = int(lib.fc_workspace_bytes(OPS[op], N, Cin, H, W, Cout, dt))
         ws, wsb = _workspace(nbytes, x.device, workspace)
@@ -176,16 +186,18 @@ def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape):
     return out
 
 
-def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None):
-    """y[N, Cout] = mean over the (H-2)x(W-2) plane of act(conv3x3(x, w) + b); fp32 output."""
+def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None, precision=None):
+    """y[N, Cout] = mean over the (H-2)x(W-2) plane of act(conv3x3(x, w) + b); fp32 output.
+    precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
     return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream,
-                 lambda N, Cout, H, W: (N, Cout))
+                 lambda N, Cout, H, W: (N, Cout), precision)
 
 
-def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None):
-    """y[N, Cout, H-2, W-2] = act(conv3x3(x, w) + b); fp32 output."""
+def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None, precision=None):
+    """y[N, Cout, H-2, W-2] = act(conv3x3(x, w) + b); fp32 output.
+    precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
     return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream,
-                 lambda N, Cout, H, W: (N, Cout, H - 2, W - 2))
+                 lambda N, Cout, H, W: (N, Cout, H - 2, W - 2), precision)
 
 
 def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,

@@ -46,14 +46,15 @@ fc_status conv_common(const void* x, const void* w, const void* b, float* y, int
     if (!x || !w || !b || !y) return FC_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
     if (N < 1 || Cin < 1 || H < 3 || W < 3 || Cout < 1) return FC_ERR_INVALID_ARG;
-    if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
+    if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return FC_ERR_INVALID_ARG;
     if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH && act != FC_ACT_GELU_TANH)
         return FC_ERR_INVALID_ARG;
     DeviceState* d = nullptr;
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;
     fc::ConvPlan plan;
-    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, dtype == FC_BF16, pool, d->sm_count) != 0) return FC_ERR_UNSUPPORTED;
+    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, static_cast<int>(dtype), pool, d->sm_count) != 0)
+        return FC_ERR_UNSUPPORTED;
     const size_t need = plan.ws_weights_bytes + plan.ws_pool_bytes;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return FC_ERR_WORKSPACE;
@@ -121,7 +122,8 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
     if (!aligned16(x) || !aligned16(W) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || Nout < 1) return FC_ERR_INVALID_ARG;
     if (!(clamp_lo <= clamp_hi)) return FC_ERR_INVALID_ARG;   // also rejects NaN bounds
-    if (dtype != FC_F32 && dtype != FC_BF16) return FC_ERR_INVALID_ARG;
+    if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return FC_ERR_INVALID_ARG;
+    if (dtype == FC_F32_3XTF32) return FC_ERR_UNSUPPORTED;                 // no split-TF32 GEMM
     if (K % (dtype == FC_BF16 ? 8 : 4) != 0) return FC_ERR_UNSUPPORTED;   // 16-byte row pitch for TMA
     DeviceState* d = nullptr;
     fc_status st = device_state(&d);
@@ -184,17 +186,17 @@ size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int 
 {
     DeviceState* d = nullptr;
     if (device_state(&d) != FC_OK) return 0;
-    if (dtype != FC_F32 && dtype != FC_BF16) return 0;
+    if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return 0;
     if (op == FC_OP_CONV3X3_ACT_POOL || op == FC_OP_CONV3X3_ACT) {
         if (n_or_m < 1 || cin_or_k < 1 || h < 3 || w < 3 || cout_or_nout < 1) return 0;
         fc::ConvPlan plan;
-        if (fc::conv_plan(&plan, n_or_m, cin_or_k, h, w, cout_or_nout, dtype == FC_BF16,
+        if (fc::conv_plan(&plan, n_or_m, cin_or_k, h, w, cout_or_nout, static_cast<int>(dtype),
                           op == FC_OP_CONV3X3_ACT_POOL, d->sm_count) != 0)
             return 0;
         return plan.ws_weights_bytes + plan.ws_pool_bytes;
     }
     if (op == FC_OP_LINEAR_LSE_MISH) {
-        if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1) return 0;
+        if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1 || dtype == FC_F32_3XTF32) return 0;
         fc::LinearPlan plan;
         if (fc::linear_plan(&plan, n_or_m, cin_or_k, cout_or_nout, dtype == FC_BF16, d->sm_count) != 0) return 0;
         return plan.ws_bytes;

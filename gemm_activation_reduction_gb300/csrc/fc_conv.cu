@@ -16,15 +16,18 @@ namespace {
 // Re-lay w [Co][Cin][3][3] for `halves` CTAs of a group (2 for a CTA pair, else 1) as
 // Cout >= Co channels (Cout a multiple of 16; channels past Co get zero weights and bias):
 // CTA r holds output channels [r hc, (r+1) hc), hc = Cout / halves.  Layout
-// [r][K block][tap][half][co'][G]
+// [r][K stage][tap][half][co'][G]
 // (G = 4 fp32 rounded to TF32, or 8 bf16; co' the channel within the half),
-// zero-padding channels past Cin; then the B operands of the bias K step,
+// zero-padding channels past Cin.  With parts = 3 (split TF32) every K block of
+// channels is three consecutive K stages whose B operands are the TF32 high part,
+// the TF32 remainder w - hi, and the high part again (the A side stages x_hi, x_hi,
+// x_lo), so the stages sum hi*hi + hi*lo + lo*hi.  Then the B operands of the bias K step,
 // [r][half][co'][G]: half 0 holds the bias (fp32: its TF32 high part in k 0 and
 // the TF32 remainder in k 2; bf16: the bias in k 0) and the padding value in k 1;
 // half 1 is zero.
 template <bool BF16>
 __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Co, int Cout,
-                                            int ncb, int halves)
+                                            int ncb, int halves, int parts)
 {
     constexpr int G = BF16 ? 8 : 4;
     const int hc = Cout / halves;
@@ -69,9 +72,11 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
         f /= 2;
         const int tap = static_cast<int>(f % 9);
         f /= 9;
-        const int cb = static_cast<int>(f % ncb);
+        const int kb = static_cast<int>(f % ncb);
         const int rank = static_cast<int>(f / ncb);
         const int co = rank * hc + col;
+        const int cb = kb / parts;
+        const bool lo_part = parts == 3 && kb - cb * parts == 1;
         const int ci = cb * 2 * G + half * G + e;
         const size_t src = (static_cast<size_t>(co) * Cin + ci) * 9 + tap;
         const bool real = ci < Cin && co < Co;
@@ -80,7 +85,9 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
             reinterpret_cast<unsigned short*>(wr)[i] = real ? ws[src] : static_cast<unsigned short>(0);
         } else {
             const float* ws = reinterpret_cast<const float*>(w);
-            reinterpret_cast<float*>(wr)[i] = real ? to_tf32(ws[src]) : 0.0f;
+            const float v = real ? ws[src] : 0.0f;
+            const float hi = to_tf32(v);
+            reinterpret_cast<float*>(wr)[i] = lo_part ? to_tf32(v - hi) : hi;
         }
     }
 }
@@ -142,9 +149,12 @@ Geometry geometry(int bf16, int pool, int pair)
 
 }  // namespace
 
-int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count)
+int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int dtype, int pool, int sm_count)
 {
     *p = ConvPlan{};
+    if (dtype < 0 || dtype > 2) return 2;
+    const int bf16 = dtype == 1 ? 1 : 0;
+    p->parts = dtype == 2 ? 3 : 1;
     if (Cout < 1 || Cout > 256) return 2;
     p->N = N; p->Cin = Cin; p->H = H; p->W = W; p->Co = Cout;
     // the MMA's N: whole 16-column slices; the padded channels are computed and dropped
@@ -154,7 +164,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int bf16, int
     p->bf16 = bf16; p->pool = pool;
     p->esize = bf16 ? 2 : 4;
     p->cb_ch = bf16 ? 16 : 8;
-    p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch;
+    p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch * p->parts;
     // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) for Cout > 128, where
     // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
     // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
@@ -245,10 +255,10 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         const int halves = p.pair ? 2 : 1;
         if (p.bf16)
             conv_weight_relayout_kernel<true><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Co, p.Cout, p.ncb,
-                                                                               halves);
+                                                                               halves, p.parts);
         else
             conv_weight_relayout_kernel<false><<<blocks, threads, 0, stream>>>(w, b, wr, p.Cin, p.Co, p.Cout, p.ncb,
-                                                                                halves);
+                                                                                halves, p.parts);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -278,7 +288,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
     a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.Co = p.Co; a.OH = p.OH; a.OW = p.OW;
-    a.ncb = p.ncb; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
+    a.ncb = p.ncb; a.parts = p.parts; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;

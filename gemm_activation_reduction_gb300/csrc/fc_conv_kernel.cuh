@@ -114,7 +114,9 @@ struct ConvArgs {
     int N, Cin, H, W, OH, OW;
     int Cout;            // tile width: output channels rounded up to 16
     int Co;              // output channels stored (<= Cout)
-    int ncb, RB, CS;
+    int ncb;             // K stages per tile (K blocks x parts)
+    int parts;           // 1, or 3 for split TF32: stages hi*hi, hi*lo, lo*hi of each K block (no other values)
+    int RB, CS;
     long long tpi;
     long long num_tiles;  // tiles of the whole call
     long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
@@ -244,11 +246,22 @@ __device__ __forceinline__ float2 ld_shared_f2(uint32_t addr)
 }
 
 // Re-lay a landed raw box into the staged strip [group][SPOS pixels][16 B].
-template <bool BF16, bool WIDE, int ROWS>
+// The TF32 operand of x for one split-TF32 part: the high part (x rounded to TF32) or,
+// with LO, the remainder x - hi rounded to TF32.
+template <bool LO>
+__device__ __forceinline__ uint32_t tf32_part(float v)
+{
+    const float hi = to_tf32(v);
+    if constexpr (LO) return __float_as_uint(to_tf32(v - hi));
+    else return __float_as_uint(hi);
+}
+
+template <bool BF16, bool WIDE, int ROWS, bool LO = false>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
 {
     using S = Shape<WIDE, ROWS>;
     using RB_ = RawBox<BF16, WIDE, ROWS>;
+    static_assert(!(BF16 && LO), "split TF32 is an fp32 mode");
     if constexpr (!BF16) {
         // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
         // (the last quad of a row holds SC % 4 staged pixels; the raw box is wider)
@@ -268,15 +281,15 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
             for (int c = 0; c < 4; ++c) v[c] = ld_shared_f4(src + static_cast<uint32_t>(c) * RB_::kChPlane);
             const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
                                  static_cast<uint32_t>(row * S::SC + 4 * cq) * 16u;
-            st_shared_v4(dst, __float_as_uint(to_tf32(v[0].x)), __float_as_uint(to_tf32(v[1].x)),
-                         __float_as_uint(to_tf32(v[2].x)), __float_as_uint(to_tf32(v[3].x)));
-            st_shared_v4(dst + 16u, __float_as_uint(to_tf32(v[0].y)), __float_as_uint(to_tf32(v[1].y)),
-                         __float_as_uint(to_tf32(v[2].y)), __float_as_uint(to_tf32(v[3].y)));
+            st_shared_v4(dst, tf32_part<LO>(v[0].x), tf32_part<LO>(v[1].x), tf32_part<LO>(v[2].x),
+                         tf32_part<LO>(v[3].x));
+            st_shared_v4(dst + 16u, tf32_part<LO>(v[0].y), tf32_part<LO>(v[1].y), tf32_part<LO>(v[2].y),
+                         tf32_part<LO>(v[3].y));
             if (4 * cq + 2 < S::SC) {
-                st_shared_v4(dst + 32u, __float_as_uint(to_tf32(v[0].z)), __float_as_uint(to_tf32(v[1].z)),
-                             __float_as_uint(to_tf32(v[2].z)), __float_as_uint(to_tf32(v[3].z)));
-                st_shared_v4(dst + 48u, __float_as_uint(to_tf32(v[0].w)), __float_as_uint(to_tf32(v[1].w)),
-                             __float_as_uint(to_tf32(v[2].w)), __float_as_uint(to_tf32(v[3].w)));
+                st_shared_v4(dst + 32u, tf32_part<LO>(v[0].z), tf32_part<LO>(v[1].z), tf32_part<LO>(v[2].z),
+                             tf32_part<LO>(v[3].z));
+                st_shared_v4(dst + 48u, tf32_part<LO>(v[0].w), tf32_part<LO>(v[1].w), tf32_part<LO>(v[2].w),
+                             tf32_part<LO>(v[3].w));
             }
         }
     } else {
@@ -305,10 +318,11 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
 
 // Fallback staging with plain loads (when x's row pitch is not a 16-byte
 // multiple and TMA cannot address it): one K block of the halo patch as
-// [group][SPOS pixels][16 B], zero past the image and past Cin.
+// [group][SPOS pixels][16 B], zero past the image and past Cin; `lo` stages the
+// split-TF32 remainder instead of the high part (fp32 only).
 template <bool BF16, bool WIDE, int ROWS>
 __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
-                                           int Cin, int H, int W, int lane)
+                                           int Cin, int H, int W, int lane, bool lo)
 {
     using S = Shape<WIDE, ROWS>;
     const size_t HW = static_cast<size_t>(H) * W;
@@ -324,10 +338,11 @@ __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = (ok && ci0 + e < Cin) ? __ldg(x + off + e * HW) : 0.0f;
-            st_shared_v4(a, __float_as_uint(to_tf32(v[0])), __float_as_uint(to_tf32(v[1])),
-                         __float_as_uint(to_tf32(v[2])), __float_as_uint(to_tf32(v[3])));
-            st_shared_v4(a + S::PLANE, __float_as_uint(to_tf32(v[4])), __float_as_uint(to_tf32(v[5])),
-                         __float_as_uint(to_tf32(v[6])), __float_as_uint(to_tf32(v[7])));
+            uint32_t t[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = lo ? tf32_part<true>(v[e]) : tf32_part<false>(v[e]);
+            st_shared_v4(a, t[0], t[1], t[2], t[3]);
+            st_shared_v4(a + S::PLANE, t[4], t[5], t[6], t[7]);
         } else {
             const unsigned short* x = reinterpret_cast<const unsigned short*>(xv);
             const int ci0 = cb * 16;
@@ -597,7 +612,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&rawfull[r], RBox::kBytes);
                     tma_load_4d(smem + a.raw_off + r * RBox::kBytes, &tmx, &rawfull[r], atc.cs * S::PC,
-                                atc.rb * S::PR, acb * RBox::kCh, atc.n);
+                                atc.rb * S::PR, (a.parts == 1 ? acb : acb / 3) * RBox::kCh, atc.n);
                 }
                 ++issued;
                 advance(atc, alt, acb, kNumProd);
@@ -628,13 +643,21 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t r = raw_buf(use);
                     ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
-                    transpose_raw<BF16, WIDE, ROWS>(smem_u32(smem + a.raw_off + r * RBox::kBytes), strip, lane);
+                    const uint32_t raw = smem_u32(smem + a.raw_off + r * RBox::kBytes);
+                    // split TF32: the third stage of each K block stages x's remainder
+                    if constexpr (!BF16) {
+                        if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, true>(raw, strip, lane);
+                        else transpose_raw<BF16, WIDE, ROWS>(raw, strip, lane);
+                    } else {
+                        transpose_raw<BF16, WIDE, ROWS>(raw, strip, lane);
+                    }
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
                     if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
-                    fill_strip<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, cb, tc.rb * S::PR, tc.cs * S::PC, a.Cin,
-                                           tc.n < a.N ? a.H : 0, a.W, lane);
+                    fill_strip<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3, tc.rb * S::PR,
+                                                 tc.cs * S::PC, a.Cin, tc.n < a.N ? a.H : 0, a.W, lane,
+                                                 a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }

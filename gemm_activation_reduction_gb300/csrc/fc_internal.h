@@ -26,9 +26,10 @@ struct ConvPlan {
     int Cout;             // Co rounded up to 16: the MMA tile width; channels >= Co carry zero
                           // weights and bias and are never stored
     int bf16, pool;
+    int parts;            // products per K block: 1, or 3 for split TF32 (hi*hi, hi*lo, lo*hi)
     int esize;            // bytes per stored element (4 or 2)
     int cb_ch;            // input channels per K block (8 fp32, 16 bf16)
-    int ncb;              // K blocks = ceil(Cin / cb_ch)
+    int ncb;              // K stages per tile = ceil(Cin / cb_ch) * parts
     int RB, CS;           // output row blocks and column strips per image (tiles of 16 x 8, or 1 x 128)
     long long tpi;        // tiles per image = RB * CS
     long long num_tiles;  // N * tpi
@@ -56,7 +57,8 @@ struct ConvPlan {
 
 // Fills `plan`; returns 0 on success, 2 (unsupported) when the shape is outside
 // what the kernels cover.
-int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int bf16, int pool, int sm_count);
+// dtype: 0 fp32 (TF32 products), 1 bf16, 2 fp32 with split-TF32 products (the fc_dtype codes).
+int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int dtype, int pool, int sm_count);
 
 cudaError_t conv_launch(const ConvPlan& plan, const void* x, const void* w, const void* b, float* y, int act,
                         void* workspace, cudaStream_t stream, int* status, long long budget);

@@ -29,7 +29,11 @@
  *     do not matter.  Two calls that share a workspace must not overlap.
  *   - Floating point: fp32 inputs run on TF32 tensor cores (operands rounded
  *     to nearest TF32), bf16 inputs on BF16 tensor cores; accumulation,
- *     activation and reduction are fp32; outputs are fp32.
+ *     activation and reduction are fp32; outputs are fp32.  FC_F32_3XTF32
+ *     (conv ops) takes the same fp32 inputs but splits each operand into a
+ *     TF32 high part and a TF32 remainder and sums three products per term
+ *     (hi*hi + hi*lo + lo*hi), which brings the contraction's error to fp32
+ *     level at three times the tensor-core work.
  */
 #ifndef FC_H_
 #define FC_H_
@@ -52,7 +56,11 @@ typedef enum {
     FC_ERR_TIMEOUT = 5        /* a kernel's bounded wait ran out (see fc_device_status) */
 } fc_status;
 
-typedef enum { FC_F32 = 0, FC_BF16 = 1 } fc_dtype;
+typedef enum {
+    FC_F32 = 0,          /* fp32 storage, TF32 tensor-core products */
+    FC_BF16 = 1,         /* bf16 storage, BF16 tensor-core products */
+    FC_F32_3XTF32 = 2    /* fp32 storage, split TF32 (3 products per term); conv ops only */
+} fc_dtype;
 
 typedef enum {
     FC_ACT_GELU_ERF = 0,      /* 0.5 v (1 + erf(v / sqrt 2)), torch's exact GELU */
@@ -82,6 +90,7 @@ typedef enum {
  *   w   [Cout, Cin, 3, 3]  same dtype, OIHW
  *   b   [Cout]             same dtype
  *   y   [N, Cout]          fp32 output
+ *   dtype FC_F32 or FC_F32_3XTF32 (fp32 x, w, b) or FC_BF16 (bf16 x, w, b).
  *   Requires N, Cin >= 1; H, W >= 3; 1 <= Cout <= 256 (else FC_ERR_UNSUPPORTED).
  *   A Cout that is not a multiple of 16 runs as the next multiple with the
  *   extra channels zero and unstored.  The mean is a fixed-order two-stage sum:
@@ -121,7 +130,8 @@ fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y,
  *   tensor-core products) or all bf16 (dtype FC_BF16); y [M] fp32 (the (M, 1)
  *   output, contiguous); fp32 accumulation and epilogue either way.
  *   Requires M, Nout >= 1, a 16-byte row pitch (K % 4 == 0 for fp32, K % 8 == 0
- *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.
+ *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.  dtype
+ *   FC_F32_3XTF32 returns FC_ERR_UNSUPPORTED (no split-TF32 GEMM).
  */
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y,
                              int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,

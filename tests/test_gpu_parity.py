@@ -8,6 +8,7 @@ are checked in the launch configuration the benchmark times, on outputs the
 oracle computes one by one (random samples plus every border row/column of
 a few planes).
 """
+import ctypes
 import math
 
 import numpy as np
@@ -99,6 +100,63 @@ def test_conv_act_small(cuda_lib, shape):
     _check(y, ref, TOL[dt], f"act {shape}")
 
 
+# ------------------------------------------------------------------ split TF32 (FC_F32_3XTF32)
+
+# Tolerance: each product of TF32 parts misses only lo*lo and the parts' own rounding (about
+# 3 * 2^-22 of |x w|), the fp32 accumulation of K <= 1152 terms adds about 2^-24 of the running
+# sum per addition, and the activations' approximate exponential / reciprocal about 1e-6: the
+# outputs land within a few 1e-6.  2e-5 (1 + |ref|) is 100x tighter than the TF32 bar and 5x
+# tighter than the pages' own atol = rtol = 1e-4, which their TF32-backed results missed.
+TOL_X3 = 2e-5
+
+X3_SHAPES = [
+    # (N, Cin, H, W, Cout, act, pool)
+    (2, 8, 32, 32, 64, "gelu", True),          # the tiny workload
+    (1, 13, 20, 37, 96, "gelu", True),         # Cin not a multiple of 8, ragged edges
+    (1, 64, 21, 18, 128, "mish", True),        # 24 K stages, streamed weights
+    (1, 8, 40, 17, 256, "gelu", True),         # CTA pairs
+    (1, 3, 11, 13, 40, "gelu_tanh", True),     # row pitch not a 16-byte multiple: plain-load staging
+    (2, 5, 13, 150, 64, "mish_mish", False),   # two-row tiles, rows wider than one tile
+    (1, 64, 12, 140, 128, "mish_mish", False), # the Mish->Mish page's channel counts
+    (1, 16, 9, 133, 200, "mish", False),       # CTA pairs, padded Cout
+    (1, 3, 9, 13, 40, "gelu", False),          # plain-load staging, full output
+]
+
+
+@pytest.mark.parametrize("shape", X3_SHAPES, ids=lambda s: "x".join(map(str, s[:5])) + f"-{s[5]}-{'pool' if s[6] else 'act'}")
+def test_conv_split_tf32_small(cuda_lib, shape):
+    N, Cin, H, W, Cout, act, pool = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout)
+    f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+    y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act, precision="3xtf32").cpu().numpy()
+    ref = (oracle.conv3x3_act_pool if pool else oracle.conv3x3_act)(d["x"], d["w"], d["b"], act)
+    _check(y, ref, TOL_X3, f"3xtf32 {shape}")
+
+
+def test_split_tf32_is_far_more_accurate_than_tf32(cuda_lib):
+    """Same inputs, both precisions: the split-TF32 error is at least 30x below the TF32 error
+    (TF32 rounds each operand to 11 significant bits, so its error is ~2^-11 of sum |x w|)."""
+    d = fc_inputs.conv_inputs(1, 64, 12, 140, 128)
+    x, w, b = _dev(d["x"]), _dev(d["w"]), _dev(d["b"])
+    ref = oracle.conv3x3_act(d["x"], d["w"], d["b"], "mish")
+    e1 = np.abs(cuda_lib.fc_conv3x3_act(x, w, b, act="mish").cpu().numpy() - ref).max()
+    e3 = np.abs(cuda_lib.fc_conv3x3_act(x, w, b, act="mish", precision="3xtf32").cpu().numpy() - ref).max()
+    assert e3 * 30 < e1, (e1, e3)
+
+
+def test_split_tf32_rejects_bf16_inputs(cuda_lib):
+    import torch
+    d = fc_inputs.conv_inputs(1, 8, 16, 16, 64, "bf16")
+    with pytest.raises(ValueError):
+        cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), precision="3xtf32")
+    lib = cuda_lib.load()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    v = torch.zeros(1024, device="cuda")
+    # the linear op has no split-TF32 mode
+    assert lib.fc_linear_lse_mish(v.data_ptr(), v.data_ptr(), v.data_ptr(), v.data_ptr(), 4, 8, 8, 2.0, -1.0, 1.0,
+                                  cuda_lib.FC_F32_3XTF32, None, 0, s) == cuda_lib.FC_ERR_UNSUPPORTED
+
+
 # ------------------------------------------------------------------ linear chain
 
 LIN_SHAPES = [
@@ -142,24 +200,26 @@ def test_linear_small_bf16(cuda_lib, shape):
 
 # ------------------------------------------------------------------ full-size workloads
 
-@pytest.mark.parametrize("key", ["B", "Bt"])
+@pytest.mark.parametrize("key", ["B", "Bt", "B3"])
 def test_workload_B_full_size_sampled(cuda_lib, key):
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
-    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act).cpu().numpy()
+    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
+                                     precision=wl.precision).cpu().numpy()
     rng = np.random.default_rng(7)
     flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 192, replace=False),
                                      np.arange(wl.Cout), np.arange((wl.N - 1) * wl.Cout, wl.N * wl.Cout)]))
     ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
-    _check(y.reshape(-1)[flat], ref, TOL["f32"], f"workload {key}")
+    _check(y.reshape(-1)[flat], ref, TOL_X3 if wl.precision == "3xtf32" else TOL["f32"], f"workload {key}")
 
 
-@pytest.mark.parametrize("key", ["C", "Cb"])
+@pytest.mark.parametrize("key", ["C", "Cb", "C3"])
 def test_workload_C_full_size_sampled(cuda_lib, key):
     import torch
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
-    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act)
+    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
+                                precision=None if wl.dtype == "bf16" else wl.precision)
     OH, OW = wl.OH, wl.OW
     rng = np.random.default_rng(8)
     total = wl.N * wl.Cout * OH * OW
@@ -173,7 +233,7 @@ def test_workload_C_full_size_sampled(cuda_lib, key):
     got = y.view(-1)[torch.from_numpy(flat).cuda()].cpu().numpy()
     del y
     ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
-    _check(got, ref, TOL[wl.dtype], f"workload {key}")
+    _check(got, ref, TOL_X3 if wl.precision == "3xtf32" else TOL[wl.dtype], f"workload {key}")
 
 
 @pytest.mark.parametrize("key", ["D", "Db"])
