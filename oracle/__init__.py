@@ -61,13 +61,13 @@ def _load():
         lib.oracle_act_mean.restype = None
         lib.oracle_scale_clamp_lse_mish_rows.argtypes = [P, I, I, D, D, D, P]
         lib.oracle_scale_clamp_lse_mish_rows.restype = I
-        lib.oracle_conv3x3_point.argtypes = [P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_conv3x3_point.argtypes = [P, P, P, I, I, I, I, I, I, I, I]
         lib.oracle_conv3x3_point.restype = D
-        lib.oracle_conv3x3_preact.argtypes = [P, P, P, P, I, I, I, I, I]
-        lib.oracle_conv3x3_act.argtypes = [P, P, P, P, I, I, I, I, I, I]
-        lib.oracle_conv3x3_act_at.argtypes = [P, P, P, I, I, I, I, I, I, P, L, P]
-        lib.oracle_conv3x3_act_pool.argtypes = [P, P, P, P, I, I, I, I, I, I]
-        lib.oracle_conv3x3_act_pool_at.argtypes = [P, P, P, I, I, I, I, I, I, P, L, P]
+        lib.oracle_conv3x3_preact.argtypes = [P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_conv3x3_act.argtypes = [P, P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_conv3x3_act_at.argtypes = [P, P, P, I, I, I, I, I, I, I, P, L, P]
+        lib.oracle_conv3x3_act_pool.argtypes = [P, P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_conv3x3_act_pool_at.argtypes = [P, P, P, I, I, I, I, I, I, I, P, L, P]
         lib.oracle_logsumexp.argtypes = [P, L]
         lib.oracle_logsumexp.restype = D
         lib.oracle_linear_lse_mish_rows.argtypes = [P, P, P, I, I, I, D, D, D, P, L, P, P]
@@ -148,53 +148,64 @@ def logsumexp(t) -> float:
     return _load().oracle_logsumexp(_p(t), t.size)
 
 
-def conv3x3_preact(x, w, b):
+def _out_hw(H, W, pad):
+    if pad < 0 or H + 2 * pad < 3 or W + 2 * pad < 3:
+        raise ValueError("padding must be >= 0 and leave an output of at least 1 x 1")
+    return H + 2 * pad - 2, W + 2 * pad - 2
+
+
+def conv3x3_preact(x, w, b, pad=0):
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
-    out = np.empty((N, Cout, H - 2, W - 2), dtype=np.float64)
-    _load().oracle_conv3x3_preact(_p(x), _p(w), _p(b), _p(out), N, Cin, H, W, Cout)
+    OH, OW = _out_hw(H, W, pad)
+    out = np.empty((N, Cout, OH, OW), dtype=np.float64)
+    _load().oracle_conv3x3_preact(_p(x), _p(w), _p(b), _p(out), N, Cin, H, W, Cout, pad)
     return out
 
 
-def conv3x3_act(x, w, b, act="mish_mish"):
+def conv3x3_act(x, w, b, act="mish_mish", pad=0):
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
-    out = np.empty((N, Cout, H - 2, W - 2), dtype=np.float64)
-    _load().oracle_conv3x3_act(_p(x), _p(w), _p(b), _p(out), N, Cin, H, W, Cout, ACT[act])
+    OH, OW = _out_hw(H, W, pad)
+    out = np.empty((N, Cout, OH, OW), dtype=np.float64)
+    _load().oracle_conv3x3_act(_p(x), _p(w), _p(b), _p(out), N, Cin, H, W, Cout, pad, ACT[act])
     return out
 
 
-def conv3x3_act_at(x, w, b, flat_idx, act="mish_mish"):
-    """act(conv) at flat indices into the (N, Cout, H-2, W-2) output."""
+def conv3x3_act_at(x, w, b, flat_idx, act="mish_mish", pad=0):
+    """act(conv) at flat indices into the (N, Cout, H+2p-2, W+2p-2) output."""
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
-    idx = _indices(flat_idx, N * Cout * (H - 2) * (W - 2), "output")
+    OH, OW = _out_hw(H, W, pad)
+    idx = _indices(flat_idx, N * Cout * OH * OW, "output")
     out = np.empty(idx.size, dtype=np.float64)
-    _load().oracle_conv3x3_act_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, ACT[act],
+    _load().oracle_conv3x3_act_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, pad, ACT[act],
                                   _p(idx), idx.size, _p(out))
     return out
 
 
-def conv3x3_act_pool(x, w, b, act="gelu"):
+def conv3x3_act_pool(x, w, b, act="gelu", pad=0):
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
+    _out_hw(H, W, pad)
     y = np.empty((N, Cout), dtype=np.float64)
-    _load().oracle_conv3x3_act_pool(_p(x), _p(w), _p(b), _p(y), N, Cin, H, W, Cout, ACT[act])
+    _load().oracle_conv3x3_act_pool(_p(x), _p(w), _p(b), _p(y), N, Cin, H, W, Cout, pad, ACT[act])
     return y
 
 
-def conv3x3_act_pool_at(x, w, b, flat_nc, act="gelu"):
+def conv3x3_act_pool_at(x, w, b, flat_nc, act="gelu", pad=0):
     """Pooled output at flat (n * Cout + co) indices."""
     x, w, b = _f32(x), _f32(w), _f32(b)
     N, Cin, H, W = x.shape
     Cout = w.shape[0]
+    _out_hw(H, W, pad)
     idx = _indices(flat_nc, N * Cout, "pooled output")
     out = np.empty(idx.size, dtype=np.float64)
-    _load().oracle_conv3x3_act_pool_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, ACT[act],
+    _load().oracle_conv3x3_act_pool_at(_p(x), _p(w), _p(b), N, Cin, H, W, Cout, pad, ACT[act],
                                        _p(idx), idx.size, _p(out))
     return out
 

@@ -46,8 +46,26 @@ ACTS = {"gelu": gelu, "mish": mish, "mish_mish": lambda v: mish(mish(v)), "gelu_
         "none": lambda v: v}
 
 
-def conv3x3(x, w, b):
-    """x: nested lists [N][Cin][H][W]; w: [Cout][Cin][3][3]; b: [Cout] -> [N][Cout][H-2][W-2]."""
+def zero_pad(x, pad):
+    """x [N][C][H][W] nested lists -> [N][C][H+2p][W+2p] with p zero rows / columns on every side."""
+    out = []
+    for img in x:
+        planes = []
+        for plane in img:
+            Wp = len(plane[0]) + 2 * pad
+            rows = [[0.0] * Wp for _ in range(pad)]
+            rows += [[0.0] * pad + list(r) + [0.0] * pad for r in plane]
+            rows += [[0.0] * Wp for _ in range(pad)]
+            planes.append(rows)
+        out.append(planes)
+    return out
+
+
+def conv3x3(x, w, b, pad=0):
+    """x: nested lists [N][Cin][H][W]; w: [Cout][Cin][3][3]; b: [Cout] -> [N][Cout][H+2p-2][W+2p-2],
+    padding p taken as an explicitly zero-extended input."""
+    if pad:
+        x = zero_pad(x, pad)
     N, Cin, H, W = len(x), len(x[0]), len(x[0][0]), len(x[0][0][0])
     Cout = len(w)
     out = []
@@ -70,14 +88,14 @@ def conv3x3(x, w, b):
     return out
 
 
-def conv3x3_act(x, w, b, act):
+def conv3x3_act(x, w, b, act, pad=0):
     f = ACTS[act]
-    return [[[[f(v) for v in row] for row in plane] for plane in img] for img in conv3x3(x, w, b)]
+    return [[[[f(v) for v in row] for row in plane] for plane in img] for img in conv3x3(x, w, b, pad)]
 
 
-def conv3x3_act_pool(x, w, b, act):
+def conv3x3_act_pool(x, w, b, act, pad=0):
     out = []
-    for img in conv3x3_act(x, w, b, act):
+    for img in conv3x3_act(x, w, b, act, pad):
         out.append([math.fsum(v for row in plane for v in row) / (len(plane) * len(plane[0]))
                     for plane in img])
     return out

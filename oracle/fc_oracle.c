@@ -68,45 +68,54 @@ double oracle_act(int act, double v)
 
 /* ------------------------------------------------------------------- conv */
 
-/* Pre-activation of Conv2d(k=3, stride 1, padding 0, dilation 1, groups 1)
- * with bias at one output point: cross-correlation (no kernel flip),
- *   v = b[co] + sum_{ci} sum_{kh<3} sum_{kw<3} x[n,ci,oh+kh,ow+kw] * w[co,ci,kh,kw].
- * x is NCHW, w is OIHW, both contiguous. */
+/* Pre-activation of Conv2d(k=3, stride 1, padding p, dilation 1, groups 1)
+ * with bias at one output point: cross-correlation (no kernel flip) over the
+ * input extended by p zero rows / columns on every side (padding_mode zeros),
+ *   v = b[co] + sum_{ci} sum_{kh<3} sum_{kw<3} x[n,ci,oh+kh-p,ow+kw-p] * w[co,ci,kh,kw],
+ * terms outside the input omitted.  x is NCHW, w is OIHW, both contiguous.
+ * The pages' operators use p = 0 (output (H-2) x (W-2)); p > 0 is the general
+ * padding variant (output (H+2p-2) x (W+2p-2)). */
 double oracle_conv3x3_point(const float* x, const float* w, const float* b,
-                            int Cin, int H, int W, int n, int co, int oh, int ow)
+                            int Cin, int H, int W, int pad, int n, int co, int oh, int ow)
 {
     double acc = (double)b[co];
     for (int ci = 0; ci < Cin; ++ci) {
-        const float* xp = x + (((int64_t)n * Cin + ci) * H + oh) * (int64_t)W + ow;
+        const float* xp = x + ((int64_t)n * Cin + ci) * H * (int64_t)W;
         const float* wp = w + ((int64_t)co * Cin + ci) * 9;
-        for (int kh = 0; kh < 3; ++kh)
-            for (int kw = 0; kw < 3; ++kw)
-                acc += (double)xp[(int64_t)kh * W + kw] * (double)wp[kh * 3 + kw];
+        for (int kh = 0; kh < 3; ++kh) {
+            const int ih = oh + kh - pad;
+            if (ih < 0 || ih >= H) continue;
+            for (int kw = 0; kw < 3; ++kw) {
+                const int iw = ow + kw - pad;
+                if (iw < 0 || iw >= W) continue;
+                acc += (double)xp[(int64_t)ih * W + iw] * (double)wp[kh * 3 + kw];
+            }
+        }
     }
     return acc;
 }
 
-/* Full pre-activation output, (N, Cout, H-2, W-2). */
+/* Full pre-activation output, (N, Cout, H+2p-2, W+2p-2). */
 void oracle_conv3x3_preact(const float* x, const float* w, const float* b, double* out,
-                           int N, int Cin, int H, int W, int Cout)
+                           int N, int Cin, int H, int W, int Cout, int pad)
 {
-    const int OH = H - 2, OW = W - 2;
+    const int OH = H + 2 * pad - 2, OW = W + 2 * pad - 2;
 #pragma omp parallel for collapse(2) schedule(static)
     for (int n = 0; n < N; ++n)
         for (int co = 0; co < Cout; ++co) {
             double* o = out + ((int64_t)n * Cout + co) * OH * (int64_t)OW;
             for (int oh = 0; oh < OH; ++oh)
                 for (int ow = 0; ow < OW; ++ow)
-                    o[(int64_t)oh * OW + ow] = oracle_conv3x3_point(x, w, b, Cin, H, W, n, co, oh, ow);
+                    o[(int64_t)oh * OW + ow] = oracle_conv3x3_point(x, w, b, Cin, H, W, pad, n, co, oh, ow);
         }
 }
 
-/* act(conv + bias), full output (N, Cout, H-2, W-2).  With act = Mish twice this
- * is the Conv->Mish->Mish chain. */
+/* act(conv + bias), full output (N, Cout, H+2p-2, W+2p-2).  With act = Mish twice
+ * and p = 0 this is the Conv->Mish->Mish chain. */
 void oracle_conv3x3_act(const float* x, const float* w, const float* b, double* out,
-                        int N, int Cin, int H, int W, int Cout, int act)
+                        int N, int Cin, int H, int W, int Cout, int pad, int act)
 {
-    const int OH = H - 2, OW = W - 2;
+    const int OH = H + 2 * pad - 2, OW = W + 2 * pad - 2;
 #pragma omp parallel for collapse(2) schedule(static)
     for (int n = 0; n < N; ++n)
         for (int co = 0; co < Cout; ++co) {
@@ -114,16 +123,16 @@ void oracle_conv3x3_act(const float* x, const float* w, const float* b, double* 
             for (int oh = 0; oh < OH; ++oh)
                 for (int ow = 0; ow < OW; ++ow)
                     o[(int64_t)oh * OW + ow] =
-                        oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, n, co, oh, ow));
+                        oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, pad, n, co, oh, ow));
         }
 }
 
-/* The same chain at a list of flat output indices into (N, Cout, H-2, W-2). */
+/* The same chain at a list of flat output indices into (N, Cout, H+2p-2, W+2p-2). */
 void oracle_conv3x3_act_at(const float* x, const float* w, const float* b,
-                           int N, int Cin, int H, int W, int Cout, int act,
+                           int N, int Cin, int H, int W, int Cout, int pad, int act,
                            const int64_t* idx, int64_t count, double* out)
 {
-    const int64_t OH = H - 2, OW = W - 2;
+    const int64_t OH = H + 2 * pad - 2, OW = W + 2 * pad - 2;
     (void)N;
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < count; ++i) {
@@ -132,43 +141,43 @@ void oracle_conv3x3_act_at(const float* x, const float* w, const float* b,
         int oh = (int)(f % OH); f /= OH;
         int co = (int)(f % Cout);
         int n = (int)(f / Cout);
-        out[i] = oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, n, co, oh, ow));
+        out[i] = oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, pad, n, co, oh, ow));
     }
 }
 
 /* Global average pool of act(conv + bias) over the OH x OW plane (adaptive
  * average pool to 1x1, then squeeze), y (N, Cout):
- *   y[n,co] = (sum_{oh,ow} act(v[n,co,oh,ow])) / ((H-2)(W-2)),
+ *   y[n,co] = (sum_{oh,ow} act(v[n,co,oh,ow])) / (OH OW),  OH = H+2p-2, OW = W+2p-2,
  * summed in row-major (oh, ow) order. */
 static double pool_one(const float* x, const float* w, const float* b,
-                       int Cin, int H, int W, int act, int n, int co)
+                       int Cin, int H, int W, int pad, int act, int n, int co)
 {
-    const int OH = H - 2, OW = W - 2;
+    const int OH = H + 2 * pad - 2, OW = W + 2 * pad - 2;
     double s = 0.0;
     for (int oh = 0; oh < OH; ++oh)
         for (int ow = 0; ow < OW; ++ow)
-            s += oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, n, co, oh, ow));
+            s += oracle_act(act, oracle_conv3x3_point(x, w, b, Cin, H, W, pad, n, co, oh, ow));
     return s / ((double)OH * (double)OW);
 }
 
 void oracle_conv3x3_act_pool(const float* x, const float* w, const float* b, double* y,
-                             int N, int Cin, int H, int W, int Cout, int act)
+                             int N, int Cin, int H, int W, int Cout, int pad, int act)
 {
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int n = 0; n < N; ++n)
         for (int co = 0; co < Cout; ++co)
-            y[(int64_t)n * Cout + co] = pool_one(x, w, b, Cin, H, W, act, n, co);
+            y[(int64_t)n * Cout + co] = pool_one(x, w, b, Cin, H, W, pad, act, n, co);
 }
 
 /* The pool at a list of flat (n * Cout + co) indices. */
 void oracle_conv3x3_act_pool_at(const float* x, const float* w, const float* b,
-                                int N, int Cin, int H, int W, int Cout, int act,
+                                int N, int Cin, int H, int W, int Cout, int pad, int act,
                                 const int64_t* idx, int64_t count, double* out)
 {
     (void)N;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < count; ++i)
-        out[i] = pool_one(x, w, b, Cin, H, W, act, (int)(idx[i] / Cout), (int)(idx[i] % Cout));
+        out[i] = pool_one(x, w, b, Cin, H, W, pad, act, (int)(idx[i] / Cout), (int)(idx[i] % Cout));
 }
 
 /* ----------------------------------------------------------------- linear */

@@ -145,6 +145,62 @@ def test_conv_act_against_brute_force(shape, act):
     np.testing.assert_array_equal(oracle.conv3x3_act_pool_at(x, w, b, flat_nc, act), got_pool.reshape(-1)[flat_nc])
 
 
+# Padding (the general-padding variant; zero padding, PyTorch's padding_mode 'zeros').
+
+def test_conv_padding_one_with_centre_delta_is_identity():
+    """'same' conv: p = 1 and w[co, ci, 1, 1] = [co == ci] reproduce the input exactly."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((2, 3, 6, 7)).astype(np.float32)
+    w = np.zeros((3, 3, 3, 3), np.float32)
+    for c in range(3):
+        w[c, c, 1, 1] = 1.0
+    pre = oracle.conv3x3_preact(x, w, np.zeros(3, np.float32), pad=1)
+    np.testing.assert_array_equal(pre, x.astype(np.float64))
+
+
+@pytest.mark.parametrize("pad", [1, 2, 5])
+def test_conv_padding_equals_conv_of_zero_extended_input(pad):
+    d = fc_inputs.conv_inputs(2, 3, 5, 7, 4, seeds=(51, 52, 53))
+    x, w, b = d["x"], d["w"], d["b"]
+    xp = np.pad(x, ((0, 0), (0, 0), (pad, pad), (pad, pad)))
+    got = oracle.conv3x3_act(x, w, b, "mish", pad=pad)
+    assert got.shape == (2, 4, 5 + 2 * pad - 2, 7 + 2 * pad - 2)
+    # the same terms in the same order apart from zero products: equal to fp64 rounding
+    np.testing.assert_allclose(got, oracle.conv3x3_act(xp, w, b, "mish"), rtol=1e-15, atol=1e-16)
+    np.testing.assert_allclose(oracle.conv3x3_act_pool(x, w, b, "gelu", pad=pad),
+                               oracle.conv3x3_act_pool(xp, w, b, "gelu"), rtol=1e-14, atol=1e-16)
+
+
+@pytest.mark.parametrize("act", ["gelu", "mish_mish"])
+def test_conv_padding_against_brute_force(act):
+    d = fc_inputs.conv_inputs(1, 2, 4, 5, 3, seeds=(54, 55, 56))
+    x, w, b = d["x"], d["w"], d["b"]
+    for pad in (1, 3):
+        ref = np.array(brute.conv3x3_act(_tolist(x), _tolist(w), _tolist(b), act, pad))
+        np.testing.assert_allclose(oracle.conv3x3_act(x, w, b, act, pad=pad), ref, rtol=1e-12, atol=1e-14)
+        ref_pool = np.array(brute.conv3x3_act_pool(_tolist(x), _tolist(w), _tolist(b), act, pad))
+        np.testing.assert_allclose(oracle.conv3x3_act_pool(x, w, b, act, pad=pad), ref_pool, rtol=1e-12,
+                                   atol=1e-14)
+        flat = np.arange(ref.size)[::2]
+        np.testing.assert_array_equal(oracle.conv3x3_act_at(x, w, b, flat, act, pad=pad),
+                                      oracle.conv3x3_act(x, w, b, act, pad=pad).reshape(-1)[flat])
+
+
+def test_conv_padding_corner_sees_one_tap():
+    """With p = 2 the output corner (0, 0) overlaps the input only at x[0, 0] through tap (2, 2)."""
+    d = fc_inputs.conv_inputs(1, 2, 6, 6, 2, seeds=(57, 58, 59))
+    x, w, b = d["x"], d["w"], d["b"]
+    pre = oracle.conv3x3_preact(x, w, b, pad=2)
+    for co in range(2):
+        v = math.fsum([float(b[co])] + [float(x[0, ci, 0, 0]) * float(w[co, ci, 2, 2]) for ci in range(2)])
+        assert pre[0, co, 0, 0] == pytest.approx(v, rel=1e-15)
+        # and the far corner through tap (0, 0)
+        v2 = math.fsum([float(b[co])] + [float(x[0, ci, 5, 5]) * float(w[co, ci, 0, 0]) for ci in range(2)])
+        assert pre[0, co, -1, -1] == pytest.approx(v2, rel=1e-15)
+    with pytest.raises(ValueError):
+        oracle.conv3x3_preact(x, w, b, pad=-1)
+
+
 def test_pool_with_zero_weights_is_act_of_bias():
     d = fc_inputs.conv_inputs(2, 3, 9, 11, 6, seeds=(31, 32, 33))
     y = oracle.conv3x3_act_pool(d["x"], np.zeros_like(d["w"]), d["b"], "gelu")
