@@ -182,12 +182,12 @@ def make_call(fc, torch, key, d, device):
     op = "conv3x3_act_pool" if wl.pool else "conv3x3_act"
     shape = (wl.N, wl.Cout) if wl.pool else (wl.N, wl.Cout, wl.OH, wl.OW)
     out = torch.empty(shape, dtype=torch.float32, device=device)
-    ws = torch.empty(max(1, fc.fc_workspace_bytes(op, wl.N, wl.Cin, wl.H, wl.W, wl.Cout, dt)), dtype=torch.uint8,
-                     device=device)
+    ws = torch.empty(max(1, fc.load().fc_workspace_bytes_pad(fc.OPS[op], wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.pad,
+                                                              dt)), dtype=torch.uint8, device=device)
     f = fc.fc_conv3x3_act_pool if wl.pool else fc.fc_conv3x3_act
 
     def call():
-        f(x, w, b, act=wl.act, out=out, workspace=ws, precision=prec)
+        f(x, w, b, act=wl.act, out=out, workspace=ws, precision=prec, pad=wl.pad)
     return call, (3 if wl.pool else 2), out
 
 
@@ -260,9 +260,9 @@ def time_e2e(fc, torch, key, d, device, steps, warmup):
         if isinstance(wl, fc_inputs.LinearWorkload):
             y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi)
         elif wl.pool:
-            y = fc.fc_conv3x3_act_pool(*dev, act=wl.act, precision=None if bf16 else wl.precision)
+            y = fc.fc_conv3x3_act_pool(*dev, act=wl.act, precision=None if bf16 else wl.precision, pad=wl.pad)
         else:
-            y = fc.fc_conv3x3_act(*dev, act=wl.act, precision=None if bf16 else wl.precision)
+            y = fc.fc_conv3x3_act(*dev, act=wl.act, precision=None if bf16 else wl.precision, pad=wl.pad)
         return y.to("cpu", non_blocking=False)
 
     for _ in range(warmup):
@@ -289,11 +289,11 @@ def oracle_sample(key, budget_s=12.0):
         total_units, what = wl.M, "rows"
     elif wl.pool:
         unit_flops = 2.0 * wl.OH * wl.OW * wl.Cin * 9   # one (n, co) pooled output
-        run = lambda idx: oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], idx, wl.act)
+        run = lambda idx: oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], idx, wl.act, pad=wl.pad)
         total_units, what = wl.N * wl.Cout, "(image, channel) pooled outputs"
     else:
         unit_flops = 2.0 * wl.Cin * 9                    # one output element
-        run = lambda idx: oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], idx, wl.act)
+        run = lambda idx: oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], idx, wl.act, pad=wl.pad)
         total_units, what = wl.N * wl.Cout * wl.OH * wl.OW, "output elements"
     n = min(total_units, max(threads, 4))
     t0 = time.perf_counter()
@@ -468,7 +468,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

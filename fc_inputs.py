@@ -54,14 +54,15 @@ class ConvWorkload:
     act: str            # "gelu" | "mish" | "mish_mish" | "gelu_tanh"
     pool: bool          # True: global mean to (N, Cout); False: full output
     precision: str = "tf32"   # fp32 storage: "tf32" or "3xtf32" (split-TF32 products); bf16: "bf16"
+    pad: int = 0              # zero padding on every side
 
     @property
     def OH(self):
-        return self.H - 2
+        return self.H + 2 * self.pad - 2
 
     @property
     def OW(self):
-        return self.W - 2
+        return self.W + 2 * self.pad - 2
 
     def flops(self) -> float:
         """Contraction flops only: 2 * outputs * (Cin * 9)."""
@@ -143,6 +144,11 @@ WORKLOADS = {
                        "3xtf32"),
     "C3": ConvWorkload("conv3x3_mish_mish_f32x3_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish",
                        False, "3xtf32"),
+    # Zero padding 1 ('same' convs: 256 x 256 outputs) at the fp32 conv pages' sizes.
+    "Bp": ConvWorkload("conv3x3_gelu_avgpool_pad1_f32_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu", True,
+                       pad=1),
+    "Cp": ConvWorkload("conv3x3_mish_mish_pad1_f32_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish",
+                       False, pad=1),
     # The pages' epilogue-only kernels at their sizes: over the conv output of the GELU->pool page,
     # the conv output of the Mish->Mish page, and the Linear output of the Linear page.
     "K1e": EpilogueWorkload("gelu_avgpool_epilogue_f32_128x64x254x254", "act_mean", (128, 64, 254, 254), "gelu"),

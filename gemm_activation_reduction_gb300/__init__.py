@@ -20,7 +20,7 @@ __all__ = [
     "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
     "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
-    "FC_F32", "FC_BF16", "ACTS", "OPS",
+    "FC_F32", "FC_BF16", "FC_F32_3XTF32", "ACTS", "OPS",
 ]
 
 FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
@@ -29,8 +29,10 @@ ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}
 OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
 # Every symbol include/fc.h declares.
-EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
-           "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
+EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_conv3x3_act_pool_pad", "fc_conv3x3_act_pad",
+           "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
+           "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_workspace_bytes_pad",
+           "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +67,11 @@ def load():
         lib.fc_conv3x3_act_pool.restype = I
         lib.fc_conv3x3_act.argtypes = conv
         lib.fc_conv3x3_act.restype = I
+        conv_pad = [P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
+        lib.fc_conv3x3_act_pool_pad.argtypes = conv_pad
+        lib.fc_conv3x3_act_pool_pad.restype = I
+        lib.fc_conv3x3_act_pad.argtypes = conv_pad
+        lib.fc_conv3x3_act_pad.restype = I
         lib.fc_linear_lse_mish.argtypes = [P, P, P, P, I, I, I, F, F, F, I, P, S, P]
         lib.fc_linear_lse_mish.restype = I
         L = ctypes.c_longlong
@@ -76,6 +83,8 @@ def load():
         lib.fc_scale_clamp_lse_mish.restype = I
         lib.fc_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.fc_workspace_bytes.restype = S
+        lib.fc_workspace_bytes_pad.argtypes = [I, I, I, I, I, I, I, I]
+        lib.fc_workspace_bytes_pad.restype = S
         lib.fc_status_string.argtypes = [I]
         lib.fc_status_string.restype = ctypes.c_char_p
         lib.fc_device_status.argtypes = [I]
@@ -158,7 +167,7 @@ def _workspace(nbytes, device, workspace):
     return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
 
 
-def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape, precision=None):
+def _conv(cname, op, x, w, b, act, out, workspace, stream, precision=None, pad=0):
     torch = _torch()
     lib = load()
     dts = (torch.float32, torch.bfloat16)
@@ -169,7 +178,8 @@ def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape, precision=
         raise ValueError("expected x [N,Cin,H,W], w [Cout,Cin,3,3], b [Cout]")
     N, Cin, H, W = (int(s) for s in x.shape)
     Cout = int(w.shape[0])
-    shape = out_shape(N, Cout, H, W)
+    pad = int(pad)
+    shape = (N, Cout) if op == "conv3x3_act_pool" else (N, Cout, H + 2 * pad - 2, W + 2 * pad - 2)
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=x.device)
     else:
@@ -178,26 +188,27 @@ def _conv(cname, op, x, w, b, act, out, workspace, stream, out_shape, precision=
             raise ValueError(f"out must have shape {shape}")
     dt = _dtype_code(x, precision)
     with torch.cuda.device(x.device):
-        nbytes = int(lib.fc_workspace_bytes(OPS[op], N, Cin, H, W, Cout, dt))
+        nbytes = int(lib.fc_workspace_bytes_pad(OPS[op], N, Cin, H, W, Cout, pad, dt))
         ws, wsb = _workspace(nbytes, x.device, workspace)
-        st = getattr(lib, cname)(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W, Cout, dt,
-                                 ACTS[act], None if ws is None else ws.data_ptr(), wsb, _stream_handle(stream))
+        st = getattr(lib, cname + "_pad")(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W,
+                                          Cout, pad, dt, ACTS[act], None if ws is None else ws.data_ptr(), wsb,
+                                          _stream_handle(stream))
     _raise(st, cname)
     return out
 
 
-def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None, precision=None):
-    """y[N, Cout] = mean over the (H-2)x(W-2) plane of act(conv3x3(x, w) + b); fp32 output.
-    precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
-    return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream,
-                 lambda N, Cout, H, W: (N, Cout), precision)
+def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None, precision=None,
+                        pad: int = 0):
+    """y[N, Cout] = mean over the OH x OW plane of act(conv3x3(x, w, padding=pad) + b), OH = H + 2 pad - 2,
+    OW = W + 2 pad - 2; fp32 output.  precision (fp32 inputs): "tf32" (default) or "3xtf32"."""
+    return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream, precision, pad)
 
 
-def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None, precision=None):
-    """y[N, Cout, H-2, W-2] = act(conv3x3(x, w) + b); fp32 output.
-    precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
-    return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream,
-                 lambda N, Cout, H, W: (N, Cout, H - 2, W - 2), precision)
+def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None, precision=None,
+                   pad: int = 0):
+    """y[N, Cout, OH, OW] = act(conv3x3(x, w, padding=pad) + b), OH = H + 2 pad - 2, OW = W + 2 pad - 2;
+    fp32 output.  precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
+    return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream, precision, pad)
 
 
 def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,

@@ -39,13 +39,21 @@ fc_status device_state(DeviceState** out)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Shape checks shared by the conv entry points and the workspace query: a padded input of
+// at least 3 x 3 (an output of at least 1 x 1) and a padding in 0 .. kMaxPad.
+bool conv_shape_ok(int N, int Cin, int H, int W, int Cout, int pad)
+{
+    return N >= 1 && Cin >= 1 && Cout >= 1 && H >= 1 && W >= 1 && pad >= 0 && pad <= fc::kMaxPad &&
+           H + 2 * pad >= 3 && W + 2 * pad >= 3;
+}
+
 fc_status conv_common(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
-                      fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes, fc_stream_t stream,
-                      int pool)
+                      int pad, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
+                      fc_stream_t stream, int pool)
 {
     if (!x || !w || !b || !y) return FC_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
-    if (N < 1 || Cin < 1 || H < 3 || W < 3 || Cout < 1) return FC_ERR_INVALID_ARG;
+    if (!conv_shape_ok(N, Cin, H, W, Cout, pad)) return FC_ERR_INVALID_ARG;
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return FC_ERR_INVALID_ARG;
     if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH && act != FC_ACT_GELU_TANH)
         return FC_ERR_INVALID_ARG;
@@ -53,7 +61,7 @@ fc_status conv_common(const void* x, const void* w, const void* b, float* y, int
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;
     fc::ConvPlan plan;
-    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, static_cast<int>(dtype), pool, d->sm_count) != 0)
+    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, pad, static_cast<int>(dtype), pool, d->sm_count) != 0)
         return FC_ERR_UNSUPPORTED;
     const size_t need = plan.ws_weights_bytes + plan.ws_pool_bytes;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -105,13 +113,29 @@ fc_status fc_conv3x3_act_pool(const void* x, const void* w, const void* b, float
                               int Cout, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
                               fc_stream_t stream)
 {
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, dtype, act, workspace, workspace_bytes, stream, 1);
+    if (H < 3 || W < 3) return FC_ERR_INVALID_ARG;
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, dtype, act, workspace, workspace_bytes, stream, 1);
 }
 
 fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
                          fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes, fc_stream_t stream)
 {
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, dtype, act, workspace, workspace_bytes, stream, 0);
+    if (H < 3 || W < 3) return FC_ERR_INVALID_ARG;
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, dtype, act, workspace, workspace_bytes, stream, 0);
+}
+
+fc_status fc_conv3x3_act_pool_pad(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H,
+                                  int W, int Cout, int pad, fc_dtype dtype, fc_act act, void* workspace,
+                                  size_t workspace_bytes, fc_stream_t stream)
+{
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, dtype, act, workspace, workspace_bytes, stream, 1);
+}
+
+fc_status fc_conv3x3_act_pad(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W,
+                             int Cout, int pad, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
+                             fc_stream_t stream)
+{
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, dtype, act, workspace, workspace_bytes, stream, 0);
 }
 
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y, int M, int K, int Nout,
@@ -182,18 +206,28 @@ fc_status fc_scale_clamp_lse_mish(const float* t, float* y, int M, int N, float 
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
+size_t fc_workspace_bytes_pad(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_dtype dtype)
+{
+    if (op != FC_OP_CONV3X3_ACT_POOL && op != FC_OP_CONV3X3_ACT) return 0;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != FC_OK) return 0;
+    if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return 0;
+    if (!conv_shape_ok(n, cin, h, w, cout, pad)) return 0;
+    fc::ConvPlan plan;
+    if (fc::conv_plan(&plan, n, cin, h, w, cout, pad, static_cast<int>(dtype), op == FC_OP_CONV3X3_ACT_POOL,
+                      d->sm_count) != 0)
+        return 0;
+    return plan.ws_weights_bytes + plan.ws_pool_bytes;
+}
+
 size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int cout_or_nout, fc_dtype dtype)
 {
     DeviceState* d = nullptr;
     if (device_state(&d) != FC_OK) return 0;
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return 0;
     if (op == FC_OP_CONV3X3_ACT_POOL || op == FC_OP_CONV3X3_ACT) {
-        if (n_or_m < 1 || cin_or_k < 1 || h < 3 || w < 3 || cout_or_nout < 1) return 0;
-        fc::ConvPlan plan;
-        if (fc::conv_plan(&plan, n_or_m, cin_or_k, h, w, cout_or_nout, static_cast<int>(dtype),
-                          op == FC_OP_CONV3X3_ACT_POOL, d->sm_count) != 0)
-            return 0;
-        return plan.ws_weights_bytes + plan.ws_pool_bytes;
+        if (h < 3 || w < 3) return 0;
+        return fc_workspace_bytes_pad(op, n_or_m, cin_or_k, h, w, cout_or_nout, 0, dtype);
     }
     if (op == FC_OP_LINEAR_LSE_MISH) {
         if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1 || dtype == FC_F32_3XTF32) return 0;

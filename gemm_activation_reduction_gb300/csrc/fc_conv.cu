@@ -130,29 +130,37 @@ struct Geometry {
     uint32_t strip_bytes, raw_bytes;
 };
 
-template <bool BF16, bool WIDE, int ROWS>
+template <bool BF16, bool WIDE, int ROWS, int XP>
 Geometry geometry_of()
 {
-    using S = Shape<WIDE, ROWS>;
-    using R = RawBox<BF16, WIDE, ROWS>;
+    using S = Shape<WIDE, ROWS, XP>;
+    using R = RawBox<BF16, WIDE, ROWS, XP>;
     return Geometry{S::PR, S::PC, S::SR, R::kCols, R::kCh, S::STRIP, R::kBytes};
 }
 
 // The kernel's tile shape: 16 x 8 patches (pool), two rows of 128 (full output, single
 // CTAs) or one row of 128 (full output, CTA pairs).
-Geometry geometry(int bf16, int pool, int pair)
+template <int XPF, int XPB>
+Geometry geometry_xp(int bf16, int pool, int pair)
 {
-    if (pool) return bf16 ? geometry_of<true, false, 1>() : geometry_of<false, false, 1>();
-    if (pair) return bf16 ? geometry_of<true, true, 1>() : geometry_of<false, true, 1>();
-    return bf16 ? geometry_of<true, true, 2>() : geometry_of<false, true, 2>();
+    if (pool) return bf16 ? geometry_of<true, false, 1, XPB>() : geometry_of<false, false, 1, XPF>();
+    if (pair) return bf16 ? geometry_of<true, true, 1, XPB>() : geometry_of<false, true, 1, XPF>();
+    return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, XPF>();
+}
+
+// padx: the padding's column shift needs XP = 4 (fp32) / 8 (bf16) extra staged columns
+Geometry geometry(int bf16, int pool, int pair, int padx)
+{
+    return padx ? geometry_xp<4, 8>(bf16, pool, pair) : geometry_xp<0, 0>(bf16, pool, pair);
 }
 
 }  // namespace
 
-int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int dtype, int pool, int sm_count)
+int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int dtype, int pool, int sm_count)
 {
     *p = ConvPlan{};
     if (dtype < 0 || dtype > 2) return 2;
+    if (pad < 0 || pad > kMaxPad || H + 2 * pad < 3 || W + 2 * pad < 3) return 2;
     const int bf16 = dtype == 1 ? 1 : 0;
     p->parts = dtype == 2 ? 3 : 1;
     if (Cout < 1 || Cout > 256) return 2;
@@ -160,16 +168,22 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int dtype, in
     // the MMA's N: whole 16-column slices; the padded channels are computed and dropped
     Cout = (Cout + 15) / 16 * 16;
     p->Cout = Cout;
-    p->OH = H - 2; p->OW = W - 2;
+    p->pad = pad;
+    p->OH = H + 2 * pad - 2; p->OW = W + 2 * pad - 2;
     p->bf16 = bf16; p->pool = pool;
     p->esize = bf16 ? 2 : 4;
+    // TMA boxes start on 16-byte boundaries: the staged patch begins dcol columns before the
+    // padded window, dcol = (-pad) mod (elements per 16 B)
+    const int align = 16 / p->esize;
+    p->dcol = (align - pad % align) % align;
+    p->padx = p->dcol != 0 ? 1 : 0;
     p->cb_ch = bf16 ? 16 : 8;
     p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch * p->parts;
     // CTA pairs (M = 256 MMAs, each CTA holding half of the weights) for Cout > 128, where
     // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
     // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
     p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
-    const Geometry geo = geometry(bf16, pool, p->pair);
+    const Geometry geo = geometry(bf16, pool, p->pair, p->padx);
     p->RB = (p->OH + geo.PR - 1) / geo.PR;
     p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
@@ -196,7 +210,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int dtype, in
     p->resident = p->w_total_bytes <= kResidentMax;
     // Shared memory: strips and (streamed) weight blocks per stage, kNumProd x raw_depth
     // TMA boxes, the indicator planes, the (resident) weights and the bias block.
-    const uint32_t fixed = kIndBytes + p->bias_block_bytes + 128u + (p->resident ? p->w_total_bytes : 0u);
+    const uint32_t fixed = ind_bytes(pool != 0) + p->bias_block_bytes + 128u + (p->resident ? p->w_total_bytes : 0u);
     const uint32_t per_stage = p->strip_bytes + (p->resident ? 0u : p->w_block_bytes);
     const uint32_t per_depth = static_cast<uint32_t>(kNumProd) * p->raw_bytes;
     const uint32_t boxes_min = p->use_tma ? per_depth : 0u;
@@ -230,7 +244,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int dtype, in
     p->strip_off = 0;
     p->raw_off = p->strip_off + static_cast<uint32_t>(p->stages) * p->strip_bytes;
     p->ind_off = p->raw_off + (p->use_tma ? static_cast<uint32_t>(kNumProd * p->raw_depth) * p->raw_bytes : 0u);
-    p->w_off = p->ind_off + kIndBytes;
+    p->w_off = p->ind_off + ind_bytes(pool != 0);
     p->bb_off = p->w_off + (p->resident ? p->w_total_bytes : static_cast<uint32_t>(p->stages) * p->w_block_bytes);
     p->bar_off = p->bb_off + p->bias_block_bytes;
     p->bar_off = (p->bar_off + 127u) & ~127u;
@@ -273,7 +287,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.Cin),
                               static_cast<cuuint64_t>(p.N)};
         cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
-        const Geometry geo = geometry(p.bf16, p.pool, p.pair);
+        const Geometry geo = geometry(p.bf16, p.pool, p.pair, p.padx);
         cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_cols), static_cast<cuuint32_t>(geo.SR),
                              static_cast<cuuint32_t>(geo.box_ch), 1u};
         cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -288,7 +302,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.x = x; a.wr = wr;
     a.out = p.pool ? pool_ws : y;
     a.N = p.N; a.Cin = p.Cin; a.H = p.H; a.W = p.W; a.Cout = p.Cout; a.Co = p.Co; a.OH = p.OH; a.OW = p.OW;
-    a.ncb = p.ncb; a.parts = p.parts; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
+    a.ncb = p.ncb; a.parts = p.parts; a.pad = p.pad; a.dcol = p.dcol; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
@@ -297,12 +311,20 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.status = status; a.budget = budget;
 
     cudaError_t e;
-    if (p.bf16)
+    if (p.padx) {
+        if (p.bf16)
+            e = p.pair ? launch_main_bf16_pair_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                       : launch_main_bf16_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+        else
+            e = p.pair ? launch_main_tf32_pair_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                       : launch_main_tf32_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+    } else if (p.bf16) {
         e = p.pair ? launch_main_bf16_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
                    : launch_main_bf16(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
-    else
+    } else {
         e = p.pair ? launch_main_tf32_pair(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
                    : launch_main_tf32(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+    }
     if (e != cudaSuccess) return e;
 
     if (p.pool) {

@@ -59,7 +59,10 @@ constexpr int kNumProd = 3;
 constexpr int kMmaWarp = kProdWarp0 + kNumProd;
 constexpr int kConvThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
-constexpr uint32_t kIndBytes = 5 * kIndPlane;            // 4 edge variants + a zero plane
+// Pooled tiles: 4 edge variants + a zero plane.  Full-output tiles store only pixels inside
+// the output, so every tile uses the all-inside plane: 1 variant + the zero plane.
+__host__ __device__ constexpr int ind_variants(bool pool) { return pool ? 4 : 1; }
+__host__ __device__ constexpr uint32_t ind_bytes(bool pool) { return (ind_variants(pool) + 1) * kIndPlane; }
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 constexpr uint32_t kResidentMax = 96 * 1024;
 constexpr int kMaxAcc = 8;                               // tensor-memory accumulator ring depth
@@ -83,13 +86,18 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // traffic per output and stage 4 input rows per 2 output rows instead of 3 per 1.
 // Either way the 8-pixel core-matrix groups of a unit lie at one constant stride
 // in the staged strip (SBO): the next patch row (16 x 8), or the next 8 pixels (1 x 128).
-template <bool WIDE, int ROWS = 1>
+//
+// With zero padding p the staged patch starts p rows above and p + d columns left of the
+// tile, d = (-p) mod (16 B / element size), so that the TMA box starts on a 16-byte
+// boundary; XP = 4 (fp32) or 8 (bf16) extra staged columns hold the d-column shift and
+// every MMA operand starts d staged pixels further (XP = 0 when d is always 0).
+template <bool WIDE, int ROWS = 1, int XP = 0>
 struct Shape {
     static constexpr int UNITS = WIDE ? ROWS : 1;          // M = 128 MMA units per tile
     static constexpr int PR = WIDE ? ROWS : 16;            // output rows per tile
     static constexpr int PC = WIDE ? 128 : 8;              // output columns per tile
     static constexpr int SR = PR + 2;                      // staged rows (halo)
-    static constexpr int SC = PC + 2;                      // staged columns (halo)
+    static constexpr int SC = PC + 2 + XP;                 // staged columns (halo + shift room)
     static constexpr int SPOS = SR * SC;                   // staged pixels
     static constexpr uint32_t PLANE = SPOS * 16;           // one channel group of the strip
     static constexpr uint32_t STRIP = (2 * PLANE + 127) / 128 * 128;  // one K block, slot pitch
@@ -98,9 +106,9 @@ struct Shape {
 
 // Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
 // order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.
-template <bool BF16, bool WIDE, int ROWS = 1>
+template <bool BF16, bool WIDE, int ROWS = 1, int XP = 0>
 struct RawBox {
-    using S = Shape<WIDE, ROWS>;
+    using S = Shape<WIDE, ROWS, XP>;
     static constexpr int kCh = BF16 ? 16 : 8;
     static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8 : (S::SC + 3) / 4 * 4;
     static constexpr uint32_t kChPlane = S::SR * kCols * (BF16 ? 2 : 4);
@@ -116,6 +124,8 @@ struct ConvArgs {
     int Co;              // output channels stored (<= Cout)
     int ncb;             // K stages per tile (K blocks x parts)
     int parts;           // 1, or 3 for split TF32: stages hi*hi, hi*lo, lo*hi of each K block (no other values)
+    int pad;             // zero padding p on every side (output = input + 2p - 2)
+    int dcol;            // (-pad) mod (16 B / element size): staged columns before the first tap column
     int RB, CS;
     long long tpi;
     long long num_tiles;  // tiles of the whole call
@@ -256,11 +266,11 @@ __device__ __forceinline__ uint32_t tf32_part(float v)
     else return __float_as_uint(hi);
 }
 
-template <bool BF16, bool WIDE, int ROWS, bool LO = false>
+template <bool BF16, bool WIDE, int ROWS, int XP, bool LO = false>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
 {
-    using S = Shape<WIDE, ROWS>;
-    using RB_ = RawBox<BF16, WIDE, ROWS>;
+    using S = Shape<WIDE, ROWS, XP>;
+    using RB_ = RawBox<BF16, WIDE, ROWS, XP>;
     static_assert(!(BF16 && LO), "split TF32 is an fp32 mode");
     if constexpr (!BF16) {
         // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
@@ -320,16 +330,16 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
 // multiple and TMA cannot address it): one K block of the halo patch as
 // [group][SPOS pixels][16 B], zero past the image and past Cin; `lo` stages the
 // split-TF32 remainder instead of the high part (fp32 only).
-template <bool BF16, bool WIDE, int ROWS>
+template <bool BF16, bool WIDE, int ROWS, int XP>
 __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
                                            int Cin, int H, int W, int lane, bool lo)
 {
-    using S = Shape<WIDE, ROWS>;
+    using S = Shape<WIDE, ROWS, XP>;
     const size_t HW = static_cast<size_t>(H) * W;
     for (int s = lane; s < S::SPOS; s += 32) {
         const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
-        const int ih = oh0 + rr, iw = ow0 + cc;
-        const bool ok = ih < H && iw < W;
+        const int ih = oh0 + rr, iw = ow0 + cc;   // negative above / left of the image (padding)
+        const bool ok = ih >= 0 && ih < H && iw >= 0 && iw < W;
         const uint32_t a = strip + static_cast<uint32_t>(s) * 16u;
         if constexpr (!BF16) {
             const float* x = reinterpret_cast<const float*>(xv);
@@ -377,19 +387,21 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
 // pixel past the image gets a 1 in k 1, whose B entry is the padding value, so
 // its accumulator starts near -1e4 and activates to exactly -0.  CTA pairs share
 // one descriptor for two tiles, so they use plane 0 (all inside) and mask in the
-// epilogue instead.
+// epilogue instead.  Full-output tiles store only the pixels inside the output and use
+// the all-inside plane alone (plane 0, then the zero plane).
 template <bool BF16, bool WIDE, int ROWS>
 __device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
                                                        int nthreads)
 {
     using S = Shape<WIDE, ROWS>;
+    constexpr int NV = ind_variants(!WIDE);
     const int rows_last = OH - (RB - 1) * S::PR;   // valid rows in the last row block
     const int cols_last = OW - (CS - 1) * S::PC;   // valid columns in the last column strip
-    for (int i = tid; i < 5 * 128; i += nthreads) {
+    for (int i = tid; i < (NV + 1) * 128; i += nthreads) {
         const int v = i >> 7, r = i & 127;
         const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
-        const bool in = v < 4 && (!(v & 2) || pr < rows_last) && (!(v & 1) || pc < cols_last);
-        const bool pad = v < 4 && !in;
+        const bool in = v < NV && (!(v & 2) || pr < rows_last) && (!(v & 1) || pc < cols_last);
+        const bool pad = v < NV && !in;
         uint32_t w0, w1, w2;
         if constexpr (BF16) {
             w0 = (in ? 0x3F80u : 0u) | ((pad ? 0x3F80u : 0u) << 16);   // bf16 1.0 in k 0 / k 1
@@ -490,7 +502,7 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -498,8 +510,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // full output on single CTAs: two-row tiles (two MMA units sharing each staged strip
     // and weight block); CTA pairs keep one row per CTA
     constexpr int ROWS = (WIDE && !PAIR) ? 2 : 1;
-    using S = Shape<WIDE, ROWS>;
-    using RBox = RawBox<BF16, WIDE, ROWS>;
+    // room for the padding's column shift a.dcol (< 16 B of elements) when it is not 0
+    constexpr int XP = PADX ? (BF16 ? 8 : 4) : 0;
+    using S = Shape<WIDE, ROWS, XP>;
+    using RBox = RawBox<BF16, WIDE, ROWS, XP>;
     constexpr int UPT = S::UNITS;   // accumulator units per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -611,8 +625,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const uint32_t r = raw_buf(issued);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&rawfull[r], RBox::kBytes);
-                    tma_load_4d(smem + a.raw_off + r * RBox::kBytes, &tmx, &rawfull[r], atc.cs * S::PC,
-                                atc.rb * S::PR, (a.parts == 1 ? acb : acb / 3) * RBox::kCh, atc.n);
+                    // the patch starts pad rows above and pad + dcol columns left of the tile: a
+                    // 16-byte-aligned column, possibly negative (TMA fills zeros outside x)
+                    tma_load_4d(smem + a.raw_off + r * RBox::kBytes, &tmx, &rawfull[r],
+                                atc.cs * S::PC - a.pad - a.dcol, atc.rb * S::PR - a.pad,
+                                (a.parts == 1 ? acb : acb / 3) * RBox::kCh, atc.n);
                 }
                 ++issued;
                 advance(atc, alt, acb, kNumProd);
@@ -646,18 +663,18 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t raw = smem_u32(smem + a.raw_off + r * RBox::kBytes);
                     // split TF32: the third stage of each K block stages x's remainder
                     if constexpr (!BF16) {
-                        if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, true>(raw, strip, lane);
-                        else transpose_raw<BF16, WIDE, ROWS>(raw, strip, lane);
+                        if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, XP, true>(raw, strip, lane);
+                        else transpose_raw<BF16, WIDE, ROWS, XP>(raw, strip, lane);
                     } else {
-                        transpose_raw<BF16, WIDE, ROWS>(raw, strip, lane);
+                        transpose_raw<BF16, WIDE, ROWS, XP>(raw, strip, lane);
                     }
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
                     if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
-                    fill_strip<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3, tc.rb * S::PR,
-                                                 tc.cs * S::PC, a.Cin, tc.n < a.N ? a.H : 0, a.W, lane,
-                                                 a.parts == 3 && cb % 3 == 2);
+                    fill_strip<BF16, WIDE, ROWS, XP>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
+                                                     tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad - a.dcol, a.Cin,
+                                                     tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -698,6 +715,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const uint64_t a_desc0 = smem_desc(smem_u32(smem + a.strip_off), S::PLANE, S::SBO, kLayoutNone);
             const uint64_t i_desc0 = smem_desc(smem_u32(smem + a.ind_off), 0u, 128u, kLayoutNone);
             constexpr uint32_t kInd16 = kIndPlane >> 4;
+            constexpr uint32_t kZeroPlane = static_cast<uint32_t>(ind_variants(!WIDE));
             const uint64_t b_desc0 = smem_desc(smem_u32(smem + a.w_off), half_co * 16u, 128u, kLayoutNone);
             const uint64_t bb_desc = smem_desc(smem_u32(smem + a.bb_off), half_co * 16u, 128u, kLayoutNone);
             const uint32_t wtap16 = 2u * half_co;   // one tap of this CTA's weights, 16-byte units
@@ -716,14 +734,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
-                const uint32_t v = PAIR ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
-                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
+                const uint32_t v = (PAIR || WIDE) ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
+                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
                 issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
-                    const uint64_t ab = a_desc0 + slot * kStrip16;
+                    const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
                     issue_mma9<BF16, PAIR, S::SC>(d, ab, bbase, wtap16, idesc);
                     commit_to<PAIR>(&empty[slot], 0x3);
@@ -757,15 +775,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
                 // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
-                const uint32_t v = PAIR ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
-                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((4u - v) * kInd16) << 16);
+                const uint32_t v = (PAIR || WIDE) ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
+                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
 #pragma unroll
                 for (int u = 0; u < UPT; ++u) issue_mma<BF16, PAIR>(d[u], i_desc, bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
-                    const uint64_t ab = a_desc0 + slot * kStrip16;
+                    const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
                     // unit u reads the strip from staged row u on (u * SC pixels, 16 B each)
 #pragma unroll
@@ -1071,11 +1089,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1100,22 +1118,27 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
                      cudaStream_t stream)
 
 // The variant switch shared by the four translation units.
-#define FC_CONV_LAUNCH_BODY(BF16, PAIR)                                                            \
+#define FC_CONV_LAUNCH_BODY(BF16, PAIR, PADX)                                                      \
     switch ((pool ? 0 : 1) * 4 + act) {                                                           \
-    case 0: return launch_variant<BF16, true, 0, PAIR>(tmx, a, grid, smem_bytes, stream);          \
-    case 1: return launch_variant<BF16, true, 1, PAIR>(tmx, a, grid, smem_bytes, stream);          \
-    case 2: return launch_variant<BF16, true, 2, PAIR>(tmx, a, grid, smem_bytes, stream);          \
-    case 3: return launch_variant<BF16, true, 3, PAIR>(tmx, a, grid, smem_bytes, stream);          \
-    case 4: return launch_variant<BF16, false, 0, PAIR>(tmx, a, grid, smem_bytes, stream);         \
-    case 5: return launch_variant<BF16, false, 1, PAIR>(tmx, a, grid, smem_bytes, stream);         \
-    case 6: return launch_variant<BF16, false, 2, PAIR>(tmx, a, grid, smem_bytes, stream);         \
-    case 7: return launch_variant<BF16, false, 3, PAIR>(tmx, a, grid, smem_bytes, stream);         \
+    case 0: return launch_variant<BF16, true, 0, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
+    case 1: return launch_variant<BF16, true, 1, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
+    case 2: return launch_variant<BF16, true, 2, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
+    case 3: return launch_variant<BF16, true, 3, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
+    case 4: return launch_variant<BF16, false, 0, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
+    case 5: return launch_variant<BF16, false, 1, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
+    case 6: return launch_variant<BF16, false, 2, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
+    case 7: return launch_variant<BF16, false, 3, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
     default: return cudaErrorInvalidValue;                                                       \
     }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair);
 FC_CONV_LAUNCH_DECL(launch_main_bf16);
 FC_CONV_LAUNCH_DECL(launch_main_bf16_pair);
+// the same with room for a padding column shift (PADX)
+FC_CONV_LAUNCH_DECL(launch_main_tf32_padx);
+FC_CONV_LAUNCH_DECL(launch_main_tf32_pair_padx);
+FC_CONV_LAUNCH_DECL(launch_main_bf16_padx);
+FC_CONV_LAUNCH_DECL(launch_main_bf16_pair_padx);
 
 }  // namespace convk
 }  // namespace fc

@@ -1,0 +1,14 @@
+// fc_conv_tf32_pair_padx.cu -- the fused conv3x3 kernel for fp32 inputs on TF32 tensor cores in CTA pairs (M = 256 MMAs),
+// with zero padding whose column shift is not a 16-byte multiple (XP extra staged columns).
+#include "fc_conv_kernel.cuh"
+
+namespace fc {
+namespace convk {
+
+FC_CONV_LAUNCH_DECL(launch_main_tf32_pair_padx)
+{
+    FC_CONV_LAUNCH_BODY(false, true, true)
+}
+
+}  // namespace convk
+}  // namespace fc

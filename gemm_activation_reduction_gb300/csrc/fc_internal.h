@@ -21,7 +21,10 @@ constexpr long long kWaitBudgetCycles = 2000000000LL;
 // Geometry and resources of one fused conv3x3 call; computed on the host by
 // conv_plan() and passed by value to the kernel.
 struct ConvPlan {
-    int N, Cin, H, W, OH, OW;
+    int N, Cin, H, W, OH, OW;   // OH = H + 2 pad - 2, OW = W + 2 pad - 2
+    int pad;              // zero padding on every side
+    int dcol;             // staged columns before the padded window: (-pad) mod (16 B / esize)
+    int padx;             // dcol != 0: the kernel variant with room for that shift
     int Co;               // output channels of the call (any count in 1 .. 256)
     int Cout;             // Co rounded up to 16: the MMA tile width; channels >= Co carry zero
                           // weights and bias and are never stored
@@ -57,8 +60,11 @@ struct ConvPlan {
 
 // Fills `plan`; returns 0 on success, 2 (unsupported) when the shape is outside
 // what the kernels cover.
-// dtype: 0 fp32 (TF32 products), 1 bf16, 2 fp32 with split-TF32 products (the fc_dtype codes).
-int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int dtype, int pool, int sm_count);
+// dtype: 0 fp32 (TF32 products), 1 bf16, 2 fp32 with split-TF32 products (the fc_dtype codes);
+// pad: zero padding, 0 .. kMaxPad.
+constexpr int kMaxPad = 64;
+int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int pad, int dtype, int pool,
+              int sm_count);
 
 cudaError_t conv_launch(const ConvPlan& plan, const void* x, const void* w, const void* b, float* y, int act,
                         void* workspace, cudaStream_t stream, int* status, long long budget);

@@ -157,6 +157,79 @@ def test_split_tf32_rejects_bf16_inputs(cuda_lib):
                                   cuda_lib.FC_F32_3XTF32, None, 0, s) == cuda_lib.FC_ERR_UNSUPPORTED
 
 
+# ------------------------------------------------------------------ zero padding
+
+PAD_SHAPES = [
+    # (N, Cin, H, W, Cout, pad, dtype, act, pool)
+    (2, 8, 32, 32, 64, 1, "f32", "gelu", True),        # 'same' conv, TMA staging, column shift 3
+    (1, 13, 20, 36, 96, 2, "f32", "gelu", True),       # shift 2, ragged edges
+    (1, 5, 17, 24, 32, 3, "f32", "mish", True),        # shift 1
+    (1, 6, 15, 20, 48, 4, "f32", "gelu", True),        # shift 0: the unshifted kernel, negative start
+    (1, 3, 9, 11, 40, 5, "f32", "gelu_tanh", True),    # plain-load staging, wide border
+    (2, 16, 18, 24, 64, 1, "bf16", "gelu", True),      # bf16, shift 7
+    (1, 8, 40, 16, 256, 1, "f32", "gelu", True),       # CTA pairs
+    (1, 40, 12, 32, 256, 2, "bf16", "gelu", True),     # CTA pairs, bf16, streamed weights
+    (1, 2, 1, 2, 16, 1, "f32", "gelu", True),          # input smaller than the kernel: 1 x 2 output
+    (2, 8, 12, 140, 64, 1, "f32", "mish_mish", False), # two-row tiles, rows wider than one tile
+    (1, 64, 9, 132, 128, 1, "f32", "mish_mish", False),# the Mish->Mish page's channel counts
+    (1, 16, 9, 136, 64, 3, "bf16", "mish", False),     # bf16, shift 5
+    (1, 16, 7, 128, 200, 1, "f32", "mish", False),     # CTA pairs, padded Cout
+    (1, 3, 5, 7, 24, 2, "f32", "gelu", False),         # plain-load staging, full output
+]
+
+
+@pytest.mark.parametrize("shape", PAD_SHAPES,
+                         ids=lambda s: "x".join(map(str, s[:5])) + f"-p{s[5]}-{s[6]}-{s[7]}-{'pool' if s[8] else 'act'}")
+def test_conv_padded_small(cuda_lib, shape):
+    N, Cin, H, W, Cout, pad, dt, act, pool = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, dt)
+    f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+    y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act, pad=pad).cpu().numpy()
+    ref = (oracle.conv3x3_act_pool if pool else oracle.conv3x3_act)(d["x32"], d["w32"], d["b32"], act, pad=pad)
+    assert y.shape == ref.shape
+    _check(y, ref, TOL[dt], f"pad {shape}")
+
+
+def test_conv_padded_split_tf32(cuda_lib):
+    d = fc_inputs.conv_inputs(1, 12, 14, 24, 64)
+    for pool, pad in ((True, 1), (False, 2)):
+        f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+        y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="gelu", pad=pad, precision="3xtf32").cpu().numpy()
+        ref = (oracle.conv3x3_act_pool if pool else oracle.conv3x3_act)(d["x"], d["w"], d["b"], "gelu", pad=pad)
+        _check(y, ref, TOL_X3, f"pad {pad} 3xtf32")
+
+
+def test_conv_pad_zero_matches_unpadded_entry_point_bit_for_bit(cuda_lib):
+    import torch
+    d = fc_inputs.conv_inputs(2, 8, 20, 36, 64)
+    x, w, b = _dev(d["x"]), _dev(d["w"]), _dev(d["b"])
+    lib = cuda_lib.load()
+    y0 = torch.empty((2, 64), device="cuda")
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    nb = lib.fc_workspace_bytes(0, 2, 8, 20, 36, 64, 0)
+    assert nb == lib.fc_workspace_bytes_pad(0, 2, 8, 20, 36, 64, 0, 0)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    assert lib.fc_conv3x3_act_pool(x.data_ptr(), w.data_ptr(), b.data_ptr(), y0.data_ptr(), 2, 8, 20, 36, 64, 0, 0,
+                                   ws.data_ptr(), nb, s) == 0
+    y1 = cuda_lib.fc_conv3x3_act_pool(x, w, b, pad=0)
+    assert torch.equal(y0, y1)
+
+
+def test_conv_pad_arguments_are_checked(cuda_lib):
+    import torch
+    lib = cuda_lib.load()
+    v = torch.zeros(4096, device="cuda")
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    p = v.data_ptr()
+    call = lambda H, W, pad: lib.fc_conv3x3_act_pad(p, p, p, p, 1, 1, H, W, 16, pad, 0, 0, None, 0, s)
+    assert call(4, 4, -1) == cuda_lib.FC_ERR_INVALID_ARG
+    assert call(4, 4, 65) == cuda_lib.FC_ERR_INVALID_ARG
+    assert call(1, 1, 0) == cuda_lib.FC_ERR_INVALID_ARG       # no output
+    assert lib.fc_workspace_bytes_pad(1, 1, 1, 4, 4, 16, -1, 0) == 0
+    assert lib.fc_workspace_bytes_pad(2, 1, 1, 4, 4, 16, 1, 0) == 0   # not a conv op
+    torch.cuda.synchronize()
+
+
 # ------------------------------------------------------------------ linear chain
 
 LIN_SHAPES = [
@@ -200,26 +273,26 @@ def test_linear_small_bf16(cuda_lib, shape):
 
 # ------------------------------------------------------------------ full-size workloads
 
-@pytest.mark.parametrize("key", ["B", "Bt", "B3"])
+@pytest.mark.parametrize("key", ["B", "Bt", "B3", "Bp"])
 def test_workload_B_full_size_sampled(cuda_lib, key):
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
     y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
-                                     precision=wl.precision).cpu().numpy()
+                                     precision=wl.precision, pad=wl.pad).cpu().numpy()
     rng = np.random.default_rng(7)
     flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 192, replace=False),
                                      np.arange(wl.Cout), np.arange((wl.N - 1) * wl.Cout, wl.N * wl.Cout)]))
-    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
+    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act, pad=wl.pad)
     _check(y.reshape(-1)[flat], ref, TOL_X3 if wl.precision == "3xtf32" else TOL["f32"], f"workload {key}")
 
 
-@pytest.mark.parametrize("key", ["C", "Cb", "C3"])
+@pytest.mark.parametrize("key", ["C", "Cb", "C3", "Cp"])
 def test_workload_C_full_size_sampled(cuda_lib, key):
     import torch
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
     y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
-                                precision=None if wl.dtype == "bf16" else wl.precision)
+                                precision=None if wl.dtype == "bf16" else wl.precision, pad=wl.pad)
     OH, OW = wl.OH, wl.OW
     rng = np.random.default_rng(8)
     total = wl.N * wl.Cout * OH * OW
@@ -232,7 +305,7 @@ def test_workload_C_full_size_sampled(cuda_lib, key):
     flat = np.unique(np.concatenate(samples))
     got = y.view(-1)[torch.from_numpy(flat).cuda()].cpu().numpy()
     del y
-    ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
+    ref = oracle.conv3x3_act_at(d["x32"], d["w32"], d["b32"], flat, wl.act, pad=wl.pad)
     _check(got, ref, TOL_X3 if wl.precision == "3xtf32" else TOL[wl.dtype], f"workload {key}")
 
 
