@@ -177,13 +177,19 @@ def make_call(fc, torch, key, d, device):
             fc.fc_linear_lse_mish(x, W, b, wl.scale, wl.clamp_lo, wl.clamp_hi, out=out, workspace=ws)
         return call, 2, out
     x, w, b = (_dev(torch, d[k], device) for k in ("x", "w", "b"))
+    nhwc = wl.layout == "nhwc"
+    if nhwc:
+        # x stored [N][H][W][Cin], passed as the channels_last view of logical shape [N, Cin, H, W]
+        x = _dev(torch, np.ascontiguousarray(np.transpose(d["x"], (0, 2, 3, 1))), device).permute(0, 3, 1, 2)
     dt = fc.FC_BF16 if wl.dtype == "bf16" else (fc.FC_F32_3XTF32 if wl.precision == "3xtf32" else fc.FC_F32)
     prec = None if wl.dtype == "bf16" else wl.precision
     op = "conv3x3_act_pool" if wl.pool else "conv3x3_act"
     shape = (wl.N, wl.Cout) if wl.pool else (wl.N, wl.Cout, wl.OH, wl.OW)
-    out = torch.empty(shape, dtype=torch.float32, device=device)
-    ws = torch.empty(max(1, fc.load().fc_workspace_bytes_pad(fc.OPS[op], wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.pad,
-                                                              dt)), dtype=torch.uint8, device=device)
+    out = torch.empty(shape, dtype=torch.float32, device=device,
+                      memory_format=torch.channels_last if (nhwc and not wl.pool) else torch.contiguous_format)
+    ws = torch.empty(max(1, fc.load().fc_workspace_bytes_ex(fc.OPS[op], wl.N, wl.Cin, wl.H, wl.W, wl.Cout, wl.pad,
+                                                             fc.FC_NHWC if nhwc else fc.FC_NCHW, dt)),
+                     dtype=torch.uint8, device=device)
     f = fc.fc_conv3x3_act_pool if wl.pool else fc.fc_conv3x3_act
 
     def call():
@@ -246,8 +252,11 @@ def time_e2e(fc, torch, key, d, device, steps, warmup):
     wl = fc_inputs.WORKLOADS[key]
     names = ("x", "W", "b") if isinstance(wl, fc_inputs.LinearWorkload) else ("x", "w", "b")
     host = []
+    nhwc = getattr(wl, "layout", "nchw") == "nhwc"
     for k in names:
         a = d[k]
+        if nhwc and k == "x":
+            a = np.ascontiguousarray(np.transpose(a, (0, 2, 3, 1)))
         t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a))
         host.append(t.pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in host)
@@ -257,6 +266,8 @@ def time_e2e(fc, torch, key, d, device, steps, warmup):
         dev = [t.to(device, non_blocking=True) for t in host]
         if bf16:
             dev = [t.view(torch.bfloat16) for t in dev]
+        if nhwc:
+            dev[0] = dev[0].permute(0, 3, 1, 2)
         if isinstance(wl, fc_inputs.LinearWorkload):
             y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi)
         elif wl.pool:
@@ -468,7 +479,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,Cn,Cbn,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -55,6 +55,7 @@ class ConvWorkload:
     pool: bool          # True: global mean to (N, Cout); False: full output
     precision: str = "tf32"   # fp32 storage: "tf32" or "3xtf32" (split-TF32 products); bf16: "bf16"
     pad: int = 0              # zero padding on every side
+    layout: str = "nchw"      # "nchw", or "nhwc": x stored [N][H][W][Cin], full output [N][OH][OW][Cout]
 
     @property
     def OH(self):
@@ -149,6 +150,11 @@ WORKLOADS = {
                        pad=1),
     "Cp": ConvWorkload("conv3x3_mish_mish_pad1_f32_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish",
                        False, pad=1),
+    # NHWC (channels_last) input and output at the Mish->Mish page's size, fp32 and bf16.
+    "Cn": ConvWorkload("conv3x3_mish_mish_nhwc_f32_64x64x256x256_c128", 64, 64, 256, 256, 128, "f32", "mish_mish",
+                       False, layout="nhwc"),
+    "Cbn": ConvWorkload("conv3x3_mish_mish_nhwc_bf16_64x64x256x256_c128", 64, 64, 256, 256, 128, "bf16",
+                        "mish_mish", False, "bf16", layout="nhwc"),
     # The pages' epilogue-only kernels at their sizes: over the conv output of the GELU->pool page,
     # the conv output of the Mish->Mish page, and the Linear output of the Linear page.
     "K1e": EpilogueWorkload("gelu_avgpool_epilogue_f32_128x64x254x254", "act_mean", (128, 64, 254, 254), "gelu"),

@@ -20,18 +20,19 @@ __all__ = [
     "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
     "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
-    "FC_F32", "FC_BF16", "FC_F32_3XTF32", "ACTS", "OPS",
+    "FC_F32", "FC_BF16", "FC_F32_3XTF32", "FC_NCHW", "FC_NHWC", "ACTS", "OPS",
 ]
 
 FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
 FC_F32, FC_BF16, FC_F32_3XTF32 = 0, 1, 2
+FC_NCHW, FC_NHWC = 0, 1
 ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}
 OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 
 # Every symbol include/fc.h declares.
-EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_conv3x3_act_pool_pad", "fc_conv3x3_act_pad",
+EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_conv3x3_act_pool_ex", "fc_conv3x3_act_ex",
            "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
-           "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_workspace_bytes_pad",
+           "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_workspace_bytes_ex",
            "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
 
 _lock = threading.Lock()
@@ -67,11 +68,11 @@ def load():
         lib.fc_conv3x3_act_pool.restype = I
         lib.fc_conv3x3_act.argtypes = conv
         lib.fc_conv3x3_act.restype = I
-        conv_pad = [P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
-        lib.fc_conv3x3_act_pool_pad.argtypes = conv_pad
-        lib.fc_conv3x3_act_pool_pad.restype = I
-        lib.fc_conv3x3_act_pad.argtypes = conv_pad
-        lib.fc_conv3x3_act_pad.restype = I
+        conv_ex = [P, P, P, P, I, I, I, I, I, I, I, I, I, P, S, P]
+        lib.fc_conv3x3_act_pool_ex.argtypes = conv_ex
+        lib.fc_conv3x3_act_pool_ex.restype = I
+        lib.fc_conv3x3_act_ex.argtypes = conv_ex
+        lib.fc_conv3x3_act_ex.restype = I
         lib.fc_linear_lse_mish.argtypes = [P, P, P, P, I, I, I, F, F, F, I, P, S, P]
         lib.fc_linear_lse_mish.restype = I
         L = ctypes.c_longlong
@@ -83,8 +84,8 @@ def load():
         lib.fc_scale_clamp_lse_mish.restype = I
         lib.fc_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         lib.fc_workspace_bytes.restype = S
-        lib.fc_workspace_bytes_pad.argtypes = [I, I, I, I, I, I, I, I]
-        lib.fc_workspace_bytes_pad.restype = S
+        lib.fc_workspace_bytes_ex.argtypes = [I, I, I, I, I, I, I, I, I]
+        lib.fc_workspace_bytes_ex.restype = S
         lib.fc_status_string.argtypes = [I]
         lib.fc_status_string.restype = ctypes.c_char_p
         lib.fc_device_status.argtypes = [I]
@@ -116,13 +117,16 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t, name, dtypes, device=None):
+def _check(t, name, dtypes, device=None, channels_last=False):
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
-    if not t.is_contiguous():
+    if channels_last:
+        if not t.is_contiguous(memory_format=torch.channels_last):
+            raise ValueError(f"{name} must be contiguous in the channels_last memory format")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if t.dtype not in dtypes:
         raise ValueError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
@@ -167,11 +171,25 @@ def _workspace(nbytes, device, workspace):
     return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
 
 
-def _conv(cname, op, x, w, b, act, out, workspace, stream, precision=None, pad=0):
+def _layout_of(x, layout):
+    """"nchw" / "nhwc" for x [N, C, H, W]: given, or "nhwc" when x is stored channels_last
+    (and not also plainly contiguous)."""
+    torch = _torch()
+    if layout is None:
+        cl = x.dim() == 4 and x.is_contiguous(memory_format=torch.channels_last) and not x.is_contiguous()
+        return "nhwc" if cl else "nchw"
+    if layout not in ("nchw", "nhwc"):
+        raise ValueError(f"unknown layout {layout!r} (expected 'nchw' or 'nhwc')")
+    return layout
+
+
+def _conv(cname, op, x, w, b, act, out, workspace, stream, precision=None, pad=0, layout=None):
     torch = _torch()
     lib = load()
     dts = (torch.float32, torch.bfloat16)
-    _check(x, "x", dts)
+    layout = _layout_of(x, layout)
+    nhwc = layout == "nhwc"
+    _check(x, "x", dts, channels_last=nhwc)
     _check(w, "w", (x.dtype,), x.device)
     _check(b, "b", (x.dtype,), x.device)
     if x.dim() != 4 or w.dim() != 4 or tuple(w.shape[1:]) != (x.shape[1], 3, 3) or b.shape != (w.shape[0],):
@@ -179,36 +197,44 @@ def _conv(cname, op, x, w, b, act, out, workspace, stream, precision=None, pad=0
     N, Cin, H, W = (int(s) for s in x.shape)
     Cout = int(w.shape[0])
     pad = int(pad)
-    shape = (N, Cout) if op == "conv3x3_act_pool" else (N, Cout, H + 2 * pad - 2, W + 2 * pad - 2)
+    pooled = op == "conv3x3_act_pool"
+    shape = (N, Cout) if pooled else (N, Cout, H + 2 * pad - 2, W + 2 * pad - 2)
+    # the full output of an NHWC call is channels_last too (logical shape N, Cout, OH, OW)
+    out_cl = nhwc and not pooled
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+        out = torch.empty(shape, dtype=torch.float32, device=x.device,
+                          memory_format=torch.channels_last if out_cl else torch.contiguous_format)
     else:
-        _check(out, "out", (torch.float32,), x.device)
+        _check(out, "out", (torch.float32,), x.device, channels_last=out_cl)
         if tuple(out.shape) != shape:
             raise ValueError(f"out must have shape {shape}")
     dt = _dtype_code(x, precision)
+    lay = FC_NHWC if nhwc else FC_NCHW
     with torch.cuda.device(x.device):
-        nbytes = int(lib.fc_workspace_bytes_pad(OPS[op], N, Cin, H, W, Cout, pad, dt))
+        nbytes = int(lib.fc_workspace_bytes_ex(OPS[op], N, Cin, H, W, Cout, pad, lay, dt))
         ws, wsb = _workspace(nbytes, x.device, workspace)
-        st = getattr(lib, cname + "_pad")(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W,
-                                          Cout, pad, dt, ACTS[act], None if ws is None else ws.data_ptr(), wsb,
-                                          _stream_handle(stream))
+        st = getattr(lib, cname + "_ex")(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W,
+                                         Cout, pad, lay, dt, ACTS[act], None if ws is None else ws.data_ptr(), wsb,
+                                         _stream_handle(stream))
     _raise(st, cname)
     return out
 
 
 def fc_conv3x3_act_pool(x, w, b, act: str = "gelu", out=None, workspace=None, stream=None, precision=None,
-                        pad: int = 0):
+                        pad: int = 0, layout=None):
     """y[N, Cout] = mean over the OH x OW plane of act(conv3x3(x, w, padding=pad) + b), OH = H + 2 pad - 2,
-    OW = W + 2 pad - 2; fp32 output.  precision (fp32 inputs): "tf32" (default) or "3xtf32"."""
-    return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream, precision, pad)
+    OW = W + 2 pad - 2; fp32 output.  precision (fp32 inputs): "tf32" (default) or "3xtf32".
+    layout: "nchw", "nhwc" (x stored channels_last), or None to follow x's memory format."""
+    return _conv("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, workspace, stream, precision, pad,
+                 layout)
 
 
 def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, stream=None, precision=None,
-                   pad: int = 0):
+                   pad: int = 0, layout=None):
     """y[N, Cout, OH, OW] = act(conv3x3(x, w, padding=pad) + b), OH = H + 2 pad - 2, OW = W + 2 pad - 2;
-    fp32 output.  precision (fp32 inputs): "tf32" (default) or "3xtf32" (split-TF32 products)."""
-    return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream, precision, pad)
+    fp32 output, channels_last when x is.  precision (fp32 inputs): "tf32" (default) or "3xtf32".
+    layout: "nchw", "nhwc" (x stored channels_last), or None to follow x's memory format."""
+    return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream, precision, pad, layout)
 
 
 def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,

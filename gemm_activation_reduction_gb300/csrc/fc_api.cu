@@ -48,12 +48,13 @@ bool conv_shape_ok(int N, int Cin, int H, int W, int Cout, int pad)
 }
 
 fc_status conv_common(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
-                      int pad, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
-                      fc_stream_t stream, int pool)
+                      int pad, fc_layout layout, fc_dtype dtype, fc_act act, void* workspace,
+                      size_t workspace_bytes, fc_stream_t stream, int pool)
 {
     if (!x || !w || !b || !y) return FC_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y)) return FC_ERR_INVALID_ARG;
     if (!conv_shape_ok(N, Cin, H, W, Cout, pad)) return FC_ERR_INVALID_ARG;
+    if (layout != FC_NCHW && layout != FC_NHWC) return FC_ERR_INVALID_ARG;
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return FC_ERR_INVALID_ARG;
     if (act != FC_ACT_GELU_ERF && act != FC_ACT_MISH && act != FC_ACT_MISH_MISH && act != FC_ACT_GELU_TANH)
         return FC_ERR_INVALID_ARG;
@@ -61,7 +62,8 @@ fc_status conv_common(const void* x, const void* w, const void* b, float* y, int
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;
     fc::ConvPlan plan;
-    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, pad, static_cast<int>(dtype), pool, d->sm_count) != 0)
+    if (fc::conv_plan(&plan, N, Cin, H, W, Cout, pad, layout == FC_NHWC, static_cast<int>(dtype), pool,
+                      d->sm_count) != 0)
         return FC_ERR_UNSUPPORTED;
     const size_t need = plan.ws_weights_bytes + plan.ws_pool_bytes;
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -114,28 +116,30 @@ fc_status fc_conv3x3_act_pool(const void* x, const void* w, const void* b, float
                               fc_stream_t stream)
 {
     if (H < 3 || W < 3) return FC_ERR_INVALID_ARG;
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, dtype, act, workspace, workspace_bytes, stream, 1);
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, FC_NCHW, dtype, act, workspace, workspace_bytes, stream, 1);
 }
 
 fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W, int Cout,
                          fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes, fc_stream_t stream)
 {
     if (H < 3 || W < 3) return FC_ERR_INVALID_ARG;
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, dtype, act, workspace, workspace_bytes, stream, 0);
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, 0, FC_NCHW, dtype, act, workspace, workspace_bytes, stream, 0);
 }
 
-fc_status fc_conv3x3_act_pool_pad(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H,
-                                  int W, int Cout, int pad, fc_dtype dtype, fc_act act, void* workspace,
-                                  size_t workspace_bytes, fc_stream_t stream)
+fc_status fc_conv3x3_act_pool_ex(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H,
+                                 int W, int Cout, int pad, fc_layout layout, fc_dtype dtype, fc_act act,
+                                 void* workspace, size_t workspace_bytes, fc_stream_t stream)
 {
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, dtype, act, workspace, workspace_bytes, stream, 1);
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, layout, dtype, act, workspace, workspace_bytes, stream,
+                       1);
 }
 
-fc_status fc_conv3x3_act_pad(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W,
-                             int Cout, int pad, fc_dtype dtype, fc_act act, void* workspace, size_t workspace_bytes,
-                             fc_stream_t stream)
+fc_status fc_conv3x3_act_ex(const void* x, const void* w, const void* b, float* y, int N, int Cin, int H, int W,
+                            int Cout, int pad, fc_layout layout, fc_dtype dtype, fc_act act, void* workspace,
+                            size_t workspace_bytes, fc_stream_t stream)
 {
-    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, dtype, act, workspace, workspace_bytes, stream, 0);
+    return conv_common(x, w, b, y, N, Cin, H, W, Cout, pad, layout, dtype, act, workspace, workspace_bytes, stream,
+                       0);
 }
 
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y, int M, int K, int Nout,
@@ -206,16 +210,18 @@ fc_status fc_scale_clamp_lse_mish(const float* t, float* y, int M, int N, float 
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
-size_t fc_workspace_bytes_pad(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_dtype dtype)
+size_t fc_workspace_bytes_ex(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_layout layout,
+                             fc_dtype dtype)
 {
     if (op != FC_OP_CONV3X3_ACT_POOL && op != FC_OP_CONV3X3_ACT) return 0;
+    if (layout != FC_NCHW && layout != FC_NHWC) return 0;
     DeviceState* d = nullptr;
     if (device_state(&d) != FC_OK) return 0;
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return 0;
     if (!conv_shape_ok(n, cin, h, w, cout, pad)) return 0;
     fc::ConvPlan plan;
-    if (fc::conv_plan(&plan, n, cin, h, w, cout, pad, static_cast<int>(dtype), op == FC_OP_CONV3X3_ACT_POOL,
-                      d->sm_count) != 0)
+    if (fc::conv_plan(&plan, n, cin, h, w, cout, pad, layout == FC_NHWC, static_cast<int>(dtype),
+                      op == FC_OP_CONV3X3_ACT_POOL, d->sm_count) != 0)
         return 0;
     return plan.ws_weights_bytes + plan.ws_pool_bytes;
 }
@@ -227,7 +233,7 @@ size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int 
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return 0;
     if (op == FC_OP_CONV3X3_ACT_POOL || op == FC_OP_CONV3X3_ACT) {
         if (h < 3 || w < 3) return 0;
-        return fc_workspace_bytes_pad(op, n_or_m, cin_or_k, h, w, cout_or_nout, 0, dtype);
+        return fc_workspace_bytes_ex(op, n_or_m, cin_or_k, h, w, cout_or_nout, 0, FC_NCHW, dtype);
     }
     if (op == FC_OP_LINEAR_LSE_MISH) {
         if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1 || dtype == FC_F32_3XTF32) return 0;

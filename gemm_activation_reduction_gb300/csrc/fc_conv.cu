@@ -130,11 +130,13 @@ struct Geometry {
     uint32_t strip_bytes, raw_bytes;
 };
 
-template <bool BF16, bool WIDE, int ROWS, int XP>
+template <bool BF16, bool WIDE, int ROWS, int XP, bool NHWC = false>
 Geometry geometry_of()
 {
-    using S = Shape<WIDE, ROWS, XP>;
+    using S = Shape<WIDE, ROWS, XP, NHWC>;
     using R = RawBox<BF16, WIDE, ROWS, XP>;
+    // NHWC: the boxes are one channel group each ([SR][SC][16 B]) and land in the strip
+    if (NHWC) return Geometry{S::PR, S::PC, S::SR, S::SC, 16 / (BF16 ? 2 : 4), S::STRIP, 0u};
     return Geometry{S::PR, S::PC, S::SR, R::kCols, R::kCh, S::STRIP, R::kBytes};
 }
 
@@ -149,14 +151,20 @@ Geometry geometry_xp(int bf16, int pool, int pair)
 }
 
 // padx: the padding's column shift needs XP = 4 (fp32) / 8 (bf16) extra staged columns
-Geometry geometry(int bf16, int pool, int pair, int padx)
+Geometry geometry(int bf16, int pool, int pair, int padx, int nhwc)
 {
+    if (nhwc) {
+        if (pool) return bf16 ? geometry_of<true, false, 1, 0, true>() : geometry_of<false, false, 1, 0, true>();
+        if (pair) return bf16 ? geometry_of<true, true, 1, 0, true>() : geometry_of<false, true, 1, 0, true>();
+        return bf16 ? geometry_of<true, true, 2, 0, true>() : geometry_of<false, true, 2, 0, true>();
+    }
     return padx ? geometry_xp<4, 8>(bf16, pool, pair) : geometry_xp<0, 0>(bf16, pool, pair);
 }
 
 }  // namespace
 
-int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int dtype, int pool, int sm_count)
+int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int nhwc, int dtype, int pool,
+              int sm_count)
 {
     *p = ConvPlan{};
     if (dtype < 0 || dtype > 2) return 2;
@@ -175,7 +183,9 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     // TMA boxes start on 16-byte boundaries: the staged patch begins dcol columns before the
     // padded window, dcol = (-pad) mod (elements per 16 B)
     const int align = 16 / p->esize;
-    p->dcol = (align - pad % align) % align;
+    p->nhwc = nhwc ? 1 : 0;
+    // NHWC boxes start at any column (channels are the 16-byte-aligned dimension)
+    p->dcol = p->nhwc ? 0 : (align - pad % align) % align;
     p->padx = p->dcol != 0 ? 1 : 0;
     p->cb_ch = bf16 ? 16 : 8;
     p->ncb = (Cin + p->cb_ch - 1) / p->cb_ch * p->parts;
@@ -183,7 +193,7 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
     // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
     p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
-    const Geometry geo = geometry(bf16, pool, p->pair, p->padx);
+    const Geometry geo = geometry(bf16, pool, p->pair, p->padx, p->nhwc);
     p->RB = (p->OH + geo.PR - 1) / geo.PR;
     p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
@@ -206,7 +216,8 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     p->raw_bytes = geo.raw_bytes;
     p->strip_bytes = geo.strip_bytes;
     // TMA needs 16-byte multiples for every global stride: the row pitch W * esize decides
-    p->use_tma = (static_cast<long long>(W) * p->esize) % 16 == 0;
+    // (NCHW), or the pixel pitch Cin * esize (NHWC)
+    p->use_tma = (static_cast<long long>(nhwc ? Cin : W) * p->esize) % 16 == 0;
     p->resident = p->w_total_bytes <= kResidentMax;
     // Shared memory: strips and (streamed) weight blocks per stage, kNumProd x raw_depth
     // TMA boxes, the indicator planes, the (resident) weights and the bias block.
@@ -222,8 +233,10 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     p->stages = static_cast<int>(std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed - boxes_min) / per_stage));
     if (p->stages < kNumProd) return 2;
     // the shared memory left buys TMA look-ahead
-    p->raw_depth = 1;
-    if (p->use_tma)
+    // (NHWC: no raw boxes; depth 2 indexes each producer's two landing barriers: the stage it
+    // rounds and the one it has requested ahead)
+    p->raw_depth = p->nhwc ? 2 : 1;
+    if (p->use_tma && !p->nhwc)
         p->raw_depth = static_cast<int>(std::min<uint32_t>(
             kMaxRawDepth, (kSmemBudget - fixed - static_cast<uint32_t>(p->stages) * per_stage) / per_depth));
     p->nacc = std::min(kMaxAcc, 512 / Cout);
@@ -277,19 +290,29 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         if (e != cudaSuccess) return e;
     }
 
-    // x as a 4-D tensor (W, H, Cin, N); one box = [K-block channels][staged rows][staged columns]
+    // NCHW x as a 4-D tensor (W, H, Cin, N), one box = [K-block channels][staged rows][staged
+    // columns]; NHWC x as (Cin, W, H, N), one box = [staged rows][staged columns][one channel group]
     CUtensorMap tmx;
     std::memset(&tmx, 0, sizeof(tmx));
     if (p.use_tma) {
         auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
         if (enc == nullptr) return cudaErrorNotSupported;
         const cuuint64_t es = static_cast<cuuint64_t>(p.esize);
-        cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.Cin),
-                              static_cast<cuuint64_t>(p.N)};
+        const Geometry geo = geometry(p.bf16, p.pool, p.pair, p.padx, p.nhwc);
+        cuuint64_t dims[4];
+        cuuint32_t box[4];
+        if (p.nhwc) {
+            dims[0] = static_cast<cuuint64_t>(p.Cin); dims[1] = static_cast<cuuint64_t>(p.W);
+            dims[2] = static_cast<cuuint64_t>(p.H); dims[3] = static_cast<cuuint64_t>(p.N);
+            box[0] = static_cast<cuuint32_t>(geo.box_ch); box[1] = static_cast<cuuint32_t>(geo.box_cols);
+            box[2] = static_cast<cuuint32_t>(geo.SR); box[3] = 1u;
+        } else {
+            dims[0] = static_cast<cuuint64_t>(p.W); dims[1] = static_cast<cuuint64_t>(p.H);
+            dims[2] = static_cast<cuuint64_t>(p.Cin); dims[3] = static_cast<cuuint64_t>(p.N);
+            box[0] = static_cast<cuuint32_t>(geo.box_cols); box[1] = static_cast<cuuint32_t>(geo.SR);
+            box[2] = static_cast<cuuint32_t>(geo.box_ch); box[3] = 1u;
+        }
         cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
-        const Geometry geo = geometry(p.bf16, p.pool, p.pair, p.padx);
-        cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_cols), static_cast<cuuint32_t>(geo.SR),
-                             static_cast<cuuint32_t>(geo.box_ch), 1u};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         CUresult r = enc(&tmx, p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                          const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -311,7 +334,14 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.status = status; a.budget = budget;
 
     cudaError_t e;
-    if (p.padx) {
+    if (p.nhwc) {
+        if (p.bf16)
+            e = p.pair ? launch_main_bf16_pair_nhwc(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                       : launch_main_bf16_nhwc(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+        else
+            e = p.pair ? launch_main_tf32_pair_nhwc(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
+                       : launch_main_tf32_nhwc(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);
+    } else if (p.padx) {
         if (p.bf16)
             e = p.pair ? launch_main_bf16_pair_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream)
                        : launch_main_bf16_padx(tmx, a, p.pool, act, p.grid, p.smem_bytes, stream);

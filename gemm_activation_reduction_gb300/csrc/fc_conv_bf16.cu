@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_bf16)
 {
-    FC_CONV_LAUNCH_BODY(true, false, false)
+    FC_CONV_LAUNCH_BODY(true, false, false, false)
 }
 
 }  // namespace convk

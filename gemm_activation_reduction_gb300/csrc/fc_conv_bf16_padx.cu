@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_bf16_padx)
 {
-    FC_CONV_LAUNCH_BODY(true, false, true)
+    FC_CONV_LAUNCH_BODY(true, false, true, false)
 }
 
 }  // namespace convk

@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_bf16_pair)
 {
-    FC_CONV_LAUNCH_BODY(true, true, false)
+    FC_CONV_LAUNCH_BODY(true, true, false, false)
 }
 
 }  // namespace convk

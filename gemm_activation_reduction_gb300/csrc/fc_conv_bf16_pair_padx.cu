@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_bf16_pair_padx)
 {
-    FC_CONV_LAUNCH_BODY(true, true, true)
+    FC_CONV_LAUNCH_BODY(true, true, true, false)
 }
 
 }  // namespace convk

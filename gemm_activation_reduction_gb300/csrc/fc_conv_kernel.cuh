@@ -91,7 +91,10 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // tile, d = (-p) mod (16 B / element size), so that the TMA box starts on a 16-byte
 // boundary; XP = 4 (fp32) or 8 (bf16) extra staged columns hold the d-column shift and
 // every MMA operand starts d staged pixels further (XP = 0 when d is always 0).
-template <bool WIDE, int ROWS = 1, int XP = 0>
+//
+// NHWC input: each channel group of a K block is one TMA box written straight into its
+// strip plane, so the planes start on 128-byte boundaries (PLANE rounded up).
+template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false>
 struct Shape {
     static constexpr int UNITS = WIDE ? ROWS : 1;          // M = 128 MMA units per tile
     static constexpr int PR = WIDE ? ROWS : 16;            // output rows per tile
@@ -99,7 +102,7 @@ struct Shape {
     static constexpr int SR = PR + 2;                      // staged rows (halo)
     static constexpr int SC = PC + 2 + XP;                 // staged columns (halo + shift room)
     static constexpr int SPOS = SR * SC;                   // staged pixels
-    static constexpr uint32_t PLANE = SPOS * 16;           // one channel group of the strip
+    static constexpr uint32_t PLANE = NHWC ? (SPOS * 16 + 127) / 128 * 128 : SPOS * 16;   // one channel group
     static constexpr uint32_t STRIP = (2 * PLANE + 127) / 128 * 128;  // one K block, slot pitch
     static constexpr uint32_t SBO = WIDE ? 128u : SC * 16u;
 };
@@ -229,6 +232,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t
     asm volatile(
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// The same with the destination as a shared-memory address.
+__device__ __forceinline__ void tma_load_4d_s(uint32_t dst, const void* map, uint64_t* bar, int c0, int c1, int c2,
+                                              int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
@@ -370,6 +384,62 @@ __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n
     }
 }
 
+// NHWC fallback staging with plain loads (when Cin's row of channels is not a 16-byte
+// multiple and TMA cannot address it): x [N][H][W][Cin]; one staged pixel's K block is
+// 8 fp32 / 16 bf16 consecutive channels, zero past the image and past Cin.
+template <bool BF16, bool WIDE, int ROWS>
+__device__ __forceinline__ void fill_strip_nhwc(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
+                                                int Cin, int H, int W, int lane, bool lo)
+{
+    using S = Shape<WIDE, ROWS, 0, true>;
+    for (int s = lane; s < S::SPOS; s += 32) {
+        const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
+        const int ih = oh0 + rr, iw = ow0 + cc;
+        const bool ok = ih >= 0 && ih < H && iw >= 0 && iw < W;
+        const size_t pix = ok ? ((static_cast<size_t>(n) * H + ih) * W + iw) * static_cast<size_t>(Cin) : 0;
+        const uint32_t a = strip + static_cast<uint32_t>(s) * 16u;
+        if constexpr (!BF16) {
+            const float* x = reinterpret_cast<const float*>(xv) + pix;
+            const int ci0 = cb * 8;
+            uint32_t t[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = (ok && ci0 + e < Cin) ? __ldg(x + ci0 + e) : 0.0f;
+                t[e] = lo ? tf32_part<true>(v) : tf32_part<false>(v);
+            }
+            st_shared_v4(a, t[0], t[1], t[2], t[3]);
+            st_shared_v4(a + S::PLANE, t[4], t[5], t[6], t[7]);
+        } else {
+            const unsigned short* x = reinterpret_cast<const unsigned short*>(xv) + pix;
+            const int ci0 = cb * 16;
+            uint32_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t l = (ok && ci0 + 2 * e < Cin) ? __ldg(x + ci0 + 2 * e) : 0u;
+                const uint32_t h = (ok && ci0 + 2 * e + 1 < Cin) ? __ldg(x + ci0 + 2 * e + 1) : 0u;
+                v[e] = l | (h << 16);
+            }
+            st_shared_v4(a, v[0], v[1], v[2], v[3]);
+            st_shared_v4(a + S::PLANE, v[4], v[5], v[6], v[7]);
+        }
+    }
+}
+
+// NHWC fp32: the TMA boxes land raw fp32 channel groups in the strip; round them in place
+// to the TF32 operand (the high part, or with LO the split-TF32 remainder).
+template <bool WIDE, int ROWS, bool LO>
+__device__ __forceinline__ void round_strip_tf32(uint32_t strip, int lane)
+{
+    using S = Shape<WIDE, ROWS, 0, true>;
+#pragma unroll 4
+    for (int i = lane; i < 2 * S::SPOS; i += 32) {
+        const int g = i >= S::SPOS ? 1 : 0;
+        const uint32_t a = strip + static_cast<uint32_t>(g) * S::PLANE + static_cast<uint32_t>(i - g * S::SPOS) * 16u;
+        const float4 v = ld_shared_f4(a);
+        st_shared_v4(a, tf32_part<LO>(v.x), tf32_part<LO>(v.y), tf32_part<LO>(v.z), tf32_part<LO>(v.w));
+    }
+}
+
 // Wait with no abort check and no status write: used to drain this warp's own
 // copies in flight before the CTA exits after an abort.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long budget)
@@ -502,7 +572,7 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -512,7 +582,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     constexpr int ROWS = (WIDE && !PAIR) ? 2 : 1;
     // room for the padding's column shift a.dcol (< 16 B of elements) when it is not 0
     constexpr int XP = PADX ? (BF16 ? 8 : 4) : 0;
-    using S = Shape<WIDE, ROWS, XP>;
+    static_assert(!(PADX && NHWC), "NHWC boxes start at any column: no shift room needed");
+    using S = Shape<WIDE, ROWS, XP, NHWC>;
     using RBox = RawBox<BF16, WIDE, ROWS, XP>;
     constexpr int UPT = S::UNITS;   // accumulator units per tile
     extern __shared__ uint8_t smem_raw[];
@@ -634,12 +705,92 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 ++issued;
                 advance(atc, alt, acb, kNumProd);
             };
-            if (a.use_tma)
+            if (!NHWC && a.use_tma)
                 while (static_cast<int>(issued) < rd && alt < n_pairs) issue_next();
             uint32_t use = 0;                         // this warp's stages whose box was waited for
             uint32_t g = static_cast<uint32_t>(pw);   // global stage index
             long long last_w = -1;                    // stage of this warp's last weight copy
-            while (lt < n_pairs) {
+            // The strip of stage `slot` is complete: arrive on its full barrier; a pair's peer then
+            // forwards "my half is complete" to the leader once its own barrier has completed.
+            // Returns false (for the whole warp) when that wait gave up.
+            auto hand_over = [&](uint32_t slot, uint32_t par) -> bool {
+                bool fok = true;
+                if (lane == 0) {
+                    mbar_arrive(&full[slot]);
+                    if (pair && !leader) {
+                        fok = mbar_wait(&full[slot], par, abort_flag, a.status, a.budget);
+                        if (fok) mbar_arrive_remote(mapa_shared(smem_u32(&full[slot]), 0));
+                    }
+                }
+                return __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
+            };
+            if (NHWC && a.use_tma) {
+                // NHWC: each channel group of a stage is one TMA box [SR rows][SC columns][16 B]
+                // written straight into its strip plane (zeros outside x: padding, channels past
+                // Cin, a tile past the end).  With at least twice as many slots as producer warps
+                // this warp requests its next stage before it rounds the current one: that
+                // stage's slot was last used by this warp's own earlier stage (g + P - S <= g - P),
+                // so the request waits on nothing later in the pipeline.  With fewer slots the
+                // slot would be another warp's stage g - 1 or later, and waiting for it before
+                // handing over stage g would order every stage behind the previous one's MMAs, so
+                // stages are then requested one at a time.
+                const bool ahead = a.stages >= 2 * kNumProd;
+                TileCoord itc = tc;   // the next stage to request: tile, K stage, global index
+                int ilt = lt, icb = cb;
+                uint32_t ig = g;
+                auto request = [&]() -> bool {
+                    const uint32_t slot = ig % S_;
+                    const uint32_t par = (ig / S_) & 1u;
+                    bool okr = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
+                    if (!__all_sync(0xffffffffu, okr)) return false;
+                    fence_proxy_async_smem();
+                    const uint32_t strip = strip0 + slot * S::STRIP;
+                    const uint32_t r = raw_buf(issued);
+                    if (lane == 0) {
+                        if (!a.resident) {
+                            last_w = ig;
+                            mbar_arrive_expect_tx(&full[slot], a.w_block_bytes);
+                            bulk_g2s(smem + a.w_off + slot * a.w_block_bytes,
+                                     wmine + static_cast<size_t>(icb) * a.w_block_bytes, a.w_block_bytes, &full[slot]);
+                        } else {
+                            mbar_arrive(&full[slot]);
+                        }
+                        constexpr int kG = BF16 ? 8 : 4;   // channels per group (16 B)
+                        mbar_arrive_expect_tx(&rawfull[r], 2u * static_cast<uint32_t>(S::SPOS) * 16u);
+                        const int c0 = (a.parts == 1 ? icb : icb / 3) * 2 * kG;
+#pragma unroll
+                        for (int gg = 0; gg < 2; ++gg)
+                            tma_load_4d_s(strip + static_cast<uint32_t>(gg) * S::PLANE, &tmx, &rawfull[r], c0 + gg * kG,
+                                          itc.cs * S::PC - a.pad, itc.rb * S::PR - a.pad, itc.n);
+                    }
+                    ++issued;
+                    advance(itc, ilt, icb, kNumProd);
+                    ig += kNumProd;
+                    return true;
+                };
+                while (lt < n_pairs) {
+                    if (issued == use && !request()) break;
+                    if (ahead && issued == use + 1 && ilt < n_pairs && !request()) break;
+                    const uint32_t slot = g % S_;
+                    const uint32_t par = (g / S_) & 1u;
+                    const uint32_t strip = strip0 + slot * S::STRIP;
+                    const uint32_t r = raw_buf(use);
+                    bool ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status,
+                                        a.budget);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    if constexpr (!BF16) {
+                        if (a.parts == 3 && cb % 3 == 2) round_strip_tf32<WIDE, ROWS, true>(strip, lane);
+                        else round_strip_tf32<WIDE, ROWS, false>(strip, lane);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (!hand_over(slot, par)) break;
+                    advance(tc, lt, cb, kNumProd);
+                    ++use;
+                    g += kNumProd;
+                }
+            }
+            while (!(NHWC && a.use_tma) && lt < n_pairs) {
                 const uint32_t slot = g % S_;
                 const uint32_t par = (g / S_) & 1u;
                 bool ok = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
@@ -656,7 +807,13 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     }
                 }
                 const uint32_t strip = strip0 + slot * S::STRIP;
-                if (a.use_tma) {
+                if (NHWC) {
+                    fill_strip_nhwc<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
+                                                      tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad, a.Cin,
+                                                      tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                } else if (a.use_tma) {
                     const uint32_t r = raw_buf(use);
                     ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
@@ -679,14 +836,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     __syncwarp();
                 }
                 // every lane fenced its strip writes and the warp has synchronised
-                if (lane == 0) {
-                    mbar_arrive(&full[slot]);
-                    if (pair && !leader) {
-                        // forward "my half of this stage is complete" to the leader
-                        if (!mbar_wait(&full[slot], par, abort_flag, a.status, a.budget)) break;
-                        mbar_arrive_remote(mapa_shared(smem_u32(&full[slot]), 0));
-                    }
-                }
+                if (!hand_over(slot, par)) break;
                 advance(tc, lt, cb, kNumProd);
                 ++use;
                 g += kNumProd;
@@ -1046,7 +1196,32 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rnext[j]);
                     if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
                     else release_and_next();
-                    if constexpr (!POOL) {
+                    if constexpr (!POOL && NHWC) {
+                        // y [N][OH][OW][Co]: this pixel's 16 channels of the slice are 64
+                        // contiguous bytes; 128-bit streaming stores when whole and aligned
+                        if (valid) {
+                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.OH + oh) * a.OW + ow) *
+                                                   static_cast<size_t>(a.Co) + c * kEpiCols;
+                            const int jmax = a.Co - c * kEpiCols;
+                            float r16[kEpiCols];
+#pragma unroll
+                            for (int j = 0; j < kEpiCols; j += 2) {
+                                float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
+                                if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
+                                r16[j] = g.x;
+                                r16[j + 1] = g.y;
+                            }
+                            if (jmax >= kEpiCols && (a.Co & 3) == 0) {
+#pragma unroll
+                                for (int j = 0; j < kEpiCols; j += 4)
+                                    __stcs(reinterpret_cast<float4*>(o + j), make_float4(r16[j], r16[j + 1], r16[j + 2], r16[j + 3]));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < kEpiCols; ++j)
+                                    if (j < jmax) __stcs(o + j, r16[j]);
+                            }
+                        }
+                    } else if constexpr (!POOL) {
                         if (valid) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Co + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
@@ -1089,11 +1264,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX, NHWC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1118,17 +1293,17 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
                      cudaStream_t stream)
 
 // The variant switch shared by the four translation units.
-#define FC_CONV_LAUNCH_BODY(BF16, PAIR, PADX)                                                      \
-    switch ((pool ? 0 : 1) * 4 + act) {                                                           \
-    case 0: return launch_variant<BF16, true, 0, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
-    case 1: return launch_variant<BF16, true, 1, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
-    case 2: return launch_variant<BF16, true, 2, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
-    case 3: return launch_variant<BF16, true, 3, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);    \
-    case 4: return launch_variant<BF16, false, 0, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
-    case 5: return launch_variant<BF16, false, 1, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
-    case 6: return launch_variant<BF16, false, 2, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
-    case 7: return launch_variant<BF16, false, 3, PAIR, PADX>(tmx, a, grid, smem_bytes, stream);   \
-    default: return cudaErrorInvalidValue;                                                       \
+#define FC_CONV_LAUNCH_BODY(BF16, PAIR, PADX, NHWC)                                                      \
+    switch ((pool ? 0 : 1) * 4 + act) {                                                                 \
+    case 0: return launch_variant<BF16, true, 0, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
+    case 1: return launch_variant<BF16, true, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
+    case 2: return launch_variant<BF16, true, 2, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
+    case 3: return launch_variant<BF16, true, 3, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
+    case 4: return launch_variant<BF16, false, 0, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
+    case 5: return launch_variant<BF16, false, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
+    case 6: return launch_variant<BF16, false, 2, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
+    case 7: return launch_variant<BF16, false, 3, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
+    default: return cudaErrorInvalidValue;                                                             \
     }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair);
@@ -1139,6 +1314,11 @@ FC_CONV_LAUNCH_DECL(launch_main_tf32_padx);
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair_padx);
 FC_CONV_LAUNCH_DECL(launch_main_bf16_padx);
 FC_CONV_LAUNCH_DECL(launch_main_bf16_pair_padx);
+// the same for NHWC (channels-last) input and full output
+FC_CONV_LAUNCH_DECL(launch_main_tf32_nhwc);
+FC_CONV_LAUNCH_DECL(launch_main_tf32_pair_nhwc);
+FC_CONV_LAUNCH_DECL(launch_main_bf16_nhwc);
+FC_CONV_LAUNCH_DECL(launch_main_bf16_pair_nhwc);
 
 }  // namespace convk
 }  // namespace fc

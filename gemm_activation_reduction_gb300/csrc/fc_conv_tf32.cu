@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_tf32)
 {
-    FC_CONV_LAUNCH_BODY(false, false, false)
+    FC_CONV_LAUNCH_BODY(false, false, false, false)
 }
 
 }  // namespace convk

@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_tf32_padx)
 {
-    FC_CONV_LAUNCH_BODY(false, false, true)
+    FC_CONV_LAUNCH_BODY(false, false, true, false)
 }
 
 }  // namespace convk

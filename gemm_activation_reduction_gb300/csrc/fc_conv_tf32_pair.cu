@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair)
 {
-    FC_CONV_LAUNCH_BODY(false, true, false)
+    FC_CONV_LAUNCH_BODY(false, true, false, false)
 }
 
 }  // namespace convk

@@ -7,7 +7,7 @@ namespace convk {
 
 FC_CONV_LAUNCH_DECL(launch_main_tf32_pair_padx)
 {
-    FC_CONV_LAUNCH_BODY(false, true, true)
+    FC_CONV_LAUNCH_BODY(false, true, true, false)
 }
 
 }  // namespace convk

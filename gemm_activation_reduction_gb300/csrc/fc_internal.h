@@ -25,6 +25,7 @@ struct ConvPlan {
     int pad;              // zero padding on every side
     int dcol;             // staged columns before the padded window: (-pad) mod (16 B / esize)
     int padx;             // dcol != 0: the kernel variant with room for that shift
+    int nhwc;             // x is [N][H][W][Cin] and the full output [N][OH][OW][Cout]
     int Co;               // output channels of the call (any count in 1 .. 256)
     int Cout;             // Co rounded up to 16: the MMA tile width; channels >= Co carry zero
                           // weights and bias and are never stored
@@ -63,7 +64,7 @@ struct ConvPlan {
 // dtype: 0 fp32 (TF32 products), 1 bf16, 2 fp32 with split-TF32 products (the fc_dtype codes);
 // pad: zero padding, 0 .. kMaxPad.
 constexpr int kMaxPad = 64;
-int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int pad, int dtype, int pool,
+int conv_plan(ConvPlan* plan, int N, int Cin, int H, int W, int Cout, int pad, int nhwc, int dtype, int pool,
               int sm_count);
 
 cudaError_t conv_launch(const ConvPlan& plan, const void* x, const void* w, const void* b, float* y, int act,

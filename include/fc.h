@@ -71,6 +71,10 @@ typedef enum {
                                  page weighs against the exact form */
 } fc_act;
 
+/* Memory layout of the conv ops' x (and of the full output y): NCHW, or NHWC
+ * (channels last, PyTorch's channels_last memory format). */
+typedef enum { FC_NCHW = 0, FC_NHWC = 1 } fc_layout;
+
 typedef enum {
     FC_OP_CONV3X3_ACT_POOL = 0,
     FC_OP_CONV3X3_ACT = 1,
@@ -117,27 +121,30 @@ fc_status fc_conv3x3_act(const void* x, const void* w, const void* b, float* y,
                          void* workspace, size_t workspace_bytes, fc_stream_t stream);
 
 /*
- * The two conv operators with zero padding p on every side (PyTorch's
- * Conv2d(padding=p), padding_mode 'zeros'), the general-padding variant of the
- * pages' padding-0 convs (the Conv2d -> GELU -> pool page raises padded convs as
- * the general case):
+ * The two conv operators with zero padding p on every side and a choice of
+ * memory layout.  Padding is PyTorch's Conv2d(padding=p), padding_mode 'zeros',
+ * the general-padding variant of the pages' padding-0 convs (the Conv2d -> GELU
+ * -> pool page raises padded convs as the general case):
  *   v[n, co, oh, ow] = b[co] + sum_{ci, kh, kw} x[n, ci, oh+kh-p, ow+kw-p] * w[co, ci, kh, kw],
  * terms outside the input omitted; output plane OH x OW = (H+2p-2) x (W+2p-2),
- * so p = 1 keeps H x W.  fc_conv3x3_act_pool_pad: y [N, Cout], the mean over
- * the OH x OW plane; fc_conv3x3_act_pad: y [N, Cout, OH, OW].
+ * so p = 1 keeps H x W.  fc_conv3x3_act_pool_ex: y [N, Cout], the mean over
+ * the OH x OW plane; fc_conv3x3_act_ex: the full output.
+ *   layout FC_NCHW: x [N, Cin, H, W], full y [N, Cout, OH, OW];
+ *   layout FC_NHWC: x [N, H, W, Cin], full y [N, OH, OW, Cout] (channels last);
+ *   w is [Cout, Cin, 3, 3] (OIHW) and b [Cout] in both layouts.
  *   Requires 0 <= pad <= 64, H, W >= 1 with H + 2 pad >= 3 and W + 2 pad >= 3
- *   (FC_ERR_INVALID_ARG otherwise); the rest as for the pad-0 entry points
- *   (pad = 0 gives exactly their results).  The workspace size comes from
- *   fc_workspace_bytes_pad.
+ *   (FC_ERR_INVALID_ARG otherwise); the rest as for the pad-0 NCHW entry points
+ *   (pad = 0, FC_NCHW gives exactly their results).  The workspace size comes
+ *   from fc_workspace_bytes_ex.
  */
-fc_status fc_conv3x3_act_pool_pad(const void* x, const void* w, const void* b, float* y,
-                                  int N, int Cin, int H, int W, int Cout, int pad,
-                                  fc_dtype dtype, fc_act act,
-                                  void* workspace, size_t workspace_bytes, fc_stream_t stream);
-fc_status fc_conv3x3_act_pad(const void* x, const void* w, const void* b, float* y,
-                             int N, int Cin, int H, int W, int Cout, int pad,
-                             fc_dtype dtype, fc_act act,
-                             void* workspace, size_t workspace_bytes, fc_stream_t stream);
+fc_status fc_conv3x3_act_pool_ex(const void* x, const void* w, const void* b, float* y,
+                                 int N, int Cin, int H, int W, int Cout, int pad, fc_layout layout,
+                                 fc_dtype dtype, fc_act act,
+                                 void* workspace, size_t workspace_bytes, fc_stream_t stream);
+fc_status fc_conv3x3_act_ex(const void* x, const void* w, const void* b, float* y,
+                            int N, int Cin, int H, int W, int Cout, int pad, fc_layout layout,
+                            fc_dtype dtype, fc_act act,
+                            void* workspace, size_t workspace_bytes, fc_stream_t stream);
 
 /*
  * t[m, j] = clamp( u + u, clamp_lo, clamp_hi ),  u = (b[j] + sum_k x[m, k] W[j, k]) * scale
@@ -218,8 +225,9 @@ fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, const void* b
 size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int cout_or_nout,
                           fc_dtype dtype);
 
-/* The same for the padded conv entry points (op = one of the two conv ops). */
-size_t fc_workspace_bytes_pad(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_dtype dtype);
+/* The same for the conv _ex entry points (op = one of the two conv ops). */
+size_t fc_workspace_bytes_ex(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_layout layout,
+                             fc_dtype dtype);
 
 /* Static English text for a status code. */
 const char* fc_status_string(fc_status status);

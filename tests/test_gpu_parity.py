@@ -207,7 +207,7 @@ def test_conv_pad_zero_matches_unpadded_entry_point_bit_for_bit(cuda_lib):
     y0 = torch.empty((2, 64), device="cuda")
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     nb = lib.fc_workspace_bytes(0, 2, 8, 20, 36, 64, 0)
-    assert nb == lib.fc_workspace_bytes_pad(0, 2, 8, 20, 36, 64, 0, 0)
+    assert nb == lib.fc_workspace_bytes_ex(0, 2, 8, 20, 36, 64, 0, cuda_lib.FC_NCHW, 0)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     assert lib.fc_conv3x3_act_pool(x.data_ptr(), w.data_ptr(), b.data_ptr(), y0.data_ptr(), 2, 8, 20, 36, 64, 0, 0,
                                    ws.data_ptr(), nb, s) == 0
@@ -221,13 +221,73 @@ def test_conv_pad_arguments_are_checked(cuda_lib):
     v = torch.zeros(4096, device="cuda")
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     p = v.data_ptr()
-    call = lambda H, W, pad: lib.fc_conv3x3_act_pad(p, p, p, p, 1, 1, H, W, 16, pad, 0, 0, None, 0, s)
+    call = lambda H, W, pad, lay=0: lib.fc_conv3x3_act_ex(p, p, p, p, 1, 1, H, W, 16, pad, lay, 0, 0, None, 0, s)
     assert call(4, 4, -1) == cuda_lib.FC_ERR_INVALID_ARG
     assert call(4, 4, 65) == cuda_lib.FC_ERR_INVALID_ARG
     assert call(1, 1, 0) == cuda_lib.FC_ERR_INVALID_ARG       # no output
-    assert lib.fc_workspace_bytes_pad(1, 1, 1, 4, 4, 16, -1, 0) == 0
-    assert lib.fc_workspace_bytes_pad(2, 1, 1, 4, 4, 16, 1, 0) == 0   # not a conv op
+    assert call(4, 4, 0, 2) == cuda_lib.FC_ERR_INVALID_ARG    # unknown layout
+    assert lib.fc_workspace_bytes_ex(1, 1, 1, 4, 4, 16, -1, 0, 0) == 0
+    assert lib.fc_workspace_bytes_ex(2, 1, 1, 4, 4, 16, 1, 0, 0) == 0   # not a conv op
+    assert lib.fc_workspace_bytes_ex(1, 1, 1, 4, 4, 16, 1, 5, 0) == 0   # unknown layout
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ NHWC (channels_last) input
+
+NHWC_SHAPES = [
+    # (N, Cin, H, W, Cout, pad, dtype, act, pool, precision)
+    (2, 8, 32, 32, 64, 0, "f32", "gelu", True, None),        # TMA channel boxes straight into the strip
+    (1, 13, 20, 37, 96, 0, "f32", "gelu", True, None),       # 13 channels: not 16-byte rows, plain loads
+    (2, 16, 18, 20, 64, 0, "bf16", "gelu", True, None),
+    (1, 8, 40, 17, 256, 0, "f32", "gelu", True, None),       # CTA pairs
+    (2, 8, 21, 19, 64, 1, "f32", "mish", True, None),        # padding: negative box origins
+    (1, 12, 14, 24, 64, 2, "f32", "gelu", True, "3xtf32"),   # split TF32 with padding
+    (2, 64, 12, 140, 128, 0, "f32", "mish_mish", False, None),  # two-row tiles
+    (1, 32, 9, 133, 64, 1, "bf16", "mish_mish", False, None),
+    (1, 16, 9, 131, 40, 0, "f32", "mish", False, None),      # Cout 40: a partial last slice
+    (1, 8, 7, 30, 7, 1, "f32", "gelu", False, None),         # Cout 7: scalar stores
+    (1, 16, 9, 130, 200, 1, "f32", "mish", False, None),     # CTA pairs
+    (1, 3, 11, 13, 32, 1, "f32", "gelu_tanh", False, None),  # 3 channels: plain loads
+    (1, 24, 10, 40, 64, 0, "f32", "mish_mish", False, "3xtf32"),
+]
+
+
+def _nhwc(arr):
+    """A CUDA tensor of logical shape [N, C, H, W] stored channels_last, from an NCHW array."""
+    import torch
+    t = _dev(np.ascontiguousarray(np.transpose(arr, (0, 2, 3, 1))))
+    return t.permute(0, 3, 1, 2)
+
+
+@pytest.mark.parametrize("shape", NHWC_SHAPES,
+                         ids=lambda s: "x".join(map(str, s[:5])) + f"-p{s[5]}-{s[6]}-{s[7]}-{'pool' if s[8] else 'act'}-{s[9]}")
+def test_conv_nhwc_small(cuda_lib, shape):
+    import torch
+    N, Cin, H, W, Cout, pad, dt, act, pool, prec = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, dt)
+    x = _nhwc(d["x"])
+    assert x.is_contiguous(memory_format=torch.channels_last) and not x.is_contiguous()
+    f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+    y = f(x, _dev(d["w"]), _dev(d["b"]), act=act, pad=pad, precision=prec)
+    if not pool:
+        assert y.is_contiguous(memory_format=torch.channels_last)
+    y = y.cpu().numpy()
+    ref = (oracle.conv3x3_act_pool if pool else oracle.conv3x3_act)(d["x32"], d["w32"], d["b32"], act, pad=pad)
+    assert y.shape == ref.shape
+    _check(y, ref, TOL_X3 if prec == "3xtf32" else TOL[dt], f"nhwc {shape}")
+
+
+def test_conv_nhwc_matches_nchw_bit_for_bit_where_the_arithmetic_is_the_same(cuda_lib):
+    """bf16 NHWC and NCHW calls stage the same operands and sum in the same order."""
+    import torch
+    d = fc_inputs.conv_inputs(2, 32, 12, 136, 64, "bf16")
+    w, b = _dev(d["w"]), _dev(d["b"])
+    y_nchw = cuda_lib.fc_conv3x3_act(_dev(d["x"]), w, b, act="mish")
+    y_nhwc = cuda_lib.fc_conv3x3_act(_nhwc(d["x"]), w, b, act="mish")
+    assert torch.equal(y_nchw, y_nhwc.contiguous())
+    p_nchw = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), w, b)
+    p_nhwc = cuda_lib.fc_conv3x3_act_pool(_nhwc(d["x"]), w, b)
+    assert torch.equal(p_nchw, p_nhwc)
 
 
 # ------------------------------------------------------------------ linear chain
@@ -286,13 +346,16 @@ def test_workload_B_full_size_sampled(cuda_lib, key):
     _check(y.reshape(-1)[flat], ref, TOL_X3 if wl.precision == "3xtf32" else TOL["f32"], f"workload {key}")
 
 
-@pytest.mark.parametrize("key", ["C", "Cb", "C3", "Cp"])
+@pytest.mark.parametrize("key", ["C", "Cb", "C3", "Cp", "Cn", "Cbn"])
 def test_workload_C_full_size_sampled(cuda_lib, key):
     import torch
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
-    y = cuda_lib.fc_conv3x3_act(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
+    x = _nhwc(d["x"]) if wl.layout == "nhwc" else _dev(d["x"])
+    y = cuda_lib.fc_conv3x3_act(x, _dev(d["w"]), _dev(d["b"]), act=wl.act,
                                 precision=None if wl.dtype == "bf16" else wl.precision, pad=wl.pad)
+    del x
+    y = y.contiguous()   # logical NCHW order for the flat sample indices
     OH, OW = wl.OH, wl.OW
     rng = np.random.default_rng(8)
     total = wl.N * wl.Cout * OH * OW
