@@ -221,6 +221,27 @@ def time_graph(torch, call, reps, replays=5):
     return statistics.median(times)
 
 
+def max_over_ranks(torch, value, dist, device):
+    """The maximum of a per-rank float over all ranks (a job's time is its slowest rank's);
+    `device` is where the collective's tensor lives (cuda for NCCL, cpu for gloo)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seeds(rank):
+    """Weak scaling: rank r owns its own shard (batch) of the workload, drawn with its own x seed
+    (weights and bias are shared)."""
+    return (fc_inputs.SEED_X + 1000 * rank, fc_inputs.SEED_W, fc_inputs.SEED_B)
+
+
+def job_tflops(flops_per_call, world, ms_per_call):
+    """Whole-job throughput: every rank's calls over the slowest rank's time per call."""
+    return flops_per_call * world / (ms_per_call * 1e-3) / 1e12
+
+
 def time_device(torch, call, steps, warmup, dist=None):
     for _ in range(warmup):
         call()
@@ -238,9 +259,7 @@ def time_device(torch, call, steps, warmup, dist=None):
     per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
     total = evs[0].elapsed_time(evs[-1])
     if dist is not None:
-        t = torch.tensor([total], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
+        total = max_over_ranks(torch, total, dist, "cuda")
         dist.barrier()
     torch.cuda.synchronize()
     return total, per
@@ -371,8 +390,7 @@ def gpu_arm(args):
     fc.load()
     key = args.workload
     wl = fc_inputs.WORKLOADS[key]
-    # weak scaling: each rank owns its own shard (batch) of the workload, seeded by rank
-    seeds = (fc_inputs.SEED_X + 1000 * rank, fc_inputs.SEED_W, fc_inputs.SEED_B)
+    seeds = rank_seeds(rank)
     if isinstance(wl, fc_inputs.LinearWorkload):
         d = fc_inputs.linear_inputs(wl.M, wl.K, wl.Nout, seeds=seeds, dtype=wl.dtype)
     else:
@@ -397,14 +415,15 @@ def gpu_arm(args):
 
     ms = total_ms / steps
     flops = wl.flops()
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms)
     pk = peaks()
     peak, peak_note = tensor_peak(wl, pk)
     kernel_ms = statistics.mean(per)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
 
     e2e_ms, h2d, d2h = time_e2e(fc, torch, key, d, device, steps=max(3, min(20, steps // 10)), warmup=2)
-    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(torch, e2e_ms, dist, "cuda")
+    e2e_value = job_tflops(flops, world, e2e_ms)
 
     if rank != 0:
         return 0
