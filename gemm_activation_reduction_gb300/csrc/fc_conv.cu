@@ -135,8 +135,8 @@ Geometry geometry_of()
 {
     using S = Shape<WIDE, ROWS, XP, NHWC>;
     using R = RawBox<BF16, WIDE, ROWS, XP>;
-    // NHWC: the boxes are one channel group each ([SR][SC][16 B]) and land in the strip
-    if (NHWC) return Geometry{S::PR, S::PC, S::SR, S::SC, 16 / (BF16 ? 2 : 4), S::STRIP, 0u};
+    // NHWC: one box per K block, [SR][SC][32 B of channels]
+    if (NHWC) return Geometry{S::PR, S::PC, S::SR, S::SC, 32 / (BF16 ? 2 : 4), S::STRIP, S::RAW_NHWC};
     return Geometry{S::PR, S::PC, S::SR, R::kCols, R::kCh, S::STRIP, R::kBytes};
 }
 
@@ -233,10 +233,8 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     p->stages = static_cast<int>(std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed - boxes_min) / per_stage));
     if (p->stages < kNumProd) return 2;
     // the shared memory left buys TMA look-ahead
-    // (NHWC: no raw boxes; depth 2 indexes each producer's two landing barriers: the stage it
-    // rounds and the one it has requested ahead)
-    p->raw_depth = p->nhwc ? 2 : 1;
-    if (p->use_tma && !p->nhwc)
+    p->raw_depth = 1;
+    if (p->use_tma)
         p->raw_depth = static_cast<int>(std::min<uint32_t>(
             kMaxRawDepth, (kSmemBudget - fixed - static_cast<uint32_t>(p->stages) * per_stage) / per_depth));
     p->nacc = std::min(kMaxAcc, 512 / Cout);

@@ -92,8 +92,9 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // boundary; XP = 4 (fp32) or 8 (bf16) extra staged columns hold the d-column shift and
 // every MMA operand starts d staged pixels further (XP = 0 when d is always 0).
 //
-// NHWC input: each channel group of a K block is one TMA box written straight into its
-// strip plane, so the planes start on 128-byte boundaries (PLANE rounded up).
+// NHWC input: a K block lands as one TMA box [SR rows][SC columns][32 B of channels] and is
+// split into the two planes; NHWC planes are 64 bytes past a 128-byte multiple apart so that
+// the split's 128-bit stores of one phase (4 pixels x 2 planes) cover all banks.
 template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false>
 struct Shape {
     static constexpr int UNITS = WIDE ? ROWS : 1;          // M = 128 MMA units per tile
@@ -102,7 +103,8 @@ struct Shape {
     static constexpr int SR = PR + 2;                      // staged rows (halo)
     static constexpr int SC = PC + 2 + XP;                 // staged columns (halo + shift room)
     static constexpr int SPOS = SR * SC;                   // staged pixels
-    static constexpr uint32_t PLANE = NHWC ? (SPOS * 16 + 127) / 128 * 128 : SPOS * 16;   // one channel group
+    static constexpr uint32_t PLANE = NHWC ? (SPOS * 16 + 127) / 128 * 128 + 64 : SPOS * 16;   // one channel group
+    static constexpr uint32_t RAW_NHWC = (SPOS * 32 + 127) / 128 * 128;   // one NHWC box: [SPOS][32 B]
     static constexpr uint32_t STRIP = (2 * PLANE + 127) / 128 * 128;  // one K block, slot pitch
     static constexpr uint32_t SBO = WIDE ? 128u : SC * 16u;
 };
@@ -425,18 +427,23 @@ __device__ __forceinline__ void fill_strip_nhwc(uint32_t strip, const void* xv, 
     }
 }
 
-// NHWC fp32: the TMA boxes land raw fp32 channel groups in the strip; round them in place
-// to the TF32 operand (the high part, or with LO the split-TF32 remainder).
-template <bool WIDE, int ROWS, bool LO>
-__device__ __forceinline__ void round_strip_tf32(uint32_t strip, int lane)
+// NHWC: a landed box holds each staged pixel's K block of channels as 32 contiguous bytes;
+// split them into the strip's two group planes -- fp32 rounded to the TF32 operand (the high
+// part, or with LO the split-TF32 remainder), bf16 as they are.  Item i is half i % 2 of pixel
+// i / 2: consecutive lanes read consecutive 16 bytes.
+template <bool BF16, bool WIDE, int ROWS, bool LO>
+__device__ __forceinline__ void copy_raw_nhwc(uint32_t raw, uint32_t strip, int lane)
 {
     using S = Shape<WIDE, ROWS, 0, true>;
 #pragma unroll 4
     for (int i = lane; i < 2 * S::SPOS; i += 32) {
-        const int g = i >= S::SPOS ? 1 : 0;
-        const uint32_t a = strip + static_cast<uint32_t>(g) * S::PLANE + static_cast<uint32_t>(i - g * S::SPOS) * 16u;
-        const float4 v = ld_shared_f4(a);
-        st_shared_v4(a, tf32_part<LO>(v.x), tf32_part<LO>(v.y), tf32_part<LO>(v.z), tf32_part<LO>(v.w));
+        const uint32_t px = static_cast<uint32_t>(i >> 1), h = static_cast<uint32_t>(i & 1);
+        const float4 v = ld_shared_f4(raw + static_cast<uint32_t>(i) * 16u);
+        const uint32_t dst = strip + h * S::PLANE + px * 16u;
+        if constexpr (BF16)
+            st_shared_v4(dst, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+        else
+            st_shared_v4(dst, tf32_part<LO>(v.x), tf32_part<LO>(v.y), tf32_part<LO>(v.z), tf32_part<LO>(v.w));
     }
 }
 
@@ -585,6 +592,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     static_assert(!(PADX && NHWC), "NHWC boxes start at any column: no shift room needed");
     using S = Shape<WIDE, ROWS, XP, NHWC>;
     using RBox = RawBox<BF16, WIDE, ROWS, XP>;
+    // one raw buffer: an NCHW box, or (NHWC) the two channel-group boxes in the strip's layout
+    constexpr uint32_t kRawBytes = NHWC ? S::RAW_NHWC : RBox::kBytes;
     constexpr int UPT = S::UNITS;   // accumulator units per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -694,7 +703,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             // a tile past the end (the peer's half of a last, odd pair) is staged as zeros by TMA
             auto issue_next = [&]() {
                 const uint32_t r = raw_buf(issued);
-                if (lane == 0) {
+                if (NHWC && lane == 0) {
+                    // x [N][H][W][Cin]: the K block is one box [SR rows][SC columns][32 B of
+                    // channels] (zeros outside x: padding, channels past Cin, a tile past the end)
+                    constexpr int kCh = BF16 ? 16 : 8;   // channels per K block (32 B)
+                    mbar_arrive_expect_tx(&rawfull[r], static_cast<uint32_t>(S::SPOS) * 32u);
+                    tma_load_4d_s(smem_u32(smem + a.raw_off) + r * kRawBytes, &tmx, &rawfull[r],
+                                  (a.parts == 1 ? acb : acb / 3) * kCh, atc.cs * S::PC - a.pad, atc.rb * S::PR - a.pad,
+                                  atc.n);
+                } else if (lane == 0) {
                     mbar_arrive_expect_tx(&rawfull[r], RBox::kBytes);
                     // the patch starts pad rows above and pad + dcol columns left of the tile: a
                     // 16-byte-aligned column, possibly negative (TMA fills zeros outside x)
@@ -705,7 +722,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 ++issued;
                 advance(atc, alt, acb, kNumProd);
             };
-            if (!NHWC && a.use_tma)
+            if (a.use_tma)
                 while (static_cast<int>(issued) < rd && alt < n_pairs) issue_next();
             uint32_t use = 0;                         // this warp's stages whose box was waited for
             uint32_t g = static_cast<uint32_t>(pw);   // global stage index
@@ -724,73 +741,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 }
                 return __shfl_sync(0xffffffffu, fok ? 1 : 0, 0) != 0;
             };
-            if (NHWC && a.use_tma) {
-                // NHWC: each channel group of a stage is one TMA box [SR rows][SC columns][16 B]
-                // written straight into its strip plane (zeros outside x: padding, channels past
-                // Cin, a tile past the end).  With at least twice as many slots as producer warps
-                // this warp requests its next stage before it rounds the current one: that
-                // stage's slot was last used by this warp's own earlier stage (g + P - S <= g - P),
-                // so the request waits on nothing later in the pipeline.  With fewer slots the
-                // slot would be another warp's stage g - 1 or later, and waiting for it before
-                // handing over stage g would order every stage behind the previous one's MMAs, so
-                // stages are then requested one at a time.
-                const bool ahead = a.stages >= 2 * kNumProd;
-                TileCoord itc = tc;   // the next stage to request: tile, K stage, global index
-                int ilt = lt, icb = cb;
-                uint32_t ig = g;
-                auto request = [&]() -> bool {
-                    const uint32_t slot = ig % S_;
-                    const uint32_t par = (ig / S_) & 1u;
-                    bool okr = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
-                    if (!__all_sync(0xffffffffu, okr)) return false;
-                    fence_proxy_async_smem();
-                    const uint32_t strip = strip0 + slot * S::STRIP;
-                    const uint32_t r = raw_buf(issued);
-                    if (lane == 0) {
-                        if (!a.resident) {
-                            last_w = ig;
-                            mbar_arrive_expect_tx(&full[slot], a.w_block_bytes);
-                            bulk_g2s(smem + a.w_off + slot * a.w_block_bytes,
-                                     wmine + static_cast<size_t>(icb) * a.w_block_bytes, a.w_block_bytes, &full[slot]);
-                        } else {
-                            mbar_arrive(&full[slot]);
-                        }
-                        constexpr int kG = BF16 ? 8 : 4;   // channels per group (16 B)
-                        mbar_arrive_expect_tx(&rawfull[r], 2u * static_cast<uint32_t>(S::SPOS) * 16u);
-                        const int c0 = (a.parts == 1 ? icb : icb / 3) * 2 * kG;
-#pragma unroll
-                        for (int gg = 0; gg < 2; ++gg)
-                            tma_load_4d_s(strip + static_cast<uint32_t>(gg) * S::PLANE, &tmx, &rawfull[r], c0 + gg * kG,
-                                          itc.cs * S::PC - a.pad, itc.rb * S::PR - a.pad, itc.n);
-                    }
-                    ++issued;
-                    advance(itc, ilt, icb, kNumProd);
-                    ig += kNumProd;
-                    return true;
-                };
-                while (lt < n_pairs) {
-                    if (issued == use && !request()) break;
-                    if (ahead && issued == use + 1 && ilt < n_pairs && !request()) break;
-                    const uint32_t slot = g % S_;
-                    const uint32_t par = (g / S_) & 1u;
-                    const uint32_t strip = strip0 + slot * S::STRIP;
-                    const uint32_t r = raw_buf(use);
-                    bool ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status,
-                                        a.budget);
-                    if (!__all_sync(0xffffffffu, ok)) break;
-                    if constexpr (!BF16) {
-                        if (a.parts == 3 && cb % 3 == 2) round_strip_tf32<WIDE, ROWS, true>(strip, lane);
-                        else round_strip_tf32<WIDE, ROWS, false>(strip, lane);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (!hand_over(slot, par)) break;
-                    advance(tc, lt, cb, kNumProd);
-                    ++use;
-                    g += kNumProd;
-                }
-            }
-            while (!(NHWC && a.use_tma) && lt < n_pairs) {
+            while (lt < n_pairs) {
                 const uint32_t slot = g % S_;
                 const uint32_t par = (g / S_) & 1u;
                 bool ok = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
@@ -807,7 +758,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     }
                 }
                 const uint32_t strip = strip0 + slot * S::STRIP;
-                if (NHWC) {
+                if (NHWC && !a.use_tma) {
                     fill_strip_nhwc<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
                                                       tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad, a.Cin,
                                                       tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
@@ -817,9 +768,12 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t r = raw_buf(use);
                     ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
-                    const uint32_t raw = smem_u32(smem + a.raw_off + r * RBox::kBytes);
+                    const uint32_t raw = smem_u32(smem + a.raw_off) + r * kRawBytes;
                     // split TF32: the third stage of each K block stages x's remainder
-                    if constexpr (!BF16) {
+                    if constexpr (NHWC) {
+                        if (!BF16 && a.parts == 3 && cb % 3 == 2) copy_raw_nhwc<BF16, WIDE, ROWS, true>(raw, strip, lane);
+                        else copy_raw_nhwc<BF16, WIDE, ROWS, false>(raw, strip, lane);
+                    } else if constexpr (!BF16) {
                         if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, XP, true>(raw, strip, lane);
                         else transpose_raw<BF16, WIDE, ROWS, XP>(raw, strip, lane);
                     } else {
@@ -1150,17 +1104,111 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 advance_units(G);
             }
         }
+        if constexpr (!POOL && NHWC) {
+            // NHWC full output y [N][OH][OW][Co]: the slices are read in the 16x256b shape, so the
+            // four threads that share a pixel hold its 16 channels as 4 pairs each, and one
+            // 8-byte store per thread writes 8 pixels x 32 contiguous bytes per instruction (whole
+            // sectors).  Same pipeline as the pooled loop: the next slice (or the next tile's
+            // first one, once this accumulator is released) loads while this one is stored.
+            auto slice_addr = [&](int acc_i, int k) {
+                return tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                       static_cast<uint32_t>(acc_i * a.Cout + (hh + hw * k) * kEpiCols);
+            };
+            const bool pairs_ok = (a.Co & 1) == 0;   // 8-byte-aligned channel pairs
+            uint32_t buf[2][kEpiCols];
+            if (lt < n_units) {
+                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), buf[0]);
+            }
+            while (ok && lt < n_units) {
+                const bool real = t_first + static_cast<long long>(step) * (lt / UPT) < a.num_tiles;
+                const int nlt = lt + G;
+                int nacc_i = acc + G;
+                uint32_t naph = aph;
+                while (nacc_i >= a.nacc) {
+                    nacc_i -= a.nacc;
+                    naph ^= 1u;
+                }
+                auto release_and_next = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (pair) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+                        else mbar_arrive(&tempty[acc]);
+                    }
+                    if (nlt < n_units) {
+                        ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                        ok = __all_sync(0xffffffffu, ok);
+                        tc_fence_after();
+                        if (ok && ms > 0) {
+                            if (ms & 1) tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), buf[1]);
+                            else tmem_ld_slice16x256_start(slice_addr(nacc_i, 0), buf[0]);
+                        }
+                    }
+                };
+                if (ms == 0) release_and_next();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (k < ms) {
+                        uint32_t(&cur)[kEpiCols] = buf[k & 1];
+                        tmem_ld16_wait(cur);
+                        if (k + 1 < ms) tmem_ld_slice16x256_start(slice_addr(acc, k + 1), buf[(k + 1) & 1]);
+                        else release_and_next();
+                        const int c = hh + hw * k;
+                        // cur[8hb + 4u + 2p + e]: pixel (lane / 4) + 16hb + 8p of the warp's quarter,
+                        // channel 16c + 8u + 2(lane % 4) + e
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+#pragma unroll
+                            for (int pp = 0; pp < 2; ++pp) {
+                                const int rr = q * 32 + (lane >> 2) + 16 * hb + 8 * pp;
+                                const int oh = tc.rb * S::PR + us + rr / S::PC, ow = tc.cs * S::PC + rr % S::PC;
+                                const bool valid = real && oh < a.OH && ow < a.OW;
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    const int base = 8 * hb + 4 * u + 2 * pp;
+                                    float2 g = act2<ACT>(make_float2(__uint_as_float(cur[base]), __uint_as_float(cur[base + 1])));
+                                    if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
+                                    const int ch = c * kEpiCols + 8 * u + 2 * (lane & 3);
+                                    if (valid && ch < a.Co) {
+                                        float* o = a.out + ((static_cast<size_t>(tc.n) * a.OH + oh) * a.OW + ow) *
+                                                               static_cast<size_t>(a.Co) + ch;
+                                        if (pairs_ok) {
+                                            __stcs(reinterpret_cast<float2*>(o), g);
+                                        } else {
+                                            __stcs(o, g.x);
+                                            if (ch + 1 < a.Co) __stcs(o + 1, g.y);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+                if ((ms & 1) && ok && nlt < n_units) {
+                    tmem_ld16_wait(buf[1]);
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; ++j) buf[0][j] = buf[1][j];
+                }
+                acc = nacc_i;
+                aph = naph;
+                lt = nlt;
+                advance_units(G);
+            }
+        }
         // Full output: the next slice's TMEM load is in flight while the current one is
         // activated and stored; a tile's accumulator is released as soon as its last slice
         // is in registers.
         uint32_t rnext[kEpiCols];
-        if (!POOL && lt < n_units) {
+        if (!POOL && !NHWC && lt < n_units) {
             ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (ok && ms > 0) tmem_ld16_start(taddr(acc, 0), rnext);
         }
-        while (!POOL && ok && lt < n_units) {
+        while (!POOL && !NHWC && ok && lt < n_units) {
             const bool real = t_first + static_cast<long long>(step) * (lt / UPT) < a.num_tiles;   // the peer's half of a last, odd pair is not
             const int oh = tc.rb * S::PR + us + pr, ow = tc.cs * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
@@ -1196,32 +1244,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     for (int j = 0; j < kEpiCols; ++j) v[j] = __uint_as_float(rnext[j]);
                     if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
                     else release_and_next();
-                    if constexpr (!POOL && NHWC) {
-                        // y [N][OH][OW][Co]: this pixel's 16 channels of the slice are 64
-                        // contiguous bytes; 128-bit streaming stores when whole and aligned
-                        if (valid) {
-                            float* o = a.out + ((static_cast<size_t>(tc.n) * a.OH + oh) * a.OW + ow) *
-                                                   static_cast<size_t>(a.Co) + c * kEpiCols;
-                            const int jmax = a.Co - c * kEpiCols;
-                            float r16[kEpiCols];
-#pragma unroll
-                            for (int j = 0; j < kEpiCols; j += 2) {
-                                float2 g = act2<ACT>(make_float2(v[j], v[j + 1]));
-                                if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
-                                r16[j] = g.x;
-                                r16[j + 1] = g.y;
-                            }
-                            if (jmax >= kEpiCols && (a.Co & 3) == 0) {
-#pragma unroll
-                                for (int j = 0; j < kEpiCols; j += 4)
-                                    __stcs(reinterpret_cast<float4*>(o + j), make_float4(r16[j], r16[j + 1], r16[j + 2], r16[j + 3]));
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < kEpiCols; ++j)
-                                    if (j < jmax) __stcs(o + j, r16[j]);
-                            }
-                        }
-                    } else if constexpr (!POOL) {
+                    if constexpr (!POOL) {
                         if (valid) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Co + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
