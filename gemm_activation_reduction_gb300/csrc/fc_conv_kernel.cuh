@@ -256,6 +256,13 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
 {
     float4 v;
@@ -318,8 +325,9 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
                              tf32_part<LO>(v[3].w));
             }
         }
-    } else {
-        // item = (group g, staged row, column pair): 8 channels x 2 columns -> two 16-byte rows
+    } else if constexpr (!WIDE) {
+        // pooled patches (10 or 18 staged columns): item = (group g, staged row, column pair):
+        // 8 channels x 2 columns -> two 16-byte rows
         constexpr int kPairs = S::SC / 2;
         constexpr int kHalf = S::SR * kPairs;
 #pragma unroll 2
@@ -338,6 +346,37 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
                          __byte_perm(w[4], w[5], 0x5410), __byte_perm(w[6], w[7], 0x5410));
             st_shared_v4(dst + 16u, __byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632),
                          __byte_perm(w[4], w[5], 0x7632), __byte_perm(w[6], w[7], 0x7632));
+        }
+    } else {
+        // wide rows (130 or 138 staged columns): item = (group g, staged row, column quad):
+        // 8 channels x 4 columns, one 64-bit read per channel -> four 16-byte rows (the last quad
+        // of a row holds SC % 4 = 2 staged pixels; the raw box is wider)
+        static_assert(RB_::kCols % 8 == 0 && RB_::kChPlane % 16 == 0, "8-byte raw reads");
+        static_assert(S::SC % 4 == 2, "a row's last quad holds 2 staged pixels");
+        constexpr int kQuads = (S::SC + 3) / 4;
+        constexpr int kHalf = S::SR * kQuads;
+#pragma unroll 2
+        for (int i = lane; i < 2 * kHalf; i += 32) {
+            const int g = i >= kHalf ? 1 : 0;
+            const int r = i - g * kHalf;
+            const int row = r / kQuads, cq = r - (r / kQuads) * kQuads;
+            const uint32_t src = raw + static_cast<uint32_t>(8 * g) * RB_::kChPlane +
+                                 static_cast<uint32_t>(row * RB_::kCols + 4 * cq) * 2u;
+            uint2 w[8];   // channel c: .x = columns 0, 1; .y = columns 2, 3
+#pragma unroll
+            for (int c = 0; c < 8; ++c) w[c] = ld_shared_u2(src + static_cast<uint32_t>(c) * RB_::kChPlane);
+            const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
+                                 static_cast<uint32_t>(row * S::SC + 4 * cq) * 16u;
+            st_shared_v4(dst, __byte_perm(w[0].x, w[1].x, 0x5410), __byte_perm(w[2].x, w[3].x, 0x5410),
+                         __byte_perm(w[4].x, w[5].x, 0x5410), __byte_perm(w[6].x, w[7].x, 0x5410));
+            st_shared_v4(dst + 16u, __byte_perm(w[0].x, w[1].x, 0x7632), __byte_perm(w[2].x, w[3].x, 0x7632),
+                         __byte_perm(w[4].x, w[5].x, 0x7632), __byte_perm(w[6].x, w[7].x, 0x7632));
+            if (4 * cq + 2 < S::SC) {
+                st_shared_v4(dst + 32u, __byte_perm(w[0].y, w[1].y, 0x5410), __byte_perm(w[2].y, w[3].y, 0x5410),
+                             __byte_perm(w[4].y, w[5].y, 0x5410), __byte_perm(w[6].y, w[7].y, 0x5410));
+                st_shared_v4(dst + 48u, __byte_perm(w[0].y, w[1].y, 0x7632), __byte_perm(w[2].y, w[3].y, 0x7632),
+                             __byte_perm(w[4].y, w[5].y, 0x7632), __byte_perm(w[6].y, w[7].y, 0x7632));
+            }
         }
     }
 }
