@@ -155,6 +155,10 @@ WORKLOADS = {
                        False, layout="nhwc"),
     "Cbn": ConvWorkload("conv3x3_mish_mish_nhwc_bf16_64x64x256x256_c128", 64, 64, 256, 256, 128, "bf16",
                         "mish_mish", False, "bf16", layout="nhwc"),
+    # Profiling-size cases of B and C (inputs still larger than L2, a fraction of the device memory):
+    # what a many-pass ncu capture runs instead of the full workloads.
+    "B64": ConvWorkload("conv3x3_gelu_avgpool_f32_64x8x256x256_c64", 64, 8, 256, 256, 64, "f32", "gelu", True),
+    "C8": ConvWorkload("conv3x3_mish_mish_f32_8x64x256x256_c128", 8, 64, 256, 256, 128, "f32", "mish_mish", False),
     # The pages' epilogue-only kernels at their sizes: over the conv output of the GELU->pool page,
     # the conv output of the Mish->Mish page, and the Linear output of the Linear page.
     "K1e": EpilogueWorkload("gelu_avgpool_epilogue_f32_128x64x254x254", "act_mean", (128, 64, 254, 254), "gelu"),
