@@ -148,6 +148,22 @@ def logsumexp(t) -> float:
     return _load().oracle_logsumexp(_p(t), t.size)
 
 
+def tf32_round_nearest(a) -> np.ndarray:
+    """fp32 values rounded to TF32 (10 stored mantissa bits) to nearest, ties away from zero:
+    add half a TF32 unit in the last place to the magnitude bits and drop the 13 low bits (a carry
+    into the exponent is the correct rounding up).  Diagnostic mode: an oracle run on operands
+    rounded this way differs from a contraction that rounds its operands the same way only by the
+    order and precision of its accumulation.  Finite inputs."""
+    u = np.array(a, dtype=np.float32).view(np.uint32)   # a copy, any shape (0-d included)
+    return ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+def tf32_truncate(a) -> np.ndarray:
+    """fp32 values with the 13 low mantissa bits dropped: TF32 rounded toward zero."""
+    u = np.array(a, dtype=np.float32).view(np.uint32)
+    return (u & np.uint32(0xFFFFE000)).view(np.float32)
+
+
 def _out_hw(H, W, pad):
     if pad < 0 or H + 2 * pad < 3 or W + 2 * pad < 3:
         raise ValueError("padding must be >= 0 and leave an output of at least 1 x 1")

@@ -331,6 +331,42 @@ def test_linear_small_bf16(cuda_lib, shape):
     _check(y, ref, TOL["bf16"], f"linear bf16 {shape}")
 
 
+# ------------------------------------------------------------------ TF32 diagnostic mode
+
+# With the oracle fed the operands the tensor cores actually multiply -- the conv path rounds fp32
+# operands to nearest TF32 (ties away from zero), the linear path's tensor core drops the 13 low
+# mantissa bits of raw fp32 -- the products are exact in fp32 and what remains is the fp32
+# accumulation of K <= 1024 terms (about 2^-24 of the running sum per addition) and the
+# activations' approximate exponential / reciprocal (about 1e-6): 1e-5 (conv) and 2e-5 (linear,
+# whose logsumexp sums 2048 exponentials and whose l * mish(l) tail doubles relative error)
+# of (1 + |ref|).  Observed on GB300: <= 2e-6 and <= 4e-6.  Against the raw operands the same
+# calls are 100-1000x further off, so these pin each path's operand rounding.
+DIAG_CONV = [(2, 8, 32, 32, 64, "gelu", True), (1, 64, 12, 140, 128, "mish_mish", False),
+             (1, 13, 20, 37, 96, "mish", False), (2, 5, 19, 13, 32, "gelu_tanh", True)]
+
+
+@pytest.mark.parametrize("shape", DIAG_CONV, ids=lambda s: "x".join(map(str, s[:5])) + f"-{s[5]}")
+def test_conv_equals_oracle_on_tf32_rounded_operands(cuda_lib, shape):
+    N, Cin, H, W, Cout, act, pool = shape
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout)
+    f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+    o = oracle.conv3x3_act_pool if pool else oracle.conv3x3_act
+    y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act).cpu().numpy()
+    xr, wr = oracle.tf32_round_nearest(d["x"]), oracle.tf32_round_nearest(d["w"])
+    _check(y, o(xr, wr, d["b"], act), 1e-5, f"conv tf32-rounded {shape}")
+
+
+@pytest.mark.parametrize("shape", [(130, 520, 300, 1.0), (256, 1024, 2048, 1.0), (129, 64, 513, 30.0)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_linear_equals_oracle_on_tf32_truncated_operands(cuda_lib, shape):
+    M, K, Nout, sx = shape
+    d = fc_inputs.linear_inputs(M, K, Nout)
+    x = (d["x"] * np.float32(sx)).astype(np.float32)
+    y = cuda_lib.fc_linear_lse_mish(_dev(x), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
+    ref = oracle.linear_lse_mish(oracle.tf32_truncate(x), oracle.tf32_truncate(d["W"]), d["b"])
+    _check(y, ref, 2e-5, f"linear tf32-truncated {shape}")
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("key", ["B", "Bt", "B3", "Bp"])
@@ -359,7 +395,7 @@ def test_workload_C_full_size_sampled(cuda_lib, key):
     OH, OW = wl.OH, wl.OW
     rng = np.random.default_rng(8)
     total = wl.N * wl.Cout * OH * OW
-    samples = [rng.choice(total, 1 << 17, replace=False)]
+    samples = [rng.choice(total, 1 << 20, replace=False)]
     for (n, co) in [(0, 0), (wl.N - 1, wl.Cout - 1), (17, 77)]:
         base = (n * wl.Cout + co) * OH * OW
         rows = np.concatenate([np.arange(OW), (OH - 1) * OW + np.arange(OW)])

@@ -94,6 +94,33 @@ def test_softplus_stable_form():
         assert oracle.softplus(z) == pytest.approx(ref, rel=1e-15, abs=1e-320)
 
 
+# ------------------------------------------------------------------ TF32 rounding (diagnostic mode)
+
+def test_tf32_round_nearest_ties_away_and_bounds():
+    one = 1.0
+    u = 2.0 ** -10                      # TF32's unit in the last place at 1
+    cases = [(one, one), (one + u, one + u), (one + u / 2, one + u),          # tie -> away from zero
+             (one + u / 4, one), (one + 3 * u / 4, one + u), (-(one + u / 2), -(one + u)),
+             (0.75, 0.75), (0.0, 0.0), (2.0 - u / 2, 2.0)]                      # carry into the exponent
+    for x, want in cases:
+        assert float(oracle.tf32_round_nearest(np.float32(x))) == want, x
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(10000) * 10.0 ** rng.uniform(-6, 6, 10000)).astype(np.float32)
+    r = oracle.tf32_round_nearest(v)
+    assert np.all(r.view(np.uint32) & np.uint32(0x1FFF) == 0)
+    assert np.all(np.abs(r.astype(np.float64) - v) <= np.abs(v.astype(np.float64)) * 2.0 ** -11)
+
+
+def test_tf32_truncate_is_toward_zero():
+    rng = np.random.default_rng(4)
+    v = (rng.standard_normal(10000) * 10.0 ** rng.uniform(-6, 6, 10000)).astype(np.float32)
+    t = oracle.tf32_truncate(v).astype(np.float64)
+    v64 = v.astype(np.float64)
+    assert np.all(np.abs(t) <= np.abs(v64)) and np.all(np.sign(t) == np.sign(v64))
+    assert np.all(np.abs(v64 - t) < np.abs(v64) * 2.0 ** -10)
+    assert float(oracle.tf32_truncate(np.float32(1.0 + 2.0 ** -11))) == 1.0
+
+
 # ------------------------------------------------------------------ conv pins
 
 def test_conv_delta_kernel_reproduces_shifted_crop():
