@@ -498,7 +498,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,Cn,Cbn,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,Cn,Cbn,Bn,En,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

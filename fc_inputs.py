@@ -155,6 +155,11 @@ WORKLOADS = {
                        False, layout="nhwc"),
     "Cbn": ConvWorkload("conv3x3_mish_mish_nhwc_bf16_64x64x256x256_c128", 64, 64, 256, 256, 128, "bf16",
                         "mish_mish", False, "bf16", layout="nhwc"),
+    # NHWC input for the pooled chains at B's and E's sizes.
+    "Bn": ConvWorkload("conv3x3_gelu_avgpool_nhwc_f32_128x8x256x256_c64", 128, 8, 256, 256, 64, "f32", "gelu", True,
+                       layout="nhwc"),
+    "En": ConvWorkload("conv3x3_gelu_avgpool_nhwc_bf16_32x128x128x128_c256", 32, 128, 128, 128, 256, "bf16", "gelu",
+                       True, "bf16", layout="nhwc"),
     # Profiling-size cases of B and C (inputs still larger than L2, a fraction of the device memory):
     # what a many-pass ncu capture runs instead of the full workloads.
     "B64": ConvWorkload("conv3x3_gelu_avgpool_f32_64x8x256x256_c64", 64, 8, 256, 256, 64, "f32", "gelu", True),

@@ -369,11 +369,12 @@ def test_linear_equals_oracle_on_tf32_truncated_operands(cuda_lib, shape):
 
 # ------------------------------------------------------------------ full-size workloads
 
-@pytest.mark.parametrize("key", ["B", "Bt", "B3", "Bp"])
+@pytest.mark.parametrize("key", ["B", "Bt", "B3", "Bp", "Bn"])
 def test_workload_B_full_size_sampled(cuda_lib, key):
     wl = fc_inputs.WORKLOADS[key]
     d = fc_inputs.workload_inputs(key)
-    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=wl.act,
+    x = _nhwc(d["x"]) if wl.layout == "nhwc" else _dev(d["x"])
+    y = cuda_lib.fc_conv3x3_act_pool(x, _dev(d["w"]), _dev(d["b"]), act=wl.act,
                                      precision=wl.precision, pad=wl.pad).cpu().numpy()
     rng = np.random.default_rng(7)
     flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 192, replace=False),
@@ -424,14 +425,16 @@ def test_workload_D_full_size_sampled(cuda_lib, key):
     assert np.all(y >= min(f(lo_l), 0.0) - 1e-3) and np.all(y <= f(hi_l) + 1e-2)
 
 
-def test_workload_E_full_size_sampled(cuda_lib):
-    wl = fc_inputs.WORKLOADS["E"]
-    d = fc_inputs.workload_inputs("E")
-    y = cuda_lib.fc_conv3x3_act_pool(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act="gelu").cpu().numpy()
+@pytest.mark.parametrize("key", ["E", "En"])
+def test_workload_E_full_size_sampled(cuda_lib, key):
+    wl = fc_inputs.WORKLOADS[key]
+    d = fc_inputs.workload_inputs(key)
+    x = _nhwc(d["x"]) if wl.layout == "nhwc" else _dev(d["x"])
+    y = cuda_lib.fc_conv3x3_act_pool(x, _dev(d["w"]), _dev(d["b"]), act="gelu").cpu().numpy()
     rng = np.random.default_rng(10)
     flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 96, replace=False), np.arange(wl.Cout)]))
     ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, "gelu")
-    _check(y.reshape(-1)[flat], ref, TOL["bf16"], "workload E")
+    _check(y.reshape(-1)[flat], ref, TOL["bf16"], f"workload {key}")
 
 
 # ------------------------------------------------------------------ properties, errors, watchdog
