@@ -29,22 +29,24 @@ template <bool BF16>
 __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* wr, int Cin, int Co, int Cout,
                                             int ncb, int halves, int parts)
 {
+    // the fused kernel may start its set-up now; it waits for these writes before reading them
+    pdl_launch_dependents();
+    // 32-bit index arithmetic: the plan keeps the re-laid tensor at 2^30 elements at most
     constexpr int G = BF16 ? 8 : 4;
     const int hc = Cout / halves;
-    const long long per_rank = static_cast<long long>(ncb) * 9 * 2 * hc * G;
-    const long long wtotal = halves * per_rank;
-    const long long total = wtotal + static_cast<long long>(halves) * 2 * hc * G;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int wtotal = halves * ncb * 9 * 2 * hc * G;
+    const int total = wtotal + halves * 2 * hc * G;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        int f = i < wtotal ? i : i - wtotal;
+        const int e = f % G;
+        f /= G;
+        const int col = f % hc;
+        f /= hc;
+        const int half = f % 2;
+        f /= 2;
         if (i >= wtotal) {
-            long long f = i - wtotal;
-            const int e = static_cast<int>(f % G);
-            f /= G;
-            const int col = static_cast<int>(f % hc);
-            f /= hc;
-            const int half = static_cast<int>(f % 2);
-            const int rank = static_cast<int>(f / 2);
-            const int co = rank * hc + col;
+            // f = rank
+            const int co = f * hc + col;
             if constexpr (BF16) {
                 const unsigned short bv = co < Co ? reinterpret_cast<const unsigned short*>(b)[co] : 0;
                 const unsigned short pad = static_cast<unsigned short>(__float_as_uint(kPadValue) >> 16);
@@ -63,17 +65,10 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
             }
             continue;
         }
-        long long f = i;
-        const int e = static_cast<int>(f % G);
-        f /= G;
-        const int col = static_cast<int>(f % hc);
-        f /= hc;
-        const int half = static_cast<int>(f % 2);
-        f /= 2;
-        const int tap = static_cast<int>(f % 9);
+        const int tap = f % 9;
         f /= 9;
-        const int kb = static_cast<int>(f % ncb);
-        const int rank = static_cast<int>(f / ncb);
+        const int kb = f % ncb;
+        const int rank = f / ncb;
         const int co = rank * hc + col;
         const int cb = kb / parts;
         const bool lo_part = parts == 3 && kb - cb * parts == 1;
@@ -92,34 +87,42 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
     }
 }
 
-// y[n, co] = (fixed-order sum of every image-n record of the CTAs whose tiles can
-// touch image n) / (OH * OW), for co < Co; records hold Cout >= Co channels.  Cluster c handles tile groups [P(c), P(c+1)) of
-// `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles step * g + r.
-// Records a CTA never reached hold zeros.
+// y[n, co] = (fixed-order sum of every image-n record of the CTAs whose tiles can touch
+// image n) / (OH * OW), for co < Co; records hold Cout >= Co channels.  Cluster c handles tile
+// groups [P(c), P(c+1)) of `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles
+// step * g + r.  Records a CTA never reached hold zeros.  One warp per output: record k of the
+// output's list (cluster, CTA of the cluster, record) goes to lane k % 32, each lane sums its
+// records in order, and a fixed shuffle tree adds the lanes -- the same order on every run.
 __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Co, int Cout, long long tpi,
                                          long long pbase, int prem, int J, int step, int recs, double inv_count)
 {
-    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    if (idx >= static_cast<long long>(N) * Co) return;
-    const int n = static_cast<int>(idx / Co);
-    const int co = static_cast<int>(idx - static_cast<long long>(n) * Co);
+    pdl_wait();   // the fused kernel's records are complete and visible
+    const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= static_cast<long long>(N) * Co) return;   // whole warps leave together
+    const int n = static_cast<int>(wid / Co);
+    const int co = static_cast<int>(wid - static_cast<long long>(n) * Co);
     const long long big = static_cast<long long>(prem) * (pbase + 1);
     auto cluster_of = [&](long long p) -> long long { return p < big ? p / (pbase + 1) : prem + (p - big) / pbase; };
     auto start_of = [&](long long c) -> long long { return c * pbase + (c < prem ? c : prem); };
     const long long t0 = static_cast<long long>(n) * tpi;
     const long long c0 = cluster_of(t0 / step), c1 = cluster_of((t0 + tpi - 1) / step);
+    const int per_cluster = step * recs;
+    const long long total = (c1 - c0 + 1) * per_cluster;
     double s = 0.0;
-    for (long long c = c0; c <= c1; ++c) {
-        for (int r = 0; r < step; ++r) {
-            const long long cta = step * c + r;
-            const long long nf = (step * start_of(c) + r) / tpi;
-            const long long slot = n - nf;
-            if (slot < 0 || slot >= J) continue;
-            const float* p = ws + ((cta * J + slot) * recs) * static_cast<long long>(Cout) + co;
-            for (int q = 0; q < recs; ++q) s += static_cast<double>(p[static_cast<long long>(q) * Cout]);
-        }
+    for (long long k = lane; k < total; k += 32) {
+        const long long c = c0 + k / per_cluster;
+        const int rq = static_cast<int>(k - (k / per_cluster) * per_cluster);
+        const int r = rq / recs, q = rq - (rq / recs) * recs;
+        const long long cta = step * c + r;
+        const long long nf = (step * start_of(c) + r) / tpi;
+        const long long slot = n - nf;
+        if (slot < 0 || slot >= J) continue;
+        s += static_cast<double>(ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
     }
-    y[idx] = static_cast<float>(s * inv_count);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) y[wid] = static_cast<float>(s * inv_count);
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -210,7 +213,8 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     // per CTA of a group: Cout / step output channels
     p->w_block_bytes = 9u * 2u * static_cast<uint32_t>(Cout / step) * 16u;
     const unsigned long long wtot = static_cast<unsigned long long>(p->w_block_bytes) * p->ncb;
-    if (wtot > 0xFFFFFFFFull) return 2;
+    // the re-layout kernel indexes elements with 32-bit integers (grid stride included)
+    if (static_cast<unsigned long long>(step) * (wtot + 2ull * (Cout / step) * 16ull) / p->esize > (1ull << 30)) return 2;
     p->w_total_bytes = static_cast<uint32_t>(wtot);
     p->bias_block_bytes = 2u * static_cast<uint32_t>(Cout / step) * 16u;
     p->raw_bytes = geo.raw_bytes;
@@ -356,13 +360,21 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     if (e != cudaSuccess) return e;
 
     if (p.pool) {
-        const long long outs = static_cast<long long>(p.N) * p.Co;
+        const long long outs = static_cast<long long>(p.N) * p.Co;   // one warp each
         const int threads = 256;
-        const int blocks = static_cast<int>((outs + threads - 1) / threads);
-        conv_pool_combine_kernel<<<blocks, threads, 0, stream>>>(pool_ws, y, p.N, p.Co, p.Cout, p.tpi, p.pbase, p.prem, p.J,
-                                                                  p.pair ? 2 : 1, 4 * p.egroups,
-                                                                  1.0 / (static_cast<double>(p.OH) * p.OW));
-        e = cudaGetLastError();
+        const int blocks = static_cast<int>((outs * 32 + threads - 1) / threads);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(threads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the fused kernel's tail
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, conv_pool_combine_kernel, static_cast<const float*>(pool_ws), y, p.N, p.Co,
+                               p.Cout, p.tpi, p.pbase, p.prem, p.J, p.pair ? 2 : 1, 4 * p.egroups,
+                               1.0 / (static_cast<double>(p.OH) * p.OW));
     }
     return e;
 }

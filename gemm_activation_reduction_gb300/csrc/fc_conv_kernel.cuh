@@ -696,6 +696,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const TileCoord first = tile_coord(t_first, a.tpi, a.CS);
+    // the set-up above overlapped the previous kernel (the weight re-layout); its results are
+    // read from here on, and the next kernel (the pool combine) may start its own set-up
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kNumProd) {
         // ------------------------------------------------------------ producers (both CTAs)
@@ -1338,13 +1342,15 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
     cfg.blockDim = dim3(kConvThreads);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the re-layout's tail
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 1 : 0;
+    cfg.numAttrs = PAIR ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, tmx, a);
 }
 

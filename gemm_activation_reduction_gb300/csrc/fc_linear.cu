@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();   // the row combine may start its set-up; it waits for the partials
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int cluster = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
+    pdl_launch_dependents();   // the row combine may start its set-up; it waits for the partials
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
@@ -448,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // lse = M + log S and y = lse * mish(lse), mish(l) = l * tanh(softplus(l)).
 __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks)
 {
+    pdl_wait();   // the GEMM's partials are complete and visible
     const int m = blockIdx.x * blockDim.x + threadIdx.x;
     if (m >= M) return;
     float mx = -INFINITY;
@@ -460,6 +463,22 @@ __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int 
     const float l = mx + logf(s);
     const float sp = fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l)));
     y[m] = l * (l * tanhf(sp));
+}
+
+// The row combine, launched so that it may start while the GEMM finishes (it waits for the
+// partials itself).
+cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_blocks, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((M + 127) / 128));
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lse_combine_kernel, partials, y, M, n_blocks);
 }
 
 // Row-major [rows][cols] fp32 or bf16 matrix, box = box_rows x one 128-byte row of K, 128-byte swizzle.
@@ -571,8 +590,7 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, a);
         if (e != cudaSuccess) return e;
-        lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);
-        return cudaGetLastError();
+        return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);
     }
     if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN, bf16))
         return cudaErrorInvalidValue;
@@ -590,8 +608,7 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
     kern<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    lse_combine_kernel<<<(p.M + 127) / 128, 128, 0, stream>>>(a.partials, y, p.M, p.n_blocks);
-    return cudaGetLastError();
+    return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);
 }
 
 }  // namespace fc

@@ -17,6 +17,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
 
 // ------------------------------------------------------------------ mbarrier
 
+// Programmatic dependent launch: let the next kernel on the stream start its prologue now (it
+// still waits for this grid's results), and wait for the previous kernel's results (complete and
+// visible) before reading them.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
