@@ -696,27 +696,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const TileCoord first = tile_coord(t_first, a.tpi, a.CS);
-    // the set-up above overlapped the previous kernel (the weight re-layout); its results are
-    // read from here on, and the next kernel (the pool combine) may start its own set-up
-    pdl_wait();
+    // The set-up above overlaps the previous kernel (the weight re-layout); only the producers
+    // read its output (the re-laid weights and bias), so only they wait for it, after requesting
+    // their first boxes of x.  The next kernel (the pool combine) may start its own set-up now.
     pdl_launch_dependents();
 
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kNumProd) {
         // ------------------------------------------------------------ producers (both CTAs)
         const int pw = warp - kProdWarp0;
         const uint8_t* wmine = reinterpret_cast<const uint8_t*>(a.wr) + static_cast<size_t>(rank) * a.w_total_bytes;
-        if (pw == 0 && lane == 0) {
-            // own bias block, plus the own half of the weights when they stay resident
-            // workspace: [weights of CTA 0 .. step-1][bias blocks of CTA 0 .. step-1]
-            const uint8_t* bias_src = reinterpret_cast<const uint8_t*>(a.wr) +
-                                      static_cast<size_t>(step) * a.w_total_bytes +
-                                      static_cast<size_t>(rank) * a.bias_block_bytes;
-            mbar_arrive_expect_tx(wfull, a.bias_block_bytes + (a.resident ? a.w_total_bytes : 0u));
-            bulk_g2s(smem + a.bb_off, bias_src, a.bias_block_bytes, wfull);
-            if (a.resident) bulk_g2s(smem + a.w_off, wmine, a.w_total_bytes, wfull);
-            if (pair && !leader && mbar_wait(wfull, 0, abort_flag, a.status, a.budget))
-                mbar_arrive_remote(mapa_shared(smem_u32(wpeer), 0));
-        }
         {
             // This warp handles stages g = pw, pw + P, ... of the (tile group, K block)
             // sequence (P producer warps); stage g fills strip slot g % S.  Its x boxes
@@ -767,6 +755,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             };
             if (a.use_tma)
                 while (static_cast<int>(issued) < rd && alt < n_pairs) issue_next();
+            pdl_wait();   // the re-laid weights and bias are complete and visible from here on
+            if (pw == 0 && lane == 0) {
+                // own bias block, plus the own half of the weights when they stay resident
+                // workspace: [weights of CTA 0 .. step-1][bias blocks of CTA 0 .. step-1]
+                const uint8_t* bias_src = reinterpret_cast<const uint8_t*>(a.wr) +
+                                          static_cast<size_t>(step) * a.w_total_bytes +
+                                          static_cast<size_t>(rank) * a.bias_block_bytes;
+                mbar_arrive_expect_tx(wfull, a.bias_block_bytes + (a.resident ? a.w_total_bytes : 0u));
+                bulk_g2s(smem + a.bb_off, bias_src, a.bias_block_bytes, wfull);
+                if (a.resident) bulk_g2s(smem + a.w_off, wmine, a.w_total_bytes, wfull);
+                if (pair && !leader && mbar_wait(wfull, 0, abort_flag, a.status, a.budget))
+                    mbar_arrive_remote(mapa_shared(smem_u32(wpeer), 0));
+            }
             uint32_t use = 0;                         // this warp's stages whose box was waited for
             uint32_t g = static_cast<uint32_t>(pw);   // global stage index
             long long last_w = -1;                    // stage of this warp's last weight copy
