@@ -439,6 +439,44 @@ def test_workload_E_full_size_sampled(cuda_lib, key):
 
 # ------------------------------------------------------------------ properties, errors, watchdog
 
+def test_calls_on_a_side_stream_and_in_a_cuda_graph_match_direct_calls(cuda_lib):
+    """Each op is several kernels with programmatic dependent launch between them; on a non-default
+    stream and captured into a CUDA graph (programmatic edges) the results are the same bits."""
+    import torch
+    d = fc_inputs.conv_inputs(2, 8, 40, 36, 64)
+    x, w, b = _dev(d["x"]), _dev(d["w"]), _dev(d["b"])
+    dl = fc_inputs.linear_inputs(200, 256, 700)
+    xl, Wl, bl = _dev(dl["x"]), _dev(dl["W"]), _dev(dl["b"])
+    ref_pool = cuda_lib.fc_conv3x3_act_pool(x, w, b)
+    ref_act = cuda_lib.fc_conv3x3_act(x, w, b, act="mish")
+    ref_lin = cuda_lib.fc_linear_lse_mish(xl, Wl, bl)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        y_pool = cuda_lib.fc_conv3x3_act_pool(x, w, b, stream=side)
+        y_act = cuda_lib.fc_conv3x3_act(x, w, b, act="mish", stream=side)
+        y_lin = cuda_lib.fc_linear_lse_mish(xl, Wl, bl, stream=side)
+    side.synchronize()
+    assert torch.equal(y_pool, ref_pool) and torch.equal(y_act, ref_act) and torch.equal(y_lin, ref_lin)
+    # graph capture: outputs and workspaces allocated up front, the calls captured and replayed
+    o_pool, o_act, o_lin = torch.empty_like(ref_pool), torch.empty_like(ref_act), torch.empty_like(ref_lin)
+    nb_pool = cuda_lib.fc_workspace_bytes("conv3x3_act_pool", 2, 8, 40, 36, 64)
+    nb_act = cuda_lib.fc_workspace_bytes("conv3x3_act", 2, 8, 40, 36, 64)
+    nb_lin = cuda_lib.fc_workspace_bytes("linear_lse_mish", 200, 256, 1, 1, 700)
+    ws = [torch.empty(max(n, 1), dtype=torch.uint8, device="cuda") for n in (nb_pool, nb_act, nb_lin)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.fc_conv3x3_act_pool(x, w, b, out=o_pool, workspace=ws[0])
+        cuda_lib.fc_conv3x3_act(x, w, b, act="mish", out=o_act, workspace=ws[1])
+        cuda_lib.fc_linear_lse_mish(xl, Wl, bl, out=o_lin, workspace=ws[2])
+    for _ in range(3):
+        o_pool.zero_(); o_act.zero_(); o_lin.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o_pool, ref_pool) and torch.equal(o_act, ref_act) and torch.equal(o_lin, ref_lin)
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
 def test_results_are_bit_identical_run_to_run(cuda_lib):
     d = fc_inputs.conv_inputs(4, 8, 64, 64, 64)
     x, w, b = _dev(d["x"]), _dev(d["w"]), _dev(d["b"])
