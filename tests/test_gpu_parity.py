@@ -290,6 +290,42 @@ def test_conv_nhwc_matches_nchw_bit_for_bit_where_the_arithmetic_is_the_same(cud
     assert torch.equal(p_nchw, p_nhwc)
 
 
+# ------------------------------------------------------------------ randomized sweep
+
+def _random_conv_cases(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        pad = int(rng.choice([0, 0, 1, 2, 3]))
+        H, W = int(rng.integers(1, 41)), int(rng.integers(1, 41))
+        if H + 2 * pad < 3 or W + 2 * pad < 3:
+            continue
+        cases.append(dict(N=int(rng.integers(1, 4)), Cin=int(rng.integers(1, 41)), H=H, W=W,
+                          Cout=int(rng.choice([int(rng.integers(1, 129)), int(rng.integers(129, 257))])), pad=pad,
+                          prec=str(rng.choice(["tf32", "tf32", "bf16", "3xtf32"])),
+                          layout=str(rng.choice(["nchw", "nhwc"])), pool=bool(rng.integers(0, 2)),
+                          act=str(rng.choice(["gelu", "mish", "mish_mish", "gelu_tanh"]))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_conv_cases(48), ids=lambda c: "{N}x{Cin}x{H}x{W}-c{Cout}-p{pad}-{prec}-{layout}-{act}-{p}".format(p="pool" if c["pool"] else "act", **c))
+def test_conv_random_shapes(cuda_lib, case):
+    """Seeded random shapes, paddings, channel counts (single CTAs and pairs), precisions, layouts and
+    activations against the oracle: the plan and kernels have no unexercised combination."""
+    c = case
+    bf16 = c["prec"] == "bf16"
+    d = fc_inputs.conv_inputs(c["N"], c["Cin"], c["H"], c["W"], c["Cout"], "bf16" if bf16 else "f32")
+    x = _nhwc(d["x"]) if c["layout"] == "nhwc" else _dev(d["x"])
+    f = cuda_lib.fc_conv3x3_act_pool if c["pool"] else cuda_lib.fc_conv3x3_act
+    y = f(x, _dev(d["w"]), _dev(d["b"]), act=c["act"], pad=c["pad"], precision=None if bf16 else c["prec"])
+    y = y.cpu().numpy()
+    o = oracle.conv3x3_act_pool if c["pool"] else oracle.conv3x3_act
+    ref = o(d["x32"], d["w32"], d["b32"], c["act"], pad=c["pad"])
+    assert y.shape == ref.shape
+    tol = TOL["bf16"] if bf16 else (TOL_X3 if c["prec"] == "3xtf32" else TOL["f32"])
+    _check(y, ref, tol, f"random {c}")
+
+
 # ------------------------------------------------------------------ linear chain
 
 LIN_SHAPES = [
@@ -365,6 +401,31 @@ def test_linear_equals_oracle_on_tf32_truncated_operands(cuda_lib, shape):
     y = cuda_lib.fc_linear_lse_mish(_dev(x), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
     ref = oracle.linear_lse_mish(oracle.tf32_truncate(x), oracle.tf32_truncate(d["W"]), d["b"])
     _check(y, ref, 2e-5, f"linear tf32-truncated {shape}")
+
+
+def _random_linear_cases(n, seed=2025):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        bf16 = bool(rng.integers(0, 2))
+        step = 8 if bf16 else 4
+        cases.append(dict(M=int(rng.integers(1, 400)), K=int(rng.integers(1, 160)) * step,
+                          Nout=int(rng.integers(1, 1500)), sx=float(rng.choice([1.0, 1.0, 8.0, 40.0])), bf16=bf16))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_linear_cases(20), ids=lambda c: "{M}x{K}x{Nout}-s{sx:g}-{t}".format(t="bf16" if c["bf16"] else "f32", **c))
+def test_linear_random_shapes(cuda_lib, case):
+    """Seeded random (M, K, Nout) -- single CTAs and CTA pairs, ragged tiles, clamp on or off -- in fp32
+    and bf16 against the oracle."""
+    c = case
+    dt = "bf16" if c["bf16"] else "f32"
+    d = fc_inputs.linear_inputs(c["M"], c["K"], c["Nout"], dtype=dt)
+    x32 = (d["x32"] * np.float32(c["sx"])).astype(np.float32)
+    xs = fc_inputs.bf16_bits(x32) if c["bf16"] else x32
+    xo = fc_inputs.bf16_bits_to_f32(xs) if c["bf16"] else x32
+    y = cuda_lib.fc_linear_lse_mish(_dev(xs), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
+    _check(y, oracle.linear_lse_mish(xo, d["W32"], d["b32"]), TOL[dt], f"random linear {c}")
 
 
 # ------------------------------------------------------------------ full-size workloads
