@@ -124,10 +124,17 @@ def kernel_sources_hash():
     return h.hexdigest()[:16]
 
 
+def traffic_profile_name(workload_key):
+    """The committed DRAM-traffic summary of a workload's dominant kernel: <kernel>_<workload>_dram_traffic.md."""
+    wl = fc_inputs.WORKLOADS[workload_key]
+    kernel = "linear_lse" if isinstance(wl, fc_inputs.LinearWorkload) else "conv3x3_fused"
+    return f"{kernel}_{wl.name}_dram_traffic.md"
+
+
 def profiled_traffic(workload_key):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     or None when that summary was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload_key}.md")
+    path = os.path.join(ROOT, "profiles", traffic_profile_name(workload_key))
     if not os.path.exists(path):
         return None
     text = open(path).read()
