@@ -18,6 +18,7 @@ from . import _build
 __all__ = [
     "FCError", "load", "build", "library_path",
     "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
+    "fc_conv3x3_act_pool_host", "fc_conv3x3_act_host", "fc_host_staging_bytes",
     "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
     "FC_F32", "FC_BF16", "FC_F32_3XTF32", "FC_NCHW", "FC_NHWC", "ACTS", "OPS",
@@ -32,6 +33,7 @@ OPS = {"conv3x3_act_pool": 0, "conv3x3_act": 1, "linear_lse_mish": 2}
 # Every symbol include/fc.h declares.
 EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_conv3x3_act_pool_ex", "fc_conv3x3_act_ex",
            "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
+           "fc_conv3x3_act_pool_host", "fc_conv3x3_act_host", "fc_host_staging_bytes",
            "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_workspace_bytes_ex",
            "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
 
@@ -73,6 +75,13 @@ def load():
         lib.fc_conv3x3_act_pool_ex.restype = I
         lib.fc_conv3x3_act_ex.argtypes = conv_ex
         lib.fc_conv3x3_act_ex.restype = I
+        conv_host = [P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, S, P]
+        lib.fc_conv3x3_act_pool_host.argtypes = conv_host
+        lib.fc_conv3x3_act_pool_host.restype = I
+        lib.fc_conv3x3_act_host.argtypes = conv_host
+        lib.fc_conv3x3_act_host.restype = I
+        lib.fc_host_staging_bytes.argtypes = [I, I, I, I, I, I, I, I, I, I]
+        lib.fc_host_staging_bytes.restype = S
         lib.fc_linear_lse_mish.argtypes = [P, P, P, P, I, I, I, F, F, F, I, P, S, P]
         lib.fc_linear_lse_mish.restype = I
         L = ctypes.c_longlong
@@ -235,6 +244,80 @@ def fc_conv3x3_act(x, w, b, act: str = "mish_mish", out=None, workspace=None, st
     fp32 output, channels_last when x is.  precision (fp32 inputs): "tf32" (default) or "3xtf32".
     layout: "nchw", "nhwc" (x stored channels_last), or None to follow x's memory format."""
     return _conv("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, workspace, stream, precision, pad, layout)
+
+
+def _conv_host(cname, op, x, w, b, act, out, staging, stream, precision, pad, layout, chunks, device):
+    """The host-buffer conv call: x, w, b and out are CPU tensors (pinned for overlapped copies)."""
+    torch = _torch()
+    lib = load()
+    dts = (torch.float32, torch.bfloat16)
+    layout = _layout_of(x, layout)
+    nhwc = layout == "nhwc"
+    for t, name in ((x, "x"), (w, "w"), (b, "b")):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{name} must be a CPU tensor (host memory) for {cname}")
+    if not (x.is_contiguous(memory_format=torch.channels_last) if nhwc else x.is_contiguous()):
+        raise ValueError("x must be contiguous" + (" in the channels_last memory format" if nhwc else ""))
+    if x.dtype not in dts or w.dtype != x.dtype or b.dtype != x.dtype or not w.is_contiguous() \
+            or not b.is_contiguous():
+        raise ValueError("x, w, b must be contiguous and share one dtype (float32 or bfloat16)")
+    if x.dim() != 4 or w.dim() != 4 or tuple(w.shape[1:]) != (x.shape[1], 3, 3) or b.shape != (w.shape[0],):
+        raise ValueError("expected x [N,Cin,H,W], w [Cout,Cin,3,3], b [Cout]")
+    N, Cin, H, W = (int(s) for s in x.shape)
+    Cout = int(w.shape[0])
+    pad = int(pad)
+    pooled = op == "conv3x3_act_pool"
+    shape = (N, Cout) if pooled else (N, Cout, H + 2 * pad - 2, W + 2 * pad - 2)
+    out_cl = nhwc and not pooled
+    fmt = torch.channels_last if out_cl else torch.contiguous_format
+    if out is None:
+        if out_cl:
+            n_, c_, oh_, ow_ = shape
+            out = torch.empty((n_, oh_, ow_, c_), dtype=torch.float32, pin_memory=True).permute(0, 3, 1, 2)
+        else:
+            out = torch.empty(shape, dtype=torch.float32, pin_memory=True)
+    elif out.device.type != "cpu" or out.dtype != torch.float32 or tuple(out.shape) != shape or \
+            not out.is_contiguous(memory_format=fmt):
+        raise ValueError(f"out must be a contiguous float32 CPU tensor of shape {shape}")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    dt = _dtype_code(x, precision)
+    lay = FC_NHWC if nhwc else FC_NCHW
+    with torch.cuda.device(dev):
+        nbytes = int(lib.fc_host_staging_bytes(OPS[op], N, Cin, H, W, Cout, pad, lay, dt, int(chunks)))
+        if staging is None:
+            staging = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        else:
+            _check(staging, "staging", (torch.uint8,), dev)
+        st = getattr(lib, cname + "_host")(x.data_ptr(), w.data_ptr(), b.data_ptr(), out.data_ptr(), N, Cin, H, W,
+                                           Cout, pad, lay, dt, ACTS[act], int(chunks), staging.data_ptr(),
+                                           staging.numel(), _stream_handle(stream))
+    _raise(st, cname + "_host")
+    return out
+
+
+def fc_host_staging_bytes(op: str, n: int, cin: int, h: int, w: int, cout: int, pad: int = 0, layout: str = "nchw",
+                          dtype: int = FC_F32, chunks: int = 8) -> int:
+    """Device staging bytes a host-buffer conv call needs on the current device (0 for invalid arguments)."""
+    lay = {"nchw": FC_NCHW, "nhwc": FC_NHWC}[layout]
+    return int(load().fc_host_staging_bytes(OPS[op], n, cin, h, w, cout, pad, lay, dtype, int(chunks)))
+
+
+def fc_conv3x3_act_pool_host(x, w, b, act: str = "gelu", out=None, staging=None, stream=None, precision=None,
+                             pad: int = 0, layout=None, chunks: int = 8, device=None):
+    """fc_conv3x3_act_pool for inputs in host memory: x, w, b are CPU tensors (pinned for overlapped
+    copies), the result is a CPU tensor (pinned when allocated here), valid once `stream` (default: the
+    current stream of `device`, default the current device) has synchronized.  The batch moves in
+    `chunks` slices whose copies overlap the kernels; `staging` is an optional uint8 device buffer of
+    fc_host_staging_bytes(...) bytes."""
+    return _conv_host("fc_conv3x3_act_pool", "conv3x3_act_pool", x, w, b, act, out, staging, stream, precision,
+                      pad, layout, chunks, device)
+
+
+def fc_conv3x3_act_host(x, w, b, act: str = "mish_mish", out=None, staging=None, stream=None, precision=None,
+                        pad: int = 0, layout=None, chunks: int = 8, device=None):
+    """fc_conv3x3_act for inputs in host memory (see fc_conv3x3_act_pool_host)."""
+    return _conv_host("fc_conv3x3_act", "conv3x3_act", x, w, b, act, out, staging, stream, precision, pad, layout,
+                      chunks, device)
 
 
 def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,

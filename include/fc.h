@@ -229,6 +229,51 @@ size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int 
 size_t fc_workspace_bytes_ex(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_layout layout,
                              fc_dtype dtype);
 
+/*
+ * Host-buffer forms of the two conv operators: the _ex operators (same
+ * arguments, limits and results) with x, w, b and y in HOST memory.  The call
+ * copies w and b to the device, then the batch in `chunks` slices of whole
+ * images (1 .. 64; fewer when N is smaller); each slice's kernels start as
+ * soon as that slice has arrived and each slice's result is copied back as
+ * soon as it is computed, so the host<->device copies of one slice overlap
+ * the kernels of another.  Per image the result is that of the device-buffer
+ * call on the slice holding it (bit-identical to a device-buffer call on the
+ * same slice).  The pages have no counterpart to this entry point; it is the
+ * end-to-end interface for data that starts in host memory.
+ *
+ *   x, w, b, y   host pointers, no alignment needed.  Page-locked (pinned)
+ *                memory gives asynchronous, overlapped copies; pageable memory
+ *                works but its copies are not overlapped.
+ *   chunks       slices of the batch (the overlap granularity).
+ *   staging      device memory of at least fc_host_staging_bytes(...) bytes,
+ *                256-byte aligned, caller-owned: the device copies of x, w, b,
+ *                y and the operator's workspace.
+ *   stream       the call is asynchronous and ordered as if all of it ran on
+ *                `stream`: the copies start after the work already enqueued
+ *                there, and work enqueued there later starts after the last
+ *                result has reached y.  y is valid after `stream` has
+ *                synchronized.  The copies run on two library-owned streams
+ *                per device (created on the first call); concurrent calls on
+ *                one device are serialised by a lock while they enqueue.
+ * Errors: FC_ERR_INVALID_ARG / FC_ERR_UNSUPPORTED as for the _ex operators
+ * (and for chunks < 1), FC_ERR_WORKSPACE for a missing, misaligned or short
+ * staging buffer (checked before anything is enqueued), FC_ERR_CUDA if a copy
+ * or launch fails (earlier slices may then already be enqueued).
+ */
+fc_status fc_conv3x3_act_pool_host(const void* x, const void* w, const void* b, float* y,
+                                   int N, int Cin, int H, int W, int Cout, int pad, fc_layout layout,
+                                   fc_dtype dtype, fc_act act, int chunks,
+                                   void* staging, size_t staging_bytes, fc_stream_t stream);
+fc_status fc_conv3x3_act_host(const void* x, const void* w, const void* b, float* y,
+                              int N, int Cin, int H, int W, int Cout, int pad, fc_layout layout,
+                              fc_dtype dtype, fc_act act, int chunks,
+                              void* staging, size_t staging_bytes, fc_stream_t stream);
+
+/* Staging bytes for the host-buffer conv operators on the CURRENT device
+ * (op = one of the two conv ops); 0 for invalid arguments. */
+size_t fc_host_staging_bytes(fc_op op, int n, int cin, int h, int w, int cout, int pad, fc_layout layout,
+                             fc_dtype dtype, int chunks);
+
 /* Static English text for a status code. */
 const char* fc_status_string(fc_status status);
 

@@ -81,3 +81,31 @@ def test_python_binding_refuses_cpu_tensors():
         fc.fc_conv3x3_act_pool(x, torch.zeros(64, 8, 3, 3), torch.zeros(64))
     with pytest.raises(ValueError, match="CUDA tensor"):
         fc.fc_linear_lse_mish(torch.zeros(4, 8), torch.zeros(8, 8), torch.zeros(8))
+
+
+def test_host_buffer_entry_points_validate_before_any_copy():
+    import torch
+    lib = fc.load()
+    host = lib.fc_conv3x3_act_pool_host
+
+    def call(x=16, y=16, N=2, chunks=4, staging=None, nb=0):
+        return host(x, 16, 16, y, N, 8, 8, 8, 64, 0, fc.FC_NCHW, fc.FC_F32, 0, chunks, staging, nb, None)
+
+    assert call(x=None) == fc.FC_ERR_INVALID_ARG
+    assert call(y=None) == fc.FC_ERR_INVALID_ARG
+    assert call(chunks=0) == fc.FC_ERR_INVALID_ARG
+    assert call(N=0) == fc.FC_ERR_INVALID_ARG
+    assert lib.fc_conv3x3_act_host(16, 16, 16, 16, 1, 8, 2, 2, 64, 0, fc.FC_NCHW, fc.FC_F32, 2, 1, None, 0,
+                                   None) == fc.FC_ERR_INVALID_ARG          # a 2 x 2 input with no padding
+    assert lib.fc_host_staging_bytes(0, 2, 8, 8, 8, 64, 0, fc.FC_NCHW, fc.FC_F32, 0) == 0
+    if not torch.cuda.is_available():
+        # a well-formed call with no device reports a CUDA error and copies nothing
+        assert call() == fc.FC_ERR_CUDA
+        assert lib.fc_host_staging_bytes(0, 2, 8, 8, 8, 64, 0, fc.FC_NCHW, fc.FC_F32, 4) == 0
+
+
+def test_python_host_binding_refuses_device_tensors():
+    import torch
+    with pytest.raises(ValueError, match="CPU tensor"):
+        fc.fc_conv3x3_act_pool_host(torch.zeros(1, 8, 8, 8, device="meta"), torch.zeros(64, 8, 3, 3),
+                                    torch.zeros(64))
