@@ -129,3 +129,21 @@ def test_host_call_argument_errors(cuda_lib):
     assert e.value.status == cuda_lib.FC_ERR_UNSUPPORTED
     with pytest.raises(ValueError, match="CPU tensor"):
         cuda_lib.fc_conv3x3_act_pool_host(x.cuda(), w, b)
+
+
+def test_workload_B_full_size_through_the_host_buffer_call(cuda_lib):
+    """The end-to-end call the benchmark times (conv3x3 + bias -> erf-GELU -> global average pool,
+    x (128, 8, 256, 256) fp32 in pinned host memory, 8 slices of 16 images): sampled outputs
+    against the oracle, every image of the first and last slice included."""
+    import torch
+    wl = fc_inputs.WORKLOADS["B"]
+    d = fc_inputs.workload_inputs("B")
+    y = cuda_lib.fc_conv3x3_act_pool_host(_host(d["x"]), _host(d["w"]), _host(d["b"]), act=wl.act, chunks=8)
+    torch.cuda.synchronize()
+    y = y.numpy()
+    rng = np.random.default_rng(8)
+    flat = np.unique(np.concatenate([rng.choice(wl.N * wl.Cout, 160, replace=False),
+                                     np.arange(0, 16 * wl.Cout, 61), np.arange(112 * wl.Cout, 128 * wl.Cout, 59)]))
+    ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
+    _check(y.reshape(-1)[flat], ref, TOL["f32"], "workload B, host-buffer call")
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
