@@ -114,11 +114,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ profile summary (ncu traffic)
 
+# Translation units with host code only (stream and copy orchestration): they cannot change
+# what a kernel reads or writes, so they are left out of the kernel-source hash.
+HOST_ONLY_SOURCES = ("fc_host.cu",)
+
+
 def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_activation_reduction_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_ONLY_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
