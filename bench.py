@@ -390,6 +390,25 @@ def oracle_sample(key, budget_s=12.0):
             total_units)
 
 
+def oracle_tiny_times(threads):
+    """Wall time of the oracle on the whole tiny workload (2, 8, 32, 32) -> 64 channels, on one
+    core and on `threads` cores (best of 3 each)."""
+    import oracle
+    wl = fc_inputs.WORKLOADS["A"]
+    d = fc_inputs.workload_inputs("A")
+    out = {}
+    for n in (1, threads):
+        oracle.set_threads(n)
+        best = float("inf")
+        for _ in range(3):
+            t0 = time.perf_counter()
+            oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], wl.act)
+            best = min(best, time.perf_counter() - t0)
+        out[f"{n}_core" if n == 1 else f"{n}_cores"] = best
+    oracle.set_threads(threads)
+    return out
+
+
 def reference_arm(args):
     """--impl reference: the fp64 oracle on the host cores, K timed steps of a bounded sample."""
     import oracle
@@ -490,7 +509,7 @@ def gpu_arm(args):
         try:
             fl, sec, sample, threads, _, _, _ = oracle_sample(key)
             cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                   "sample": sample, "seconds": sec}
+                   "sample": sample, "seconds": sec, "tiny_workload_seconds": oracle_tiny_times(threads)}
         except Exception as e:  # the line still prints; the failure is recorded
             cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
     cfg = {"workload": wl.name, "l2": "inputs larger than L2" if wl.compulsory_bytes() > 129e6 else

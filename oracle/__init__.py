@@ -97,6 +97,14 @@ def threads() -> int:
     return _load().oracle_threads()
 
 
+def set_threads(n: int) -> None:
+    """Use n OpenMP threads from now on (results do not depend on it)."""
+    lib = _load()
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_set_threads(int(n))
+
+
 def gelu(v: float) -> float:
     return _load().oracle_gelu(float(v))
 

@@ -303,3 +303,14 @@ int oracle_threads(void)
     return 1;
 #endif
 }
+
+/* Threads for the following calls (n >= 1).  Every unit (image and channel, pixel, row)
+ * is summed in a fixed order by one thread, so the results do not depend on it. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -398,3 +398,18 @@ def test_scale_clamp_lse_mish_pins():
     np.testing.assert_allclose(oracle.scale_clamp_lse_mish(t)[:, 0],
                                oracle.linear_lse_mish(d["x"], d["W"], d["b"], 2.0, -10.0, 10.0).reshape(-1),
                                rtol=1e-6)
+
+
+def test_oracle_results_do_not_depend_on_the_thread_count():
+    """Each pooled output is summed in a fixed order by one thread: 1 thread and all threads agree bit for bit."""
+    d = fc_inputs.conv_inputs(2, 3, 12, 11, 5)
+    n = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        one = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu")
+        full = oracle.conv3x3_act(d["x32"], d["w32"], d["b32"], "mish_mish")
+    finally:
+        oracle.set_threads(n)
+    assert oracle.threads() == n
+    assert np.array_equal(one, oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu"))
+    assert np.array_equal(full, oracle.conv3x3_act(d["x32"], d["w32"], d["b32"], "mish_mish"))
