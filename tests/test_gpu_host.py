@@ -147,3 +147,26 @@ def test_workload_B_full_size_through_the_host_buffer_call(cuda_lib):
     ref = oracle.conv3x3_act_pool_at(d["x32"], d["w32"], d["b32"], flat, wl.act)
     _check(y.reshape(-1)[flat], ref, TOL["f32"], "workload B, host-buffer call")
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
+def _random_host_cases(n, seed=2026):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        pad = int(rng.choice([0, 0, 1, 2]))
+        H, W = int(rng.integers(1, 40)), int(rng.integers(1, 40))
+        if H + 2 * pad < 3 or W + 2 * pad < 3:
+            continue
+        cases.append((int(rng.integers(1, 9)), int(rng.integers(1, 33)), H, W,
+                      int(rng.choice([int(rng.integers(1, 129)), int(rng.integers(129, 257))])), pad,
+                      str(rng.choice(["f32", "bf16"])), str(rng.choice(["gelu", "mish", "mish_mish", "gelu_tanh"])),
+                      bool(rng.integers(0, 2)), str(rng.choice(["nchw", "nhwc"])), int(rng.integers(1, 10))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_host_cases(24),
+                         ids=lambda c: "x".join(map(str, c[:5])) + f"-p{c[5]}-{c[6]}-{c[7]}-{'pool' if c[8] else 'act'}-{c[9]}-k{c[10]}")
+def test_host_call_random_shapes(cuda_lib, case):
+    """Seeded random shapes, slice counts (some above N), layouts and activations through the
+    host-buffer call, against the oracle."""
+    test_host_call_matches_oracle_and_the_device_call_per_slice(cuda_lib, case)

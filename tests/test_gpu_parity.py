@@ -308,7 +308,7 @@ def _random_conv_cases(n, seed=2024):
     return cases
 
 
-@pytest.mark.parametrize("case", _random_conv_cases(48), ids=lambda c: "{N}x{Cin}x{H}x{W}-c{Cout}-p{pad}-{prec}-{layout}-{act}-{p}".format(p="pool" if c["pool"] else "act", **c))
+@pytest.mark.parametrize("case", _random_conv_cases(120), ids=lambda c: "{N}x{Cin}x{H}x{W}-c{Cout}-p{pad}-{prec}-{layout}-{act}-{p}".format(p="pool" if c["pool"] else "act", **c))
 def test_conv_random_shapes(cuda_lib, case):
     """Seeded random shapes, paddings, channel counts (single CTAs and pairs), precisions, layouts and
     activations against the oracle: the plan and kernels have no unexercised combination."""
@@ -403,6 +403,24 @@ def test_linear_equals_oracle_on_tf32_truncated_operands(cuda_lib, shape):
     _check(y, ref, 2e-5, f"linear tf32-truncated {shape}")
 
 
+def _check_linear_tf32_bound(y, ref, x, W, b, what):
+    """|y - y_exact| within the worst-case error of TF32 operands: each operand truncated to 10
+    mantissa bits (relative error < 2^-10), so |dt_j| <= 2^-9 sum_k |x_k W_jk| (plus fp32
+    accumulation, K 2^-24 of the same sum); u = clamp(4 t) moves by at most 4 |dt|; the row
+    logsumexp l by at most max_j |du_j|; y = l mish(l) has |dy/dl| <= 2.2 |l| + 1 (mish' <= 1.1,
+    |mish(l)| <= max(l, 0.31)).  l itself (for the slope only) comes from fp64 numpy."""
+    x64, W64 = x.astype(np.float64), W.astype(np.float64)
+    K = x.shape[1]
+    dl = 4.0 * (2.0 ** -9 + K * 2.0 ** -24) * (np.abs(x64) @ np.abs(W64).T).max(axis=1)
+    u = np.clip(4.0 * (x64 @ W64.T + b.astype(np.float64)), -10.0, 10.0)
+    m = u.max(axis=1)
+    l = m + np.log(np.exp(u - m[:, None]).sum(axis=1))
+    bound = (2.2 * (np.abs(l) + dl) + 1.0) * dl + 1e-6
+    err = np.abs(np.asarray(y, dtype=np.float64).reshape(-1) - np.asarray(ref, dtype=np.float64).reshape(-1))
+    i = int(np.argmax(err - bound))
+    assert err[i] <= bound[i], f"{what}: error {err[i]:.3e} above the TF32 bound {bound[i]:.3e} at {i}"
+
+
 def _random_linear_cases(n, seed=2025):
     rng = np.random.default_rng(seed)
     cases = []
@@ -414,7 +432,7 @@ def _random_linear_cases(n, seed=2025):
     return cases
 
 
-@pytest.mark.parametrize("case", _random_linear_cases(20), ids=lambda c: "{M}x{K}x{Nout}-s{sx:g}-{t}".format(t="bf16" if c["bf16"] else "f32", **c))
+@pytest.mark.parametrize("case", _random_linear_cases(50), ids=lambda c: "{M}x{K}x{Nout}-s{sx:g}-{t}".format(t="bf16" if c["bf16"] else "f32", **c))
 def test_linear_random_shapes(cuda_lib, case):
     """Seeded random (M, K, Nout) -- single CTAs and CTA pairs, ragged tiles, clamp on or off -- in fp32
     and bf16 against the oracle."""
@@ -425,7 +443,18 @@ def test_linear_random_shapes(cuda_lib, case):
     xs = fc_inputs.bf16_bits(x32) if c["bf16"] else x32
     xo = fc_inputs.bf16_bits_to_f32(xs) if c["bf16"] else x32
     y = cuda_lib.fc_linear_lse_mish(_dev(xs), _dev(d["W"]), _dev(d["b"])).cpu().numpy()
-    _check(y, oracle.linear_lse_mish(xo, d["W32"], d["b32"]), TOL[dt], f"random linear {c}")
+    ref = oracle.linear_lse_mish(xo, d["W32"], d["b32"])
+    if c["bf16"] or c["sx"] == 1.0:
+        # bf16 products are exact in fp32; N(0, 1) inputs are the workloads' distribution
+        _check(y, ref, TOL[dt], f"random linear {c}")
+    else:
+        # Inputs scaled up: TF32 operands (10 mantissa bits) give an absolute error that grows with
+        # the scale and with cancellation in the dot products, beyond the tolerance stated for the
+        # workloads' N(0, 1) inputs.  The kernel is pinned to the oracle on the operands the tensor
+        # core sees, and the exact result must lie within the TF32 error bound.
+        _check(y, oracle.linear_lse_mish(oracle.tf32_truncate(x32), oracle.tf32_truncate(d["W32"]), d["b32"]),
+               2e-5, f"random linear {c}, TF32 operands")
+        _check_linear_tf32_bound(y, ref, x32, d["W32"], d["b32"], f"random linear {c}")
 
 
 # ------------------------------------------------------------------ full-size workloads
