@@ -181,13 +181,15 @@ def make_call(fc, torch, key, d, device):
     if isinstance(wl, fc_inputs.LinearWorkload):
         x, W, b = (_dev(torch, d[k], device) for k in ("x", "W", "b"))
         out = torch.empty((wl.M, 1), dtype=torch.float32, device=device)
-        ldt = fc.FC_BF16 if wl.dtype == "bf16" else fc.FC_F32
+        split = wl.dtype != "bf16" and wl.precision == "3xtf32"
+        ldt = fc.FC_BF16 if wl.dtype == "bf16" else (fc.FC_F32_3XTF32 if split else fc.FC_F32)
         ws = torch.empty(fc.fc_workspace_bytes("linear_lse_mish", wl.M, wl.K, 1, 1, wl.Nout, ldt), dtype=torch.uint8,
                          device=device)
+        prec = None if wl.dtype == "bf16" else wl.precision
 
         def call():
-            fc.fc_linear_lse_mish(x, W, b, wl.scale, wl.clamp_lo, wl.clamp_hi, out=out, workspace=ws)
-        return call, 2, out
+            fc.fc_linear_lse_mish(x, W, b, wl.scale, wl.clamp_lo, wl.clamp_hi, out=out, workspace=ws, precision=prec)
+        return call, 4 if split else 2, out
     x, w, b = (_dev(torch, d[k], device) for k in ("x", "w", "b"))
     nhwc = wl.layout == "nhwc"
     if nhwc:
@@ -306,7 +308,8 @@ def time_e2e(fc, torch, key, d, device, steps, warmup, chunks=8):
         if nhwc:
             dev[0] = dev[0].permute(0, 3, 1, 2)
         if isinstance(wl, fc_inputs.LinearWorkload):
-            y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi)
+            y = fc.fc_linear_lse_mish(*dev, wl.scale, wl.clamp_lo, wl.clamp_hi,
+                                      precision=None if bf16 else wl.precision)
         elif wl.pool:
             y = fc.fc_conv3x3_act_pool(*dev, act=wl.act, precision=None if bf16 else wl.precision, pad=wl.pad)
         else:
@@ -573,7 +576,7 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,B3,C3,Bp,Cp,Cn,Cbn,Bn,En,K1e,K2e,K3e",
+    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,D3,B3,C3,Bp,Cp,Cn,Cbn,Bn,En,K1e,K2e,K3e",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,

@@ -85,6 +85,7 @@ class LinearWorkload:
     clamp_lo: float = -10.0
     clamp_hi: float = 10.0
     dtype: str = "f32"
+    precision: str = "tf32"   # fp32 inputs: "tf32" or "3xtf32" (split TF32)
 
     def flops(self) -> float:
         return 2.0 * self.M * self.K * self.Nout
@@ -133,6 +134,8 @@ WORKLOADS = {
     "D": LinearWorkload("linear_lse_mish_f32_1024x8192x8192", 1024, 8192, 8192),
     # bf16 variants of the Linear and Mish->Mish chains at the same sizes (precision variants)
     "Db": LinearWorkload("linear_lse_mish_bf16_1024x8192x8192", 1024, 8192, 8192, dtype="bf16"),
+    # split-TF32 (fp32-level error) variant of the Linear chain at the same size
+    "D3": LinearWorkload("linear_lse_mish_3xtf32_1024x8192x8192", 1024, 8192, 8192, precision="3xtf32"),
     "Cb": ConvWorkload("conv3x3_mish_mish_bf16_64x64x256x256_c128", 64, 64, 256, 256, 128, "bf16", "mish_mish", False),
     # bf16 variant of the conv->GELU->pool chain at a tensor-core-bound size.
     "E": ConvWorkload("conv3x3_gelu_avgpool_bf16_32x128x128x128_c256", 32, 128, 128, 128, 256, "bf16", "gelu", True),

@@ -321,8 +321,9 @@ def fc_conv3x3_act_host(x, w, b, act: str = "mish_mish", out=None, staging=None,
 
 
 def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, clamp_hi: float = 10.0,
-                       out=None, workspace=None, stream=None):
-    """y[M, 1] = l * mish(l), l = logsumexp_j clamp(u + u), u = (x W^T + b) * scale."""
+                       out=None, workspace=None, stream=None, precision=None):
+    """y[M, 1] = l * mish(l), l = logsumexp_j clamp(u + u), u = (x W^T + b) * scale.
+    precision (fp32 inputs): "tf32" (default) or "3xtf32" (split TF32, fp32-level error)."""
     torch = _torch()
     lib = load()
     _check(x, "x", (torch.float32, torch.bfloat16))
@@ -338,7 +339,7 @@ def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, cla
         _check(out, "out", (torch.float32,), x.device)
         if out.numel() != M:
             raise ValueError(f"out must hold {M} values")
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, precision)
     with torch.cuda.device(x.device):
         nbytes = int(lib.fc_workspace_bytes(OPS["linear_lse_mish"], M, K, 1, 1, Nout, dt))
         ws, wsb = _workspace(nbytes, x.device, workspace)

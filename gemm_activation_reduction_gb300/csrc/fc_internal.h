@@ -96,6 +96,13 @@ cudaError_t linear_launch(const LinearPlan& plan, const void* x, const void* W, 
                           float scale, float lo, float hi, void* workspace, cudaStream_t stream, int* status,
                           long long budget);
 
+// Split-TF32 Linear: bytes of the [hi | hi | lo] copy of x and the [hi | lo | hi] copy of W
+// (rows of 3K fp32, each array 256-byte aligned), and the kernels that write them into `dst`
+// (K % 4 == 0); *xs and *Ws receive the two arrays' addresses.
+size_t linear_split_bytes(int M, int K, int Nout);
+cudaError_t linear_split_launch(const float* x, const float* W, int M, int K, int Nout, void* dst, int sm_count,
+                                cudaStream_t stream, const float** xs, const float** Ws);
+
 // ---------------------------------------------------------------- misc
 
 cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int* status);

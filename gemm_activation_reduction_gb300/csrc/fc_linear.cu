@@ -498,7 +498,61 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int rows, int cols, int
     return r == CUDA_SUCCESS;
 }
 
+// Split-TF32 operands (the FC_F32_3XTF32 precision of the Linear op): each fp32 value v becomes
+// hi = v rounded to TF32 (round to nearest, ties away) and lo = (v - hi) rounded to TF32.  Both
+// have their 13 low mantissa bits zero, so the tensor core's truncation of fp32 operands leaves
+// them exact.  A row of x becomes [hi | hi | lo] and a row of W [hi | lo | hi] (3K values
+// each), so one TF32 GEMM over 3K sums hi*hi + hi*lo + lo*hi for every term -- the product
+// less lo*lo, an error near 2^-22 of each term.
+__global__ void tf32_split_rows_kernel(const float4* __restrict__ src, float4* __restrict__ dst, int rows, int k4,
+                                       int lo_second)
+{
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4* s = src + static_cast<size_t>(r) * k4;
+        float4* d = dst + static_cast<size_t>(r) * 3 * k4;
+        for (int c = threadIdx.x; c < k4; c += blockDim.x) {
+            const float4 v = s[c];
+            float4 h, l;
+            h.x = to_tf32(v.x); l.x = to_tf32(v.x - h.x);
+            h.y = to_tf32(v.y); l.y = to_tf32(v.y - h.y);
+            h.z = to_tf32(v.z); l.z = to_tf32(v.z - h.z);
+            h.w = to_tf32(v.w); l.w = to_tf32(v.w - h.w);
+            d[c] = h;
+            d[k4 + c] = lo_second ? l : h;
+            d[2 * k4 + c] = lo_second ? h : l;
+        }
+    }
+}
+
+size_t align256_sz(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
 }  // namespace
+
+size_t linear_split_bytes(int M, int K, int Nout)
+{
+    return align256_sz(static_cast<size_t>(M) * 3 * K * sizeof(float)) +
+           align256_sz(static_cast<size_t>(Nout) * 3 * K * sizeof(float));
+}
+
+cudaError_t linear_split_launch(const float* x, const float* W, int M, int K, int Nout, void* dst, int sm_count,
+                                cudaStream_t stream, const float** xs, const float** Ws)
+{
+    float* a = static_cast<float*>(dst);
+    float* w = reinterpret_cast<float*>(static_cast<char*>(dst) +
+                                        align256_sz(static_cast<size_t>(M) * 3 * K * sizeof(float)));
+    const int k4 = K / 4;
+    const int cap = std::max(sm_count, 1) * 8;
+    tf32_split_rows_kernel<<<std::min(M, cap), 256, 0, stream>>>(reinterpret_cast<const float4*>(x),
+                                                                  reinterpret_cast<float4*>(a), M, k4, 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    tf32_split_rows_kernel<<<std::min(Nout, cap), 256, 0, stream>>>(reinterpret_cast<const float4*>(W),
+                                                                     reinterpret_cast<float4*>(w), Nout, k4, 1);
+    e = cudaGetLastError();
+    *xs = a;
+    *Ws = w;
+    return e;
+}
 
 void* tensor_map_encoder()
 {

@@ -27,13 +27,14 @@
  *   - `workspace` is caller-owned device scratch of at least
  *     fc_workspace_bytes(...) bytes (256-byte aligned); its contents on entry
  *     do not matter.  Two calls that share a workspace must not overlap.
- *   - Floating point: fp32 inputs run on TF32 tensor cores (operands rounded
- *     to nearest TF32), bf16 inputs on BF16 tensor cores; accumulation,
- *     activation and reduction are fp32; outputs are fp32.  FC_F32_3XTF32
- *     (conv ops) takes the same fp32 inputs but splits each operand into a
- *     TF32 high part and a TF32 remainder and sums three products per term
- *     (hi*hi + hi*lo + lo*hi), which brings the contraction's error to fp32
- *     level at three times the tensor-core work.
+ *   - Floating point: fp32 inputs run on TF32 tensor cores (the conv ops
+ *     round operands to nearest TF32; the Linear op's tensor core truncates
+ *     them), bf16 inputs on BF16 tensor cores; accumulation, activation and
+ *     reduction are fp32; outputs are fp32.  FC_F32_3XTF32 takes the same fp32
+ *     inputs but splits each operand into a TF32 high part and a TF32
+ *     remainder and sums three products per term (hi*hi + hi*lo + lo*hi),
+ *     which brings the contraction's error to fp32 level at three times the
+ *     tensor-core work.
  */
 #ifndef FC_H_
 #define FC_H_
@@ -59,7 +60,7 @@ typedef enum {
 typedef enum {
     FC_F32 = 0,          /* fp32 storage, TF32 tensor-core products */
     FC_BF16 = 1,         /* bf16 storage, BF16 tensor-core products */
-    FC_F32_3XTF32 = 2    /* fp32 storage, split TF32 (3 products per term); conv ops only */
+    FC_F32_3XTF32 = 2    /* fp32 storage, split TF32 (3 products per term) */
 } fc_dtype;
 
 typedef enum {
@@ -160,8 +161,13 @@ fc_status fc_conv3x3_act_ex(const void* x, const void* w, const void* b, float* 
  *   tensor-core products) or all bf16 (dtype FC_BF16); y [M] fp32 (the (M, 1)
  *   output, contiguous); fp32 accumulation and epilogue either way.
  *   Requires M, Nout >= 1, a 16-byte row pitch (K % 4 == 0 for fp32, K % 8 == 0
- *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.  dtype
- *   FC_F32_3XTF32 returns FC_ERR_UNSUPPORTED (no split-TF32 GEMM).
+ *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.
+ *   dtype FC_F32_3XTF32 (fp32 x, W, b): split TF32 for fp32-level error -- two
+ *   small kernels write x as rows [hi | hi | lo] and W as rows [hi | lo | hi]
+ *   (hi = v rounded to TF32, lo = (v - hi) rounded to TF32) into the
+ *   workspace, and the same GEMM runs over 3K, summing hi*hi + hi*lo + lo*hi;
+ *   the workspace then holds those copies too (3 (M + Nout) K fp32 values,
+ *   see fc_workspace_bytes).  Inputs must be finite.
  */
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y,
                              int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,
