@@ -48,6 +48,26 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# SFU work of one activation evaluation, in SM clock cycles per element per SM: each activation
+# takes one reciprocal (rcp.approx: 16 lanes per clock per SM) and one exponential (ex2.approx: 32
+# lanes per clock per SM), rates microbenchmarked on this GB300; Mish twice takes two of each.
+SFU_CYCLES_PER_ELEMENT = {"gelu": 1 / 16 + 1 / 32, "gelu_tanh": 1 / 16 + 1 / 32, "mish": 1 / 16 + 1 / 32,
+                          "mish_mish": 2 * (1 / 16 + 1 / 32)}
+
+
+def epilogue_roofline(wl, call_ms, sm_count, sm_mhz):
+    """The conv epilogue's own floor: every one of the N x Cout x OH x OW contraction outputs takes
+    one activation evaluation on the special-function units, a rate that the tensor roofline does
+    not see (it binds workload B, whose contraction is short)."""
+    elems = wl.N * wl.Cout * wl.OH * wl.OW
+    peak = sm_count * sm_mhz * 1e6 / SFU_CYCLES_PER_ELEMENT[wl.act] / 1e9
+    achieved = elems / (call_ms * 1e-3) / 1e9
+    return {"bound": "alu", "unit": "Gelem/s", "achieved": achieved, "peak": peak, "frac": achieved / peak,
+            "peak_source": f"SFU: rcp 16 + ex2 32 lanes/clk/SM (microbenchmarked) x {sm_count} SMs x "
+                           f"{sm_mhz:.0f} MHz (median SM clock in the timed region)",
+            "elements": elems}
+
+
 def tensor_peak(wl, pk):
     bf16 = pk["bf16_tflops"]
     if getattr(wl, "dtype", "f32") == "bf16":
@@ -507,6 +527,10 @@ def gpu_arm(args):
                 "peak_source": peak_note,
                 "duration_source": "CUDA events around each call on its stream (relayout + fused kernel"
                                    + (" + combine" if launches_per_call == 3 else "") + ")"}
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    sm_mhz = float((clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
+    epi = None if isinstance(wl, (fc_inputs.LinearWorkload, fc_inputs.EpilogueWorkload)) else \
+        epilogue_roofline(wl, kernel_ms, sm_count, sm_mhz)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         try:
@@ -524,7 +548,7 @@ def gpu_arm(args):
             "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if getattr(wl, "dtype", "f32") == "bf16" else "tf32",
             "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(fan_in)) weights)", "config": cfg,
-            "roofline": roofline, "cpu_baseline": cpu,
+            "roofline": roofline, "epilogue_roofline": epi, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "api": "linear: H2D + fc_linear_lse_mish + D2H" if isinstance(wl, fc_inputs.LinearWorkload)
@@ -558,6 +582,8 @@ def gpu_arm(args):
                 rl = max(owl.flops() / (opeak * 1e12), owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3
                 others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
                              "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+                if isinstance(owl, fc_inputs.ConvWorkload):
+                    others[k]["epilogue_sfu_frac"] = epilogue_roofline(owl, oms, sm_count, sm_mhz)["frac"]
             del od, ocall, oout
             torch.cuda.empty_cache()
         line["other_workloads"] = others
