@@ -153,32 +153,26 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
     if (dtype != FC_F32 && dtype != FC_BF16 && dtype != FC_F32_3XTF32) return FC_ERR_INVALID_ARG;
     if (K % (dtype == FC_BF16 ? 8 : 4) != 0) return FC_ERR_UNSUPPORTED;   // 16-byte row pitch for TMA
     const bool split = dtype == FC_F32_3XTF32;
-    if (split && K > 0x7FFFFFFF / 3) return FC_ERR_UNSUPPORTED;
     DeviceState* d = nullptr;
     fc_status st = device_state(&d);
     if (st != FC_OK) return st;
     fc::LinearPlan plan;
-    // split TF32: one TF32 GEMM over the 3K-long split rows
-    if (fc::linear_plan(&plan, M, split ? 3 * K : K, Nout, dtype == FC_BF16, d->sm_count) != 0)
-        return FC_ERR_UNSUPPORTED;
+    if (fc::linear_plan(&plan, M, K, Nout, dtype == FC_BF16, d->sm_count, split) != 0) return FC_ERR_UNSUPPORTED;
     const size_t part = (plan.ws_bytes + 255) & ~static_cast<size_t>(255);
     const size_t need = part + (split ? fc::linear_split_bytes(M, K, Nout) : 0);
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FC_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const void* xa = x;
-    const void* wa = W;
+    const float* x_lo = nullptr;
+    const float* W_lo = nullptr;
     if (split) {
-        const float* xs = nullptr;
-        const float* ws = nullptr;
         cudaError_t e = fc::linear_split_launch(static_cast<const float*>(x), static_cast<const float*>(W), M, K,
-                                                Nout, static_cast<char*>(workspace) + part, d->sm_count, s, &xs, &ws);
+                                                Nout, static_cast<char*>(workspace) + part, d->sm_count, s, &x_lo,
+                                                &W_lo);
         if (e != cudaSuccess) return FC_ERR_CUDA;
-        xa = xs;
-        wa = ws;
     }
-    cudaError_t e = fc::linear_launch(plan, xa, wa, b, y, scale, clamp_lo, clamp_hi, workspace, s, d->status,
-                                      fc::kWaitBudgetCycles);
+    cudaError_t e = fc::linear_launch(plan, x, W, b, y, scale, clamp_lo, clamp_hi, workspace, s, d->status,
+                                      fc::kWaitBudgetCycles, x_lo, W_lo);
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
@@ -255,10 +249,8 @@ size_t fc_workspace_bytes(fc_op op, int n_or_m, int cin_or_k, int h, int w, int 
     if (op == FC_OP_LINEAR_LSE_MISH) {
         if (n_or_m < 1 || cin_or_k < 1 || cout_or_nout < 1) return 0;
         const bool split = dtype == FC_F32_3XTF32;
-        if (split && (cin_or_k % 4 != 0 || cin_or_k > 0x7FFFFFFF / 3)) return 0;
         fc::LinearPlan plan;
-        if (fc::linear_plan(&plan, n_or_m, split ? 3 * cin_or_k : cin_or_k, cout_or_nout, dtype == FC_BF16,
-                            d->sm_count) != 0)
+        if (fc::linear_plan(&plan, n_or_m, cin_or_k, cout_or_nout, dtype == FC_BF16, d->sm_count, split) != 0)
             return 0;
         if (!split) return plan.ws_bytes;
         return ((plan.ws_bytes + 255) & ~static_cast<size_t>(255)) +

@@ -80,6 +80,7 @@ struct LinearPlan {
     int use_pair;         // CTA pairs with M = 256 MMAs (tcgen05 cta_group::2)
     int m_pairs;          // 256-row blocks in pair mode
     int bn;               // pair mode: columns per tile (a multiple of 32, <= 256)
+    int kseg;             // split TF32: K blocks per segment (k_blocks = 3 kseg), else 0
     uint32_t smem_bytes;
     size_t ws_bytes;      // (max, sum-exp) partial per row and column tile
 };
@@ -90,18 +91,20 @@ cudaError_t act_mean_launch(const void* v, float* y, long long planes, long long
                             cudaStream_t st);
 cudaError_t lse_row_launch(const float* t, float* out, int M, int N, float scale, float lo, float hi, cudaStream_t st);
 
-int linear_plan(LinearPlan* plan, int M, int K, int Nout, int bf16, int sm_count);
+// split != 0: split TF32 (fp32 only), the K loop over three segments (x, W), (x, W_lo), (x_lo, W).
+int linear_plan(LinearPlan* plan, int M, int K, int Nout, int bf16, int sm_count, int split = 0);
 
+// x_lo, W_lo: the TF32 remainders of x and W (split plans only; nullptr otherwise).
 cudaError_t linear_launch(const LinearPlan& plan, const void* x, const void* W, const void* b, float* y,
                           float scale, float lo, float hi, void* workspace, cudaStream_t stream, int* status,
-                          long long budget);
+                          long long budget, const void* x_lo = nullptr, const void* W_lo = nullptr);
 
-// Split-TF32 Linear: bytes of the [hi | hi | lo] copy of x and the [hi | lo | hi] copy of W
-// (rows of 3K fp32, each array 256-byte aligned), and the kernels that write them into `dst`
-// (K % 4 == 0); *xs and *Ws receive the two arrays' addresses.
+// Split-TF32 Linear: bytes of the TF32 remainders of x [M][K] and W [Nout][K] (fp32, each array
+// 256-byte aligned), and the kernels that write them into `dst` (K % 4 == 0); *x_lo and *W_lo
+// receive the two arrays' addresses.
 size_t linear_split_bytes(int M, int K, int Nout);
 cudaError_t linear_split_launch(const float* x, const float* W, int M, int K, int Nout, void* dst, int sm_count,
-                                cudaStream_t stream, const float** xs, const float** Ws);
+                                cudaStream_t stream, const float** x_lo, const float** W_lo);
 
 // ---------------------------------------------------------------- misc
 

@@ -40,6 +40,7 @@ struct LinArgs {
     float2* partials;   // [n_blocks][M]
     int M, N, K;
     int m_blocks, n_blocks, k_blocks, num_tiles;
+    int kseg;           // split TF32: K blocks per segment (k_blocks = 3 kseg), else 0
     float scale, lo, hi;
     int* status;
     long long budget;
@@ -66,6 +67,22 @@ __device__ __forceinline__ void mma_kstep(uint32_t d, uint64_t ad, uint64_t bd, 
     else mma_tf32(d, ad, bd, idesc, acc);
 }
 
+// Split TF32 runs the K loop over three segments of K blocks: (x, W), (x, W_lo), (x_lo, W).
+// The tensor core truncates the raw fp32 x and W to TF32 (their high parts); x_lo and W_lo
+// hold the TF32-rounded remainders.  Returns the K block within its segment and sets the maps.
+__device__ __forceinline__ int k_segment(int kb, int kseg, const CUtensorMap* tmx, const CUtensorMap* tmw,
+                                         const CUtensorMap* tmx_lo, const CUtensorMap* tmw_lo,
+                                         const CUtensorMap** mx, const CUtensorMap** mw)
+{
+    *mx = tmx;
+    *mw = tmw;
+    if (kseg == 0) return kb;
+    const int seg = kb / kseg;
+    if (seg == 1) *mw = tmw_lo;
+    else if (seg == 2) *mx = tmx_lo;
+    return kb - seg * kseg;
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long long budget)
 {
     const long long t0 = clock64();
@@ -76,7 +93,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    linear_lse_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const LinArgs a)
+    linear_lse_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                      const __grid_constant__ CUtensorMap tmx_lo, const __grid_constant__ CUtensorMap tmw_lo,
+                      const LinArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,6 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmx);
         prefetch_tmap(&tmw);
+        if (a.kseg > 0) {
+            prefetch_tmap(&tmx_lo);
+            prefetch_tmap(&tmw_lo);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -131,8 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-                    tma_load_2d(sA + stage * kABytes, &tmx, &full[stage], kb * kKElems<BF16>, mb * kBM);
-                    tma_load_2d(sB + stage * kBBytes, &tmw, &full[stage], kb * kKElems<BF16>, nb * kBN);
+                    const CUtensorMap* mx;
+                    const CUtensorMap* mw;
+                    const int kk = k_segment(kb, a.kseg, &tmx, &tmw, &tmx_lo, &tmw_lo, &mx, &mw);
+                    tma_load_2d(sA + stage * kABytes, mx, &full[stage], kk * kKElems<BF16>, mb * kBM);
+                    tma_load_2d(sB + stage * kBBytes, mw, &full[stage], kk * kKElems<BF16>, nb * kBN);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -265,6 +291,7 @@ struct LinPairArgs {
     float2* partials;   // [n_blocks][M]
     int M, N, K;
     int m_pairs, n_blocks, k_blocks, num_tiles;
+    int kseg;           // split TF32: K blocks per segment (k_blocks = 3 kseg), else 0
     int bn;             // columns per pair tile: a multiple of 32, <= kPBN
     float scale, lo, hi;
     int* status;
@@ -274,6 +301,7 @@ struct LinPairArgs {
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_lse_pair_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                           const __grid_constant__ CUtensorMap tmx_lo, const __grid_constant__ CUtensorMap tmw_lo,
                            const LinPairArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -311,6 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmx);
         prefetch_tmap(&tmw);
+        if (a.kseg > 0) {
+            prefetch_tmap(&tmx_lo);
+            prefetch_tmap(&tmw_lo);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, 512);
@@ -336,8 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kPABytes + b_bytes));
-                    tma_load_2d_pair(sA + stage * kPABytes, &tmx, fbar, kb * kKElems<BF16>, m0);
-                    tma_load_2d_pair(sB + stage * kPBBytes, &tmw, fbar, kb * kKElems<BF16>, n0);
+                    const CUtensorMap* mx;
+                    const CUtensorMap* mw;
+                    const int kk = k_segment(kb, a.kseg, &tmx, &tmw, &tmx_lo, &tmw_lo, &mx, &mw);
+                    tma_load_2d_pair(sA + stage * kPABytes, mx, fbar, kk * kKElems<BF16>, m0);
+                    tma_load_2d_pair(sB + stage * kPBBytes, mw, fbar, kk * kKElems<BF16>, n0);
                     if (++stage == kPStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -498,29 +533,23 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int rows, int cols, int
     return r == CUDA_SUCCESS;
 }
 
-// Split-TF32 operands (the FC_F32_3XTF32 precision of the Linear op): each fp32 value v becomes
-// hi = v rounded to TF32 (round to nearest, ties away) and lo = (v - hi) rounded to TF32.  Both
-// have their 13 low mantissa bits zero, so the tensor core's truncation of fp32 operands leaves
-// them exact.  A row of x becomes [hi | hi | lo] and a row of W [hi | lo | hi] (3K values
-// each), so one TF32 GEMM over 3K sums hi*hi + hi*lo + lo*hi for every term -- the product
-// less lo*lo, an error near 2^-22 of each term.
-__global__ void tf32_split_rows_kernel(const float4* __restrict__ src, float4* __restrict__ dst, int rows, int k4,
-                                       int lo_second)
+// Split-TF32 operands (the FC_F32_3XTF32 precision of the Linear op).  The tensor core reads
+// raw fp32 operands as TF32 by dropping their 13 low mantissa bits, so the high part of a value
+// v is hi = v with those bits cleared, and the GEMM reads it straight from x and W.  This kernel
+// writes the remainders lo = (v - hi) rounded to TF32 (v - hi is exact in fp32): |lo| < 2^-10
+// |v|, and lo's own rounding error is below 2^-22 |v|.  The GEMM's three K segments then sum
+// hi*hi + hi*lo + lo*hi for every term -- the product less lo*lo (< 2^-20 of it).
+__global__ void tf32_remainder_kernel(const float4* __restrict__ src, float4* __restrict__ dst, long long n4)
 {
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const float4* s = src + static_cast<size_t>(r) * k4;
-        float4* d = dst + static_cast<size_t>(r) * 3 * k4;
-        for (int c = threadIdx.x; c < k4; c += blockDim.x) {
-            const float4 v = s[c];
-            float4 h, l;
-            h.x = to_tf32(v.x); l.x = to_tf32(v.x - h.x);
-            h.y = to_tf32(v.y); l.y = to_tf32(v.y - h.y);
-            h.z = to_tf32(v.z); l.z = to_tf32(v.z - h.z);
-            h.w = to_tf32(v.w); l.w = to_tf32(v.w - h.w);
-            d[c] = h;
-            d[k4 + c] = lo_second ? l : h;
-            d[2 * k4 + c] = lo_second ? h : l;
-        }
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 v = src[i];
+        float4 l;
+        l.x = to_tf32(v.x - __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u));
+        l.y = to_tf32(v.y - __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u));
+        l.z = to_tf32(v.z - __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u));
+        l.w = to_tf32(v.w - __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u));
+        dst[i] = l;
     }
 }
 
@@ -530,27 +559,26 @@ size_t align256_sz(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 size_t linear_split_bytes(int M, int K, int Nout)
 {
-    return align256_sz(static_cast<size_t>(M) * 3 * K * sizeof(float)) +
-           align256_sz(static_cast<size_t>(Nout) * 3 * K * sizeof(float));
+    return align256_sz(static_cast<size_t>(M) * K * sizeof(float)) +
+           align256_sz(static_cast<size_t>(Nout) * K * sizeof(float));
 }
 
 cudaError_t linear_split_launch(const float* x, const float* W, int M, int K, int Nout, void* dst, int sm_count,
-                                cudaStream_t stream, const float** xs, const float** Ws)
+                                cudaStream_t stream, const float** x_lo, const float** W_lo)
 {
     float* a = static_cast<float*>(dst);
     float* w = reinterpret_cast<float*>(static_cast<char*>(dst) +
-                                        align256_sz(static_cast<size_t>(M) * 3 * K * sizeof(float)));
-    const int k4 = K / 4;
-    const int cap = std::max(sm_count, 1) * 8;
-    tf32_split_rows_kernel<<<std::min(M, cap), 256, 0, stream>>>(reinterpret_cast<const float4*>(x),
-                                                                  reinterpret_cast<float4*>(a), M, k4, 0);
+                                        align256_sz(static_cast<size_t>(M) * K * sizeof(float)));
+    const unsigned blocks = static_cast<unsigned>(std::max(sm_count, 1) * 8);
+    tf32_remainder_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(x), reinterpret_cast<float4*>(a),
+                                                      static_cast<long long>(M) * K / 4);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    tf32_split_rows_kernel<<<std::min(Nout, cap), 256, 0, stream>>>(reinterpret_cast<const float4*>(W),
-                                                                     reinterpret_cast<float4*>(w), Nout, k4, 1);
+    tf32_remainder_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(W), reinterpret_cast<float4*>(w),
+                                                      static_cast<long long>(Nout) * K / 4);
     e = cudaGetLastError();
-    *xs = a;
-    *Ws = w;
+    *x_lo = a;
+    *W_lo = w;
     return e;
 }
 
@@ -568,16 +596,20 @@ void* tensor_map_encoder()
     return fn;
 }
 
-int linear_plan(LinearPlan* p, int M, int K, int Nout, int bf16, int sm_count)
+int linear_plan(LinearPlan* p, int M, int K, int Nout, int bf16, int sm_count, int split)
 {
     *p = LinearPlan{};
     // TMA needs a 16-byte row pitch: K a multiple of 4 fp32 or 8 bf16
     if (K % (bf16 ? 8 : 4) != 0) return 2;
+    if (split && bf16) return 2;
     p->M = M; p->K = K; p->Nout = Nout; p->bf16 = bf16;
     p->m_blocks = (M + kBM - 1) / kBM;
     p->n_blocks = (Nout + kBN - 1) / kBN;
     const int kelems = bf16 ? kKElems<true> : kKElems<false>;
     p->k_blocks = (K + kelems - 1) / kelems;
+    // split TF32: three segments of K blocks, (x, W), (x, W_lo), (x_lo, W)
+    p->kseg = split ? p->k_blocks : 0;
+    if (split) p->k_blocks *= 3;
     const long long tiles = static_cast<long long>(p->m_blocks) * p->n_blocks;
     if (tiles > 0x7FFFFFFFLL) return 2;
     p->num_tiles = static_cast<int>(tiles);
@@ -611,18 +643,26 @@ int linear_plan(LinearPlan* p, int M, int K, int Nout, int bf16, int sm_count)
 }
 
 cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, const void* b, float* y, float scale,
-                          float lo, float hi, void* workspace, cudaStream_t stream, int* status, long long budget)
+                          float lo, float hi, void* workspace, cudaStream_t stream, int* status, long long budget,
+                          const void* x_lo, const void* W_lo)
 {
-    CUtensorMap tmx, tmw;
+    CUtensorMap tmx, tmw, tmxl, tmwl;
     const bool bf16 = p.bf16 != 0;
+    // split TF32 reads the remainders through their own maps; otherwise those maps repeat x and W
+    if (p.kseg > 0 && (x_lo == nullptr || W_lo == nullptr)) return cudaErrorInvalidValue;
+    const void* xl = p.kseg > 0 ? x_lo : x;
+    const void* wl = p.kseg > 0 ? W_lo : W;
     if (p.use_pair) {
-        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2, bf16))
+        if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2, bf16) ||
+            !make_kmajor_map(&tmxl, xl, p.M, p.K, kPBM, bf16) ||
+            !make_kmajor_map(&tmwl, wl, p.Nout, p.K, p.bn / 2, bf16))
             return cudaErrorInvalidValue;
         LinPairArgs a{};
         a.bias = b;
         a.partials = reinterpret_cast<float2*>(workspace);
         a.M = p.M; a.N = p.Nout; a.K = p.K;
         a.m_pairs = p.m_pairs; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
+        a.kseg = p.kseg;
         a.bn = p.bn;
         a.scale = scale; a.lo = lo; a.hi = hi;
         a.status = status; a.budget = budget;
@@ -642,24 +682,26 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, a);
+        e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmxl, tmwl, a);
         if (e != cudaSuccess) return e;
         return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);
     }
-    if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN, bf16))
+    if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN, bf16) ||
+        !make_kmajor_map(&tmxl, xl, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmwl, wl, p.Nout, p.K, kBN, bf16))
         return cudaErrorInvalidValue;
     LinArgs a{};
     a.bias = b;
     a.partials = reinterpret_cast<float2*>(workspace);
     a.M = p.M; a.N = p.Nout; a.K = p.K;
     a.m_blocks = p.m_blocks; a.n_blocks = p.n_blocks; a.k_blocks = p.k_blocks; a.num_tiles = p.num_tiles;
+    a.kseg = p.kseg;
     a.scale = scale; a.lo = lo; a.hi = hi;
     a.status = status; a.budget = budget;
     auto kern = bf16 ? linear_lse_kernel<true> : linear_lse_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(p.smem_bytes));
     if (e != cudaSuccess) return e;
-    kern<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, a);
+    kern<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, tmxl, tmwl, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);

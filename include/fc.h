@@ -162,12 +162,13 @@ fc_status fc_conv3x3_act_ex(const void* x, const void* w, const void* b, float* 
  *   output, contiguous); fp32 accumulation and epilogue either way.
  *   Requires M, Nout >= 1, a 16-byte row pitch (K % 4 == 0 for fp32, K % 8 == 0
  *   for bf16; FC_ERR_UNSUPPORTED otherwise), clamp_lo <= clamp_hi.
- *   dtype FC_F32_3XTF32 (fp32 x, W, b): split TF32 for fp32-level error -- two
- *   small kernels write x as rows [hi | hi | lo] and W as rows [hi | lo | hi]
- *   (hi = v rounded to TF32, lo = (v - hi) rounded to TF32) into the
- *   workspace, and the same GEMM runs over 3K, summing hi*hi + hi*lo + lo*hi;
- *   the workspace then holds those copies too (3 (M + Nout) K fp32 values,
- *   see fc_workspace_bytes).  Inputs must be finite.
+ *   dtype FC_F32_3XTF32 (fp32 x, W, b): split TF32 for fp32-level product
+ *   error.  The tensor core reads raw fp32 as TF32 by dropping 13 low mantissa
+ *   bits (the high part hi); a small kernel writes the remainders
+ *   lo = (v - hi) rounded to TF32 of x and W into the workspace, and the GEMM's
+ *   K loop runs three times -- over (x, W), (x, W_lo), (x_lo, W) -- summing
+ *   hi*hi + hi*lo + lo*hi.  The workspace then also holds the remainders
+ *   ((M + Nout) K fp32 values, see fc_workspace_bytes).  Inputs must be finite.
  */
 fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float* y,
                              int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,
