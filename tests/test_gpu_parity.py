@@ -536,7 +536,7 @@ def test_workload_D_full_size_sampled(cuda_lib, key):
     ref = oracle.linear_lse_mish(d["x32"], d["W32"], d["b32"], wl.scale, wl.clamp_lo, wl.clamp_hi, rows=rows)
     # Split TF32 removes the operands' TF32 error (7.9e-4 at this size with TF32 alone); what is left
     # over K = 8192 (3K = 24576 products, 3072 MMA steps per logit) is the rounding of the tensor
-    # core's fp32 accumulator at every step, measured 9.3e-5 -- hence 2e-4 here, while the short
+    # core's fp32 accumulator at every step, measured 9.8e-5 -- hence 2e-4 here, while the short
     # dot products of the small split-TF32 cases meet 2e-5.
     tol = 2e-4 if wl.precision == "3xtf32" else TOL[wl.dtype]
     _check(y[rows], ref, tol, f"workload {key}")
