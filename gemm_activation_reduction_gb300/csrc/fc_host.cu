@@ -121,6 +121,13 @@ fc_status host_call(fc_op op, const void* x, const void* w, const void* b, float
     if (pipe_init(p) != cudaSuccess) return FC_ERR_CUDA;
 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // On a failure after copies were enqueued, the caller's stream still waits for them, so that
+    // the staging buffer and the host buffers stay in use until they have finished.
+    auto fail = [&](fc_status st) {
+        if (cudaEventRecord(p.params_in, p.in) == cudaSuccess) cudaStreamWaitEvent(cs, p.params_in, 0);
+        if (cudaEventRecord(p.y_out, p.out) == cudaSuccess) cudaStreamWaitEvent(cs, p.y_out, 0);
+        return st;
+    };
     char* base = static_cast<char*>(staging);
     char* w_d = base;
     char* b_d = base + s.off_b;
@@ -144,24 +151,24 @@ fc_status host_call(fc_op op, const void* x, const void* w, const void* b, float
         if (e == cudaSuccess) e = cudaEventRecord(p.x_in[i], p.in);
     }
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p.params_in, 0);
-    if (e != cudaSuccess) return FC_ERR_CUDA;
+    if (e != cudaSuccess) return fail(FC_ERR_CUDA);
     for (int i = 0; i < s.chunks; ++i) {
         const int n = i + 1 < s.chunks ? s.n0 : N - i * s.n0;
         void* x_d = base + s.off_x + i * s.x_slot;
         float* y_d = reinterpret_cast<float*>(base + s.off_y + i * s.y_slot);
-        if (cudaStreamWaitEvent(cs, p.x_in[i], 0) != cudaSuccess) return FC_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, p.x_in[i], 0) != cudaSuccess) return fail(FC_ERR_CUDA);
         const fc_status st =
             op == FC_OP_CONV3X3_ACT_POOL
                 ? fc_conv3x3_act_pool_ex(x_d, w_d, b_d, y_d, n, Cin, H, W, Cout, pad, layout, dtype, act, ws_d,
                                          s.ws_bytes, stream)
                 : fc_conv3x3_act_ex(x_d, w_d, b_d, y_d, n, Cin, H, W, Cout, pad, layout, dtype, act, ws_d,
                                     s.ws_bytes, stream);
-        if (st != FC_OK) return st;
+        if (st != FC_OK) return fail(st);
         e = cudaEventRecord(p.done[i], cs);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(p.out, p.done[i], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(yh + static_cast<size_t>(i) * s.n0 * s.img_y, y_d, n * s.img_y, d2h, p.out);
-        if (e != cudaSuccess) return FC_ERR_CUDA;
+        if (e != cudaSuccess) return fail(FC_ERR_CUDA);
     }
     // The caller's stream ends after the last result has reached the host.
     e = cudaEventRecord(p.y_out, p.out);

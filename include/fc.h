@@ -265,7 +265,8 @@ size_t fc_workspace_bytes_ex(fc_op op, int n, int cin, int h, int w, int cout, i
  * Errors: FC_ERR_INVALID_ARG / FC_ERR_UNSUPPORTED as for the _ex operators
  * (and for chunks < 1), FC_ERR_WORKSPACE for a missing, misaligned or short
  * staging buffer (checked before anything is enqueued), FC_ERR_CUDA if a copy
- * or launch fails (earlier slices may then already be enqueued).
+ * or launch fails (earlier slices may then already be enqueued; `stream` still
+ * waits for every copy that was, so the buffers stay in use until then).
  */
 fc_status fc_conv3x3_act_pool_host(const void* x, const void* w, const void* b, float* y,
                                    int N, int Cin, int H, int W, int Cout, int pad, fc_layout layout,
