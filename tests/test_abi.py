@@ -109,3 +109,67 @@ def test_python_host_binding_refuses_device_tensors():
     with pytest.raises(ValueError, match="CPU tensor"):
         fc.fc_conv3x3_act_pool_host(torch.zeros(1, 8, 8, 8, device="meta"), torch.zeros(64, 8, 3, 3),
                                     torch.zeros(64))
+
+
+def _compile_c_client(out_path):
+    """Build tests/c_abi_client.c as plain C99 against include/fc.h and the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    libdir = os.path.dirname(fc.library_path())
+    lib = os.path.basename(fc.library_path())[3:-3]
+    # C11: the CUDA runtime's own headers use anonymous unions; fc.h alone is checked as C99 below
+    cmd = [cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-o", out_path,
+           os.path.join(ROOT, "tests", "c_abi_client.c"), "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda, "include"), "-L", libdir, "-l" + lib, "-Wl,-rpath," + libdir,
+           "-L", os.path.join(cuda, "lib64"), "-lcudart", "-Wl,-rpath," + os.path.join(cuda, "lib64")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_plain_c_client_compiles_and_links(tmp_path):
+    """The header is valid C99 and the library links into a C program with the CUDA runtime alone."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    fc.load()
+    _compile_c_client(str(tmp_path / "c_abi_client"))
+    assert os.path.exists(tmp_path / "c_abi_client")
+
+
+@pytest.mark.gpu
+def test_plain_c_client_runs_the_tiny_workload(tmp_path):
+    """The C client on a GPU: the tiny conv -> GELU -> pool workload (2, 8, 32, 32) -> 64 channels
+    through the C ABI from C, against the oracle."""
+    import subprocess
+    import numpy as np
+    import fc_inputs
+    import oracle
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fc.load()
+    exe = str(tmp_path / "c_abi_client")
+    _compile_c_client(exe)
+    N, Cin, H, W, Cout = 2, 8, 32, 32, 64
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout)
+    paths = {}
+    for k in ("x", "w", "b"):
+        paths[k] = str(tmp_path / f"{k}.bin")
+        np.ascontiguousarray(d[k], dtype="<f4").tofile(paths[k])
+    y_path = str(tmp_path / "y.bin")
+    r = subprocess.run([exe, str(N), str(Cin), str(H), str(W), str(Cout), paths["x"], paths["w"], paths["b"], y_path],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    y = np.fromfile(y_path, dtype="<f4").reshape(N, Cout).astype(np.float64)
+    ref = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu")
+    err = np.abs(y - ref) / (1.0 + np.abs(ref))
+    assert err.max() <= 2e-3, err.max()
