@@ -545,7 +545,8 @@ def gpu_arm(args):
            "roofline_ms": max(flops / (peak * 1e12), wl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3,
            "parallelism": f"shard-by-batch x{world}" if world > 1 else "single GPU"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
-            "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": warmup, "ms_per_step": ms, "ms_median": statistics.median(per), "ms_best": min(per),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if getattr(wl, "dtype", "f32") == "bf16" else "tf32",
             "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(fan_in)) weights)", "config": cfg,
             "roofline": roofline, "epilogue_roofline": epi, "cpu_baseline": cpu,
