@@ -666,3 +666,36 @@ def test_activation_accuracy_through_a_delta_kernel(cuda_lib, act):
     ref = np.array([oracle.act(act, float(v)) for v in pts])
     err = np.abs(y - ref[None, :]) / np.maximum(1.0, np.abs(ref[None, :]))
     assert err.max() <= 2e-6, f"{act}: max error {err.max():.3e} at x = {pts[int(np.argmax(err.max(0)))]}"
+
+
+# ------------------------------------------------------------------ extreme but valid shapes
+
+EXTREME_CONV = [
+    # (N, Cin, H, W, Cout, dtype, act, pool, pad)
+    (2048, 3, 34, 34, 64, "f32", "gelu", True, 0),       # thousands of small images: many records per CTA
+    (1, 8, 2050, 2050, 64, "f32", "gelu", True, 0),      # one large image: 32k tiles of one plane
+    (1, 16, 5, 4100, 128, "f32", "mish_mish", False, 1),  # very wide rows
+    (512, 128, 10, 10, 256, "bf16", "gelu", True, 0),    # CTA pairs over many small images
+    (4096, 1, 3, 3, 16, "f32", "gelu", True, 0),         # 1 x 1 output planes
+]
+
+
+@pytest.mark.parametrize("case", EXTREME_CONV, ids=lambda c: "x".join(map(str, c[:5])) + f"-{c[5]}-{c[6]}-p{c[8]}")
+def test_conv_extreme_shapes_sampled(cuda_lib, case):
+    N, Cin, H, W, Cout, dt, act, pool, pad = case
+    d = fc_inputs.conv_inputs(N, Cin, H, W, Cout, dt)
+    f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
+    y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act, pad=pad).cpu().numpy().reshape(-1)
+    rng = np.random.default_rng(11)
+    idx = np.unique(np.concatenate([rng.choice(y.size, min(y.size, 300), replace=False), [0, y.size - 1]]))
+    at = oracle.conv3x3_act_pool_at if pool else oracle.conv3x3_act_at
+    _check(y[idx], at(d["x32"], d["w32"], d["b32"], idx, act, pad=pad), TOL[dt], f"extreme {case}")
+
+
+@pytest.mark.parametrize("shape", [(65536, 64, 16), (1, 65536, 1), (3, 4, 70000)], ids=lambda s: "x".join(map(str, s)))
+def test_linear_extreme_shapes_sampled(cuda_lib, shape):
+    M, K, Nout = shape
+    d = fc_inputs.linear_inputs(M, K, Nout)
+    y = cuda_lib.fc_linear_lse_mish(_dev(d["x"]), _dev(d["W"]), _dev(d["b"])).cpu().numpy().reshape(-1)
+    rows = np.unique(np.concatenate([np.random.default_rng(12).choice(M, min(M, 64), replace=False), [0, M - 1]]))
+    _check(y[rows], oracle.linear_lse_mish(d["x32"], d["W32"], d["b32"], rows=rows), TOL["f32"], f"extreme {shape}")
