@@ -31,28 +31,35 @@ __device__ __forceinline__ float rcp_approx(float x)
 // instruction count by about 40 %.
 __device__ __forceinline__ float2 splat2(float c) { return make_float2(c, c); }
 
-// 2 GELU(z) for two lanes, GELU the exact (erf) form 0.5 z (1 + erf(z / sqrt 2)).
-// erf is Hastings' rational approximation as printed in Abramowitz & Stegun, Handbook of
-// Mathematical Functions, eq. 7.1.26: for u >= 0, erf(u) = 1 - t q(t) e^{-u^2} with
-// q(t) = a1 + t (a2 + t (a3 + t (a4 + t a5))), t = 1 / (1 + p u), |error| <= 1.5e-7.
-// With u = |z| / sqrt 2: p u = (p / sqrt 2) |z| and e^{-u^2} = 2^{-(log2 e / 2) z^2}.
-// erf is odd, so z erf(z / sqrt 2) = |z| erf(u) and 2 GELU(z) = z + |z| erf(u): one
-// fused multiply-add after erf.  The factor 1/2 is applied by the caller (once per
-// pooled sum, or per stored value).
+// 2 GELU(z) for two lanes, GELU the exact (erf) form z Phi(z).  With Phi(z) = erfc(-z / sqrt 2) / 2
+// and erfc(-x) = 2 - erfc(x):  2 GELU(z) = z + |z| - |z| erfc(|z| / sqrt 2).  The erfc factor is
+// 2^P(min(|z|, 10)), P the degree-6 polynomial below: log2 erfc(a / sqrt 2) fitted on [0, 10] by
+// weighted least squares iteratively reweighted toward minimax of the GELU error
+// (gen_gelu_coeffs.py prints these values); GELU's error stays below 1.2e-7 (absolute, or
+// relative above 1) before the exponential's own rounding.  Past 10 the factor is below 2^-73:
+// the padding pre-activation -1e4 gives a term under 1e-18.  Per pair: two clamps, six paired
+// FMAs (Horner), one paired add and one paired FMA for the result, two exponentials -- no
+// reciprocal.  The factor 1/2 is applied by the caller (once per pooled sum, or per stored value).
+constexpr float kGeluP0 = 6.876672159705777e-06f;
+constexpr float kGeluP1 = -1.1512012481689453f;
+constexpr float kGeluP2 = -0.4587721824645996f;
+constexpr float kGeluP3 = -0.053410667926073074f;
+constexpr float kGeluP4 = 0.008079877123236656f;
+constexpr float kGeluP5 = -0.0007689839112572372f;
+constexpr float kGeluP6 = 3.306757935206406e-05f;
+
 __device__ __forceinline__ float2 gelu2(float2 z)
 {
     const float2 a = make_float2(fabsf(z.x), fabsf(z.y));
-    const float2 d = __ffma2_rn(a, splat2(0.3275911f * 0.70710678118654752f), splat2(1.0f));
-    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    float2 q = __ffma2_rn(splat2(1.061405429f), t, splat2(-1.453152027f));
-    q = __ffma2_rn(q, t, splat2(1.421413741f));
-    q = __ffma2_rn(q, t, splat2(-0.284496736f));
-    q = __ffma2_rn(q, t, splat2(0.254829592f));
-    const float2 w = __fmul2_rn(__fmul2_rn(z, z), splat2(0.72134752044448170f));   // (log2 e / 2) z^2
-    const float2 e = make_float2(ex2_approx(-w.x), ex2_approx(-w.y));
-    const float2 tq = __fmul2_rn(q, t);
-    const float2 erfv = __ffma2_rn(make_float2(-tq.x, -tq.y), e, splat2(1.0f));   // erf(|z| / sqrt 2)
-    return __ffma2_rn(a, erfv, z);
+    const float2 ac = make_float2(fminf(a.x, 10.0f), fminf(a.y, 10.0f));
+    float2 p = __ffma2_rn(splat2(kGeluP6), ac, splat2(kGeluP5));
+    p = __ffma2_rn(p, ac, splat2(kGeluP4));
+    p = __ffma2_rn(p, ac, splat2(kGeluP3));
+    p = __ffma2_rn(p, ac, splat2(kGeluP2));
+    p = __ffma2_rn(p, ac, splat2(kGeluP1));
+    p = __ffma2_rn(p, ac, splat2(kGeluP0));
+    const float2 e = make_float2(ex2_approx(p.x), ex2_approx(p.y));   // erfc(|z| / sqrt 2)
+    return __ffma2_rn(make_float2(-a.x, -a.y), e, __fadd2_rn(z, a));
 }
 
 // Mish(z) = z tanh(softplus(z)) for two lanes, with tanh(log(1 + e^z)) = n / (n + 2),
