@@ -48,22 +48,31 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-# SFU work of one activation evaluation, in SM clock cycles per element per SM: each activation
-# takes one reciprocal (rcp.approx: 16 lanes per clock per SM) and one exponential (ex2.approx: 32
-# lanes per clock per SM), rates microbenchmarked on this GB300; Mish twice takes two of each.
-SFU_CYCLES_PER_ELEMENT = {"gelu": 1 / 16 + 1 / 32, "gelu_tanh": 1 / 16 + 1 / 32, "mish": 1 / 16 + 1 / 32,
-                          "mish_mish": 2 * (1 / 16 + 1 / 32)}
+# Per-element cost of the conv epilogue's activation (and its pool accumulate or store scaling),
+# from the instruction sequences in csrc/fc_act.cuh: FMA-pipe results (each paired-FP32
+# instruction yields one result per element; 128 results per clock per SM) and SFU cycles per
+# SM (ex2.approx 32 lanes per clock, rcp.approx 16; microbenchmarked on this GB300).
+#   erf-GELU: 6 Horner FMAs, z + |z|, the final FMA, the accumulate; one exponential
+#   tanh-GELU: 3 for the exponent, 1 + e, the product, the accumulate; one exponential, one reciprocal
+#   Mish: 6 arithmetic, the accumulate; one exponential, one reciprocal; Mish twice: 12 + 1, two of each
+EPILOGUE_COST = {"gelu": (9, 1 / 32), "gelu_tanh": (6, 1 / 32 + 1 / 16), "mish": (7, 1 / 32 + 1 / 16),
+                 "mish_mish": (13, 2 * (1 / 32 + 1 / 16))}
+FMA_RESULTS_PER_CLK_SM = 128
 
 
 def epilogue_roofline(wl, call_ms, sm_count, sm_mhz):
     """The conv epilogue's own floor: every one of the N x Cout x OH x OW contraction outputs takes
-    one activation evaluation on the special-function units, a rate that the tensor roofline does
-    not see (it binds workload B, whose contraction is short)."""
+    one activation evaluation on the FMA pipe and the special-function units, a rate that the tensor
+    roofline does not see (it binds workload B, whose contraction is short).  Peak = SMs x clock /
+    the busier unit's cycles per element."""
     elems = wl.N * wl.Cout * wl.OH * wl.OW
-    peak = sm_count * sm_mhz * 1e6 / SFU_CYCLES_PER_ELEMENT[wl.act] / 1e9
+    fma, sfu = EPILOGUE_COST[wl.act]
+    cycles = max(fma / FMA_RESULTS_PER_CLK_SM, sfu)
+    peak = sm_count * sm_mhz * 1e6 / cycles / 1e9
     achieved = elems / (call_ms * 1e-3) / 1e9
     return {"bound": "alu", "unit": "Gelem/s", "achieved": achieved, "peak": peak, "frac": achieved / peak,
-            "peak_source": f"SFU: rcp 16 + ex2 32 lanes/clk/SM (microbenchmarked) x {sm_count} SMs x "
+            "peak_source": f"{'FMA pipe' if fma / FMA_RESULTS_PER_CLK_SM >= sfu else 'SFU'}: {fma} FMA-pipe results "
+                           f"(128 / clk / SM) and {sfu:.4f} SFU cycles per element x {sm_count} SMs x "
                            f"{sm_mhz:.0f} MHz (median SM clock in the timed region)",
             "elements": elems}
 
@@ -584,7 +593,7 @@ def gpu_arm(args):
                 others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
                              "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
                 if isinstance(owl, fc_inputs.ConvWorkload):
-                    others[k]["epilogue_sfu_frac"] = epilogue_roofline(owl, oms, sm_count, sm_mhz)["frac"]
+                    others[k]["epilogue_frac"] = epilogue_roofline(owl, oms, sm_count, sm_mhz)["frac"]
             del od, ocall, oout
             torch.cuda.empty_cache()
         line["other_workloads"] = others
