@@ -173,3 +173,18 @@ def test_plain_c_client_runs_the_tiny_workload(tmp_path):
     ref = oracle.conv3x3_act_pool(d["x32"], d["w32"], d["b32"], "gelu")
     err = np.abs(y - ref) / (1.0 + np.abs(ref))
     assert err.max() <= 2e-3, err.max()
+
+
+def test_python_host_binding_validates_before_any_cuda_call():
+    import torch
+    x = torch.zeros(2, 8, 8, 8)
+    w = torch.zeros(64, 8, 3, 3)
+    b = torch.zeros(64)
+    with pytest.raises(ValueError, match="share one dtype"):
+        fc.fc_conv3x3_act_pool_host(x, w.to(torch.bfloat16), b)
+    with pytest.raises(ValueError, match="expected x"):
+        fc.fc_conv3x3_act_pool_host(x, torch.zeros(64, 8, 5, 5), b)
+    with pytest.raises(ValueError, match="contiguous"):
+        fc.fc_conv3x3_act_host(x.transpose(2, 3), w, b, layout="nchw")
+    with pytest.raises(ValueError, match="out must be"):
+        fc.fc_conv3x3_act_pool_host(x, w, b, out=torch.zeros(2, 63))
