@@ -133,35 +133,39 @@ struct Geometry {
     uint32_t strip_bytes, raw_bytes;
 };
 
-template <bool BF16, bool WIDE, int ROWS, int XP, bool NHWC = false>
+template <bool BF16, bool WIDE, int ROWS, int XP, bool NHWC = false, int UPW = 1>
 Geometry geometry_of()
 {
-    using S = Shape<WIDE, ROWS, XP, NHWC>;
-    using R = RawBox<BF16, WIDE, ROWS, XP>;
+    using S = Shape<WIDE, ROWS, XP, NHWC, UPW>;
+    using R = RawBox<BF16, WIDE, ROWS, XP, UPW>;
     // NHWC: one box per K block, [SR][SC][32 B of channels]
     if (NHWC) return Geometry{S::PR, S::PC, S::SR, S::SC, 32 / (BF16 ? 2 : 4), S::STRIP, S::RAW_NHWC};
     return Geometry{S::PR, S::PC, S::SR, R::kCols, R::kCh, S::STRIP, R::kBytes};
 }
 
-// The kernel's tile shape: 16 x 8 patches (pool), two rows of 128 (full output, single
-// CTAs) or one row of 128 (full output, CTA pairs).
+// The kernel's tile shape: 16 x 8 patches or 16 x 32 patches of four units (pool), two rows
+// of 128 (full output, single CTAs) or one row of 128 (full output, CTA pairs).
 template <int XPF, int XPB>
-Geometry geometry_xp(int bf16, int pool, int pair)
+Geometry geometry_xp(int bf16, int pool, int pair, int upw)
 {
+    if (pool && upw == 4)
+        return bf16 ? geometry_of<true, false, 1, XPB, false, 4>() : geometry_of<false, false, 1, XPF, false, 4>();
     if (pool) return bf16 ? geometry_of<true, false, 1, XPB>() : geometry_of<false, false, 1, XPF>();
     if (pair) return bf16 ? geometry_of<true, true, 1, XPB>() : geometry_of<false, true, 1, XPF>();
     return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, XPF>();
 }
 
 // padx: the padding's column shift needs XP = 4 (fp32) / 8 (bf16) extra staged columns
-Geometry geometry(int bf16, int pool, int pair, int padx, int nhwc)
+Geometry geometry(int bf16, int pool, int pair, int padx, int nhwc, int upw)
 {
     if (nhwc) {
+        if (pool && upw == 4)
+            return bf16 ? geometry_of<true, false, 1, 0, true, 4>() : geometry_of<false, false, 1, 0, true, 4>();
         if (pool) return bf16 ? geometry_of<true, false, 1, 0, true>() : geometry_of<false, false, 1, 0, true>();
         if (pair) return bf16 ? geometry_of<true, true, 1, 0, true>() : geometry_of<false, true, 1, 0, true>();
         return bf16 ? geometry_of<true, true, 2, 0, true>() : geometry_of<false, true, 2, 0, true>();
     }
-    return padx ? geometry_xp<4, 8>(bf16, pool, pair) : geometry_xp<0, 0>(bf16, pool, pair);
+    return padx ? geometry_xp<4, 8>(bf16, pool, pair, upw) : geometry_xp<0, 0>(bf16, pool, pair, upw);
 }
 
 }  // namespace
@@ -196,7 +200,11 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
     // a warp would otherwise hold more than 8 accumulator slices; single CTAs otherwise
     // (cheaper per-tile hand-offs between the MMA issuer and the epilogue).
     p->pair = (Cout > 128 && sm_count >= 2) ? 1 : 0;
-    const Geometry geo = geometry(bf16, pool, p->pair, p->padx, p->nhwc);
+    // Pooled single-CTA tiles of up to 64 channels: four 16 x 8 units side by side share one
+    // staged strip (one TMA box, one re-layout, one stage hand-off per 512 outputs); the eight
+    // accumulators still hold two such tiles.  Wider channel counts keep one unit per tile.
+    p->upw = (pool && !p->pair && Cout <= 64) ? 4 : 1;
+    const Geometry geo = geometry(bf16, pool, p->pair, p->padx, p->nhwc, p->upw);
     p->RB = (p->OH + geo.PR - 1) / geo.PR;
     p->CS = (p->OW + geo.PC - 1) / geo.PC;
     p->tpi = static_cast<long long>(p->RB) * p->CS;
@@ -300,7 +308,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
         if (enc == nullptr) return cudaErrorNotSupported;
         const cuuint64_t es = static_cast<cuuint64_t>(p.esize);
-        const Geometry geo = geometry(p.bf16, p.pool, p.pair, p.padx, p.nhwc);
+        const Geometry geo = geometry(p.bf16, p.pool, p.pair, p.padx, p.nhwc, p.upw);
         cuuint64_t dims[4];
         cuuint32_t box[4];
         if (p.nhwc) {
@@ -330,6 +338,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.ncb = p.ncb; a.parts = p.parts; a.pad = p.pad; a.dcol = p.dcol; a.RB = p.RB; a.CS = p.CS; a.tpi = p.tpi; a.num_tiles = p.num_tiles;
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
+    a.upw = p.upw;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
     a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.raw_off = p.raw_off;
     a.bar_off = p.bar_off; a.use_tma = p.use_tma;

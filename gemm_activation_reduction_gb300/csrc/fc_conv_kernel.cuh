@@ -6,8 +6,11 @@
 // GEMM view (the Mish page's implicit-GEMM sizing: M x N x K =
 // pixels x Cout x Cin*9):  D[pixel, co] = sum_{ci, kh, kw} x[ci, oh+kh, ow+kw] * w[co, ci, kh, kw].
 //
-// Tile: M = 128 output pixels arranged as a 16-row x 8-column patch, N = Cout
-// (<= 256), K stepped as (K block of 8 fp32 / 16 bf16 input channels) x (9 taps).
+// Unit: M = 128 output pixels arranged as a 16-row x 8-column patch, N = Cout
+// (<= 256), K stepped as (K block of 8 fp32 / 16 bf16 input channels) x (9 taps).  A pooled
+// single-CTA tile of up to 64 channels holds four such units side by side (16 x 32 outputs):
+// they share one staged strip, so one TMA box, one re-layout and one stage hand-off serve 512
+// outputs.
 //
 // The operand trick that makes shifted windows free: the producer warps stage
 // the input patch plus its halo (18 rows x 10 columns) in shared memory as
@@ -59,9 +62,10 @@ constexpr int kNumProd = 3;
 constexpr int kMmaWarp = kProdWarp0 + kNumProd;
 constexpr int kConvThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kIndPlane = 128 * 16;                 // one indicator plane: 2048 B
-// Pooled tiles: 4 edge variants + a zero plane.  Full-output tiles store only pixels inside
+// Pooled units: 6 edge variants + a zero plane.  Full-output tiles store only pixels inside
 // the output, so every tile uses the all-inside plane: 1 variant + the zero plane.
-__host__ __device__ constexpr int ind_variants(bool pool) { return pool ? 4 : 1; }
+// Pooled units: (full rows, last row block) x (8 valid columns, OW % 8, none) = 6 variants.
+__host__ __device__ constexpr int ind_variants(bool pool) { return pool ? 6 : 1; }
 __host__ __device__ constexpr uint32_t ind_bytes(bool pool) { return (ind_variants(pool) + 1) * kIndPlane; }
 constexpr float kPadValue = -1.0e4f;                     // pre-activation of padding pixels
 constexpr uint32_t kResidentMax = 96 * 1024;
@@ -76,9 +80,9 @@ static_assert(kMaxStages >= kNumProd, "one strip slot per producer warp at least
 // block and the 1 KB base alignment
 constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 
-// Output pixels of one staged tile.  The pooled ops use a 16-row x 8-column
-// patch, one 128-row MMA tile (least halo: 18 x 10 staged pixels per 128
-// outputs); the full-output op uses ROWS rows of 128 columns so that each warp
+// Output pixels of one staged tile.  The pooled ops use UPW 16-row x 8-column
+// units side by side, each one 128-row MMA tile (18 x 10 staged pixels for one unit,
+// 18 x 34 for four); the full-output op uses ROWS rows of 128 columns so that each warp
 // stores 32 consecutive pixels of a row (128 contiguous bytes) per output
 // channel.  Each row of a wide tile is one M = 128 MMA "unit" with its own
 // accumulator; the rows share the staged strip (row u starts u * SC pixels
@@ -95,11 +99,11 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // NHWC input: a K block lands as one TMA box [SR rows][SC columns][32 B of channels] and is
 // split into the two planes; NHWC planes are 64 bytes past a 128-byte multiple apart so that
 // the split's 128-bit stores of one phase (4 pixels x 2 planes) cover all banks.
-template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false>
+template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false, int UPW = 1>
 struct Shape {
-    static constexpr int UNITS = WIDE ? ROWS : 1;          // M = 128 MMA units per tile
+    static constexpr int UNITS = WIDE ? ROWS : UPW;        // M = 128 MMA units per tile
     static constexpr int PR = WIDE ? ROWS : 16;            // output rows per tile
-    static constexpr int PC = WIDE ? 128 : 8;              // output columns per tile
+    static constexpr int PC = WIDE ? 128 : 8 * UPW;        // output columns per tile
     static constexpr int SR = PR + 2;                      // staged rows (halo)
     static constexpr int SC = PC + 2 + XP;                 // staged columns (halo + shift room)
     static constexpr int SPOS = SR * SC;                   // staged pixels
@@ -107,13 +111,16 @@ struct Shape {
     static constexpr uint32_t RAW_NHWC = (SPOS * 32 + 127) / 128 * 128;   // one NHWC box: [SPOS][32 B]
     static constexpr uint32_t STRIP = (2 * PLANE + 127) / 128 * 128;  // one K block, slot pitch
     static constexpr uint32_t SBO = WIDE ? 128u : SC * 16u;
+    // staged pixels between consecutive units' A operands: the next output row (wide rows) or
+    // the next 8 columns (pooled units side by side)
+    static constexpr int UOFF = WIDE ? SC : 8;
 };
 
 // Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
 // order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.
-template <bool BF16, bool WIDE, int ROWS = 1, int XP = 0>
+template <bool BF16, bool WIDE, int ROWS = 1, int XP = 0, int UPW = 1>
 struct RawBox {
-    using S = Shape<WIDE, ROWS, XP>;
+    using S = Shape<WIDE, ROWS, XP, false, UPW>;
     static constexpr int kCh = BF16 ? 16 : 8;
     static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8 : (S::SC + 3) / 4 * 4;
     static constexpr uint32_t kChPlane = S::SR * kCols * (BF16 ? 2 : 4);
@@ -137,6 +144,7 @@ struct ConvArgs {
     long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
     int prem, J, stages, raw_depth, resident, nacc, tmem_cols;
     int egroups;          // epilogue tile groups G (1, 2, 4): group g takes every G-th tile
+    int upw;              // pooled single-CTA tiles: 1 (16 x 8) or 4 units side by side (16 x 32)
     int pair;             // 1: CTA pairs with M = 256 MMAs (group = 2 tiles); 0: single CTAs
     uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;   // per CTA of the pair (its half of Cout)
     uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
@@ -289,11 +297,11 @@ __device__ __forceinline__ uint32_t tf32_part(float v)
     else return __float_as_uint(hi);
 }
 
-template <bool BF16, bool WIDE, int ROWS, int XP, bool LO = false>
+template <bool BF16, bool WIDE, int ROWS, int XP, bool LO, int UPW>
 __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int lane)
 {
-    using S = Shape<WIDE, ROWS, XP>;
-    using RB_ = RawBox<BF16, WIDE, ROWS, XP>;
+    using S = Shape<WIDE, ROWS, XP, false, UPW>;
+    using RB_ = RawBox<BF16, WIDE, ROWS, XP, UPW>;
     static_assert(!(BF16 && LO), "split TF32 is an fp32 mode");
     if constexpr (!BF16) {
         // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
@@ -326,7 +334,7 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
             }
         }
     } else if constexpr (!WIDE) {
-        // pooled patches (10 or 18 staged columns): item = (group g, staged row, column pair):
+        // pooled patches (an even number of staged columns): item = (group g, staged row, column pair):
         // 8 channels x 2 columns -> two 16-byte rows
         constexpr int kPairs = S::SC / 2;
         constexpr int kHalf = S::SR * kPairs;
@@ -385,11 +393,11 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
 // multiple and TMA cannot address it): one K block of the halo patch as
 // [group][SPOS pixels][16 B], zero past the image and past Cin; `lo` stages the
 // split-TF32 remainder instead of the high part (fp32 only).
-template <bool BF16, bool WIDE, int ROWS, int XP>
+template <bool BF16, bool WIDE, int ROWS, int XP, int UPW>
 __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
                                            int Cin, int H, int W, int lane, bool lo)
 {
-    using S = Shape<WIDE, ROWS, XP>;
+    using S = Shape<WIDE, ROWS, XP, false, UPW>;
     const size_t HW = static_cast<size_t>(H) * W;
     for (int s = lane; s < S::SPOS; s += 32) {
         const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
@@ -428,11 +436,11 @@ __device__ __forceinline__ void fill_strip(uint32_t strip, const void* xv, int n
 // NHWC fallback staging with plain loads (when Cin's row of channels is not a 16-byte
 // multiple and TMA cannot address it): x [N][H][W][Cin]; one staged pixel's K block is
 // 8 fp32 / 16 bf16 consecutive channels, zero past the image and past Cin.
-template <bool BF16, bool WIDE, int ROWS>
+template <bool BF16, bool WIDE, int ROWS, int UPW>
 __device__ __forceinline__ void fill_strip_nhwc(uint32_t strip, const void* xv, int n, int cb, int oh0, int ow0,
                                                 int Cin, int H, int W, int lane, bool lo)
 {
-    using S = Shape<WIDE, ROWS, 0, true>;
+    using S = Shape<WIDE, ROWS, 0, true, UPW>;
     for (int s = lane; s < S::SPOS; s += 32) {
         const int rr = s / S::SC, cc = s - (s / S::SC) * S::SC;
         const int ih = oh0 + rr, iw = ow0 + cc;
@@ -470,10 +478,10 @@ __device__ __forceinline__ void fill_strip_nhwc(uint32_t strip, const void* xv, 
 // split them into the strip's two group planes -- fp32 rounded to the TF32 operand (the high
 // part, or with LO the split-TF32 remainder), bf16 as they are.  Item i is half i % 2 of pixel
 // i / 2: consecutive lanes read consecutive 16 bytes.
-template <bool BF16, bool WIDE, int ROWS, bool LO>
+template <bool BF16, bool WIDE, int ROWS, bool LO, int UPW>
 __device__ __forceinline__ void copy_raw_nhwc(uint32_t raw, uint32_t strip, int lane)
 {
-    using S = Shape<WIDE, ROWS, 0, true>;
+    using S = Shape<WIDE, ROWS, 0, true, UPW>;
 #pragma unroll 4
     for (int i = lane; i < 2 * S::SPOS; i += 32) {
         const uint32_t px = static_cast<uint32_t>(i >> 1), h = static_cast<uint32_t>(i & 1);
@@ -496,27 +504,28 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
     }
 }
 
-// A operand of the bias K step, one 128-row plane per edge variant v (bit 1: the
-// tile is in the last row block, bit 0: in the last column strip) plus a zero
-// plane (the second K core matrix).  A pixel inside the output gets a 1 in the
-// bias columns (fp32: k 0 and k 2 for the two TF32 halves; bf16: k 0); a padding
-// pixel past the image gets a 1 in k 1, whose B entry is the padding value, so
-// its accumulator starts near -1e4 and activates to exactly -0.  CTA pairs share
-// one descriptor for two tiles, so they use plane 0 (all inside) and mask in the
-// epilogue instead.  Full-output tiles store only the pixels inside the output and use
-// the all-inside plane alone (plane 0, then the zero plane).
-template <bool BF16, bool WIDE, int ROWS>
-__device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int CS, int tid,
-                                                       int nthreads)
+// A operand of the bias K step, one 128-row plane per edge variant of a pooled unit (16 rows x 8
+// columns): v = 3 re + cc, re = 1 for a unit in the last row block (rows past the image are
+// padding), cc = 0 for 8 columns inside the image, 1 for the first OW % 8 columns only (the unit
+// that straddles the right edge), 2 for none (a unit wholly past the edge); then a zero plane
+// (the second K core matrix).  A pixel inside the output gets a 1 in the bias columns (fp32: k 0
+// and k 2 for the two TF32 halves; bf16: k 0); a padding pixel gets a 1 in k 1, whose B entry is
+// the padding value, so its accumulator starts near -1e4 and activates to exactly -0.  CTA pairs
+// share one descriptor for two tiles, so they use plane 0 (all inside) and mask in the epilogue
+// instead.  Full-output tiles store only the pixels inside the output and use the all-inside
+// plane alone (plane 0, then the zero plane).
+template <bool BF16, bool WIDE, int ROWS, int UPW>
+__device__ __forceinline__ void build_indicator_planes(uint8_t* ind, int OH, int OW, int RB, int tid, int nthreads)
 {
-    using S = Shape<WIDE, ROWS>;
+    using S = Shape<WIDE, ROWS, 0, false, UPW>;
     constexpr int NV = ind_variants(!WIDE);
     const int rows_last = OH - (RB - 1) * S::PR;   // valid rows in the last row block
-    const int cols_last = OW - (CS - 1) * S::PC;   // valid columns in the last column strip
+    const int cols_part = OW % 8;                  // valid columns of a unit on the right edge
     for (int i = tid; i < (NV + 1) * 128; i += nthreads) {
         const int v = i >> 7, r = i & 127;
-        const int pr = r / S::PC, pc = r - (r / S::PC) * S::PC;
-        const bool in = v < NV && (!(v & 2) || pr < rows_last) && (!(v & 1) || pc < cols_last);
+        const int pr = r >> 3, pc = r & 7;           // a pooled unit's pixel r
+        const int re = v / 3, cc = v - (v / 3) * 3;
+        const bool in = v < NV && (re == 0 || pr < rows_last) && (cc == 0 || (cc == 1 && pc < cols_part));
         const bool pad = v < NV && !in;
         uint32_t w0, w1, w2;
         if constexpr (BF16) {
@@ -618,7 +627,7 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -629,8 +638,9 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // room for the padding's column shift a.dcol (< 16 B of elements) when it is not 0
     constexpr int XP = PADX ? (BF16 ? 8 : 4) : 0;
     static_assert(!(PADX && NHWC), "NHWC boxes start at any column: no shift room needed");
-    using S = Shape<WIDE, ROWS, XP, NHWC>;
-    using RBox = RawBox<BF16, WIDE, ROWS, XP>;
+    static_assert(UPW == 1 || (POOL && !PAIR), "side-by-side units: single-CTA pooled tiles only");
+    using S = Shape<WIDE, ROWS, XP, NHWC, UPW>;
+    using RBox = RawBox<BF16, WIDE, ROWS, XP, UPW>;
     // one raw buffer: an NCHW box, or (NHWC) the two channel-group boxes in the strip's layout
     constexpr uint32_t kRawBytes = NHWC ? S::RAW_NHWC : RBox::kBytes;
     constexpr int UPT = S::UNITS;   // accumulator units per tile
@@ -678,7 +688,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         if (a.use_tma) prefetch_tmap(&tmx);
     }
     if (warp < kEpiWarps) {
-        build_indicator_planes<BF16, WIDE, ROWS>(smem + a.ind_off, a.OH, a.OW, a.RB, a.CS, threadIdx.x, kEpiWarps * 32);
+        build_indicator_planes<BF16, WIDE, ROWS, UPW>(smem + a.ind_off, a.OH, a.OW, a.RB, threadIdx.x, kEpiWarps * 32);
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
@@ -803,7 +813,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 }
                 const uint32_t strip = strip0 + slot * S::STRIP;
                 if (NHWC && !a.use_tma) {
-                    fill_strip_nhwc<BF16, WIDE, ROWS>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
+                    fill_strip_nhwc<BF16, WIDE, ROWS, UPW>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
                                                       tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad, a.Cin,
                                                       tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
@@ -815,19 +825,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t raw = smem_u32(smem + a.raw_off) + r * kRawBytes;
                     // split TF32: the third stage of each K block stages x's remainder
                     if constexpr (NHWC) {
-                        if (!BF16 && a.parts == 3 && cb % 3 == 2) copy_raw_nhwc<BF16, WIDE, ROWS, true>(raw, strip, lane);
-                        else copy_raw_nhwc<BF16, WIDE, ROWS, false>(raw, strip, lane);
+                        if (!BF16 && a.parts == 3 && cb % 3 == 2) copy_raw_nhwc<BF16, WIDE, ROWS, true, UPW>(raw, strip, lane);
+                        else copy_raw_nhwc<BF16, WIDE, ROWS, false, UPW>(raw, strip, lane);
                     } else if constexpr (!BF16) {
-                        if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, XP, true>(raw, strip, lane);
-                        else transpose_raw<BF16, WIDE, ROWS, XP>(raw, strip, lane);
+                        if (a.parts == 3 && cb % 3 == 2) transpose_raw<BF16, WIDE, ROWS, XP, true, UPW>(raw, strip, lane);
+                        else transpose_raw<BF16, WIDE, ROWS, XP, false, UPW>(raw, strip, lane);
                     } else {
-                        transpose_raw<BF16, WIDE, ROWS, XP>(raw, strip, lane);
+                        transpose_raw<BF16, WIDE, ROWS, XP, false, UPW>(raw, strip, lane);
                     }
                     fence_proxy_async_smem();   // order the raw reads before the next box overwrites it
                     __syncwarp();
                     if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
-                    fill_strip<BF16, WIDE, ROWS, XP>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
+                    fill_strip<BF16, WIDE, ROWS, XP, UPW>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
                                                      tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad - a.dcol, a.Cin,
                                                      tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
@@ -864,6 +874,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const uint64_t i_desc0 = smem_desc(smem_u32(smem + a.ind_off), 0u, 128u, kLayoutNone);
             constexpr uint32_t kInd16 = kIndPlane >> 4;
             constexpr uint32_t kZeroPlane = static_cast<uint32_t>(ind_variants(!WIDE));
+            // indicator plane of unit u of a tile (see build_indicator_planes); LBO points at the zero plane
+            auto unit_ind = [&](const TileCoord& c, int u) -> uint64_t {
+                uint32_t v = 0u;
+                if constexpr (!PAIR && !WIDE) {
+                    const int valid = a.OW - (c.cs * S::PC + 8 * u);
+                    v = (c.rb == a.RB - 1 ? 3u : 0u) + (valid >= 8 ? 0u : (valid > 0 ? 1u : 2u));
+                }
+                return i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
+            };
             const uint64_t b_desc0 = smem_desc(smem_u32(smem + a.w_off), half_co * 16u, 128u, kLayoutNone);
             const uint64_t bb_desc = smem_desc(smem_u32(smem + a.bb_off), half_co * 16u, 128u, kLayoutNone);
             const uint32_t wtap16 = 2u * half_co;   // one tap of this CTA's weights, 16-byte units
@@ -881,10 +900,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
-                // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
-                const uint32_t v = (PAIR || WIDE) ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
-                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
-                issue_mma<BF16, PAIR>(d, i_desc, bb_desc, idesc, 0u);
+                // bias (+ padding) K step, overwriting the accumulator
+                issue_mma<BF16, PAIR>(d, unit_ind(tc, 0), bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
@@ -922,21 +939,19 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 }
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
-                // bias (+ padding) K step, overwriting the accumulator; LBO points at the zero plane
-                const uint32_t v = (PAIR || WIDE) ? 0u : ((tc.rb == a.RB - 1 ? 2u : 0u) | (tc.cs == a.CS - 1 ? 1u : 0u));
-                const uint64_t i_desc = i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
+                // bias (+ padding) K step of every unit, overwriting its accumulator
 #pragma unroll
-                for (int u = 0; u < UPT; ++u) issue_mma<BF16, PAIR>(d[u], i_desc, bb_desc, idesc, 0u);
+                for (int u = 0; u < UPT; ++u) issue_mma<BF16, PAIR>(d[u], unit_ind(tc, u), bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
                     ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
-                    // unit u reads the strip from staged row u on (u * SC pixels, 16 B each)
+                    // unit u reads the strip u * UOFF staged pixels (16 B each) further
 #pragma unroll
                     for (int u = 0; u < UPT; ++u)
-                        issue_mma9<BF16, PAIR, S::SC>(d[u], ab + static_cast<uint64_t>(u * S::SC), bbase, wtap16, idesc);
+                        issue_mma9<BF16, PAIR, S::SC>(d[u], ab + static_cast<uint64_t>(u * S::UOFF), bbase, wtap16, idesc);
                     commit_to<PAIR>(&empty[slot], 0x3);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
                         slot = 0;
@@ -1331,11 +1346,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW = 1>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX, NHWC>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX, NHWC, UPW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1361,9 +1376,17 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
     cudaError_t name(const CUtensorMap& tmx, const ConvArgs& a, int pool, int act, int grid, uint32_t smem_bytes, \
                      cudaStream_t stream)
 
-// The variant switch shared by the four translation units.
+// Single-CTA pooled tiles of four side-by-side units (a.upw == 4); CTA pairs have none.
+template <bool BF16, int ACT, bool PAIR, bool PADX, bool NHWC>
+cudaError_t launch_units4(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream)
+{
+    if constexpr (PAIR) return cudaErrorInvalidValue;
+    else return launch_variant<BF16, true, ACT, false, PADX, NHWC, 4>(tmx, a, grid, smem_bytes, stream);
+}
+
+// The variant switch shared by the translation units.
 #define FC_CONV_LAUNCH_BODY(BF16, PAIR, PADX, NHWC)                                                      \
-    switch ((pool ? 0 : 1) * 4 + act) {                                                                 \
+    switch ((pool ? (a.upw == 4 ? 2 : 0) : 1) * 4 + act) {                                              \
     case 0: return launch_variant<BF16, true, 0, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
     case 1: return launch_variant<BF16, true, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
     case 2: return launch_variant<BF16, true, 2, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
@@ -1372,6 +1395,10 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
     case 5: return launch_variant<BF16, false, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
     case 6: return launch_variant<BF16, false, 2, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
     case 7: return launch_variant<BF16, false, 3, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);   \
+    case 8: return launch_units4<BF16, 0, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);          \
+    case 9: return launch_units4<BF16, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);          \
+    case 10: return launch_units4<BF16, 2, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);         \
+    case 11: return launch_units4<BF16, 3, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);         \
     default: return cudaErrorInvalidValue;                                                             \
     }
 FC_CONV_LAUNCH_DECL(launch_main_tf32);

@@ -47,6 +47,7 @@ struct ConvPlan {
     int resident;         // whole re-laid weight tensor kept in shared memory
     int nacc;             // tensor-memory accumulator buffers
     int egroups;          // epilogue tile groups (1, 2, 4): each takes every egroups-th tile
+    int upw;              // pooled single-CTA tiles: units side by side (1: 16 x 8, 4: 16 x 32)
     int tmem_cols;        // tensor-memory columns allocated
     uint32_t w_block_bytes;   // one CTA's re-laid weights of one K block: 9 taps * 2 halves * (Cout/2) * 16 B
     uint32_t w_total_bytes;   // ncb * w_block_bytes (one CTA of the pair)
