@@ -261,6 +261,8 @@ int conv_plan(ConvPlan* p, int N, int Cin, int H, int W, int Cout, int pad, int 
             p->egroups = g;
             break;
         }
+    // the four-unit kernel folds these as constants
+    if (p->upw == 4 && (p->nacc != 8 || p->egroups != 4)) return 2;
     int cols = 32;
     while (cols < p->nacc * Cout) cols <<= 1;
     p->tmem_cols = cols;

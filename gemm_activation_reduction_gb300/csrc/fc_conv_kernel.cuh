@@ -948,19 +948,20 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
                     const uint64_t bbase = b_desc0 + (a.resident ? static_cast<uint32_t>(cb) : slot) * wblk16;
-                    // unit u reads the strip u * UOFF staged pixels (16 B each) further
+                    // unit u reads the strip u * UOFF staged pixels (16 B each) further.  In the last K
+                    // block each unit's accumulator is committed right after its own MMAs (a commit
+                    // tracks every MMA issued before it), so the tile groups start staggered.
+                    const bool last = cb == a.ncb - 1;
 #pragma unroll
-                    for (int u = 0; u < UPT; ++u)
+                    for (int u = 0; u < UPT; ++u) {
                         issue_mma9<BF16, PAIR, S::SC>(d[u], ab + static_cast<uint64_t>(u * S::UOFF), bbase, wtap16, idesc);
+                        if (last) commit_to<PAIR>(&tfull[accu[u]], 0x3);
+                    }
                     commit_to<PAIR>(&empty[slot], 0x3);
                     if (++slot == static_cast<uint32_t>(a.stages)) {
                         slot = 0;
                         sph ^= 1u;
                     }
-                }
-                if (ok) {
-#pragma unroll
-                    for (int u = 0; u < UPT; ++u) commit_to<PAIR>(&tfull[accu[u]], 0x3);
                 }
                 next_tile(tc, a.RB, a.CS);
                 if constexpr (PAIR) next_tile(tc, a.RB, a.CS);
@@ -980,7 +981,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         // and within a tile this warp owns the slices c = hh + hw k.  More columns per
         // warp and tile amortise the per-tile hand-offs; groups on different tiles keep
         // the pipes busy while others wait.
-        const int G = a.egroups;
+        // four side-by-side units: the plan always gives 4 tile groups and 8 accumulators (Cout <= 64),
+        // constants the compiler folds into the ring and tile arithmetic below
+        const int G = UPW == 4 ? 4 : a.egroups;
+        const int nacc = UPW == 4 ? 8 : a.nacc;
         const int hw = 4 / G;
         const int gi = h / hw;
         const int hh = h - gi * hw;
@@ -1063,8 +1067,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         };
         advance_units(gi);
         int lt = gi;
-        int acc = gi % a.nacc;
-        uint32_t aph = static_cast<uint32_t>(gi / a.nacc) & 1u;
+        int acc = gi % nacc;
+        uint32_t aph = static_cast<uint32_t>(gi / nacc) & 1u;
         auto taddr = [&](int acc_i, int k) {
             return tmem + (static_cast<uint32_t>(q * 32) << 16) +
                    static_cast<uint32_t>(acc_i * a.Cout + (hh + hw * k) * kEpiCols);
@@ -1109,8 +1113,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const int nlt = lt + G;
                 int nacc_i = acc + G;
                 uint32_t naph = aph;
-                while (nacc_i >= a.nacc) {
-                    nacc_i -= a.nacc;
+                while (nacc_i >= nacc) {
+                    nacc_i -= nacc;
                     naph ^= 1u;
                 }
                 auto release_and_next = [&]() {
@@ -1186,8 +1190,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const int nlt = lt + G;
                 int nacc_i = acc + G;
                 uint32_t naph = aph;
-                while (nacc_i >= a.nacc) {
-                    nacc_i -= a.nacc;
+                while (nacc_i >= nacc) {
+                    nacc_i -= nacc;
                     naph ^= 1u;
                 }
                 auto release_and_next = [&]() {
@@ -1274,8 +1278,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const int nlt = lt + G;
             int nacc_i = acc + G;
             uint32_t naph = aph;
-            while (nacc_i >= a.nacc) {
-                nacc_i -= a.nacc;
+            while (nacc_i >= nacc) {
+                nacc_i -= nacc;
                 naph ^= 1u;
             }
             auto release_and_next = [&]() {
