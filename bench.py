@@ -77,14 +77,53 @@ def epilogue_roofline(wl, call_ms, sm_count, sm_mhz):
             "elements": elems}
 
 
+def tf32_peak(pk):
+    """TF32 dense peak: the larger of the nominal-ratio figure (measured BF16 x 1.1/2.25) and the
+    TF32 library GEMM measured in this run (pk["tf32_measured_tflops"], when present)."""
+    nominal = pk["bf16_tflops"] * TF32_OVER_BF16
+    measured = pk.get("tf32_measured_tflops")
+    if measured and measured > nominal:
+        return measured, f"tf32 = measured library TF32 GEMM {measured:.1f} TFLOP/s ({pk['tf32_how']})"
+    return nominal, f"tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25" + \
+        (f"; measured TF32 GEMM {measured:.1f} TFLOP/s is lower" if measured else "")
+
+
 def tensor_peak(wl, pk):
     bf16 = pk["bf16_tflops"]
     if getattr(wl, "dtype", "f32") == "bf16":
         return bf16, f"bf16 burst ({pk['source']})"
+    tf32, note = tf32_peak(pk)
     if getattr(wl, "precision", "tf32") == "3xtf32":
         # three TF32 products per term: the contraction's flops take three times the TF32 tensor time
-        return bf16 * TF32_OVER_BF16 / 3.0, f"3xtf32 = tf32 / 3, tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25"
-    return bf16 * TF32_OVER_BF16, f"tf32 = bf16 burst ({pk['source']}) x nominal 1.1/2.25"
+        return tf32 / 3.0, f"3xtf32 = tf32 / 3, {note}"
+    return tf32, note
+
+
+def measure_tf32_gemm(torch, device, n=8192, reps=10):
+    """Peak measurement only (not the operator's path): best time of an fp32 n^3 library matmul
+    with TF32 tensor-core math enabled, CUDA events around each call; returns TFLOP/s."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device=device)
+        b = torch.randn(n, n, device=device)
+        for _ in range(3):
+            torch.matmul(a, b)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 # ------------------------------------------------------------------ clocks
@@ -264,6 +303,27 @@ def time_graph(torch, call, reps, replays=5):
     return statistics.median(times)
 
 
+def time_cold(torch, call, reps=10, flush_bytes=512 << 20):
+    """Median ms of `reps` calls, each preceded by a write of a `flush_bytes` scratch buffer (more
+    than 4x the L2), with the CUDA events placed after the write: the inputs come from HBM."""
+    scratch = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    call()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(reps):
+        scratch.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    del scratch
+    return statistics.median(times)
+
+
 def max_over_ranks(torch, value, dist, device):
     """The maximum of a per-rank float over all ranks (a job's time is its slowest rank's);
     `device` is where the collective's tensor lives (cuda for NCCL, cpu for gloo)."""
@@ -278,6 +338,11 @@ def rank_seeds(rank):
     """Weak scaling: rank r owns its own shard (batch) of the workload, drawn with its own x seed
     (weights and bias are shared)."""
     return (fc_inputs.SEED_X + 1000 * rank, fc_inputs.SEED_W, fc_inputs.SEED_B)
+
+
+def r4(v):
+    """v to 4 significant digits (keeps the JSON line short)."""
+    return None if v is None else float(f"{v:.4g}")
 
 
 def job_tflops(flops_per_call, world, ms_per_call):
@@ -520,6 +585,13 @@ def gpu_arm(args):
     flops = wl.flops()
     value = job_tflops(flops, world, ms)
     pk = peaks()
+    if not args.no_tf32_peak:
+        try:
+            pk["tf32_measured_tflops"] = measure_tf32_gemm(torch, device)
+            pk["tf32_how"] = "torch.matmul fp32 8192^3 with TF32 math, best of 10 in this run"
+        except Exception as e:  # the line still prints; the nominal figure is used
+            pk["tf32_how"] = f"failed: {e}"
+    cold_ms = time_cold(torch, call) if world == 1 else None
     peak, peak_note = tensor_peak(wl, pk)
     kernel_ms = statistics.mean(per)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
@@ -565,7 +637,12 @@ def gpu_arm(args):
                     else f"{'fc_conv3x3_act_pool_host' if wl.pool else 'fc_conv3x3_act_host'}"
                          f" (pinned host buffers, {args.e2e_chunks} overlapped slices)"},
             "gpu_launches": steps * launches_per_call, "clocks": clocks,
-            "pct_of_roofline": 100.0 * cfg["roofline_ms"] / ms}
+            "pct_of_roofline": 100.0 * cfg["roofline_ms"] / ms,
+            "cold_l2": {"ms_median": cold_ms, "warm_ms_median": statistics.median(per),
+                        "how": "each of 10 calls after a 512 MB scratch write, events after the write"}
+            if cold_ms is not None else None,
+            "tf32_peak_tflops": {"measured_gemm": pk.get("tf32_measured_tflops"),
+                                 "nominal": pk["bf16_tflops"] * TF32_OVER_BF16, "used": tf32_peak(pk)[0]}}
     if not args.no_others and world == 1:
         others = {}
         for k in args.others.split(","):
@@ -584,19 +661,28 @@ def gpu_arm(args):
             if isinstance(owl, fc_inputs.EpilogueWorkload):
                 # HBM-bound: the roofline is one pass over the compulsory bytes
                 rl = owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9) * 1e3
-                others[k] = {"workload": owl.name, "ms_per_call": oms,
-                             "gbs": owl.compulsory_bytes() / (oms * 1e-3) / 1e9, "bound": "hbm",
-                             "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+                others[k] = {"workload": owl.name, "ms_per_call": r4(oms),
+                             "gbs": r4(owl.compulsory_bytes() / (oms * 1e-3) / 1e9), "bound": "hbm",
+                             "roofline_ms": r4(rl), "pct_of_roofline": r4(100.0 * rl / oms)}
             else:
                 opeak, _ = tensor_peak(owl, pk)
                 rl = max(owl.flops() / (opeak * 1e12), owl.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)) * 1e3
-                others[k] = {"workload": owl.name, "ms_per_call": oms, "tflops": owl.flops() / (oms * 1e-3) / 1e12,
-                             "roofline_ms": rl, "pct_of_roofline": 100.0 * rl / oms}
+                others[k] = {"workload": owl.name, "ms_per_call": r4(oms),
+                             "tflops": r4(owl.flops() / (oms * 1e-3) / 1e12),
+                             "roofline_ms": r4(rl), "pct_of_roofline": r4(100.0 * rl / oms),
+                             "ms_cold_l2": r4(time_cold(torch, ocall))}
                 if isinstance(owl, fc_inputs.ConvWorkload):
-                    others[k]["epilogue_frac"] = epilogue_roofline(owl, oms, sm_count, sm_mhz)["frac"]
+                    others[k]["epilogue_frac"] = r4(epilogue_roofline(owl, oms, sm_count, sm_mhz)["frac"])
             del od, ocall, oout
             torch.cuda.empty_cache()
         line["other_workloads"] = others
+        # the five configurations of the problem statements, compact and last on the line (so that a
+        # record that keeps only the line's end still shows each): ms per call and % of roofline
+        summ = {key: [r4(ms), r4(line["pct_of_roofline"])]}
+        for k in ("A", "B", "C", "D", "E"):
+            if k in others:
+                summ[k] = [others[k]["ms_per_call"], others[k]["pct_of_roofline"]]
+        line["configs_ms_pct"] = {k: summ[k] for k in ("A", "B", "C", "D", "E") if k in summ}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -612,12 +698,13 @@ def main():
                     choices=sorted(k for k, w in fc_inputs.WORKLOADS.items()
                                    if not isinstance(w, fc_inputs.EpilogueWorkload)))
     ap.add_argument("--impl", default="fc", choices=["fc", "reference"])
-    ap.add_argument("--others", default="C,D,E,Bt,Cb,Db,D3,B3,C3,Bp,Cp,Cn,Cbn,Bn,En,K1e,K2e,K3e",
+    ap.add_argument("--others", default="Bt,Cb,Db,D3,B3,C3,Bp,Cp,Cn,Cbn,Bn,En,K1e,K2e,K3e,A,C,D,E",
                     help="other workloads timed briefly into other_workloads")
     ap.add_argument("--no-others", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="slices of the batch whose host copies overlap the kernels in the end-to-end timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tf32-peak", action="store_true", help="skip the TF32 library GEMM peak measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)

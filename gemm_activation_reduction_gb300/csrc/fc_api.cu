@@ -5,6 +5,7 @@
 #include "fc_internal.h"
 #include "fc_ptx.cuh"
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -15,24 +16,34 @@ constexpr int kMaxDevices = 64;
 __device__ int g_fc_status = 0;
 
 struct DeviceState {
-    std::once_flag once;
+    std::atomic<bool> ready{false};   // set once sm_count and status hold this device's values
     int sm_count = 0;
-    int* status = nullptr;   // device address of g_fc_status on this device
-    cudaError_t err = cudaSuccess;
+    int* status = nullptr;            // device address of g_fc_status on this device
 };
 DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
 
-// SM count and status-word address of the current device.
+// SM count and status-word address of the current device.  Only a successful look-up is kept:
+// a failed one (say, a first call made while a stream capture forbids it) is tried again on the
+// next call.
 fc_status device_state(DeviceState** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FC_ERR_CUDA;
     DeviceState& d = g_dev[dev];
-    std::call_once(d.once, [&d, dev]() {
-        d.err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fc_status);
-    });
-    if (d.err != cudaSuccess) return FC_ERR_CUDA;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int sms = 0;
+            int* st = nullptr;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaGetSymbolAddress(reinterpret_cast<void**>(&st), g_fc_status) != cudaSuccess || st == nullptr)
+                return FC_ERR_CUDA;
+            d.sm_count = sms;
+            d.status = st;
+            d.ready.store(true, std::memory_order_release);
+        }
+    }
     *out = &d;
     return FC_OK;
 }

@@ -94,12 +94,18 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
 // output's list (cluster, CTA of the cluster, record) goes to lane k % 32, each lane sums its
 // records in order, and a fixed shuffle tree adds the lanes -- the same order on every run.
 __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Co, int Cout, long long tpi,
-                                         long long pbase, int prem, int J, int step, int recs, double inv_count)
+                                         long long pbase, int prem, int J, int step, int recs, double inv_count,
+                                         const int* status)
 {
     pdl_wait();   // the fused kernel's records are complete and visible
     const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= static_cast<long long>(N) * Co) return;   // whole warps leave together
+    // a bounded wait that gave up leaves records the fused kernel never wrote: say so in the output
+    if (*reinterpret_cast<const volatile int*>(status) == FC_DEVICE_TIMEOUT) {
+        if (lane == 0) y[wid] = __int_as_float(0x7fc00000);
+        return;
+    }
     const int n = static_cast<int>(wid / Co);
     const int co = static_cast<int>(wid - static_cast<long long>(n) * Co);
     const long long big = static_cast<long long>(prem) * (pbase + 1);
@@ -385,7 +391,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, conv_pool_combine_kernel, static_cast<const float*>(pool_ws), y, p.N, p.Co,
                                p.Cout, p.tpi, p.pbase, p.prem, p.J, p.pair ? 2 : 1, 4 * p.egroups,
-                               1.0 / (static_cast<double>(p.OH) * p.OW));
+                               1.0 / (static_cast<double>(p.OH) * p.OW), static_cast<const int*>(status));
     }
     return e;
 }

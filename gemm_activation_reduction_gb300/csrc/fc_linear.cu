@@ -483,11 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge the per-column-tile (max, sum) pairs of each row in fixed order, then
 // lse = M + log S and y = lse * mish(lse), mish(l) = l * tanh(softplus(l)).
-__global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks)
+__global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks, const int* status)
 {
     pdl_wait();   // the GEMM's partials are complete and visible
     const int m = blockIdx.x * blockDim.x + threadIdx.x;
     if (m >= M) return;
+    // a bounded wait that gave up leaves partials the GEMM never wrote: say so in the output
+    if (*reinterpret_cast<const volatile int*>(status) == FC_DEVICE_TIMEOUT) {
+        y[m] = __int_as_float(0x7fc00000);
+        return;
+    }
     float mx = -INFINITY;
     for (int i = 0; i < n_blocks; ++i) mx = fmaxf(mx, partials[static_cast<size_t>(i) * M + m].x);
     float s = 0.0f;
@@ -502,7 +507,8 @@ __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int 
 
 // The row combine, launched so that it may start while the GEMM finishes (it waits for the
 // partials itself).
-cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_blocks, cudaStream_t stream)
+cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_blocks, const int* status,
+                               cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>((M + 127) / 128));
@@ -513,7 +519,7 @@ cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_bl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lse_combine_kernel, partials, y, M, n_blocks);
+    return cudaLaunchKernelEx(&cfg, lse_combine_kernel, partials, y, M, n_blocks, status);
 }
 
 // Row-major [rows][cols] fp32 or bf16 matrix, box = box_rows x one 128-byte row of K, 128-byte swizzle.
@@ -684,7 +690,7 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmxl, tmwl, a);
         if (e != cudaSuccess) return e;
-        return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);
+        return launch_lse_combine(a.partials, y, p.M, p.n_blocks, status, stream);
     }
     if (!make_kmajor_map(&tmx, x, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, kBN, bf16) ||
         !make_kmajor_map(&tmxl, xl, p.M, p.K, kBM, bf16) || !make_kmajor_map(&tmwl, wl, p.Nout, p.K, kBN, bf16))
@@ -704,7 +710,7 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
     kern<<<p.grid, kThreads, p.smem_bytes, stream>>>(tmx, tmw, tmxl, tmwl, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_lse_combine(a.partials, y, p.M, p.n_blocks, stream);
+    return launch_lse_combine(a.partials, y, p.M, p.n_blocks, status, stream);
 }
 
 }  // namespace fc

@@ -11,6 +11,7 @@
 #include "../../include/fc.h"
 #include "fc_internal.h"
 
+#include <atomic>
 #include <mutex>
 
 namespace {
@@ -25,12 +26,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 
-struct ScratchAddress {
-    std::once_flag once;
-    void* ptr = nullptr;      // device address of g_noalloc_scratch on this device
-    cudaError_t err = cudaSuccess;
-};
-ScratchAddress g_scratch[kMaxDevices];
+// Device address of g_noalloc_scratch per device; only a successful look-up is kept, so a
+// failed first call (for instance one made during a stream capture) is retried on the next.
+std::atomic<void*> g_scratch[kMaxDevices];
+std::mutex g_scratch_mutex;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -49,19 +48,27 @@ extern "C" fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, co
     // Host code cannot use g_noalloc_scratch's name as a device address: look the
     // address up once per device, with that device current (it is: this call runs
     // on the caller's current device).
-    ScratchAddress& s = g_scratch[dev];
-    std::call_once(s.once, [&s]() { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
-    if (s.err != cudaSuccess || s.ptr == nullptr) return FC_ERR_CUDA;
+    void* scratch = g_scratch[dev].load(std::memory_order_acquire);
+    if (scratch == nullptr) {
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        scratch = g_scratch[dev].load(std::memory_order_relaxed);
+        if (scratch == nullptr) {
+            if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+                return FC_ERR_CUDA;
+            g_scratch[dev].store(scratch, std::memory_order_release);
+        }
+    }
     int sm_count = 0;
     int* status = nullptr;
     if (fc::current_device_info(&sm_count, &status) != cudaSuccess) return FC_ERR_CUDA;
     fc::LinearPlan plan;
     if (fc::linear_plan(&plan, M, K, Nout, 0, sm_count) != 0) return FC_ERR_UNSUPPORTED;
     if (plan.ws_bytes > kNoAllocScratchBytes) return FC_ERR_UNSUPPORTED;
-    // Every (max, sum-exp) pair the combine kernel reads is written by the main
-    // kernel of the same call, so the array needs no clearing between calls.
+    // Every (max, sum-exp) pair the combine kernel reads is written by the main kernel of the
+    // same call, so the array needs no clearing between calls -- unless a bounded wait of that
+    // kernel gives up, in which case the combine writes NaN instead of reading the array.
     cudaError_t e = fc::linear_launch(plan, static_cast<const float*>(x), static_cast<const float*>(W),
-                                      static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, s.ptr,
+                                      static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, scratch,
                                       reinterpret_cast<cudaStream_t>(stream), status, fc::kWaitBudgetCycles);
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }

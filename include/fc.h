@@ -216,9 +216,10 @@ fc_status fc_scale_clamp_lse_mish(const float* t, float* y, int M, int N, float 
  * reports for the same shape) exceeds 1 MiB return FC_ERR_UNSUPPORTED.
  * The call allocates nothing.  The first call on a device looks up that
  * array's device address (a one-time set-up); make that first call before
- * any stream capture.  All calls share the one array: calls that overlap on
- * the GPU (other streams, or other host threads) race on it and give wrong
- * results.  Nothing in it needs to start at zero.
+ * any stream capture (a look-up that fails returns FC_ERR_CUDA and is tried
+ * again by the next call).  All calls share the one array: calls that
+ * overlap on the GPU (other streams, or other host threads) race on it and
+ * give wrong results.  Nothing in it needs to start at zero.
  */
 fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, const void* b, float* y,
                                      int M, int K, int Nout, float scale, float clamp_lo, float clamp_hi,
@@ -288,7 +289,10 @@ const char* fc_status_string(fc_status status);
 /*
  * Watchdog word of the current device.  Every spin-wait in the kernels is
  * bounded; on expiry a kernel records FC_ERR_TIMEOUT here, stops its loops,
- * drains its own copies and returns (the context stays usable).  This call
+ * drains its own copies and returns (the context stays usable).  While the
+ * word holds FC_ERR_TIMEOUT, the pooled conv and Linear operators write NaN
+ * to their outputs (their partial results cannot be trusted); a full-output
+ * conv whose kernel gave up leaves its output undefined.  This call
  * synchronizes the device, returns the recorded status (FC_OK if none) and,
  * when clear != 0, resets it.
  */

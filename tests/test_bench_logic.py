@@ -21,6 +21,23 @@ def test_tensor_peaks_per_precision():
     assert bench.tensor_peak(fc_inputs.WORKLOADS["Db"], PK)[0] == pytest.approx(PK["bf16_tflops"])
 
 
+def test_tf32_peak_is_the_larger_of_nominal_and_measured():
+    nominal = PK["bf16_tflops"] * 1.1 / 2.25
+    pk = dict(PK, tf32_measured_tflops=1022.2, tf32_how="test")
+    peak, note = bench.tf32_peak(pk)
+    assert peak == pytest.approx(1022.2) and "measured" in note
+    assert bench.tensor_peak(fc_inputs.WORKLOADS["B"], pk)[0] == pytest.approx(1022.2)
+    assert bench.tensor_peak(fc_inputs.WORKLOADS["B3"], pk)[0] == pytest.approx(1022.2 / 3)
+    assert bench.tensor_peak(fc_inputs.WORKLOADS["E"], pk)[0] == pytest.approx(PK["bf16_tflops"])   # bf16: unchanged
+    low = dict(PK, tf32_measured_tflops=500.0, tf32_how="test")
+    assert bench.tf32_peak(low)[0] == pytest.approx(nominal)
+    assert bench.tf32_peak(PK)[0] == pytest.approx(nominal)                                          # not measured
+
+
+def test_round_to_four_significant_digits():
+    assert bench.r4(0.23412345) == 0.2341 and bench.r4(1234.5678) == 1235.0 and bench.r4(None) is None
+
+
 def test_workload_b_roofline_figures():
     wl = fc_inputs.WORKLOADS["B"]
     assert wl.flops() == 2 * 128 * 64 * 254 * 254 * 8 * 9

@@ -648,6 +648,25 @@ def test_watchdog_times_out_and_context_stays_usable(cuda_lib):
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
 
 
+def test_outputs_are_nan_while_a_timeout_is_recorded(cuda_lib):
+    """A recorded timeout (made by the watchdog self-test's bounded wait, no fault) means some
+    kernel's partial results may be missing: the pooled conv and the Linear chain then write NaN
+    instead of combining them, and are exact again once the status is cleared."""
+    import torch
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+    dc = fc_inputs.conv_inputs(2, 8, 32, 32, 64)
+    dl = fc_inputs.linear_inputs(64, 256, 512)
+    conv = lambda: cuda_lib.fc_conv3x3_act_pool(_dev(dc["x"]), _dev(dc["w"]), _dev(dc["b"])).cpu().numpy()
+    lin = lambda: cuda_lib.fc_linear_lse_mish(_dev(dl["x"]), _dev(dl["W"]), _dev(dl["b"])).cpu().numpy()
+    cuda_lib.fc_selftest_watchdog(2_000_000)
+    torch.cuda.synchronize()
+    assert np.all(np.isnan(conv())) and np.all(np.isnan(lin()))
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_ERR_TIMEOUT
+    _check(conv(), oracle.conv3x3_act_pool(dc["x32"], dc["w32"], dc["b32"], "gelu"), TOL["f32"], "after clearing")
+    _check(lin(), oracle.linear_lse_mish(dl["x"], dl["W"], dl["b"]), TOL["f32"], "after clearing")
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
 @pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish", "gelu_tanh"])
 def test_activation_accuracy_through_a_delta_kernel(cuda_lib, act):
     """A delta 3x3 kernel makes the pre-activation equal to the input (values on a
