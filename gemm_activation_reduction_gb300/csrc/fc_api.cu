@@ -15,6 +15,9 @@ constexpr int kMaxDevices = 64;
 
 __device__ int g_fc_status = 0;
 
+// Wait budget of the next launches (see fc::wait_budget); only the testing hook below changes it.
+std::atomic<long long> g_wait_budget{fc::kWaitBudgetCycles};
+
 struct DeviceState {
     std::atomic<bool> ready{false};   // set once sm_count and status hold this device's values
     int sm_count = 0;
@@ -80,7 +83,7 @@ fc_status conv_common(const void* x, const void* w, const void* b, float* y, int
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return FC_ERR_WORKSPACE;
     cudaError_t e = fc::conv_launch(plan, x, w, b, y, static_cast<int>(act), workspace,
-                                    reinterpret_cast<cudaStream_t>(stream), d->status, fc::kWaitBudgetCycles);
+                                    reinterpret_cast<cudaStream_t>(stream), d->status, fc::wait_budget());
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
@@ -109,6 +112,8 @@ cudaError_t watchdog_selftest_launch(long long budget, cudaStream_t stream, int*
     watchdog_kernel<<<1, 32, 0, stream>>>(budget, status);
     return cudaGetLastError();
 }
+
+long long wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
 
 cudaError_t current_device_info(int* sm_count, int** status)
 {
@@ -183,7 +188,7 @@ fc_status fc_linear_lse_mish(const void* x, const void* W, const void* b, float*
         if (e != cudaSuccess) return FC_ERR_CUDA;
     }
     cudaError_t e = fc::linear_launch(plan, x, W, b, y, scale, clamp_lo, clamp_hi, workspace, s, d->status,
-                                      fc::kWaitBudgetCycles, x_lo, W_lo);
+                                      fc::wait_budget(), x_lo, W_lo);
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }
 
@@ -310,5 +315,14 @@ fc_status fc_selftest_watchdog(unsigned long long budget_cycles, fc_stream_t str
 }
 
 int fc_version(void) { return 100; }
+
+// Testing hook, deliberately not declared in fc.h: sets the spin budget (SM clock cycles) that
+// every later launch's bounded waits get, so that a test can make a real operator's waits give
+// up.  cycles <= 0 restores the default.  Drains after a wait gives up keep the full budget.
+// Returns the previous budget.  Affects every thread of the process; for tests only.
+long long fc_testing_set_wait_budget(long long cycles)
+{
+    return g_wait_budget.exchange(cycles > 0 ? cycles : fc::kWaitBudgetCycles);
+}
 
 }  // extern "C"

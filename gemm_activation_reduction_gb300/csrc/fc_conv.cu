@@ -347,6 +347,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     a.pbase = p.pbase; a.prem = p.prem; a.J = p.J; a.pair = p.pair;
     a.stages = p.stages; a.raw_depth = p.raw_depth; a.resident = p.resident; a.nacc = p.nacc; a.egroups = p.egroups; a.tmem_cols = p.tmem_cols;
     a.upw = p.upw;
+    a.poll = polling_budget(budget) ? 1 : 0;
     a.w_block_bytes = p.w_block_bytes; a.w_total_bytes = p.w_total_bytes; a.bias_block_bytes = p.bias_block_bytes;
     a.strip_off = p.strip_off; a.ind_off = p.ind_off; a.w_off = p.w_off; a.bb_off = p.bb_off; a.raw_off = p.raw_off;
     a.bar_off = p.bar_off; a.use_tma = p.use_tma;

@@ -145,6 +145,7 @@ struct ConvArgs {
     int prem, J, stages, raw_depth, resident, nacc, tmem_cols;
     int egroups;          // epilogue tile groups G (1, 2, 4): group g takes every G-th tile
     int upw;              // pooled single-CTA tiles: 1 (16 x 8) or 4 units side by side (16 x 32)
+    int poll;             // a test shortened the wait budget: launch the polling instantiation
     int pair;             // 1: CTA pairs with M = 256 MMAs (group = 2 tiles); 0: single CTAs
     uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;   // per CTA of the pair (its half of Cout)
     uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
@@ -600,13 +601,14 @@ __device__ __forceinline__ void issue_mma9(uint32_t d, uint64_t a, uint64_t b, u
 #undef FC_MMA9
 }
 
-// Bounded wait; barriers that the peer CTA signals need cluster-scope acquire.
-template <bool PAIR>
+// Bounded wait; barriers that the peer CTA signals need cluster-scope acquire.  POLL: see mbar_wait.
+template <bool PAIR, bool POLL = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                          long long budget)
 {
+    static_assert(!(PAIR && POLL), "CTA pairs have no polling instantiation");
     if constexpr (PAIR) return mbar_wait_cluster(bar, parity, abort_flag, status, budget);
-    else return mbar_wait(bar, parity, abort_flag, status, budget);
+    else return mbar_wait<POLL>(bar, parity, abort_flag, status, budget);
 }
 
 // Commit this thread's MMAs to `bar` in the CTAs of `mask` (pair) or in this CTA.
@@ -627,7 +629,9 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW>
+// POLL: the waits poll instead of suspending (see mbar_wait); only launched while a test has
+// shortened the wait budget.
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW, bool POLL = false>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv3x3_fused_kernel(const __grid_constant__ CUtensorMap tmx, const ConvArgs a)
 {
@@ -798,7 +802,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             while (lt < n_pairs) {
                 const uint32_t slot = g % S_;
                 const uint32_t par = (g / S_) & 1u;
-                bool ok = wait_bar<PAIR>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
+                bool ok = wait_bar<PAIR, POLL>(&empty[slot], par ^ 1u, abort_flag, a.status, a.budget);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 fence_proxy_async_smem();
                 if (lane == 0) {
@@ -820,7 +824,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     __syncwarp();
                 } else if (a.use_tma) {
                     const uint32_t r = raw_buf(use);
-                    ok = mbar_wait(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
+                    ok = mbar_wait<POLL>(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
                     const uint32_t raw = smem_u32(smem + a.raw_off) + r * kRawBytes;
                     // split TF32: the third stage of each K block stages x's remainder
@@ -853,14 +857,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 if (last_w >= 0) {
                     // the weight copy of this warp's last stage
                     const uint32_t gl = static_cast<uint32_t>(last_w);
-                    drain_wait(&full[gl % S_], (gl / S_) & 1u, a.budget);
+                    drain_wait(&full[gl % S_], (gl / S_) & 1u, kDrainBudgetCycles);
                 }
                 // boxes requested but not yet waited for
                 for (uint32_t i = use; i < issued; ++i)
-                    drain_wait(&rawfull[raw_buf(i)], (i / static_cast<uint32_t>(rd)) & 1u, a.budget);
+                    drain_wait(&rawfull[raw_buf(i)], (i / static_cast<uint32_t>(rd)) & 1u, kDrainBudgetCycles);
             }
         }
-        if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, a.budget);
+        if (pw == 0 && lane == 0 && *abort_flag) drain_wait(wfull, 0, kDrainBudgetCycles);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (leader)
         if (leader) {
@@ -888,7 +892,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const uint32_t wtap16 = 2u * half_co;   // one tap of this CTA's weights, 16-byte units
             const uint32_t wblk16 = a.w_block_bytes >> 4;
             constexpr uint32_t kStrip16 = S::STRIP >> 4;
-            bool ok = mbar_wait(wfull, 0, abort_flag, a.status, a.budget) &&
+            bool ok = mbar_wait<POLL>(wfull, 0, abort_flag, a.status, a.budget) &&
                       (!pair || mbar_wait_cluster(wpeer, 0, abort_flag, a.status, a.budget));
             ok = __all_sync(0xffffffffu, ok);
             int acc = 0;   // accumulator ring position of the next unit
@@ -896,14 +900,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             TileCoord tc = first;
             for (int lt = 0; ok && lt < n_pairs && UPT == 1; ++lt) {
                 // one accumulator per tile (pooled tiles, CTA pairs)
-                ok = wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                ok = wait_bar<PAIR, POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 // bias (+ padding) K step, overwriting the accumulator
                 issue_mma<BF16, PAIR>(d, unit_ind(tc, 0), bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
-                    ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
+                    ok = wait_bar<PAIR, POLL>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
@@ -931,7 +935,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 for (int u = 0; u < UPT; ++u) {
                     accu[u] = acc;
                     d[u] = tmem + static_cast<uint32_t>(acc * a.Cout);
-                    ok = ok && wait_bar<PAIR>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
+                    ok = ok && wait_bar<PAIR, POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
                     if (++acc == a.nacc) {
                         acc = 0;
                         aph ^= 1u;
@@ -943,7 +947,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
 #pragma unroll
                 for (int u = 0; u < UPT; ++u) issue_mma<BF16, PAIR>(d[u], unit_ind(tc, u), bb_desc, idesc, 0u);
                 for (int cb = 0; cb < a.ncb; ++cb) {
-                    ok = wait_bar<PAIR>(&full[slot], sph, abort_flag, a.status, a.budget);
+                    ok = wait_bar<PAIR, POLL>(&full[slot], sph, abort_flag, a.status, a.budget);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc_fence_after();
                     const uint64_t ab = a_desc0 + slot * kStrip16 + static_cast<uint32_t>(a.dcol);
@@ -967,7 +971,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 if constexpr (PAIR) next_tile(tc, a.RB, a.CS);
             }
             commit_to<PAIR>(mdone, 0x1);
-            drain_wait(mdone, 0, a.budget);
+            drain_wait(mdone, 0, kDrainBudgetCycles);
         }
         __syncwarp();
     } else if (warp < kEpiWarps) {
@@ -1092,7 +1096,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             // odd number of slices leaves the next tile's slice 0 in buf[1], moved after its wait
             uint32_t buf[2][kEpiCols];
             if (lt < n_units) {
-                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+                ok = wait_bar<PAIR, POLL>(&tfull[acc], aph, abort_flag, a.status, a.budget);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
                 if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), buf[0]);
@@ -1125,7 +1129,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         else mbar_arrive(&tempty[acc]);
                     }
                     if (nlt < n_units) {
-                        ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                        ok = wait_bar<PAIR, POLL>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                         ok = __all_sync(0xffffffffu, ok);
                         tc_fence_after();
                         if (ok && ms > 0) {
@@ -1180,7 +1184,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             const bool pairs_ok = (a.Co & 1) == 0;   // 8-byte-aligned channel pairs
             uint32_t buf[2][kEpiCols];
             if (lt < n_units) {
-                ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+                ok = wait_bar<PAIR, POLL>(&tfull[acc], aph, abort_flag, a.status, a.budget);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
                 if (ok && ms > 0) tmem_ld_slice16x256_start(slice_addr(acc, 0), buf[0]);
@@ -1202,7 +1206,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         else mbar_arrive(&tempty[acc]);
                     }
                     if (nlt < n_units) {
-                        ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                        ok = wait_bar<PAIR, POLL>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                         ok = __all_sync(0xffffffffu, ok);
                         tc_fence_after();
                         if (ok && ms > 0) {
@@ -1266,7 +1270,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         // is in registers.
         uint32_t rnext[kEpiCols];
         if (!POOL && !NHWC && lt < n_units) {
-            ok = wait_bar<PAIR>(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            ok = wait_bar<PAIR, POLL>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (ok && ms > 0) tmem_ld16_start(taddr(acc, 0), rnext);
@@ -1290,7 +1294,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     else mbar_arrive(&tempty[acc]);
                 }
                 if (nlt < n_units) {
-                    ok = wait_bar<PAIR>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
+                    ok = wait_bar<PAIR, POLL>(&tfull[nacc_i], naph, abort_flag, a.status, a.budget);
                     ok = __all_sync(0xffffffffu, ok);
                     tc_fence_after();
                     if (ok && ms > 0) tmem_ld16_start(taddr(nacc_i, 0), rnext);
@@ -1350,11 +1354,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     }
 }
 
-template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW = 1>
+template <bool BF16, bool POOL, int ACT, bool PAIR, bool PADX, bool NHWC, int UPW = 1, bool POLL = false>
 cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes,
                            cudaStream_t stream)
 {
-    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX, NHWC, UPW>;
+    auto kern = conv3x3_fused_kernel<BF16, POOL, ACT, PAIR, PADX, NHWC, UPW, POLL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1381,15 +1385,24 @@ cudaError_t launch_variant(const CUtensorMap& tmx, const ConvArgs& a, int grid, 
                      cudaStream_t stream)
 
 // Single-CTA pooled tiles of four side-by-side units (a.upw == 4); CTA pairs have none.
+// With a shortened (test) wait budget, only the fp32 erf-GELU variant has a polling instantiation.
 template <bool BF16, int ACT, bool PAIR, bool PADX, bool NHWC>
 cudaError_t launch_units4(const CUtensorMap& tmx, const ConvArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream)
 {
-    if constexpr (PAIR) return cudaErrorInvalidValue;
-    else return launch_variant<BF16, true, ACT, false, PADX, NHWC, 4>(tmx, a, grid, smem_bytes, stream);
+    if constexpr (PAIR) {
+        return cudaErrorInvalidValue;
+    } else if constexpr (!BF16 && ACT == 0 && !PADX && !NHWC) {
+        if (a.poll) return launch_variant<BF16, true, ACT, false, PADX, NHWC, 4, true>(tmx, a, grid, smem_bytes, stream);
+        return launch_variant<BF16, true, ACT, false, PADX, NHWC, 4>(tmx, a, grid, smem_bytes, stream);
+    } else {
+        if (a.poll) return cudaErrorNotSupported;
+        return launch_variant<BF16, true, ACT, false, PADX, NHWC, 4>(tmx, a, grid, smem_bytes, stream);
+    }
 }
 
 // The variant switch shared by the translation units.
 #define FC_CONV_LAUNCH_BODY(BF16, PAIR, PADX, NHWC)                                                      \
+    if (a.poll && !(pool && a.upw == 4)) return cudaErrorNotSupported;                                 \
     switch ((pool ? (a.upw == 4 ? 2 : 0) : 1) * 4 + act) {                                              \
     case 0: return launch_variant<BF16, true, 0, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \
     case 1: return launch_variant<BF16, true, 1, PAIR, PADX, NHWC>(tmx, a, grid, smem_bytes, stream);    \

@@ -15,6 +15,18 @@ namespace fc {
 
 // Default spin budget of every mbarrier wait, in SM clock cycles (~1 s at 2 GHz).
 constexpr long long kWaitBudgetCycles = 2000000000LL;
+// Budget of the drains that run after a wait gave up (a kernel waiting for its own copies and
+// MMAs in flight before it frees shared and tensor memory): always the full one, whatever
+// budget the call's waits have.
+constexpr long long kDrainBudgetCycles = kWaitBudgetCycles;
+// The wait budget kernels are launched with: kWaitBudgetCycles, unless a test shortened it
+// through the library's testing hook.
+long long wait_budget();
+// A budget this short comes only from a test; the kernels launched with it poll their barriers
+// (see mbar_wait), and only the single-CTA fp32 pooled erf-GELU conv with 16 x 32 tiles and the
+// single-CTA fp32 Linear chain have such instantiations (other calls then fail with an error).
+constexpr long long kPollBelowCycles = 2000000;
+constexpr bool polling_budget(long long budget) { return budget < kPollBelowCycles; }
 
 // ---------------------------------------------------------------- conv
 

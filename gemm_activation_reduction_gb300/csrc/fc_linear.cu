@@ -91,7 +91,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, long 
     }
 }
 
-template <bool BF16>
+// POLL: the waits poll instead of suspending (see mbar_wait); only launched while a test has
+// shortened the wait budget.
+template <bool BF16, bool POLL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_lse_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                       const __grid_constant__ CUtensorMap tmx_lo, const __grid_constant__ CUtensorMap tmw_lo,
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
                 const int mb = t % a.m_blocks, nb = t / a.m_blocks;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!(ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
+                    if (!(ok = mbar_wait<POLL>(&empty[stage], phase ^ 1u, abort_flag, a.status, a.budget))) break;
                     mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
                     const CUtensorMap* mx;
                     const CUtensorMap* mw;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // after an abort, wait for the most recent fill of each slot to land
                 const long long first = issued > kStages ? issued - kStages : 0;
                 for (long long i = first; i < issued; ++i)
-                    drain_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1), a.budget);
+                    drain_wait(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1), kDrainBudgetCycles);
             }
         }
         __syncwarp();
@@ -189,11 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
-                if (!(ok = mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
+                if (!(ok = mbar_wait<POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!(ok = mbar_wait(&full[stage], phase, abort_flag, a.status, a.budget))) break;
+                    if (!(ok = mbar_wait<POLL>(&full[stage], phase, abort_flag, a.status, a.budget))) break;
                     const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (kABytes >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (kBBytes >> 4);
 #pragma unroll
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mma_commit(&tfull[acc]);
             }
             mma_commit(mdone);
-            drain_wait(mdone, 0, a.budget);
+            drain_wait(mdone, 0, kDrainBudgetCycles);
         }
         __syncwarp();
     } else {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mb = t % a.m_blocks, nb = t / a.m_blocks;
             const int acc = it & 1;
             const uint32_t aph = static_cast<uint32_t>((it >> 1) & 1);
-            const bool ok = mbar_wait(&tfull[acc], aph, abort_flag, a.status, a.budget);
+            const bool ok = mbar_wait<POLL>(&tfull[acc], aph, abort_flag, a.status, a.budget);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 // after an abort, give copies already issued time to land before the CTA exits
                 const long long t0 = clock64();
-                while (clock64() - t0 < a.budget / 8) {
+                while (clock64() - t0 < kDrainBudgetCycles / 8) {
                 }
             }
         }
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit_pair_multicast(mdone, 0x1);
             const long long t0 = clock64();
-            while (!mbar_try_wait(mdone, 0) && clock64() - t0 < a.budget) {
+            while (!mbar_try_wait(mdone, 0) && clock64() - t0 < kDrainBudgetCycles) {
             }
         }
         __syncwarp();
@@ -659,6 +661,7 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
     const void* xl = p.kseg > 0 ? x_lo : x;
     const void* wl = p.kseg > 0 ? W_lo : W;
     if (p.use_pair) {
+        if (polling_budget(budget)) return cudaErrorNotSupported;   // no polling instantiation of the pair kernel
         if (!make_kmajor_map(&tmx, x, p.M, p.K, kPBM, bf16) || !make_kmajor_map(&tmw, W, p.Nout, p.K, p.bn / 2, bf16) ||
             !make_kmajor_map(&tmxl, xl, p.M, p.K, kPBM, bf16) ||
             !make_kmajor_map(&tmwl, wl, p.Nout, p.K, p.bn / 2, bf16))
@@ -703,7 +706,8 @@ cudaError_t linear_launch(const LinearPlan& p, const void* x, const void* W, con
     a.kseg = p.kseg;
     a.scale = scale; a.lo = lo; a.hi = hi;
     a.status = status; a.budget = budget;
-    auto kern = bf16 ? linear_lse_kernel<true> : linear_lse_kernel<false>;
+    if (polling_budget(budget) && bf16) return cudaErrorNotSupported;
+    auto kern = bf16 ? linear_lse_kernel<true> : (polling_budget(budget) ? linear_lse_kernel<false, true> : linear_lse_kernel<false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(p.smem_bytes));
     if (e != cudaSuccess) return e;

@@ -69,6 +69,6 @@ extern "C" fc_status fc_linear_lse_mish_noalloc(const void* x, const void* W, co
     // kernel gives up, in which case the combine writes NaN instead of reading the array.
     cudaError_t e = fc::linear_launch(plan, static_cast<const float*>(x), static_cast<const float*>(W),
                                       static_cast<const float*>(b), y, scale, clamp_lo, clamp_hi, scratch,
-                                      reinterpret_cast<cudaStream_t>(stream), status, fc::kWaitBudgetCycles);
+                                      reinterpret_cast<cudaStream_t>(stream), status, fc::wait_budget());
     return e == cudaSuccess ? FC_OK : FC_ERR_CUDA;
 }

@@ -63,22 +63,54 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking check whether the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Gives up when the
 // CTA-wide abort flag is raised by another role, or after `budget` SM clock
 // cycles, in which case it records FC_ERR_TIMEOUT in the device status word
 // and raises the abort flag.  Returns true when the phase completed.
+// A try_wait may stay suspended until its phase completes, whatever its hint, so a kernel
+// instantiated with POLL polls with test_wait instead: the instantiations a test launches with a
+// shortened budget, which must notice that budget in time.  The kernels launched normally use
+// POLL = false and this exact code path.
+template <bool POLL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, long long budget)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
+    if constexpr (POLL) {
+        const long long t0 = clock64();
+        while (true) {
+            if (mbar_test(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (clock64() - t0 > budget) {
+                *abort_flag = 1;
+                atomicExch(status, FC_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    } else {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > budget) {
-            *abort_flag = 1;
-            atomicExch(status, FC_DEVICE_TIMEOUT);
-            return false;
+        const long long t0 = clock64();
+        while (true) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (clock64() - t0 > budget) {
+                *abort_flag = 1;
+                atomicExch(status, FC_DEVICE_TIMEOUT);
+                return false;
+            }
         }
     }
 }

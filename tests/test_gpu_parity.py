@@ -667,6 +667,41 @@ def test_outputs_are_nan_while_a_timeout_is_recorded(cuda_lib):
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
 
 
+def test_real_operators_give_up_through_their_bounded_waits(cuda_lib):
+    """A short wait budget (set through the library's testing hook, which fc.h does not declare)
+    makes the single-CTA pooled conv kernel and the single-CTA Linear kernel give up mid-pipeline:
+    every role stops at its next wait, drains its own copies and MMAs in flight, and the CTA frees
+    its tensor memory and returns.  The status word then reads FC_ERR_TIMEOUT and the outputs are
+    NaN; with the default budget back, the next calls match the oracle and leave no status."""
+    import torch
+    lib = cuda_lib.load()
+    set_budget = lib.fc_testing_set_wait_budget
+    set_budget.argtypes = [ctypes.c_longlong]
+    set_budget.restype = ctypes.c_longlong
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+    dc = fc_inputs.conv_inputs(16, 8, 128, 128, 64)   # 16 x 32 pooled tiles on single CTAs
+    dl = fc_inputs.linear_inputs(128, 1024, 4096)     # M <= 128: the single-CTA Linear kernel
+    xc, wc, bc = _dev(dc["x"]), _dev(dc["w"]), _dev(dc["b"])
+    xl, wl, bl = _dev(dl["x"]), _dev(dl["W"]), _dev(dl["b"])
+    torch.cuda.synchronize()
+    prev = set_budget(64)   # SM cycles: far below the first TMA load's latency
+    try:
+        yc = cuda_lib.fc_conv3x3_act_pool(xc, wc, bc).cpu().numpy()
+        st_conv = cuda_lib.fc_device_status(clear=True)
+        yl = cuda_lib.fc_linear_lse_mish(xl, wl, bl).cpu().numpy()
+        st_lin = cuda_lib.fc_device_status(clear=True)
+    finally:
+        set_budget(0)
+    assert prev > 10 ** 9
+    assert st_conv == cuda_lib.FC_ERR_TIMEOUT and st_lin == cuda_lib.FC_ERR_TIMEOUT
+    assert np.all(np.isnan(yc)) and np.all(np.isnan(yl))
+    _check(cuda_lib.fc_conv3x3_act_pool(xc, wc, bc).cpu().numpy(),
+           oracle.conv3x3_act_pool(dc["x32"], dc["w32"], dc["b32"], "gelu"), TOL["f32"], "conv after the timeout")
+    _check(cuda_lib.fc_linear_lse_mish(xl, wl, bl).cpu().numpy(), oracle.linear_lse_mish(dl["x"], dl["W"], dl["b"]),
+           TOL["f32"], "linear after the timeout")
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+
+
 @pytest.mark.parametrize("act", ["gelu", "mish", "mish_mish", "gelu_tanh"])
 def test_activation_accuracy_through_a_delta_kernel(cuda_lib, act):
     """A delta 3x3 kernel makes the pre-activation equal to the input (values on a
