@@ -19,7 +19,7 @@ __all__ = [
     "FCError", "load", "build", "library_path",
     "fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
     "fc_conv3x3_act_pool_host", "fc_conv3x3_act_host", "fc_host_staging_bytes",
-    "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version",
+    "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_last_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
     "FC_F32", "FC_BF16", "FC_F32_3XTF32", "FC_NCHW", "FC_NHWC", "ACTS", "OPS",
 ]
@@ -35,7 +35,7 @@ EXPORTS = ("fc_conv3x3_act_pool", "fc_conv3x3_act", "fc_conv3x3_act_pool_ex", "f
            "fc_linear_lse_mish", "fc_linear_lse_mish_noalloc",
            "fc_conv3x3_act_pool_host", "fc_conv3x3_act_host", "fc_host_staging_bytes",
            "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_workspace_bytes_ex",
-           "fc_status_string", "fc_device_status", "fc_selftest_watchdog", "fc_version")
+           "fc_status_string", "fc_device_status", "fc_last_device_status", "fc_selftest_watchdog", "fc_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +99,8 @@ def load():
         lib.fc_status_string.restype = ctypes.c_char_p
         lib.fc_device_status.argtypes = [I]
         lib.fc_device_status.restype = I
+        lib.fc_last_device_status.argtypes = [P]
+        lib.fc_last_device_status.restype = I
         lib.fc_selftest_watchdog.argtypes = [Z, P]
         lib.fc_selftest_watchdog.restype = I
         lib.fc_version.restype = I
@@ -353,6 +355,12 @@ def fc_linear_lse_mish(x, W, b, scale: float = 2.0, clamp_lo: float = -10.0, cla
 def fc_device_status(clear: bool = True) -> int:
     """Synchronize the current device and return (and by default clear) its watchdog word."""
     return int(load().fc_device_status(1 if clear else 0))
+
+
+def fc_last_device_status(stream=None) -> int:
+    """The watchdog word once `stream`'s enqueued work has finished (other streams are not waited
+    for, and the word is not cleared)."""
+    return int(load().fc_last_device_status(_stream_handle(stream)))
 
 
 def fc_selftest_watchdog(budget_cycles: int, stream=None) -> None:

@@ -303,6 +303,19 @@ fc_status fc_device_status(int clear)
     return v == 0 ? FC_OK : static_cast<fc_status>(v);
 }
 
+fc_status fc_last_device_status(fc_stream_t stream)
+{
+    DeviceState* d = nullptr;
+    fc_status st = device_state(&d);
+    if (st != FC_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    // read on the stream itself: ordered after its enqueued work, and only that stream waits
+    if (cudaMemcpyAsync(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FC_ERR_CUDA;
+    return v == 0 ? FC_OK : static_cast<fc_status>(v);
+}
+
 fc_status fc_selftest_watchdog(unsigned long long budget_cycles, fc_stream_t stream)
 {
     DeviceState* d = nullptr;

@@ -299,6 +299,14 @@ const char* fc_status_string(fc_status status);
 fc_status fc_device_status(int clear);
 
 /*
+ * The same word read after the work enqueued on `stream` so far has finished,
+ * without synchronizing the rest of the device, and without clearing it (the
+ * word is shared by every stream of the device; fc_device_status(1) clears it).
+ * Returns FC_OK, FC_ERR_TIMEOUT, or FC_ERR_CUDA if the stream or the read fails.
+ */
+fc_status fc_last_device_status(fc_stream_t stream);
+
+/*
  * Self-test of the watchdog path: enqueues one tiny kernel that waits on an
  * mbarrier nothing will ever arrive on, with a budget of `budget_cycles`
  * SM clock cycles.  The wait must give up, record FC_ERR_TIMEOUT and return.

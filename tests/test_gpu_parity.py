@@ -648,6 +648,20 @@ def test_watchdog_times_out_and_context_stays_usable(cuda_lib):
     assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
 
 
+def test_stream_scoped_status_sees_a_timeout_on_its_stream(cuda_lib):
+    """fc_last_device_status(stream) waits for that stream only and reads the word without
+    clearing it."""
+    import torch
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_OK
+    s = torch.cuda.Stream()
+    assert cuda_lib.fc_last_device_status(s) == cuda_lib.FC_OK
+    cuda_lib.fc_selftest_watchdog(2_000_000, stream=s)
+    assert cuda_lib.fc_last_device_status(s) == cuda_lib.FC_ERR_TIMEOUT
+    assert cuda_lib.fc_last_device_status(s) == cuda_lib.FC_ERR_TIMEOUT   # not cleared
+    assert cuda_lib.fc_device_status(clear=True) == cuda_lib.FC_ERR_TIMEOUT
+    assert cuda_lib.fc_last_device_status(s) == cuda_lib.FC_OK
+
+
 def test_outputs_are_nan_while_a_timeout_is_recorded(cuda_lib):
     """A recorded timeout (made by the watchdog self-test's bounded wait, no fault) means some
     kernel's partial results may be missing: the pooled conv and the Linear chain then write NaN
