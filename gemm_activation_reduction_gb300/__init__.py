@@ -21,10 +21,11 @@ __all__ = [
     "fc_conv3x3_act_pool_host", "fc_conv3x3_act_host", "fc_host_staging_bytes",
     "fc_act_map", "fc_act_mean", "fc_scale_clamp_lse_mish", "fc_workspace_bytes", "fc_status_string", "fc_device_status", "fc_last_device_status", "fc_selftest_watchdog", "fc_version",
     "FC_OK", "FC_ERR_INVALID_ARG", "FC_ERR_UNSUPPORTED", "FC_ERR_WORKSPACE", "FC_ERR_CUDA", "FC_ERR_TIMEOUT",
+    "FC_ERR_BOUNDS",
     "FC_F32", "FC_BF16", "FC_F32_3XTF32", "FC_NCHW", "FC_NHWC", "ACTS", "OPS",
 ]
 
-FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT = range(6)
+FC_OK, FC_ERR_INVALID_ARG, FC_ERR_UNSUPPORTED, FC_ERR_WORKSPACE, FC_ERR_CUDA, FC_ERR_TIMEOUT, FC_ERR_BOUNDS = range(7)
 FC_F32, FC_BF16, FC_F32_3XTF32 = 0, 1, 2
 FC_NCHW, FC_NHWC = 0, 1
 ACTS = {"gelu": 0, "mish": 1, "mish_mish": 2, "gelu_tanh": 3}

@@ -1,7 +1,9 @@
 """In-tree build of the CUDA library (sm_103a only).
 
 Compiles every ``csrc/*.cu`` translation unit in parallel with nvcc and links
-them into ``_build/libfcgb300.so``.  No cmake, one ``-gencode``.
+them into ``_build/libfcgb300.so``.  No cmake, one ``-gencode``.  ``debug=True``
+builds the same sources with ``-DFC_DEBUG`` (kernel index checks that record
+FC_ERR_BOUNDS and skip the access) into ``_build/debug/libfcgb300_debug.so``.
 """
 from __future__ import annotations
 
@@ -17,6 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIB_NAME = "libfcgb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
+BUILD_DEBUG = os.path.join(BUILD, "debug")
+LIB_DEBUG_PATH = os.path.join(BUILD_DEBUG, "libfcgb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -39,22 +43,27 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(debug: bool = False) -> bool:
+    lib = LIB_DEBUG_PATH if debug else LIB_PATH
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link the library (or, with debug, its FC_DEBUG build); returns its path."""
+    if not force and up_to_date(debug):
+        return LIB_DEBUG_PATH if debug else LIB_PATH
+    out_dir = BUILD_DEBUG if debug else BUILD
+    lib_path = LIB_DEBUG_PATH if debug else LIB_PATH
+    if debug:
+        extra_flags = (*extra_flags, "-DFC_DEBUG")
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -284,6 +284,7 @@ const char* fc_status_string(fc_status s)
     case FC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case FC_ERR_CUDA: return "CUDA error";
     case FC_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    case FC_ERR_BOUNDS: return "a kernel's index check failed (FC_DEBUG build)";
     default: return "unknown status";
     }
 }

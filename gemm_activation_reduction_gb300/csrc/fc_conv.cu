@@ -95,14 +95,15 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
 // records in order, and a fixed shuffle tree adds the lanes -- the same order on every run.
 __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Co, int Cout, long long tpi,
                                          long long pbase, int prem, int J, int step, int recs, double inv_count,
-                                         const int* status)
+                                         int* status, int grid)
 {
     pdl_wait();   // the fused kernel's records are complete and visible
     const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= static_cast<long long>(N) * Co) return;   // whole warps leave together
-    // a bounded wait that gave up leaves records the fused kernel never wrote: say so in the output
-    if (*reinterpret_cast<const volatile int*>(status) == FC_DEVICE_TIMEOUT) {
+    // a bounded wait that gave up (or a failed index check of a debug build) leaves records the
+    // fused kernel never wrote: say so in the output
+    if (*reinterpret_cast<const volatile int*>(status) != 0) {
         if (lane == 0) y[wid] = __int_as_float(0x7fc00000);
         return;
     }
@@ -124,7 +125,8 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
         const long long nf = (step * start_of(c) + r) / tpi;
         const long long slot = n - nf;
         if (slot < 0 || slot >= J) continue;
-        s += static_cast<double>(ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
+        if (FC_DEBUG_OK(cta >= 0 && cta < grid && q < recs && co < Cout, status))
+            s += static_cast<double>(ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -392,7 +394,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, conv_pool_combine_kernel, static_cast<const float*>(pool_ws), y, p.N, p.Co,
                                p.Cout, p.tpi, p.pbase, p.prem, p.J, p.pair ? 2 : 1, 4 * p.egroups,
-                               1.0 / (static_cast<double>(p.OH) * p.OW), static_cast<const int*>(status));
+                               1.0 / (static_cast<double>(p.OH) * p.OW), status, p.grid);
     }
     return e;
 }

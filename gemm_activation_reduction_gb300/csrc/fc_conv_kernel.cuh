@@ -815,6 +815,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                         mbar_arrive(&full[slot]);
                     }
                 }
+                if (!FC_DEBUG_OK(slot < S_ && cb < a.ncb, a.status)) {
+                    *abort_flag = 1;   // the other roles stop at their next wait, the status kept
+                    break;
+                }
                 const uint32_t strip = strip0 + slot * S::STRIP;
                 if (NHWC && !a.use_tma) {
                     fill_strip_nhwc<BF16, WIDE, ROWS, UPW>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
@@ -826,6 +830,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     const uint32_t r = raw_buf(use);
                     ok = mbar_wait<POLL>(&rawfull[r], (use / static_cast<uint32_t>(rd)) & 1u, abort_flag, a.status, a.budget);
                     if (!__all_sync(0xffffffffu, ok)) break;
+                    if (!FC_DEBUG_OK(r < static_cast<uint32_t>(kNumProd * rd), a.status)) {
+                        *abort_flag = 1;
+                        break;
+                    }
                     const uint32_t raw = smem_u32(smem + a.raw_off) + r * kRawBytes;
                     // split TF32: the third stage of each K block stages x's remainder
                     if constexpr (NHWC) {
@@ -903,6 +911,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 ok = wait_bar<PAIR, POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
+                if (!(ok = FC_DEBUG_OK((acc + 1) * a.Cout <= a.tmem_cols && slot < static_cast<uint32_t>(a.stages), a.status))) {
+                    *abort_flag = 1;
+                    break;
+                }
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * a.Cout);
                 // bias (+ padding) K step, overwriting the accumulator
                 issue_mma<BF16, PAIR>(d, unit_ind(tc, 0), bb_desc, idesc, 0u);
@@ -934,6 +946,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
 #pragma unroll
                 for (int u = 0; u < UPT; ++u) {
                     accu[u] = acc;
+                    if (!FC_DEBUG_OK((acc + 1) * a.Cout <= a.tmem_cols, a.status)) {
+                        ok = false;
+                        *abort_flag = 1;
+                    }
                     d[u] = tmem + static_cast<uint32_t>(acc * a.Cout);
                     ok = ok && wait_bar<PAIR, POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
                     if (++acc == a.nacc) {
@@ -1016,6 +1032,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                        static_cast<size_t>(a.Cout);
         };
         auto zero_slot = [&](int sl) {
+            if (!FC_DEBUG_OK(sl >= 0 && sl < a.J, a.status)) return;
             float* dst = record(sl);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -1039,7 +1056,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                             v4[e] += __shfl_xor_sync(0xffffffffu, v4[e], 8);
                             v4[e] += __shfl_xor_sync(0xffffffffu, v4[e], 16);
                         }
-                        if (lane < 4) {
+                        if (lane < 4 && FC_DEBUG_OK(n_img - n_first >= 0 && n_img - n_first < a.J, a.status)) {
                             float* o = dst + c * kEpiCols + 2 * lane;
                             o[0] = v4[0] * kActScale<ACT>;
                             o[1] = v4[1] * kActScale<ACT>;
@@ -1239,7 +1256,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                                     float2 g = act2<ACT>(make_float2(__uint_as_float(cur[base]), __uint_as_float(cur[base + 1])));
                                     if constexpr (ACT == 0) g = __fmul2_rn(g, splat2(kActScale<ACT>));
                                     const int ch = c * kEpiCols + 8 * u + 2 * (lane & 3);
-                                    if (valid && ch < a.Co) {
+                                    if (valid && ch < a.Co && FC_DEBUG_OK(tc.n < a.N && oh >= 0 && ow >= 0, a.status)) {
                                         float* o = a.out + ((static_cast<size_t>(tc.n) * a.OH + oh) * a.OW + ow) *
                                                                static_cast<size_t>(a.Co) + ch;
                                         if (pairs_ok) {
@@ -1312,7 +1329,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     if (k + 1 < ms) tmem_ld16_start(taddr(acc, k + 1), rnext);
                     else release_and_next();
                     if constexpr (!POOL) {
-                        if (valid) {
+                        if (valid && FC_DEBUG_OK(tc.n < a.N && c * kEpiCols < a.Co && oh >= 0 && ow >= 0, a.status)) {
                             float* o = a.out + ((static_cast<size_t>(tc.n) * a.Co + c * kEpiCols) * a.OH + oh) *
                                                    static_cast<size_t>(a.OW) + ow;
                             const size_t plane = static_cast<size_t>(a.OH) * a.OW;

@@ -10,6 +10,18 @@
 // Value a kernel writes into the device status word when a bounded wait runs
 // out; equal to FC_ERR_TIMEOUT of the public header.
 #define FC_DEVICE_TIMEOUT 5
+// Value a kernel of an FC_DEBUG build writes there when one of its index checks fails (the
+// checked access is then skipped); equal to FC_ERR_BOUNDS of the public header.
+#define FC_DEVICE_BOUNDS 6
+
+// FC_DEBUG_OK(cond, status): true when `cond` holds.  In an FC_DEBUG build a false `cond`
+// records FC_DEVICE_BOUNDS in the status word and the caller skips the guarded access; in
+// other builds the check compiles to `true` and costs nothing.
+#ifdef FC_DEBUG
+#define FC_DEBUG_OK(cond, status) ((cond) || (atomicExch((status), FC_DEVICE_BOUNDS), false))
+#else
+#define FC_DEBUG_OK(cond, status) true
+#endif
 
 namespace fc {
 

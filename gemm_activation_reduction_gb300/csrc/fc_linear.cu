@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
             const int m = mb * kBM + row;
-            if (m < a.M) a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
+            if (m < a.M && FC_DEBUG_OK(nb < a.n_blocks, a.status))
+                a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
         }
     }
 
@@ -471,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
             const int m = mp * 2 * kPBM + static_cast<int>(rank) * kPBM + row;
-            if (m < a.M) a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
+            if (m < a.M && FC_DEBUG_OK(nb < a.n_blocks, a.status))
+                a.partials[static_cast<size_t>(nb) * a.M + m] = make_float2(run_m, run_s);
         }
     }
 
@@ -485,13 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge the per-column-tile (max, sum) pairs of each row in fixed order, then
 // lse = M + log S and y = lse * mish(lse), mish(l) = l * tanh(softplus(l)).
-__global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks, const int* status)
+__global__ void lse_combine_kernel(const float2* partials, float* y, int M, int n_blocks, int* status)
 {
     pdl_wait();   // the GEMM's partials are complete and visible
     const int m = blockIdx.x * blockDim.x + threadIdx.x;
     if (m >= M) return;
-    // a bounded wait that gave up leaves partials the GEMM never wrote: say so in the output
-    if (*reinterpret_cast<const volatile int*>(status) == FC_DEVICE_TIMEOUT) {
+    // a bounded wait that gave up (or a failed index check of a debug build) leaves partials the
+    // GEMM never wrote: say so in the output
+    if (*reinterpret_cast<const volatile int*>(status) != 0) {
         y[m] = __int_as_float(0x7fc00000);
         return;
     }
@@ -509,7 +512,7 @@ __global__ void lse_combine_kernel(const float2* partials, float* y, int M, int 
 
 // The row combine, launched so that it may start while the GEMM finishes (it waits for the
 // partials itself).
-cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_blocks, const int* status,
+cudaError_t launch_lse_combine(const float2* partials, float* y, int M, int n_blocks, int* status,
                                cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg{};

@@ -54,7 +54,9 @@ typedef enum {
     FC_ERR_UNSUPPORTED = 2,   /* valid request outside the shapes the kernels cover */
     FC_ERR_WORKSPACE = 3,     /* workspace missing or smaller than fc_workspace_bytes() */
     FC_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
-    FC_ERR_TIMEOUT = 5        /* a kernel's bounded wait ran out (see fc_device_status) */
+    FC_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (see fc_device_status) */
+    FC_ERR_BOUNDS = 6         /* FC_DEBUG builds only: a kernel's index check failed and the
+                                 access was skipped (see fc_device_status) */
 } fc_status;
 
 typedef enum {
@@ -290,7 +292,7 @@ const char* fc_status_string(fc_status status);
  * Watchdog word of the current device.  Every spin-wait in the kernels is
  * bounded; on expiry a kernel records FC_ERR_TIMEOUT here, stops its loops,
  * drains its own copies and returns (the context stays usable).  While the
- * word holds FC_ERR_TIMEOUT, the pooled conv and Linear operators write NaN
+ * word holds FC_ERR_TIMEOUT (or FC_ERR_BOUNDS), the pooled conv and Linear operators write NaN
  * to their outputs (their partial results cannot be trusted); a full-output
  * conv whose kernel gave up leaves its output undefined.  This call
  * synchronizes the device, returns the recorded status (FC_OK if none) and,

@@ -40,6 +40,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 def test_status_strings_and_version():
     assert fc.fc_status_string(fc.FC_OK) == "ok"
     assert "timed out" in fc.fc_status_string(fc.FC_ERR_TIMEOUT)
+    assert "index check" in fc.fc_status_string(fc.FC_ERR_BOUNDS)
     assert fc.fc_version() >= 100
 
 
