@@ -145,72 +145,104 @@ __global__ void __launch_bounds__(kRedThreads) act_mean_kernel(const void* v, fl
     if (threadIdx.x == 0) y[p] = tot * kActScale<ACT> / static_cast<float>(plane);
 }
 
-// Merge two online (max, sum of exp(x - max)) pairs.
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2)
+// Three-input maximum (one instruction on sm_100 and later); NaN inputs are ignored.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Merge two online (max, sum of 2^(x - max)) pairs of base-2 logsumexp.
+__device__ __forceinline__ void lse2_merge(float& m, float& s, float m2, float s2)
 {
     const float nm = fmaxf(m, m2);
     if (nm == -INFINITY) return;
-    s = s * __expf(m - nm) + s2 * __expf(m2 - nm);
+    s = s * convk::ex2_approx(m - nm) + s2 * convk::ex2_approx(m2 - nm);
     m = nm;
 }
 
-// One CTA per row: t = clamp(y * scale + y * scale, lo, hi); online max / sum over the row
-// (16-byte loads when the row is aligned), merged in a fixed order; then l = m + log s and
-// out[m] = l * mish(l) = l^2 tanh(softplus(l)).
-__global__ void __launch_bounds__(kRedThreads) lse_row_kernel(const float* t, float* out, int N, float scale, float lo,
-                                                           float hi)
+constexpr float kLn2 = 0.69314718055994531f;
+
+// One CTA per row.  The row's logsumexp of u = clamp(y * scale + y * scale, lo, hi) is taken in
+// base 2: w = y * k2 with k2 = 2 scale log2(e), clamped to [lo2, hi2] = [lo, hi] log2(e), and
+// l = ln 2 (max w + log2 sum 2^(w - max w)).  Since clamping is monotone, the max is taken over
+// the unclamped w (three at a time) and clamped once; each term is then 2^-d with
+// d = clamp(cm - w, 0, cm - lo2), which equals cm - clamp(w, lo2, hi2) exactly (a NaN input
+// counts as lo, as clamp(NaN) = lo does for fminf / fmaxf).  Per element that is a paired
+// multiply, a third of a max, a paired subtract, two min/max, one ex2 and half a paired add:
+// the ex2 unit (16 per clock per SM) is the arithmetic bound, below the HBM time at 8192
+// columns.  Up to 8 of a thread's 16-byte chunks are loaded before any is reduced; missing
+// chunks of a short batch add nothing.  out[m] = l * mish(l) = l^2 tanh(softplus(l)).
+// Launched as a programmatic dependent: the wait comes before the first read of t.
+__global__ void __launch_bounds__(kRedThreads) lse_row_kernel(const float* t, float* out, int N, float k2, float lo2,
+                                                           float hi2)
 {
     __shared__ float red_m[kRedThreads / 32], red_s[kRedThreads / 32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float* row = t + static_cast<long long>(blockIdx.x) * N;
     float m = -INFINITY, s = 0.0f;
-    auto take = [&](float yv) {
-        float u = yv * scale;
-        u = u + u;
-        u = fminf(fmaxf(u, lo), hi);
-        if (u > m) {
-            s = s * __expf(m - u) + 1.0f;
-            m = u;
-        } else {
-            s += __expf(u - m);
-        }
-    };
     int done = 0;
     if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
-        // up to 8 of this thread's 16-byte chunks loaded before any is reduced
         const int quads = N / 4;
         for (int q0 = threadIdx.x; q0 < quads; q0 += 8 * kRedThreads) {
-            // the chunk's clamped values, their max, then the exponentials independently of
-            // each other (missing chunks count as -inf)
-            float u[32];
+            float2 w[16];
+            bool have[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
-                float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                const bool have = q0 + h * kRedThreads < quads;
-                if (have) v = __ldcs(reinterpret_cast<const float4*>(row) + q0 + h * kRedThreads);
-                const float e[4] = {v.x, v.y, v.z, v.w};
+                have[h] = q0 + h * kRedThreads < quads;
+                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (have[h]) v = __ldcs(reinterpret_cast<const float4*>(row) + q0 + h * kRedThreads);
+                w[2 * h] = __fmul2_rn(make_float2(v.x, v.y), make_float2(k2, k2));
+                w[2 * h + 1] = __fmul2_rn(make_float2(v.z, v.w), make_float2(k2, k2));
+                if (!have[h]) w[2 * h] = w[2 * h + 1] = make_float2(-INFINITY, -INFINITY);
+            }
+            float a0 = max3(w[0].x, w[0].y, w[1].x), a1 = max3(w[1].y, w[2].x, w[2].y);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float w = e[k] * scale;
-                    w = w + w;
-                    u[4 * h + k] = have ? fminf(fmaxf(w, lo), hi) : -INFINITY;
+            for (int k = 3; k < 15; k += 3) {
+                a0 = max3(a0, w[k].x, w[k].y);
+                a1 = max3(a1, w[k + 1].x, w[k + 1].y);
+                a0 = max3(a0, w[k + 2].x, w[k + 2].y);
+            }
+            const float cm = fminf(fmaxf(max3(a0, a1, fmaxf(w[15].x, w[15].y)), lo2), hi2);
+            const float dl = cm - lo2;
+            float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float2 d = __fadd2_rn(make_float2(cm, cm), make_float2(-w[2 * h + j].x, -w[2 * h + j].y));
+                    d.x = fmaxf(fminf(d.x, dl), 0.0f);
+                    d.y = fmaxf(fminf(d.y, dl), 0.0f);
+                    float2 e = make_float2(convk::ex2_approx(-d.x), convk::ex2_approx(-d.y));
+                    if (!have[h]) e = make_float2(0.0f, 0.0f);
+                    if (j == 0)
+                        acc0 = __fadd2_rn(acc0, e);
+                    else
+                        acc1 = __fadd2_rn(acc1, e);
                 }
             }
-            float cm = u[0];
-#pragma unroll
-            for (int k = 1; k < 32; ++k) cm = fmaxf(cm, u[k]);
-            float cs = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) cs += __expf(u[k] - cm);
-            lse_merge(m, s, cm, cs);
+            const float2 acc = __fadd2_rn(acc0, acc1);
+            lse2_merge(m, s, cm, acc.x + acc.y);
         }
         done = quads * 4;
     }
-    for (int j = done + threadIdx.x; j < N; j += kRedThreads) take(row[j]);
+    // rows that are not 16-byte aligned, and the N % 4 tail: one element at a time
+    for (int j = done + threadIdx.x; j < N; j += kRedThreads) {
+        const float w = fminf(fmaxf(row[j] * k2, lo2), hi2);
+        if (w > m) {
+            s = s * convk::ex2_approx(m - w) + 1.0f;
+            m = w;
+        } else {
+            s += convk::ex2_approx(w - m);
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
         const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        lse_merge(m, s, m2, s2);
+        lse2_merge(m, s, m2, s2);
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -220,8 +252,8 @@ __global__ void __launch_bounds__(kRedThreads) lse_row_kernel(const float* t, fl
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = red_m[0], S = red_s[0];
-        for (int w = 1; w < kRedThreads / 32; ++w) lse_merge(M, S, red_m[w], red_s[w]);
-        const float l = M + logf(S);
+        for (int w = 1; w < kRedThreads / 32; ++w) lse2_merge(M, S, red_m[w], red_s[w]);
+        const float l = (M + log2f(S)) * kLn2;
         const float sp = fmaxf(l, 0.0f) + log1pf(expf(-fabsf(l)));
         out[blockIdx.x] = l * (l * tanhf(sp));
     }
@@ -276,8 +308,23 @@ cudaError_t act_mean_launch(const void* v, float* y, long long planes, long long
 cudaError_t lse_row_launch(const float* t, float* out, int M, int N, float scale, float lo, float hi, cudaStream_t st)
 {
     if (M <= 0) return cudaSuccess;
-    lse_row_kernel<<<M, kRedThreads, 0, st>>>(t, out, N, scale, lo, hi);
-    return cudaGetLastError();
+    // the base-2 constants, each rounded once from double
+    const double log2e = 1.4426950408889634;
+    const float k2 = static_cast<float>(2.0 * static_cast<double>(scale) * log2e);
+    const float lo2 = static_cast<float>(static_cast<double>(lo) * log2e);
+    const float hi2 = static_cast<float>(static_cast<double>(hi) * log2e);
+    // a programmatic dependent launch: the CTAs may be scheduled while the previous kernel on
+    // the stream finishes; each waits for its results before reading t
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(kRedThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lse_row_kernel, t, out, N, k2, lo2, hi2);
 }
 
 }  // namespace fc

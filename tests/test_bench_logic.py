@@ -86,3 +86,10 @@ def test_host_only_sources_do_not_move_the_kernel_hash(tmp_path, monkeypatch):
     assert bench.kernel_sources_hash() == h0
     (csrc / "fc_conv.cu").write_text("__global__ void k() { }\n")
     assert bench.kernel_sources_hash() != h0
+
+
+def test_inputs_smaller_than_l2_are_rotated_over_copies_twice_its_size():
+    k3e = fc_inputs.WORKLOADS["K3e"].compulsory_bytes()          # 1024 x 8192 fp32 rows, 33.6 MB
+    n = bench.rotation_copies(k3e)
+    assert n == 8 and n * k3e >= 2 * bench.L2_BYTES > (n - 1) * k3e
+    assert bench.rotation_copies(fc_inputs.WORKLOADS["K1e"].compulsory_bytes()) == 1   # 2.1 GB: one copy
