@@ -160,7 +160,7 @@ Geometry geometry_xp(int bf16, int pool, int pair, int upw)
         return bf16 ? geometry_of<true, false, 1, XPB, false, 4>() : geometry_of<false, false, 1, XPF, false, 4>();
     if (pool) return bf16 ? geometry_of<true, false, 1, XPB>() : geometry_of<false, false, 1, XPF>();
     if (pair) return bf16 ? geometry_of<true, true, 1, XPB>() : geometry_of<false, true, 1, XPF>();
-    return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, XPF>();
+    return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, staged_xp(false, true, 2, XPF != 0, false)>();
 }
 
 // padx: the padding's column shift needs XP = 4 (fp32) / 8 (bf16) extra staged columns

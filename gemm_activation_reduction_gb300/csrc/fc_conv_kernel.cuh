@@ -94,11 +94,19 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // With zero padding p the staged patch starts p rows above and p + d columns left of the
 // tile, d = (-p) mod (16 B / element size), so that the TMA box starts on a 16-byte
 // boundary; XP = 4 (fp32) or 8 (bf16) extra staged columns hold the d-column shift and
-// every MMA operand starts d staged pixels further (XP = 0 when d is always 0).
+// every MMA operand starts d staged pixels further (XP = 0 when d is always 0).  fp32 two-row
+// full-output tiles stage an odd number of columns instead (XP = 1, or 5 with the shift:
+// 131 or 135): the re-layout then maps a quarter-warp to 4 rows x 2 column quads whose
+// 16-byte strip stores, 16 * SC bytes per row apart, fall in 8 different bank groups.
 //
 // NHWC input: a K block lands as one TMA box [SR rows][SC columns][32 B of channels] and is
 // split into the two planes; NHWC planes are 64 bytes past a 128-byte multiple apart so that
 // the split's 128-bit stores of one phase (4 pixels x 2 planes) cover all banks.
+__host__ __device__ constexpr int staged_xp(bool bf16, bool wide, int rows, bool padx, bool nhwc)
+{
+    return nhwc ? 0 : (!bf16 && wide && rows == 2) ? (padx ? 5 : 1) : (padx ? (bf16 ? 8 : 4) : 0);
+}
+
 template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false, int UPW = 1>
 struct Shape {
     static constexpr int UNITS = WIDE ? ROWS : UPW;        // M = 128 MMA units per tile
@@ -117,12 +125,17 @@ struct Shape {
 };
 
 // Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
-// order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.
+// order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.  The
+// fp32 two-row full-output box is 8 columns past a multiple of 32 wide (136 for 131 or 135
+// staged columns), so that the re-layout's 16-byte reads of a quarter-warp (4 rows x 2
+// column quads) fall in 8 different bank groups too.
 template <bool BF16, bool WIDE, int ROWS = 1, int XP = 0, int UPW = 1>
 struct RawBox {
     using S = Shape<WIDE, ROWS, XP, false, UPW>;
+    static constexpr bool kQuarterMap = !BF16 && WIDE && ROWS == 2;
     static constexpr int kCh = BF16 ? 16 : 8;
-    static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8 : (S::SC + 3) / 4 * 4;
+    static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8
+                                      : (kQuarterMap ? (S::SC - 8 + 31) / 32 * 32 + 8 : (S::SC + 3) / 4 * 4);
     static constexpr uint32_t kChPlane = S::SR * kCols * (BF16 ? 2 : 4);
     static constexpr uint32_t kBytes = (kCh * kChPlane + 127) / 128 * 128;
 };
@@ -288,14 +301,14 @@ __device__ __forceinline__ float2 ld_shared_f2(uint32_t addr)
 }
 
 // Re-lay a landed raw box into the staged strip [group][SPOS pixels][16 B].
-// The TF32 operand of x for one split-TF32 part: the high part (x rounded to TF32) or,
-// with LO, the remainder x - hi rounded to TF32.
+// The TF32 operand of x for one split-TF32 part.  The high part is x as stored: the tensor core
+// reads an fp32 word as TF32 by dropping its 13 low mantissa bits (as the Linear op's operands,
+// which TMA hands to the MMA untouched); with LO, the remainder x - trunc(x) rounded to TF32.
 template <bool LO>
 __device__ __forceinline__ uint32_t tf32_part(float v)
 {
-    const float hi = to_tf32(v);
-    if constexpr (LO) return __float_as_uint(to_tf32(v - hi));
-    else return __float_as_uint(hi);
+    if constexpr (LO) return __float_as_uint(to_tf32(v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u)));
+    else return __float_as_uint(v);
 }
 
 template <bool BF16, bool WIDE, int ROWS, int XP, bool LO, int UPW>
@@ -304,7 +317,41 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
     using S = Shape<WIDE, ROWS, XP, false, UPW>;
     using RB_ = RawBox<BF16, WIDE, ROWS, XP, UPW>;
     static_assert(!(BF16 && LO), "split TF32 is an fp32 mode");
-    if constexpr (!BF16) {
+    if constexpr (RB_::kQuarterMap) {
+        // fp32 two-row full-output tiles: item = (group g, staged row, column quad), 4 channels x
+        // 4 pixels -> four 16-byte rows; a quarter-warp takes the 4 staged rows x 2 adjacent
+        // quads of one (g, quad pair), so that with SC odd and the box 8 columns past a multiple
+        // of 32 wide both its 16-byte reads and its 16-byte stores hit 8 different bank groups
+        static_assert(S::SR == 4 && S::SC % 2 == 1 && RB_::kCols % 32 == 8 && RB_::kCols >= S::SC, "quarter map");
+        constexpr int kQuads = (S::SC + 3) / 4;
+        constexpr int kPairs = (kQuads + 1) / 2;
+        const int row = lane & 3;
+        const int cq_lo = (lane >> 2) & 1;
+#pragma unroll 2
+        for (int qs = lane >> 3; qs < 2 * kPairs; qs += 4) {
+            const int g = qs >= kPairs ? 1 : 0;
+            const int cq = 2 * (qs - g * kPairs) + cq_lo;
+            if (cq < kQuads) {
+                const uint32_t src = raw + static_cast<uint32_t>(4 * g) * RB_::kChPlane +
+                                     static_cast<uint32_t>(row * RB_::kCols + 4 * cq) * 4u;
+                float4 v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = ld_shared_f4(src + static_cast<uint32_t>(c) * RB_::kChPlane);
+                const uint32_t dst = strip + static_cast<uint32_t>(g) * S::PLANE +
+                                     static_cast<uint32_t>(row * S::SC + 4 * cq) * 16u;
+                st_shared_v4(dst, tf32_part<LO>(v[0].x), tf32_part<LO>(v[1].x), tf32_part<LO>(v[2].x),
+                             tf32_part<LO>(v[3].x));
+                st_shared_v4(dst + 16u, tf32_part<LO>(v[0].y), tf32_part<LO>(v[1].y), tf32_part<LO>(v[2].y),
+                             tf32_part<LO>(v[3].y));
+                if (4 * cq + 2 < S::SC)
+                    st_shared_v4(dst + 32u, tf32_part<LO>(v[0].z), tf32_part<LO>(v[1].z), tf32_part<LO>(v[2].z),
+                                 tf32_part<LO>(v[3].z));
+                if (4 * cq + 3 < S::SC)
+                    st_shared_v4(dst + 48u, tf32_part<LO>(v[0].w), tf32_part<LO>(v[1].w), tf32_part<LO>(v[2].w),
+                                 tf32_part<LO>(v[3].w));
+            }
+        }
+    } else if constexpr (!BF16) {
         // item = (group g, staged row, column quad): 4 channels x 4 pixels -> four 16-byte rows
         // (the last quad of a row holds SC % 4 staged pixels; the raw box is wider)
         static_assert(RB_::kCols % 4 == 0 && RB_::kChPlane % 16 == 0, "16-byte raw reads");
@@ -640,7 +687,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // and weight block); CTA pairs keep one row per CTA
     constexpr int ROWS = (WIDE && !PAIR) ? 2 : 1;
     // room for the padding's column shift a.dcol (< 16 B of elements) when it is not 0
-    constexpr int XP = PADX ? (BF16 ? 8 : 4) : 0;
+    constexpr int XP = staged_xp(BF16, WIDE, ROWS, PADX, NHWC);
     static_assert(!(PADX && NHWC), "NHWC boxes start at any column: no shift room needed");
     static_assert(UPW == 1 || (POOL && !PAIR), "side-by-side units: single-CTA pooled tiles only");
     using S = Shape<WIDE, ROWS, XP, NHWC, UPW>;

@@ -27,9 +27,10 @@
  *   - `workspace` is caller-owned device scratch of at least
  *     fc_workspace_bytes(...) bytes (256-byte aligned); its contents on entry
  *     do not matter.  Two calls that share a workspace must not overlap.
- *   - Floating point: fp32 inputs run on TF32 tensor cores (the conv ops
- *     round operands to nearest TF32; the Linear op's tensor core truncates
- *     them), bf16 inputs on BF16 tensor cores; accumulation, activation and
+ *   - Floating point: fp32 inputs run on TF32 tensor cores (the tensor core
+ *     reads x, and the Linear op's W, as stored, dropping 13 low mantissa
+ *     bits; the conv ops' weights are rounded to nearest TF32 by their per-call
+ *     weight re-layout), bf16 inputs on BF16 tensor cores; accumulation, activation and
  *     reduction are fp32; outputs are fp32.  FC_F32_3XTF32 takes the same fp32
  *     inputs but splits each operand into a TF32 high part and a TF32
  *     remainder and sums three products per term (hi*hi + hi*lo + lo*hi),

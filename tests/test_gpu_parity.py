@@ -394,9 +394,10 @@ def test_linear_small_bf16(cuda_lib, shape):
 
 # ------------------------------------------------------------------ TF32 diagnostic mode
 
-# With the oracle fed the operands the tensor cores actually multiply -- the conv path rounds fp32
-# operands to nearest TF32 (ties away from zero), the linear path's tensor core drops the 13 low
-# mantissa bits of raw fp32 -- the products are exact in fp32 and what remains is the fp32
+# With the oracle fed the operands the tensor cores actually multiply -- the tensor core drops the
+# 13 low mantissa bits of the raw fp32 it is handed (x of both ops, W of the linear op), the conv
+# path's weight re-layout rounds w to nearest TF32 (ties away from zero) -- the products are exact
+# in fp32 and what remains is the fp32
 # accumulation of K <= 1024 terms (about 2^-24 of the running sum per addition) and the
 # activations' approximate exponential / reciprocal (about 1e-6): 1e-5 (conv) and 2e-5 (linear,
 # whose logsumexp sums 2048 exponentials and whose l * mish(l) tail doubles relative error)
@@ -407,14 +408,14 @@ DIAG_CONV = [(2, 8, 32, 32, 64, "gelu", True), (1, 64, 12, 140, 128, "mish_mish"
 
 
 @pytest.mark.parametrize("shape", DIAG_CONV, ids=lambda s: "x".join(map(str, s[:5])) + f"-{s[5]}")
-def test_conv_equals_oracle_on_tf32_rounded_operands(cuda_lib, shape):
+def test_conv_equals_oracle_on_its_tf32_operands(cuda_lib, shape):
     N, Cin, H, W, Cout, act, pool = shape
     d = fc_inputs.conv_inputs(N, Cin, H, W, Cout)
     f = cuda_lib.fc_conv3x3_act_pool if pool else cuda_lib.fc_conv3x3_act
     o = oracle.conv3x3_act_pool if pool else oracle.conv3x3_act
     y = f(_dev(d["x"]), _dev(d["w"]), _dev(d["b"]), act=act).cpu().numpy()
-    xr, wr = oracle.tf32_round_nearest(d["x"]), oracle.tf32_round_nearest(d["w"])
-    _check(y, o(xr, wr, d["b"], act), 1e-5, f"conv tf32-rounded {shape}")
+    xt, wr = oracle.tf32_truncate(d["x"]), oracle.tf32_round_nearest(d["w"])
+    _check(y, o(xt, wr, d["b"], act), 1e-5, f"conv tf32 operands {shape}")
 
 
 @pytest.mark.parametrize("shape", [(130, 520, 300, 1.0), (256, 1024, 2048, 1.0), (129, 64, 513, 30.0)],
