@@ -958,7 +958,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 ok = wait_bar<PAIR, POLL>(&tempty[acc], aph ^ 1u, abort_flag, a.status, a.budget);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc_fence_after();
-                if (!(ok = FC_DEBUG_OK((acc + 1) * a.Cout <= a.tmem_cols && slot < static_cast<uint32_t>(a.stages), a.status))) {
+                ok = FC_DEBUG_OK((acc + 1) * a.Cout <= a.tmem_cols && slot < static_cast<uint32_t>(a.stages), a.status);
+                if (!ok) {
                     *abort_flag = 1;
                     break;
                 }
