@@ -620,10 +620,12 @@ def gpu_arm(args):
     kernel_ms = statistics.mean(per)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
 
-    e2e_ms, h2d, d2h = time_e2e(fc, torch, key, d, device, steps=max(3, min(20, steps // 10)), warmup=2,
-                                chunks=args.e2e_chunks)
-    e2e_ms = max_over_ranks(torch, e2e_ms, dist, "cuda")
-    e2e_value = job_tflops(flops, world, e2e_ms)
+    e2e_ms = h2d = d2h = e2e_value = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(fc, torch, key, d, device, steps=max(3, min(20, steps // 10)), warmup=2,
+                                    chunks=args.e2e_chunks)
+        e2e_ms = max_over_ranks(torch, e2e_ms, dist, "cuda")
+        e2e_value = job_tflops(flops, world, e2e_ms)
 
     if rank != 0:
         return 0
@@ -655,11 +657,12 @@ def gpu_arm(args):
             "vs_baseline": None, "dtype": "bf16" if getattr(wl, "dtype", "f32") == "bf16" else "tf32",
             "data": "synthetic (seeded N(0,1) inputs, U(+-1/sqrt(fan_in)) weights)", "config": cfg,
             "roofline": roofline, "epilogue_roofline": epi, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "api": "linear: H2D + fc_linear_lse_mish + D2H" if isinstance(wl, fc_inputs.LinearWorkload)
-                    else f"{'fc_conv3x3_act_pool_host' if wl.pool else 'fc_conv3x3_act_host'}"
-                         f" (pinned host buffers, {args.e2e_chunks} overlapped slices)"},
+            "e2e": None if args.no_e2e else
+            {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h,
+             "api": "linear: H2D + fc_linear_lse_mish + D2H" if isinstance(wl, fc_inputs.LinearWorkload)
+             else f"{'fc_conv3x3_act_pool_host' if wl.pool else 'fc_conv3x3_act_host'}"
+                  f" (pinned host buffers, {args.e2e_chunks} overlapped slices)"},
             "gpu_launches": steps * launches_per_call, "clocks": clocks,
             "pct_of_roofline": 100.0 * cfg["roofline_ms"] / ms,
             "cold_l2": {"ms_median": cold_ms, "warm_ms_median": statistics.median(per),
@@ -741,6 +744,8 @@ def main():
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="slices of the batch whose host copies overlap the kernels in the end-to-end timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end leg (for launch lists of the device-resident calls alone)")
     ap.add_argument("--no-tf32-peak", action="store_true", help="skip the TF32 library GEMM peak measurement")
     args = ap.parse_args()
     if args.impl == "reference":
