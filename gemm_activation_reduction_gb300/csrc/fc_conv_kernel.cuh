@@ -160,6 +160,7 @@ struct ConvArgs {
     int upw;              // pooled single-CTA tiles: 1 (16 x 8) or 4 units side by side (16 x 32)
     int poll;             // a test shortened the wait budget: launch the polling instantiation
     int pair;             // 1: CTA pairs with M = 256 MMAs (group = 2 tiles); 0: single CTAs
+    int split_cs;         // pooled CTA pairs: the pair's two tiles at strips j and j + CS / 2 (strip_col)
     uint32_t w_block_bytes, w_total_bytes, bias_block_bytes;   // per CTA of the pair (its half of Cout)
     uint32_t strip_off, ind_off, w_off, bb_off, raw_off, bar_off;
     int use_tma;         // x staged by TMA boxes + in-warp transpose (else plain loads)
@@ -236,6 +237,19 @@ __device__ __forceinline__ TileCoord tile_coord(long long t, long long tpi, int 
     c.rb = r / CS;
     c.cs = r - c.rb * CS;
     return c;
+}
+
+// Column strip of tile c.  CTA pairs take the even (rank 0) and odd (rank 1) tiles of the tile
+// order.  With split_cs (pooled pairs, CS a multiple of 4) tile cs of a row block sits at strip
+// cs / 2 (even cs) or CS / 2 + cs / 2 (odd cs), so that the two CTAs of a pair stage strips j and
+// j + CS / 2 of one row block: both x boxes of a stage then start at the same 32-byte parity, and
+// the pair's stages alternate between boxes of one and of two sectors per row instead of one CTA
+// always fetching two (its 16-byte-aligned strip starting mid-sector).
+template <bool PAIR>
+__device__ __forceinline__ int strip_col(const TileCoord& c, const ConvArgs& a)
+{
+    if constexpr (PAIR) return a.split_cs ? (c.cs >> 1) + (c.cs & 1) * (a.CS >> 1) : c.cs;
+    else return c.cs;
 }
 
 // Next tile in (image, row block, column strip) order.
@@ -801,14 +815,14 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     constexpr int kCh = BF16 ? 16 : 8;   // channels per K block (32 B)
                     mbar_arrive_expect_tx(&rawfull[r], static_cast<uint32_t>(S::SPOS) * 32u);
                     tma_load_4d_s(smem_u32(smem + a.raw_off) + r * kRawBytes, &tmx, &rawfull[r],
-                                  (a.parts == 1 ? acb : acb / 3) * kCh, atc.cs * S::PC - a.pad, atc.rb * S::PR - a.pad,
+                                  (a.parts == 1 ? acb : acb / 3) * kCh, strip_col<PAIR>(atc, a) * S::PC - a.pad, atc.rb * S::PR - a.pad,
                                   atc.n);
                 } else if (lane == 0) {
                     mbar_arrive_expect_tx(&rawfull[r], RBox::kBytes);
                     // the patch starts pad rows above and pad + dcol columns left of the tile: a
                     // 16-byte-aligned column, possibly negative (TMA fills zeros outside x)
                     tma_load_4d(smem + a.raw_off + r * RBox::kBytes, &tmx, &rawfull[r],
-                                atc.cs * S::PC - a.pad - a.dcol, atc.rb * S::PR - a.pad,
+                                strip_col<PAIR>(atc, a) * S::PC - a.pad - a.dcol, atc.rb * S::PR - a.pad,
                                 (a.parts == 1 ? acb : acb / 3) * RBox::kCh, atc.n);
                 }
                 ++issued;
@@ -869,7 +883,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 const uint32_t strip = strip0 + slot * S::STRIP;
                 if (NHWC && !a.use_tma) {
                     fill_strip_nhwc<BF16, WIDE, ROWS, UPW>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
-                                                      tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad, a.Cin,
+                                                      tc.rb * S::PR - a.pad, strip_col<PAIR>(tc, a) * S::PC - a.pad, a.Cin,
                                                       tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -897,7 +911,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                     if (alt < n_pairs) issue_next();   // reuses buffer r: issued - use == rd
                 } else {
                     fill_strip<BF16, WIDE, ROWS, XP, UPW>(strip, a.x, tc.n < a.N ? tc.n : 0, a.parts == 1 ? cb : cb / 3,
-                                                     tc.rb * S::PR - a.pad, tc.cs * S::PC - a.pad - a.dcol, a.Cin,
+                                                     tc.rb * S::PR - a.pad, strip_col<PAIR>(tc, a) * S::PC - a.pad - a.dcol, a.Cin,
                                                      tc.n < a.N ? a.H : 0, a.W, lane, a.parts == 3 && cb % 3 == 2);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -937,7 +951,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             auto unit_ind = [&](const TileCoord& c, int u) -> uint64_t {
                 uint32_t v = 0u;
                 if constexpr (!PAIR && !WIDE) {
-                    const int valid = a.OW - (c.cs * S::PC + 8 * u);
+                    const int valid = a.OW - (strip_col<PAIR>(c, a) * S::PC + 8 * u);
                     v = (c.rb == a.RB - 1 ? 3u : 0u) + (valid >= 8 ? 0u : (valid > 0 ? 1u : 2u));
                 }
                 return i_desc0 + v * kInd16 + (static_cast<uint64_t>((kZeroPlane - v) * kInd16) << 16);
@@ -1155,7 +1169,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             auto pixel_valid = [&](const TileCoord& c, int j) {
                 const int rr = q * 32 + (lane >> 2) + 8 * j;
                 const int pr_ = rr / S::PC, pc_ = rr - (rr / S::PC) * S::PC;
-                return c.rb * S::PR + pr_ < a.OH && c.cs * S::PC + pc_ < a.OW;
+                return c.rb * S::PR + pr_ < a.OH && strip_col<PAIR>(c, a) * S::PC + pc_ < a.OW;
             };
             // two load buffers, used alternately (slice k of a tile in buf[k & 1]); a tile with an
             // odd number of slices leaves the next tile's slice 0 in buf[1], moved after its wait
@@ -1175,7 +1189,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
                 // padding pixels of a single CTA's tile already activate to -0 (padding K column);
                 // CTA pairs mask the edge tiles here
                 float m4[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-                if (PAIR && (!real || tc.rb == a.RB - 1 || tc.cs == a.CS - 1)) {
+                if (PAIR && (!real || tc.rb == a.RB - 1 || strip_col<PAIR>(tc, a) == a.CS - 1)) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) m4[j] = (real && pixel_valid(tc, j)) ? 1.0f : 0.0f;
                 }
@@ -1296,7 +1310,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
 #pragma unroll
                             for (int pp = 0; pp < 2; ++pp) {
                                 const int rr = q * 32 + (lane >> 2) + 16 * hb + 8 * pp;
-                                const int oh = tc.rb * S::PR + us + rr / S::PC, ow = tc.cs * S::PC + rr % S::PC;
+                                const int oh = tc.rb * S::PR + us + rr / S::PC, ow = strip_col<PAIR>(tc, a) * S::PC + rr % S::PC;
                                 const bool valid = real && oh < a.OH && ow < a.OW;
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
@@ -1342,7 +1356,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         }
         while (!POOL && !NHWC && ok && lt < n_units) {
             const bool real = t_first + static_cast<long long>(step) * (lt / UPT) < a.num_tiles;   // the peer's half of a last, odd pair is not
-            const int oh = tc.rb * S::PR + us + pr, ow = tc.cs * S::PC + pc;
+            const int oh = tc.rb * S::PR + us + pr, ow = strip_col<PAIR>(tc, a) * S::PC + pc;
             const bool valid = real && oh < a.OH && ow < a.OW;
             const int nlt = lt + G;
             int nacc_i = acc + G;

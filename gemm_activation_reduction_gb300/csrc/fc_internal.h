@@ -63,6 +63,7 @@ struct ConvPlan {
     long long num_tiles;  // N * tpi
     int grid;             // CTAs (persistent)
     int pair;             // CTA pairs (clusters of 2, M = 256 MMAs) instead of single CTAs
+    int split_cs;         // pooled pairs: the pair's tiles at column strips j and j + CS / 2
     long long pbase;      // tile groups per cluster (the first `prem` clusters take one more)
     int prem;
     int J;                // image slots per CTA in the pool partial buffer
