@@ -64,6 +64,13 @@ POOL_SHAPES = [
     (1, 3, 10, 9, 1, "bf16", "mish"),
     (2, 12, 18, 22, 200, "f32", "gelu"),     # CTA pairs, 104 channels each
     (1, 24, 15, 16, 145, "bf16", "gelu_tanh"),
+    # CTA pairs whose column-strip count is a multiple of 4 (the pair's two tiles at strips j and
+    # j + CS/2), with a ragged last strip or row block, and the neighbouring counts that keep the
+    # plain order
+    (2, 16, 34, 34, 256, "bf16", "gelu"),    # OW 32: 4 strips
+    (1, 16, 21, 61, 144, "bf16", "mish"),    # OW 59: 8 strips, the last one 3 wide
+    (3, 8, 19, 50, 160, "f32", "gelu"),      # OW 48: 6 strips
+    (1, 8, 40, 66, 256, "f32", "gelu"),      # OW 64: 8 strips, 3 row blocks (the last 6 rows)
 ]
 
 
