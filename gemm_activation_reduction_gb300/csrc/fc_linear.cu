@@ -26,9 +26,8 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256, kStages = 4;
 constexpr int kKRowBytes = 128;                       // K per stage: one 128-byte swizzle row
-constexpr int kBK = kKRowBytes / 4;                   // fp32 elements of it (bf16: twice as many)
 template <bool BF16>
-constexpr int kKElems = BF16 ? kKRowBytes / 2 : kKRowBytes / 4;
+constexpr int kKElems = BF16 ? kKRowBytes / 2 : kKRowBytes / 4;   // its elements: 32 fp32 or 64 bf16
 constexpr uint32_t kABytes = kBM * kKRowBytes;        // 16 KB
 constexpr uint32_t kBBytes = kBN * kKRowBytes;        // 32 KB
 constexpr int kThreads = 192;
@@ -151,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // x's row blocks are re-read by every column tile while W streams through the L2 once:
+            // W's lines go first when the L2 needs room, so x's stay
+            const uint64_t stream_ = l2_policy_evict_first();
             for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
                 const int mb = t % a.m_blocks, nb = t / a.m_blocks;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const CUtensorMap* mw;
                     const int kk = k_segment(kb, a.kseg, &tmx, &tmw, &tmx_lo, &tmw_lo, &mx, &mw);
                     tma_load_2d(sA + stage * kABytes, mx, &full[stage], kk * kKElems<BF16>, mb * kBM);
-                    tma_load_2d(sB + stage * kBBytes, mw, &full[stage], kk * kKElems<BF16>, nb * kBN);
+                    tma_load_2d_hint(sB + stage * kBBytes, mw, &full[stage], kk * kKElems<BF16>, nb * kBN, stream_);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -362,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // x's row blocks are re-read by every column tile while W streams through the L2 once:
+            // W's lines go first when the L2 needs room, so x's stay
+            const uint64_t stream_ = l2_policy_evict_first();
             for (int t = cluster; ok && t < a.num_tiles; t += nclusters) {
                 const int mp = t % a.m_pairs, nb = t / a.m_pairs;
                 const int m0 = mp * 2 * kPBM + static_cast<int>(rank) * kPBM;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const CUtensorMap* mw;
                     const int kk = k_segment(kb, a.kseg, &tmx, &tmw, &tmx_lo, &tmw_lo, &mx, &mw);
                     tma_load_2d_pair(sA + stage * kPABytes, mx, fbar, kk * kKElems<BF16>, m0);
-                    tma_load_2d_pair(sB + stage * kPBBytes, mw, fbar, kk * kKElems<BF16>, n0);
+                    tma_load_2d_pair_hint(sB + stage * kPBBytes, mw, fbar, kk * kKElems<BF16>, n0, stream_);
                     if (++stage == kPStages) {
                         stage = 0;
                         phase ^= 1u;
