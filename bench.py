@@ -54,9 +54,10 @@ def peaks():
 # SM (ex2.approx 32 lanes per clock, rcp.approx 16; microbenchmarked on this GB300).
 #   erf-GELU: 5 Horner FMAs, z + |z|, the final FMA, the accumulate; one exponential
 #   tanh-GELU: 3 for the exponent, 1 + e, the product, the accumulate; one exponential, one reciprocal
-#   Mish: 6 arithmetic, the accumulate; one exponential, one reciprocal; Mish twice: 12 + 1, two of each
-EPILOGUE_COST = {"gelu": (8, 1 / 32), "gelu_tanh": (6, 1 / 32 + 1 / 16), "mish": (7, 1 / 32 + 1 / 16),
-                 "mish_mish": (13, 2 * (1 / 32 + 1 / 16))}
+#   Mish: 4 arithmetic (the scaled exponent, v, h, z - z / h), the accumulate; one exponential, one
+#   reciprocal; Mish twice: 8 + 1, two of each
+EPILOGUE_COST = {"gelu": (8, 1 / 32), "gelu_tanh": (6, 1 / 32 + 1 / 16), "mish": (5, 1 / 32 + 1 / 16),
+                 "mish_mish": (9, 2 * (1 / 32 + 1 / 16))}
 FMA_RESULTS_PER_CLK_SM = 128
 
 
