@@ -207,6 +207,8 @@ PAD_SHAPES = [
     (1, 16, 9, 136, 64, 3, "bf16", "mish", False),     # bf16, shift 5
     (1, 16, 7, 128, 200, 1, "f32", "mish", False),     # CTA pairs, padded Cout
     (1, 3, 5, 7, 24, 2, "f32", "gelu", False),         # plain-load staging, full output
+    (1, 16, 20, 62, 256, 1, "bf16", "gelu", True),     # CTA pairs at strips j and j + 4 (8 strips), shift 7
+    (2, 8, 18, 30, 160, 1, "f32", "mish", True),       # CTA pairs at strips j and j + 2 (4 strips), shift 3
 ]
 
 
@@ -281,6 +283,8 @@ NHWC_SHAPES = [
     (1, 16, 9, 130, 200, 1, "f32", "mish", False, None),     # CTA pairs
     (1, 3, 11, 13, 32, 1, "f32", "gelu_tanh", False, None),  # 3 channels: plain loads
     (1, 24, 10, 40, 64, 0, "f32", "mish_mish", False, "3xtf32"),
+    (1, 16, 20, 34, 256, 0, "bf16", "gelu", True, None),     # CTA pairs at strips j and j + 2 (4 strips)
+    (1, 8, 19, 64, 160, 1, "f32", "gelu", True, None),       # CTA pairs at strips j and j + 4, padding
 ]
 
 
