@@ -157,10 +157,11 @@ template <int XPF, int XPB>
 Geometry geometry_xp(int bf16, int pool, int pair, int upw)
 {
     if (pool && upw == 4)
-        return bf16 ? geometry_of<true, false, 1, XPB, false, 4>() : geometry_of<false, false, 1, XPF, false, 4>();
+        return bf16 ? geometry_of<true, false, 1, XPB, false, 4>()
+                    : geometry_of<false, false, 1, staged_xp(false, false, 1, 4, XPF != 0, false), false, 4>();
     if (pool) return bf16 ? geometry_of<true, false, 1, XPB>() : geometry_of<false, false, 1, XPF>();
     if (pair) return bf16 ? geometry_of<true, true, 1, XPB>() : geometry_of<false, true, 1, XPF>();
-    return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, staged_xp(false, true, 2, XPF != 0, false)>();
+    return bf16 ? geometry_of<true, true, 2, XPB>() : geometry_of<false, true, 2, staged_xp(false, true, 2, 1, XPF != 0, false)>();
 }
 
 // padx: the padding's column shift needs XP = 4 (fp32) / 8 (bf16) extra staged columns

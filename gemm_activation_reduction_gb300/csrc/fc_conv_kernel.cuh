@@ -95,16 +95,22 @@ constexpr uint32_t kSmemBudget = 227 * 1024 - kBarBytes - 1024 - 128;
 // tile, d = (-p) mod (16 B / element size), so that the TMA box starts on a 16-byte
 // boundary; XP = 4 (fp32) or 8 (bf16) extra staged columns hold the d-column shift and
 // every MMA operand starts d staged pixels further (XP = 0 when d is always 0).  fp32 two-row
-// full-output tiles stage an odd number of columns instead (XP = 1, or 5 with the shift:
-// 131 or 135): the re-layout then maps a quarter-warp to 4 rows x 2 column quads whose
-// 16-byte strip stores, 16 * SC bytes per row apart, fall in 8 different bank groups.
+// full-output tiles and fp32 pooled four-unit tiles stage an odd number of columns instead
+// (XP = 1, or 5 with the shift: 131 / 135, or 35 / 39): the re-layout then maps a quarter-warp to
+// 4 rows x 2 column quads whose 16-byte strip stores, 16 * SC bytes per row apart, fall in 8
+// different bank groups.
 //
 // NHWC input: a K block lands as one TMA box [SR rows][SC columns][32 B of channels] and is
 // split into the two planes; NHWC planes are 64 bytes past a 128-byte multiple apart so that
 // the split's 128-bit stores of one phase (4 pixels x 2 planes) cover all banks.
-__host__ __device__ constexpr int staged_xp(bool bf16, bool wide, int rows, bool padx, bool nhwc)
+__host__ __device__ constexpr bool fp32_quarter_map(bool bf16, bool wide, int rows, int upw)
 {
-    return nhwc ? 0 : (!bf16 && wide && rows == 2) ? (padx ? 5 : 1) : (padx ? (bf16 ? 8 : 4) : 0);
+    return !bf16 && ((wide && rows == 2) || (!wide && upw == 4));
+}
+
+__host__ __device__ constexpr int staged_xp(bool bf16, bool wide, int rows, int upw, bool padx, bool nhwc)
+{
+    return nhwc ? 0 : fp32_quarter_map(bf16, wide, rows, upw) ? (padx ? 5 : 1) : (padx ? (bf16 ? 8 : 4) : 0);
 }
 
 template <bool WIDE, int ROWS = 1, int XP = 0, bool NHWC = false, int UPW = 1>
@@ -126,13 +132,13 @@ struct Shape {
 
 // Raw TMA box of one K block: [channel][SR rows][cols] in x's own (channel-major)
 // order; cols covers the SC staged columns and keeps each box row a 16-byte multiple.  The
-// fp32 two-row full-output box is 8 columns past a multiple of 32 wide (136 for 131 or 135
-// staged columns), so that the re-layout's 16-byte reads of a quarter-warp (4 rows x 2
-// column quads) fall in 8 different bank groups too.
+// fp32 boxes of the quarter map are 8 columns past a multiple of 32 wide (136 for 131 or 135
+// staged columns, 40 for 35 or 39), so that the re-layout's 16-byte reads of a quarter-warp
+// (4 rows x 2 column quads) fall in 8 different bank groups too.
 template <bool BF16, bool WIDE, int ROWS = 1, int XP = 0, int UPW = 1>
 struct RawBox {
     using S = Shape<WIDE, ROWS, XP, false, UPW>;
-    static constexpr bool kQuarterMap = !BF16 && WIDE && ROWS == 2;
+    static constexpr bool kQuarterMap = fp32_quarter_map(BF16, WIDE, ROWS, UPW);
     static constexpr int kCh = BF16 ? 16 : 8;
     static constexpr int kCols = BF16 ? (S::SC + 7) / 8 * 8
                                       : (kQuarterMap ? (S::SC - 8 + 31) / 32 * 32 + 8 : (S::SC + 3) / 4 * 4);
@@ -332,20 +338,26 @@ __device__ __forceinline__ void transpose_raw(uint32_t raw, uint32_t strip, int 
     using RB_ = RawBox<BF16, WIDE, ROWS, XP, UPW>;
     static_assert(!(BF16 && LO), "split TF32 is an fp32 mode");
     if constexpr (RB_::kQuarterMap) {
-        // fp32 two-row full-output tiles: item = (group g, staged row, column quad), 4 channels x
-        // 4 pixels -> four 16-byte rows; a quarter-warp takes the 4 staged rows x 2 adjacent
-        // quads of one (g, quad pair), so that with SC odd and the box 8 columns past a multiple
-        // of 32 wide both its 16-byte reads and its 16-byte stores hit 8 different bank groups
-        static_assert(S::SR == 4 && S::SC % 2 == 1 && RB_::kCols % 32 == 8 && RB_::kCols >= S::SC, "quarter map");
+        // fp32 two-row full-output tiles (4 staged rows) and pooled four-unit tiles (18 staged
+        // rows, taken in row groups of 4, the last one holding 2): item = (group g, staged row,
+        // column quad), 4 channels x 4 pixels -> four 16-byte rows; a quarter-warp takes the 4
+        // rows of one row group x 2 adjacent quads of one (g, row group, quad pair), so that
+        // with SC odd and the box 8 columns past a multiple of 32 wide both its 16-byte reads
+        // and its 16-byte stores hit 8 different bank groups
+        static_assert(S::SC % 2 == 1 && RB_::kCols % 32 == 8 && RB_::kCols >= S::SC, "quarter map");
         constexpr int kQuads = (S::SC + 3) / 4;
         constexpr int kPairs = (kQuads + 1) / 2;
-        const int row = lane & 3;
+        constexpr int kSlots = (S::SR + 3) / 4 * kPairs;   // quarter-warp slots per channel group
         const int cq_lo = (lane >> 2) & 1;
 #pragma unroll 2
-        for (int qs = lane >> 3; qs < 2 * kPairs; qs += 4) {
-            const int g = qs >= kPairs ? 1 : 0;
-            const int cq = 2 * (qs - g * kPairs) + cq_lo;
-            if (cq < kQuads) {
+        for (int qs = lane >> 3; qs < 2 * kSlots; qs += 4) {
+            const int g = qs >= kSlots ? 1 : 0;
+            const int rem = qs - g * kSlots;
+            // one row group (the two-row tiles): no division, no row bound
+            const int rg = S::SR == 4 ? 0 : rem / kPairs;
+            const int cq = 2 * (rem - rg * kPairs) + cq_lo;
+            const int row = 4 * rg + (lane & 3);
+            if (cq < kQuads && (S::SR % 4 == 0 || row < S::SR)) {
                 const uint32_t src = raw + static_cast<uint32_t>(4 * g) * RB_::kChPlane +
                                      static_cast<uint32_t>(row * RB_::kCols + 4 * cq) * 4u;
                 float4 v[4];
@@ -701,7 +713,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // and weight block); CTA pairs keep one row per CTA
     constexpr int ROWS = (WIDE && !PAIR) ? 2 : 1;
     // room for the padding's column shift a.dcol (< 16 B of elements) when it is not 0
-    constexpr int XP = staged_xp(BF16, WIDE, ROWS, PADX, NHWC);
+    constexpr int XP = staged_xp(BF16, WIDE, ROWS, UPW, PADX, NHWC);
     static_assert(!(PADX && NHWC), "NHWC boxes start at any column: no shift room needed");
     static_assert(UPW == 1 || (POOL && !PAIR), "side-by-side units: single-CTA pooled tiles only");
     using S = Shape<WIDE, ROWS, XP, NHWC, UPW>;
