@@ -93,6 +93,9 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
 // step * g + r.  Records a CTA never reached hold zeros.  One warp per output: record k of the
 // output's list (cluster, CTA of the cluster, record) goes to lane k % 32, each lane sums its
 // records in order, and a fixed shuffle tree adds the lanes -- the same order on every run.
+// The sums are fp32: a few dozen partial sums per output, each already a sum over thousands of
+// values, so the rounding stays near 1e-6 relative, far inside every tolerance; fp64 adds and
+// shuffles took about a third of this kernel's time on this GPU.
 __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int Co, int Cout, long long tpi,
                                          long long pbase, int prem, int J, int step, int recs, double inv_count,
                                          int* status, int grid)
@@ -116,7 +119,7 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
     const long long c0 = cluster_of(t0 / step), c1 = cluster_of((t0 + tpi - 1) / step);
     const int per_cluster = step * recs;
     const long long total = (c1 - c0 + 1) * per_cluster;
-    double s = 0.0;
+    float s = 0.0f;
     for (long long k = lane; k < total; k += 32) {
         const long long c = c0 + k / per_cluster;
         const int rq = static_cast<int>(k - (k / per_cluster) * per_cluster);
@@ -126,11 +129,11 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
         const long long slot = n - nf;
         if (slot < 0 || slot >= J) continue;
         if (FC_DEBUG_OK(cta >= 0 && cta < grid && q < recs && co < Cout, status))
-            s += static_cast<double>(ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
+            s += (ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) y[wid] = static_cast<float>(s * inv_count);
+    if (lane == 0) y[wid] = static_cast<float>(static_cast<double>(s) * inv_count);
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
