@@ -90,9 +90,10 @@ __global__ void conv_weight_relayout_kernel(const void* w, const void* b, void* 
 // y[n, co] = (fixed-order sum of every image-n record of the CTAs whose tiles can touch
 // image n) / (OH * OW), for co < Co; records hold Cout >= Co channels.  Cluster c handles tile
 // groups [P(c), P(c+1)) of `step` tiles (2 for CTA pairs, else 1); its CTA r handles tiles
-// step * g + r.  Records a CTA never reached hold zeros.  One warp per output: record k of the
-// output's list (cluster, CTA of the cluster, record) goes to lane k % 32, each lane sums its
-// records in order, and a fixed shuffle tree adds the lanes -- the same order on every run.
+// step * g + r.  Records a CTA never reached hold zeros.  One warp per 4 consecutive channels of
+// an image: record k of the image's list (cluster, CTA of the cluster, record) goes to lane
+// k % 32, which loads the 4 channels with one 16-byte load (Cout is a multiple of 16) and sums
+// its records in order; a fixed shuffle tree adds the lanes -- the same order on every run.
 // The sums are fp32: a few dozen partial sums per output, each already a sum over thousands of
 // values, so the rounding stays near 1e-6 relative, far inside every tolerance; fp64 adds and
 // shuffles took about a third of this kernel's time on this GPU.
@@ -101,17 +102,20 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
                                          int* status, int grid)
 {
     pdl_wait();   // the fused kernel's records are complete and visible
+    const int quads = (Co + 3) / 4;
     const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (wid >= static_cast<long long>(N) * Co) return;   // whole warps leave together
+    if (wid >= static_cast<long long>(N) * quads) return;   // whole warps leave together
+    const int n = static_cast<int>(wid / quads);
+    const int co0 = 4 * static_cast<int>(wid - static_cast<long long>(n) * quads);
+    const int nco = Co - co0 < 4 ? Co - co0 : 4;
+    float* yo = y + static_cast<long long>(n) * Co + co0;
     // a bounded wait that gave up (or a failed index check of a debug build) leaves records the
     // fused kernel never wrote: say so in the output
     if (*reinterpret_cast<const volatile int*>(status) != 0) {
-        if (lane == 0) y[wid] = __int_as_float(0x7fc00000);
+        if (lane < nco) yo[lane] = __int_as_float(0x7fc00000);
         return;
     }
-    const int n = static_cast<int>(wid / Co);
-    const int co = static_cast<int>(wid - static_cast<long long>(n) * Co);
     const long long big = static_cast<long long>(prem) * (pbase + 1);
     auto cluster_of = [&](long long p) -> long long { return p < big ? p / (pbase + 1) : prem + (p - big) / pbase; };
     auto start_of = [&](long long c) -> long long { return c * pbase + (c < prem ? c : prem); };
@@ -119,7 +123,7 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
     const long long c0 = cluster_of(t0 / step), c1 = cluster_of((t0 + tpi - 1) / step);
     const int per_cluster = step * recs;
     const long long total = (c1 - c0 + 1) * per_cluster;
-    float s = 0.0f;
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (long long k = lane; k < total; k += 32) {
         const long long c = c0 + k / per_cluster;
         const int rq = static_cast<int>(k - (k / per_cluster) * per_cluster);
@@ -128,12 +132,22 @@ __global__ void conv_pool_combine_kernel(const float* ws, float* y, int N, int C
         const long long nf = (step * start_of(c) + r) / tpi;
         const long long slot = n - nf;
         if (slot < 0 || slot >= J) continue;
-        if (FC_DEBUG_OK(cta >= 0 && cta < grid && q < recs && co < Cout, status))
-            s += (ws[((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co]);
+        if (FC_DEBUG_OK(cta >= 0 && cta < grid && q < recs && co0 + 4 <= Cout, status)) {
+            const float4 v = *reinterpret_cast<const float4*>(ws + ((cta * J + slot) * recs + q) * static_cast<long long>(Cout) + co0);
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) y[wid] = static_cast<float>(static_cast<double>(s) * inv_count);
+    for (int off = 16; off > 0; off >>= 1) {
+        s.x += __shfl_xor_sync(0xffffffffu, s.x, off);
+        s.y += __shfl_xor_sync(0xffffffffu, s.y, off);
+        s.z += __shfl_xor_sync(0xffffffffu, s.z, off);
+        s.w += __shfl_xor_sync(0xffffffffu, s.w, off);
+    }
+    if (lane < nco) {
+        const float v = lane == 0 ? s.x : (lane == 1 ? s.y : (lane == 2 ? s.z : s.w));
+        yo[lane] = static_cast<float>(static_cast<double>(v) * inv_count);
+    }
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -390,7 +404,7 @@ cudaError_t conv_launch(const ConvPlan& p, const void* x, const void* w, const v
     if (e != cudaSuccess) return e;
 
     if (p.pool) {
-        const long long outs = static_cast<long long>(p.N) * p.Co;   // one warp each
+        const long long outs = static_cast<long long>(p.N) * ((p.Co + 3) / 4);   // one warp per 4 channels
         const int threads = 256;
         const int blocks = static_cast<int>((outs * 32 + threads - 1) / threads);
         cudaLaunchConfig_t cfg{};
